@@ -1,0 +1,150 @@
+/*
+ * mla.h - C ABI of the GB300 (sm_103a) absorbed, NoPE, causal Gated MLA forward.
+ *
+ * The method is the one on the course-notes page "Gated MLA（矩阵吸收版）"
+ * (Gated MLA with matrix absorption): keys and values are never decompressed;
+ * each head's query is absorbed into the latent space, q_abs = q . W_UK,
+ * scored directly against the shared rank-r latent c, softmax-weighted sums
+ * are taken over c itself, and only then are they up-projected by W_UV^T and
+ * gated by sigmoid(W_g x) (section "完整计算流（四步）", steps 2-4; shapes from
+ * the symbol-table page "符号表", table "MLA 变量").
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates, frees or retains them past the call.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Nothing is launched when a status other than MLA_OK is returned.
+ *  - Layouts are dense row-major (C order) with the shapes given; all float
+ *    tensors of one call share one dtype; accumulation is fp32; `out` has the
+ *    input dtype.
+ *  - Arguments are validated on the host before any launch.  Errors raised on
+ *    the device (a bounded wait that gave up) are recorded in a per-device
+ *    error word read by mla_get_device_error().
+ *  - There is no CPU fallback and no silent slow path: a shape outside the
+ *    supported set returns MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(_WIN32)
+#define MLA_API
+#else
+#define MLA_API __attribute__((visibility("default")))
+#endif
+
+/* Element types. */
+typedef enum {
+    MLA_DTYPE_BF16 = 0, /* bfloat16 inputs and output, fp32 accumulation */
+    MLA_DTYPE_F32 = 1   /* fp32 inputs and output, fp32 FMA (no TF32)    */
+} mla_dtype_t;
+
+/* Status codes (0 = success, negative = error). */
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_NULL = -1,           /* a required pointer is NULL                       */
+    MLA_ERR_SHAPE = -2,          /* a size is negative, zero where it may not be, or overflows */
+    MLA_ERR_DTYPE = -3,          /* unknown dtype                                   */
+    MLA_ERR_ALIGN = -4,          /* a pointer or stride is not 16-byte aligned      */
+    MLA_ERR_WORKSPACE = -5,      /* workspace missing or smaller than required      */
+    MLA_ERR_UNSUPPORTED = -6,    /* valid shape that no kernel of this build serves  */
+    MLA_ERR_CUDA = -7,           /* a CUDA runtime/driver call failed               */
+    MLA_ERR_DEVICE_TIMEOUT = -8, /* a bounded device-side wait gave up              */
+    MLA_ERR_DEVICE_BOUNDS = -9   /* a device-side bounds check rejected an index    */
+} mla_status_t;
+
+/*
+ * mla_absorbed_attn_fwd - causal prefill of the absorbed Gated MLA.
+ *
+ * Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）":
+ *   step 2  q_abs[b,t,h,:] = q[b,t,h,:] . W_UK[h]                  [B,T,H,r]
+ *           score[b,h,t,u] = scale * q_abs[b,t,h,:] . c[b,u,:]     (u <= t)
+ *           attn = softmax over u of the causally masked score
+ *   step 3  o_lat[b,h,t,:] = sum_u attn[b,h,t,u] * c[b,u,:]        [B,H,T,r]
+ *           o[b,h,t,v]     = o_lat[b,h,t,:] . W_UV[h,v,:]
+ *   step 4  out[b,t,h*d_v+v] = sigmoid(gate[b,t,h*d_v+v]) * o[b,h,t,v]
+ * The output projection W_o of step 4 is not part of this call.
+ *
+ * Arguments (shapes in elements, dense row-major):
+ *   q     [B,T,H,d_q]   queries (the step-1 low-rank query path's output)
+ *   c     [B,T,r]       shared latent, used as both key and value
+ *   w_uk  [H,d_q,r]     key up-projection W_UK (first block of kv_up.weight)
+ *   w_uv  [H,d_v,r]     value up-projection W_UV (second block of kv_up.weight)
+ *   gate  [B,T,H*d_v]   pre-sigmoid gate logits W_g x, or NULL for no gate
+ *   scale               softmax scale applied to the score (1.0 = the page's listing)
+ *   out   [B,T,H*d_v]   result, flat index h*d_v + v; must not alias an input
+ * Masking: token t attends to tokens 0..t of its own sequence.
+ * Supported: F32 with r, d_q, d_v <= 64; BF16 with (r, d_q, d_v) = (512, 128, 128)
+ * or (32, 16, 16).  B*T == 0 is a no-op returning MLA_OK.
+ * Alignment: every pointer 16-byte aligned.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                  const void *gate, float scale, void *out,
+                                  int B, int T, int H, int d_q, int d_v, int r,
+                                  int dtype, void *stream);
+
+/*
+ * mla_latent_decode_workspace_size - bytes of device workspace mla_latent_decode
+ * needs for these sizes on the CURRENT device (it depends on the SM count).
+ * Returns 0 for sizes that are invalid or unsupported.
+ */
+MLA_API size_t mla_latent_decode_workspace_size(int B, int H, int r, int max_len);
+
+/*
+ * mla_latent_decode - one decode step over the cached latent.
+ *
+ * Only the latent c is cached (page "Gated MLA（矩阵吸收版）", sections
+ * "标准 MHA 的 KV cache 问题" and "形状与参数对比", KV-cache table: r values
+ * per token instead of 2*H*d).  Each sequence b has one new query, already
+ * absorbed (q_abs = q . W_UK, step 2), that attends, without a mask, to its
+ * cache rows 0 .. lens[b]-1 (the caller has appended the new token's own
+ * latent first).  Steps 2-4 then follow as in the prefill.
+ *
+ * Arguments:
+ *   q_abs     [B,H,r]         absorbed queries
+ *   c_cache   element (b,u,j) at b*max_len*ld_cache + u*ld_cache + j
+ *   ld_cache  row stride of the cache in elements (>= r, multiple of 8)
+ *   lens      int32 [B] on the device, 0 <= lens[b] <= max_len;
+ *             lens[b] == 0 writes a zero output row.  Rows at or beyond
+ *             lens[b] are never used, whatever they hold.
+ *   max_len   rows allocated per sequence
+ *   w_uv      [H,d_v,r]       value up-projection
+ *   gate      [B,H*d_v]       pre-sigmoid gate logits, or NULL
+ *   scale     softmax scale
+ *   out       [B,H*d_v]
+ *   workspace device buffer of >= mla_latent_decode_workspace_size(...) bytes,
+ *             16-byte aligned, not used by any other call in flight
+ * Supported: BF16 with r = 512, d_v = 128, 1 <= H <= 128.
+ * A lens[b] outside [0, max_len] found on the device is clamped to that
+ * range and reported as MLA_ERR_DEVICE_BOUNDS by mla_get_device_error().
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long ld_cache, const int *lens,
+                              int max_len, const void *w_uv, const void *gate, float scale, void *out,
+                              int B, int H, int d_v, int r, int dtype,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mla_get_device_error - synchronise `stream`, then read and clear the current
+ * device's error word.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT,
+ * MLA_ERR_DEVICE_BOUNDS, or MLA_ERR_CUDA if the synchronisation itself failed.
+ */
+MLA_API int mla_get_device_error(void *stream);
+
+/* mla_status_string - static, NUL-terminated description of a status code. */
+MLA_API const char *mla_status_string(int status);
+
+/* mla_version - library version as major*10000 + minor*100 + patch. */
+MLA_API int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

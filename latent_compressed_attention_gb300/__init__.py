@@ -1,1 +1,193 @@
-"""GB300-native absorbed causal Gated MLA (placeholder; binding follows)."""
+"""GB300-native (sm_103a) absorbed, NoPE, causal Gated MLA forward.
+
+A thin ctypes binding over the C ABI in ``include/mla.h`` (``libmla_gb300.so``,
+built in-tree by ``_build.build()``).  The binding only marshals arguments:
+PyTorch provides device memory and the current stream, and every step of the
+computation runs in the library's CUDA kernels.  There is no CPU fallback: if
+the library is missing or a call fails, an exception is raised.
+
+Entry points (same names as the C functions):
+    mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale=1.0, out=None)
+    mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale=1.0, out=None, workspace=None)
+    mla_latent_decode_workspace_size(B, H, r, max_len)
+    mla_get_device_error(stream=None)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from ._build import LIB_PATH, build
+
+__all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
+           "mla_latent_decode_workspace_size", "mla_get_device_error", "mla_status_string", "mla_version",
+           "DTYPE_BF16", "DTYPE_F32"]
+
+DTYPE_BF16 = 0
+DTYPE_F32 = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MLAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({mla_status_string(status)})")
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def library():
+    """The loaded C library (ctypes.CDLL) with argument types declared."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library {LIB_PATH} is not built; run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
+            lib.mla_absorbed_attn_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, i, i, i, i, i, i, i, vp]
+            lib.mla_absorbed_attn_fwd.restype = i
+            lib.mla_latent_decode_workspace_size.argtypes = [i, i, i, i]
+            lib.mla_latent_decode_workspace_size.restype = sz
+            lib.mla_latent_decode.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp, sz, vp]
+            lib.mla_latent_decode.restype = i
+            lib.mla_get_device_error.argtypes = [vp]
+            lib.mla_get_device_error.restype = i
+            lib.mla_status_string.argtypes = [i]
+            lib.mla_status_string.restype = ctypes.c_char_p
+            lib.mla_version.argtypes = []
+            lib.mla_version.restype = i
+            _lib = lib
+    return _lib
+
+
+def mla_status_string(status: int) -> str:
+    try:
+        return library().mla_status_string(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def mla_version() -> int:
+    return int(library().mla_version())
+
+
+# ----------------------------------------------------------------------------- torch marshalling
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float32")
+
+
+def _check(t, name, dtype, device, shape=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU fallback exists)")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream_ptr(stream, device):
+    torch = _torch()
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=None, stream=None):
+    """Causal absorbed Gated-MLA prefill; returns out [B,T,H*d_v] (allocated if not given).
+
+    q [B,T,H,d_q], c [B,T,r], w_uk [H,d_q,r], w_uv [H,d_v,r], gate [B,T,H*d_v]
+    (pre-sigmoid logits) or None; all CUDA, contiguous, one dtype (bf16/fp32).
+    """
+    torch = _torch()
+    B, T, H, d_q = q.shape
+    r = c.shape[-1]
+    d_v = w_uv.shape[1]
+    dev, dt = q.device, q.dtype
+    _check(q, "q", dt, dev)
+    _check(c, "c", dt, dev, (B, T, r))
+    _check(w_uk, "w_uk", dt, dev, (H, d_q, r))
+    _check(w_uv, "w_uv", dt, dev, (H, d_v, r))
+    if gate is not None:
+        _check(gate, "gate", dt, dev, (B, T, H * d_v))
+    if out is None:
+        out = torch.empty((B, T, H * d_v), dtype=dt, device=dev)
+    _check(out, "out", dt, dev, (B, T, H * d_v))
+    rc = library().mla_absorbed_attn_fwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(),
+                                         None if gate is None else gate.data_ptr(), float(scale), out.data_ptr(),
+                                         B, T, H, d_q, d_v, r, _dtype_code(q), _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_absorbed_attn_fwd")
+    return out
+
+
+def mla_latent_decode_workspace_size(B: int, H: int, r: int, max_len: int) -> int:
+    return int(library().mla_latent_decode_workspace_size(B, H, r, max_len))
+
+
+def mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0, out=None, workspace=None,
+                      stream=None):
+    """One decode step over the cached latent; returns out [B,H*d_v].
+
+    q_abs [B,H,r], c_cache [B,max_len,r] (or a row-strided view with unit
+    inner stride), lens int32 [B] on the device, w_uv [H,d_v,r], gate
+    [B,H*d_v] or None.  A workspace (uint8 CUDA tensor) is allocated when not given.
+    """
+    torch = _torch()
+    B, H, r = q_abs.shape
+    max_len = c_cache.shape[1]
+    d_v = w_uv.shape[1]
+    dev, dt = q_abs.device, q_abs.dtype
+    _check(q_abs, "q_abs", dt, dev)
+    if c_cache.dtype != dt or c_cache.device != dev or c_cache.dim() != 3 or c_cache.shape[0] != B \
+            or c_cache.shape[2] != r or c_cache.stride(2) != 1 or c_cache.stride(0) != max_len * c_cache.stride(1):
+        raise ValueError("c_cache must be [B,max_len,r] with unit inner stride and batch stride max_len*row_stride")
+    ld_cache = c_cache.stride(1)
+    _check(lens, "lens", torch.int32, dev, (B,))
+    _check(w_uv, "w_uv", dt, dev, (H, d_v, r))
+    if gate is not None:
+        _check(gate, "gate", dt, dev, (B, H * d_v))
+    if out is None:
+        out = torch.empty((B, H * d_v), dtype=dt, device=dev)
+    _check(out, "out", dt, dev, (B, H * d_v))
+    lib = library()
+    need = int(lib.mla_latent_decode_workspace_size(B, H, r, max_len))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_latent_decode(q_abs.data_ptr(), c_cache.data_ptr(), ld_cache, lens.data_ptr(), max_len,
+                               w_uv.data_ptr(), None if gate is None else gate.data_ptr(), float(scale),
+                               out.data_ptr(), B, H, d_v, r, _dtype_code(q_abs), ws_ptr, ws_bytes,
+                               _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_latent_decode")
+    return out
+
+
+def mla_get_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    return int(library().mla_get_device_error(_stream_ptr(stream, dev)))

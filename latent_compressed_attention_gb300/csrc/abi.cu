@@ -1,0 +1,175 @@
+// C ABI of the library (declared in include/mla.h): host-side validation,
+// dispatch to the kernels, and the per-device error word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/mla.h"
+#include "internal.h"
+
+namespace mla {
+namespace {
+
+// Device error word: kernels record the first device-side failure here.
+__device__ int g_device_error = 0;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int *err_word = nullptr;
+    int num_sms = 0;
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+
+cudaError_t device_info(DeviceInfo *&out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_error);
+        if (e != cudaSuccess) return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        d.err_word = static_cast<int *>(p);
+        d.num_sms = sms;
+        d.ready = true;
+    }
+    out = &d;
+    return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool mul_fits(long long a, long long b, long long limit) { return a == 0 || b <= limit / a; }
+
+}  // namespace
+
+void *tensor_map_encode_fn() {
+    static void *fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = p;
+    });
+    return fn;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+MLA_API const char *mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_NULL: return "a required pointer is NULL";
+        case MLA_ERR_SHAPE: return "invalid size";
+        case MLA_ERR_DTYPE: return "unknown dtype";
+        case MLA_ERR_ALIGN: return "pointer or stride not 16-byte aligned";
+        case MLA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MLA_ERR_UNSUPPORTED: return "shape or dtype not supported by this build";
+        case MLA_ERR_CUDA: return "CUDA call failed";
+        case MLA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case MLA_ERR_DEVICE_BOUNDS: return "device-side bounds check failed";
+        default: return "unknown status";
+    }
+}
+
+MLA_API int mla_version(void) { return 100; }
+
+MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                  const void *gate, float scale, void *out, int B, int T, int H, int d_q,
+                                  int d_v, int r, int dtype, void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0) return MLA_ERR_SHAPE;
+    const long long rows = static_cast<long long>(B) * T;
+    if (!mul_fits(rows, static_cast<long long>(H) * (d_q > d_v ? d_q : d_v), LLONG_MAX / 8) ||
+        !mul_fits(rows, r, LLONG_MAX / 8) || rows > INT_MAX)
+        return MLA_ERR_SHAPE;
+    if (!q || !c || !w_uk || !w_uv || !out) return MLA_ERR_NULL;
+    if (!aligned16(q) || !aligned16(c) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(out) ||
+        (gate && !aligned16(gate)))
+        return MLA_ERR_ALIGN;
+    const bool f32 = dtype == MLA_DTYPE_F32;
+    const bool ok_shape = f32 ? prefill_f32_simt_supports(r, d_q, d_v)
+                              : (prefill_bf16_r512_supports(r, d_q, d_v) || prefill_bf16_small_supports(r, d_q, d_v));
+    if (!ok_shape) return MLA_ERR_UNSUPPORTED;
+    if (rows == 0) return MLA_OK;
+
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    PrefillArgs a{q, c, w_uk, w_uv, gate, out, scale, B, T, H, d_q, d_v, r, dev->err_word, dev->num_sms};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (f32)
+        e = launch_prefill_f32_simt(a, s);
+    else if (prefill_bf16_r512_supports(r, d_q, d_v))
+        e = launch_prefill_bf16_r512(a, s);
+    else
+        e = launch_prefill_bf16_small(a, s);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API size_t mla_latent_decode_workspace_size(int B, int H, int r, int max_len) {
+    if (B <= 0 || H <= 0 || r <= 0 || max_len < 0) return 0;
+    if (!decode_bf16_supports(H, 128, r)) return 0;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return 0;
+    return decode_bf16_workspace_bytes(B, H, r, max_len, dev->num_sms);
+}
+
+MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long ld_cache, const int *lens,
+                              int max_len, const void *w_uv, const void *gate, float scale, void *out, int B,
+                              int H, int d_v, int r, int dtype, void *workspace, size_t workspace_bytes,
+                              void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || H <= 0 || d_v <= 0 || r <= 0 || max_len < 0 || ld_cache < r) return MLA_ERR_SHAPE;
+    if (!mul_fits(static_cast<long long>(B) * max_len, ld_cache, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (!q_abs || !c_cache || !lens || !w_uv || !out) return MLA_ERR_NULL;
+    if (!aligned16(q_abs) || !aligned16(c_cache) || !aligned16(w_uv) || !aligned16(out) ||
+        !aligned16(lens) || (gate && !aligned16(gate)) || (ld_cache % 8) != 0)
+        return MLA_ERR_ALIGN;
+    if (dtype != MLA_DTYPE_BF16 || !decode_bf16_supports(H, d_v, r)) return MLA_ERR_UNSUPPORTED;
+    if (B == 0) return MLA_OK;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const size_t need = decode_bf16_workspace_bytes(B, H, r, max_len, dev->num_sms);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return MLA_ERR_ALIGN;
+    DecodeArgs a{q_abs, c_cache, w_uv, gate, lens, out, ld_cache, max_len, scale, B, H, d_v, r,
+                 workspace, workspace_bytes, dev->err_word, dev->num_sms};
+    const cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_get_device_error(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, dev->err_word, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(dev->err_word, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return MLA_ERR_CUDA;
+    }
+    return word;
+}
+
+}  // extern "C"

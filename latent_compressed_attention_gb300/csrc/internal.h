@@ -1,0 +1,53 @@
+// Internal host-side interface between the C ABI (abi.cu) and the kernel
+// translation units.  Not exported from the shared library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+struct PrefillArgs {
+    const void *q, *c, *w_uk, *w_uv, *gate;
+    void *out;
+    float scale;
+    int B, T, H, d_q, d_v, r;
+    int *dev_err;  // device error word of the current device
+    int num_sms;
+};
+
+struct DecodeArgs {
+    const void *q_abs, *c_cache, *w_uv, *gate;
+    const int *lens;
+    void *out;
+    long long ld_cache;
+    int max_len;
+    float scale;
+    int B, H, d_v, r;
+    void *workspace;
+    size_t workspace_bytes;
+    int *dev_err;
+    int num_sms;
+};
+
+// Each launcher validates nothing the ABI already checked; it returns a
+// cudaError_t from the launch (or cudaErrorInvalidValue for an internal
+// precondition) and never synchronises.
+cudaError_t launch_prefill_f32_simt(const PrefillArgs &a, cudaStream_t s);
+bool prefill_f32_simt_supports(int r, int d_q, int d_v);
+
+cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s);
+bool prefill_bf16_r512_supports(int r, int d_q, int d_v);
+
+cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s);
+bool prefill_bf16_small_supports(int r, int d_q, int d_v);
+
+size_t decode_bf16_workspace_bytes(int B, int H, int r, int max_len, int num_sms);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+bool decode_bf16_supports(int H, int d_v, int r);
+
+// Driver entry point for cuTensorMapEncodeTiled, resolved once through the runtime.
+void *tensor_map_encode_fn();
+
+}  // namespace mla

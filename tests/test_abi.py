@@ -1,0 +1,126 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+function include/mla.h declares, and host-side validation rejects bad
+arguments before any CUDA call (fault injection on the host)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import latent_compressed_attention_gb300 as lca
+from latent_compressed_attention_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_WORKSPACE, ERR_UNSUPPORTED = 0, -1, -2, -3, -4, -5, -6
+BF16, F32 = 0, 1
+FAKE = 0x10000  # a 16-byte aligned address that is never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return lca.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("mla_absorbed_attn_fwd", "mla_latent_decode", "mla_latent_decode_workspace_size",
+              "mla_get_device_error", "mla_status_string", "mla_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared in mla.h but not exported: {missing}"
+
+
+def test_status_strings(lib):
+    for code in range(-9, 1):
+        assert lca.mla_status_string(code) != "unknown status"
+    assert lca.mla_status_string(-99) == "unknown status"
+    assert lca.mla_version() >= 100
+
+
+def prefill(lib, q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=None, out=FAKE, B=1, T=16, H=2, dq=16, dv=16, r=32,
+            dtype=F32):
+    return lib.mla_absorbed_attn_fwd(q, c, wuk, wuv, gate, 1.0, out, B, T, H, dq, dv, r, dtype, None)
+
+
+@pytest.mark.parametrize("field", ["q", "c", "wuk", "wuv", "out"])
+def test_prefill_null_pointer(lib, field):
+    assert prefill(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("field", ["q", "c", "wuk", "wuv", "out", "gate"])
+def test_prefill_misaligned_pointer(lib, field):
+    assert prefill(lib, **{field: FAKE + 4}) == ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(T=-1), dict(H=0), dict(dq=0), dict(dv=-3), dict(r=0),
+                                dict(B=1 << 20, T=1 << 20)])
+def test_prefill_bad_shape(lib, kw):
+    assert prefill(lib, **kw) == ERR_SHAPE
+
+
+def test_prefill_bad_dtype(lib):
+    assert prefill(lib, dtype=7) == ERR_DTYPE
+
+
+@pytest.mark.parametrize("kw", [dict(r=65), dict(dq=100), dict(dtype=BF16, r=48, dq=16, dv=16),
+                                dict(dtype=BF16, r=512, dq=64, dv=128)])
+def test_prefill_unsupported_shape(lib, kw):
+    assert prefill(lib, **kw) == ERR_UNSUPPORTED
+
+
+def test_prefill_empty_is_noop(lib):
+    assert prefill(lib, B=0) == OK
+    assert prefill(lib, T=0) == OK
+
+
+def decode(lib, q=FAKE, cache=FAKE, ld=512, lens=FAKE, max_len=64, wuv=FAKE, gate=None, out=FAKE, B=2, H=8,
+           dv=128, r=512, dtype=BF16, ws=None, ws_bytes=0):
+    return lib.mla_latent_decode(q, cache, ld, lens, max_len, wuv, gate, 1.0, out, B, H, dv, r, dtype, ws,
+                                 ws_bytes, None)
+
+
+@pytest.mark.parametrize("field", ["q", "cache", "lens", "wuv", "out"])
+def test_decode_null_pointer(lib, field):
+    assert decode(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(H=0), dict(dv=0), dict(r=0), dict(max_len=-1), dict(ld=100)])
+def test_decode_bad_shape(lib, kw):
+    assert decode(lib, **kw) == ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(q=FAKE + 2), dict(lens=FAKE + 4), dict(ld=520 + 4)])
+def test_decode_misaligned(lib, kw):
+    assert decode(lib, **kw) == ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=F32), dict(H=129), dict(r=256, ld=256), dict(dv=64)])
+def test_decode_unsupported(lib, kw):
+    assert decode(lib, **kw) == ERR_UNSUPPORTED
+
+
+def test_decode_bad_dtype(lib):
+    assert decode(lib, dtype=3) == ERR_DTYPE
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    assert lib.mla_latent_decode_workspace_size(0, 8, 512, 64) == 0
+    assert lib.mla_latent_decode_workspace_size(2, 0, 512, 64) == 0
+    assert lib.mla_latent_decode_workspace_size(2, 8, 48, 64) == 0
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 4, 2, 16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lca.mla_absorbed_attn_fwd(x, torch.zeros(1, 4, 32), torch.zeros(2, 16, 32), torch.zeros(2, 16, 32))
