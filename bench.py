@@ -1,0 +1,389 @@
+"""Benchmark of the absorbed causal Gated-MLA forward on GB300.
+
+A step is one causal prefill of the K3-size layer (B=1, T=8192, H=96,
+d_q=d_v=128, r=512, bf16, scale 1): the W_UK absorb, the latent scores, the
+causal softmax, the latent weighting, the W_UV up-projection and the gate, all
+in the library's fused kernel.  The cached-latent decode (B=64, cache lengths
+uniform in [1024, 32768], H=96, r=512) is timed in the same run and reported
+under "decode".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One JSON line on stdout (rank 0).  ``value`` is TFLOP/s on the algorithmic
+causal FLOP count B*H*[2 r T(T+1) + 2 T r (d_q+d_v)], device time of the
+kernel launches, L2 flushed between steps; ``e2e`` is the same metric through
+the public API with pinned host buffers, copies included.  Under torchrun each
+rank runs its own replica (the path needs no exchange: weak scaling).
+``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from latent_compressed_attention_gb300 import workloads as W  # noqa: E402
+
+PREFILL = W.K3_PREFILL_BF16
+DECODE = W.K3_DECODE_BF16
+KERNEL_SRC = os.path.join(ROOT, "latent_compressed_attention_gb300", "csrc", "prefill_bf16_r512.cu")
+DECODE_SRC = os.path.join(ROOT, "latent_compressed_attention_gb300", "csrc", "decode_bf16.cu")
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def src_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, src: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)[kernel]
+        if d.get("src_sha") == src_hash(src):
+            return float(d["bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 6:
+                self.rows.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- our arm
+def prefill_inputs(torch, dev):
+    d = W.draw_prefill_direct(PREFILL, seed=0)
+    to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)  # noqa: E731
+    host = {k: to(v).pin_memory() for k, v in d.items() if v is not None}
+    devt = {k: v.to(dev) for k, v in host.items()}
+    return host, devt
+
+
+def decode_inputs(torch, dev):
+    d = W.draw_decode(DECODE, seed=0)
+    lens = d["lens"]
+    cache = torch.empty((DECODE.B, DECODE.max_len, DECODE.r), dtype=torch.bfloat16, device=dev)
+    for b in range(DECODE.B):
+        rows = W.decode_cache_rows(DECODE, b, int(lens[b]), seed=0)
+        cache[b, : lens[b]].copy_(torch.from_numpy(rows.astype(np.float32)).to(torch.bfloat16))
+        cache[b, lens[b]:].zero_()
+    to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
+    return dict(q_abs=to(d["q_abs"]), w_uv=to(d["w_uv"]), cache=cache,
+                lens=torch.from_numpy(lens).to(dev), lens_np=lens)
+
+
+def timed_steps(torch, fn, steps, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step (outside the events)."""
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return times
+
+
+def run_ours(args):
+    import torch
+
+    import latent_compressed_attention_gb300 as lca
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    if world == 1:
+        lca.build()
+    lca.library()
+    pk = peaks()
+
+    host, d = prefill_inputs(torch, dev)
+    out = torch.empty((PREFILL.B, PREFILL.T, PREFILL.H * PREFILL.d_v), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    step = lambda: lca.mla_absorbed_attn_fwd(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"],  # noqa: E731
+                                             PREFILL.scale, out=out)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lca.mla_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        times = timed_steps(torch, step, args.steps, flush, stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(sum(times), world)
+    flops = PREFILL.prefill_flops()
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(times)
+    achieved = flops / (kernel_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, host result out
+    out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    scratch = {}
+
+    def e2e_step():
+        for k, v in host.items():
+            scratch[k] = v.to(dev, non_blocking=True)
+        lca.mla_absorbed_attn_fwd(scratch["q"], scratch["c"], scratch["w_uk"], scratch["w_uv"], scratch["gate"],
+                                  PREFILL.scale, out=out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_times = timed_steps(torch, e2e_step, max(3, args.steps // 2), flush, stream)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    decode = run_decode(torch, lca, dev, stream, flush, args, pk) if not args.no_decode else None
+    if lca.mla_get_device_error() != 0:
+        raise RuntimeError("device error word set after the timed region")
+
+    if rank == 0:
+        line = {
+            "metric": "MLA fwd TFLOP/s (causal) and decode GB/s, % of GB300 roofline, vs CPU oracle",
+            "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": PREFILL.name, "B": PREFILL.B, "T": PREFILL.T, "H": PREFILL.H,
+                       "d_q": PREFILL.d_q, "d_v": PREFILL.d_v, "r": PREFILL.r, "scale": PREFILL.scale,
+                       "causal": True, "gate": True, "flops_per_step": flops,
+                       "l2": "flushed between steps (512 MB write outside the timed events)",
+                       "parallelism": f"replicas x{world}"},
+            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "roofline": {"kernel": "prefill_r512_kernel", "bound": "tensor", "achieved": round(achieved, 2),
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                         "peak_source": pk["source"] + " (burst bf16)",
+                         "traffic": committed_traffic("prefill_r512_kernel", KERNEL_SRC)},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+        }
+        if decode is not None:
+            line["decode"] = decode
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_decode(torch, lca, dev, stream, flush, args, pk):
+    try:
+        ws_bytes = lca.mla_latent_decode_workspace_size(DECODE.B, DECODE.H, DECODE.r, DECODE.max_len)
+        if ws_bytes == 0:
+            return {"unavailable": "decode kernel not built for this shape"}
+    except Exception as e:  # noqa: BLE001
+        return {"unavailable": str(e)}
+    d = decode_inputs(torch, dev)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((DECODE.B, DECODE.H * DECODE.d_v), dtype=torch.bfloat16, device=dev)
+    step = lambda: lca.mla_latent_decode(d["q_abs"], d["cache"], d["lens"], d["w_uv"], None,  # noqa: E731
+                                         DECODE.scale, out=out, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
+    cache_bytes = int(d["lens_np"].astype(np.int64).sum()) * DECODE.r * 2
+    gbs = cache_bytes / (ms * 1e-3) / 1e9
+    return {"workload": DECODE.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "cache_bytes_per_step": cache_bytes, "sum_lens": int(d["lens_np"].sum()),
+            "roofline": {"kernel": "decode (split + merge)", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "peak_source": pk["source"],
+                         "traffic": committed_traffic("decode", DECODE_SRC)},
+            "gpu_launches": 2 * args.steps}
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+def oracle_inputs():
+    return W.draw_prefill_direct(PREFILL, seed=0)
+
+
+def oracle_sample(d, seconds: float, seed: int = 0):
+    """Time the fp64 oracle on sampled query rows (all heads) of the K3 prefill.
+
+    Returns (tflops, rows, elapsed, threads).  Rows are drawn uniformly over
+    the sequence; work per row is counted with the same algorithmic formula.
+    """
+    import oracle
+
+    w = PREFILL
+    rng = np.random.default_rng(seed)
+    per_row = lambda t: w.H * (4.0 * w.r * (t + 1) + 2.0 * w.r * (w.d_q + w.d_v))  # noqa: E731
+    # calibrate on two rows, then size the sample to about `seconds`
+    rows = rng.integers(0, w.T, 2)
+    t0 = time.perf_counter()
+    oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], w.scale, rows=rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rate = sum(per_row(int(t)) for t in rows) / dt
+    n = int(max(2, min(4096, seconds * rate / per_row(w.T // 2))))
+    rows = rng.integers(0, w.T, n)
+    t0 = time.perf_counter()
+    oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], w.scale, rows=rows)
+    elapsed = time.perf_counter() - t0
+    flops = sum(per_row(int(t)) for t in rows)
+    return flops / elapsed / 1e12, n, elapsed, oracle.num_threads()
+
+
+def cpu_baseline(seconds: float):
+    tflops, n, elapsed, threads = oracle_sample(oracle_inputs(), seconds)
+    return {"value": round(tflops, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} query rows x {PREFILL.H} heads of {PREFILL.name}, uniform over t, {elapsed:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    d = oracle_inputs()
+    per_step = []
+    rows_total, threads = 0, 1
+    seconds = min(args.ref_seconds, 150.0 / (args.warmup + args.steps))
+    for i in range(args.warmup + args.steps):
+        tflops, n, elapsed, threads = oracle_sample(d, seconds, seed=100 + i)
+        if i >= args.warmup:
+            per_step.append((tflops, n, elapsed))
+            rows_total += n
+    value = statistics.mean(t for t, _, _ in per_step)
+    ms = statistics.mean(e for _, _, e in per_step) * 1e3
+    line = {
+        "impl": "reference", "metric": "MLA fwd TFLOP/s (causal) and decode GB/s, % of GB300 roofline, vs CPU oracle",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": PREFILL.name, "B": PREFILL.B, "T": PREFILL.T, "H": PREFILL.H, "d_q": PREFILL.d_q,
+                   "d_v": PREFILL.d_v, "r": PREFILL.r, "scale": PREFILL.scale, "causal": True, "gate": True},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_total} query rows x {PREFILL.H} heads over {args.steps} steps "
+                                   f"(about {seconds:.1f} s each)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,131 @@
+"""GPU parity of the bf16 prefill paths against the fp64 oracle, through the C ABI.
+
+Bar (the bf16 tolerance): max|gpu - oracle| <= 2e-2 * max|oracle|, on the same
+bf16-rounded inputs.  Small cases span several 128-token tiles and a ragged
+tail; the full mid-size and K3-size workloads run in the benchmark's launch
+configuration and are checked on sampled rows (all heads) that the oracle
+computes one by one.
+"""
+import numpy as np
+import pytest
+
+from latent_compressed_attention_gb300 import workloads as W
+from tests.conftest import gpu_available
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not gpu_available():
+        pytest.skip("no CUDA device")
+    import torch
+
+    import latent_compressed_attention_gb300 as lca
+    import oracle
+    from latent_compressed_attention_gb300 import _build
+    _build.build()
+    oracle.build()
+    return torch, lca, oracle
+
+
+def dev(torch, a):
+    return None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)
+
+
+def run_prefill(env, d, scale):
+    torch, lca, _ = env
+    out = lca.mla_absorbed_attn_fwd(dev(torch, d["q"]), dev(torch, d["c"]), dev(torch, d["w_uk"]),
+                                    dev(torch, d["w_uv"]), dev(torch, d["gate"]), scale)
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    return out.float().double().cpu().numpy()
+
+
+def rel_err(got, ref):
+    return float(np.max(np.abs(got - ref)) / max(float(np.max(np.abs(ref))), 1e-30))
+
+
+def r512(B, T, H, seed=0, wuk_std=W.WEIGHT_STD, gate=True, q_std=None):
+    w = W.MID_PREFILL_BF16
+    d = W.draw_prefill_direct(w, seed=seed, T=T, B=B, H=H, wuk_std=wuk_std)
+    if q_std is not None:
+        d["q"] = W.round_bf16(d["q"] / w.q_std * q_std)
+    if not gate:
+        d["gate"] = None
+    return d
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 1, 1), (1, 5, 3), (1, 128, 1), (2, 300, 2), (1, 513, 2), (1, 1000, 1)])
+@pytest.mark.parametrize("scale", [1.0 / np.sqrt(128.0), 1.0])
+def test_r512_shapes(env, B, T, H, scale):
+    _, _, oracle = env
+    d = r512(B, T, H, seed=B * 7 + T)
+    got = run_prefill(env, d, scale).reshape(B, T, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_r512_no_gate(env):
+    _, _, oracle = env
+    d = r512(2, 260, 2, seed=3, gate=False)
+    got = run_prefill(env, d, 1.0).reshape(2, 260, -1)
+    assert rel_err(got, oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], None, 1.0)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("wuk_std", [0.02, 0.04])
+def test_r512_peaky_attention(env, wuk_std):
+    """Larger q and W_UK spread the scores (std about 5 and 10 in natural-log
+    units): attention is peaky, exercising the mask, the lazy rescale of the
+    latent accumulator and the online maximum.  The bf16 rounding of q_abs
+    bounds the accuracy: its score error grows with the spread (about
+    2^-9/sqrt(3) * |q_abs| * rms(c)), so the spread stays where the bf16 bar holds."""
+    _, _, oracle = env
+    d = r512(1, 700, 2, seed=11, wuk_std=wuk_std, q_std=1.0)
+    got = run_prefill(env, d, 1.0).reshape(1, 700, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_r512_causality_bitwise(env):
+    torch, lca, _ = env
+    d = r512(1, 400, 2, seed=5)
+    base = run_prefill(env, d, 1.0).reshape(400, -1)
+    t0 = 200
+    d2 = dict(d)
+    d2["q"] = d["q"].copy()
+    d2["c"] = d["c"].copy()
+    d2["q"][:, t0 + 1:] = W.round_bf16(-d["q"][:, t0 + 1:])
+    d2["c"][:, t0 + 1:] = W.round_bf16(d["c"][:, t0 + 1:] * 2 + 0.5)
+    out = run_prefill(env, d2, 1.0).reshape(400, -1)
+    assert np.array_equal(out[: t0 + 1], base[: t0 + 1])
+
+
+def test_r512_repeatable(env):
+    d = r512(1, 300, 2, seed=9)
+    a = run_prefill(env, d, 1.0)
+    b = run_prefill(env, d, 1.0)
+    assert np.array_equal(a, b)
+
+
+def sample_rows(B, T, n, seed):
+    rng = np.random.default_rng(seed)
+    t = np.unique(np.concatenate([[0, 1, 127, 128, 129, T // 2, T - 129, T - 128, T - 2, T - 1],
+                                  rng.integers(0, T, n)]))
+    b = rng.integers(0, B, t.size)
+    return b * T + t
+
+
+@pytest.mark.parametrize("name", ["mid_prefill_bf16", "k3_prefill_bf16"])
+def test_full_size_sampled_rows(env, name):
+    """The full workload, launched as the benchmark launches it; oracle on sampled rows."""
+    _, _, oracle = env
+    w = W.WORKLOADS[name]
+    d = W.draw_prefill_direct(w, seed=0)
+    got = run_prefill(env, d, w.scale).reshape(w.B * w.T, -1)
+    rows = sample_rows(w.B, w.T, 14, seed=1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], w.scale, rows=rows)
+    assert rel_err(got[rows], ref) <= TOL_BF16
+    assert np.all(np.isfinite(got))
