@@ -230,12 +230,14 @@ def run_ours(args):
                                   PREFILL.scale, out=out)
         out_host.copy_(out, non_blocking=True)
 
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_times = timed_steps(torch, e2e_step, max(3, args.steps // 2), flush, stream)
-    e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
-    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+    e2e_value = e2e_ms = None
+    if not args.no_e2e:
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_times = timed_steps(torch, e2e_step, max(3, args.steps // 2), flush, stream)
+        e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
+        e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
     decode = run_decode(torch, lca, dev, stream, flush, args, pk) if not args.no_decode else None
     if lca.mla_get_device_error() != 0:
@@ -252,8 +254,9 @@ def run_ours(args):
                        "causal": True, "gate": True, "flops_per_step": flops,
                        "l2": "flushed between steps (512 MB write outside the timed events)",
                        "parallelism": f"replicas x{world}"},
-            "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "e2e": None if e2e_value is None else {
+                "value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "roofline": {"kernel": "prefill_r512_kernel", "bound": "tensor", "achieved": round(achieved, 2),
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                          "peak_source": pk["source"] + " (burst bf16)",
@@ -376,9 +379,14 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
+                    help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    global PREFILL
+    PREFILL = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args)
     else:
