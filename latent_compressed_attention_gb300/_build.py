@@ -24,6 +24,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libmla_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE]
+# Extra nvcc flags from the environment, e.g. MLA_NVCC_FLAGS=-DMLA_TIMEOUT_PRINT for the diagnostic build.
+NVCC_FLAGS += os.environ.get("MLA_NVCC_FLAGS", "").split()
 
 
 def _nvcc() -> str:
