@@ -131,6 +131,35 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * mla_latent_decode_noalloc - mla_latent_decode for callers that cannot
+ * allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc: a host framework that owns all device memory
+ * and hands the library only its inputs and outputs, or a service that must
+ * not allocate (or pay cudaMalloc's synchronisation) once it is running.  It
+ * computes exactly what mla_latent_decode computes, with the same arguments
+ * except that there is no workspace: the partial results live in a scratch
+ * array that the library reserves in device memory when it is loaded, 48 MiB
+ * on every device that loads the library, held until the process exits.
+ *
+ * - Sizes whose scratch need (mla_latent_decode_workspace_size) exceeds
+ *   48 MiB return MLA_ERR_WORKSPACE and launch nothing.  The K3 decode
+ *   workload (B = 64, H = 96, r = 512 on a 152-SM GB300) needs 42.6 MB.
+ * - The call allocates and frees nothing, on the host or the device.
+ * - The first call on a device looks up the scratch array's device address
+ *   on that device (cudaGetSymbolAddress); make that first call before any
+ *   stream capture.
+ * - Every call uses the same scratch array: calls whose kernels can overlap
+ *   on the GPU (different streams, no ordering between them) race on it and
+ *   give wrong results.  Calls on one stream, or otherwise ordered, are safe.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_latent_decode_noalloc(const void *q_abs, const void *c_cache, long long ld_cache, const int *lens,
+                                      int max_len, const void *w_uv, const void *gate, float scale, void *out,
+                                      int B, int H, int d_v, int r, int dtype, void *stream);
+
+/*
  * mla_get_device_error - synchronise `stream`, then read and clear the current
  * device's error word.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT,
  * MLA_ERR_DEVICE_BOUNDS, or MLA_ERR_CUDA if the synchronisation itself failed.

@@ -21,7 +21,7 @@ import threading
 from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
-           "mla_latent_decode_workspace_size", "mla_get_device_error", "mla_status_string", "mla_version",
+           "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error", "mla_status_string", "mla_version",
            "DTYPE_BF16", "DTYPE_F32"]
 
 DTYPE_BF16 = 0
@@ -57,6 +57,8 @@ def library():
             lib.mla_latent_decode_workspace_size.restype = sz
             lib.mla_latent_decode.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp, sz, vp]
             lib.mla_latent_decode.restype = i
+            lib.mla_latent_decode_noalloc.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp]
+            lib.mla_latent_decode_noalloc.restype = i
             lib.mla_get_device_error.argtypes = [vp]
             lib.mla_get_device_error.restype = i
             lib.mla_status_string.argtypes = [i]
@@ -183,6 +185,42 @@ def mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0,
                                _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_latent_decode")
+    return out
+
+
+def mla_latent_decode_noalloc(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0, out=None, stream=None):
+    """mla_latent_decode without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps the partial results in its own 48 MiB device scratch
+    array (reserved when the library loads); sizes that need more raise
+    MLAError(MLA_ERR_WORKSPACE).  Calls that overlap on the GPU share that
+    array and race; ordered calls (e.g. on one stream) are safe.  The first
+    call on a device resolves the array's address there.  ``out`` is
+    allocated with torch only when the caller does not pass it.
+    """
+    torch = _torch()
+    B, H, r = q_abs.shape
+    max_len = c_cache.shape[1]
+    d_v = w_uv.shape[1]
+    dev, dt = q_abs.device, q_abs.dtype
+    _check(q_abs, "q_abs", dt, dev)
+    if c_cache.dtype != dt or c_cache.device != dev or c_cache.dim() != 3 or c_cache.shape[0] != B \
+            or c_cache.shape[2] != r or c_cache.stride(2) != 1 or c_cache.stride(0) != max_len * c_cache.stride(1):
+        raise ValueError("c_cache must be [B,max_len,r] with unit inner stride and batch stride max_len*row_stride")
+    _check(lens, "lens", torch.int32, dev, (B,))
+    _check(w_uv, "w_uv", dt, dev, (H, d_v, r))
+    if gate is not None:
+        _check(gate, "gate", dt, dev, (B, H * d_v))
+    if out is None:
+        out = torch.empty((B, H * d_v), dtype=dt, device=dev)
+    _check(out, "out", dt, dev, (B, H * d_v))
+    rc = library().mla_latent_decode_noalloc(q_abs.data_ptr(), c_cache.data_ptr(), c_cache.stride(1),
+                                             lens.data_ptr(), max_len, w_uv.data_ptr(),
+                                             None if gate is None else gate.data_ptr(), float(scale),
+                                             out.data_ptr(), B, H, d_v, r, _dtype_code(q_abs),
+                                             _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_latent_decode_noalloc")
     return out
 
 

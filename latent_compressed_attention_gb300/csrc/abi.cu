@@ -158,6 +158,30 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+MLA_API int mla_latent_decode_noalloc(const void *q_abs, const void *c_cache, long long ld_cache, const int *lens,
+                                      int max_len, const void *w_uv, const void *gate, float scale, void *out,
+                                      int B, int H, int d_v, int r, int dtype, void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || H <= 0 || d_v <= 0 || r <= 0 || max_len < 0 || ld_cache < r) return MLA_ERR_SHAPE;
+    if (!mul_fits(static_cast<long long>(B) * max_len, ld_cache, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (!q_abs || !c_cache || !lens || !w_uv || !out) return MLA_ERR_NULL;
+    if (!aligned16(q_abs) || !aligned16(c_cache) || !aligned16(w_uv) || !aligned16(out) ||
+        !aligned16(lens) || (gate && !aligned16(gate)) || (ld_cache % 8) != 0)
+        return MLA_ERR_ALIGN;
+    if (dtype != MLA_DTYPE_BF16 || !decode_bf16_supports(H, d_v, r)) return MLA_ERR_UNSUPPORTED;
+    if (B == 0) return MLA_OK;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const size_t need = decode_bf16_workspace_bytes(B, H, r, max_len, dev->num_sms);
+    if (need > decode_noalloc_scratch_capacity()) return MLA_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    if (decode_noalloc_scratch(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
+    DecodeArgs a{q_abs, c_cache, w_uv, gate, lens, out, ld_cache, max_len, scale, B, H, d_v, r,
+                 scratch, decode_noalloc_scratch_capacity(), dev->err_word, dev->num_sms};
+    const cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API int mla_get_device_error(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
     DeviceInfo *dev = nullptr;

@@ -24,6 +24,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -37,6 +39,9 @@ constexpr int kHMax = 96;
 constexpr int kThreads = 256;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLog2e = 1.4426950408889634f;
+// Largest scratch the no-alloc decode entry point can use (48 MiB: the K3 decode
+// workload, B = 64 and H = 96 on 152 SMs, needs 42.6 MB).
+constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 
 constexpr uint32_t kSlab = 16384;            // c tile [128 rows x 64 latent columns], 128B swizzle
 constexpr uint32_t kQSlab = kHMax * 128;     // q_abs tile [96 heads x 64 latent columns]
@@ -606,6 +611,43 @@ CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t 
 size_t slot_count(int B, int G) { return static_cast<size_t>(G) + static_cast<size_t>(B); }
 
 }  // namespace
+
+// ----------------------------------------------------------------------------- no-alloc scratch
+// Scratch for mla_latent_decode_noalloc: callers that cannot call cudaMalloc
+// (all device memory is owned by a host framework that hands the library only
+// its inputs and outputs, or no allocation may happen after start-up) get the
+// decode's partial results kept here instead of in a caller workspace.  Every
+// device that loads the library holds this array until the process exits.
+// Calls share it: two calls whose kernels overlap on the GPU race on it.
+// Nothing in it needs to start at zero: the merge reads only the slots the
+// split kernel of the same call wrote.
+namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+constexpr int kMaxDevices = 64;
+void *g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+}  // namespace
+
+size_t decode_noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch array on the current device.  Resolved once
+// per device (the first call on a device does it), with that device current;
+// in host code the array's name is only a stand-in, not a device address.
+cudaError_t decode_noalloc_scratch(void **ptr) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
 
 bool decode_bf16_supports(int H, int d_v, int r) { return r == kR && d_v == kDV && H >= 1 && H <= kHMax; }
 

@@ -47,6 +47,11 @@ size_t decode_bf16_workspace_bytes(int B, int H, int r, int max_len, int num_sms
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 bool decode_bf16_supports(int H, int d_v, int r);
 
+// Scratch of the no-alloc decode entry point: capacity in bytes, and its
+// device address on the current device (set up once per device).
+size_t decode_noalloc_scratch_capacity();
+cudaError_t decode_noalloc_scratch(void **ptr);
+
 // Driver entry point for cuTensorMapEncodeTiled, resolved once through the runtime.
 void *tensor_map_encode_fn();
 
