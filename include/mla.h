@@ -79,8 +79,9 @@ typedef enum {
  *   scale               softmax scale applied to the score (1.0 = the page's listing)
  *   out   [B,T,H*d_v]   result, flat index h*d_v + v; must not alias an input
  * Masking: token t attends to tokens 0..t of its own sequence.
- * Supported: F32 with r, d_q, d_v <= 64; BF16 with (r, d_q, d_v) = (512, 128, 128)
- * or (32, 16, 16).  B*T == 0 is a no-op returning MLA_OK.
+ * Supported: F32 with r, d_q, d_v <= 64; BF16 with (r, d_q, d_v) = (512, 128, 128),
+ * or r in {32, 64} with d_q, d_v in {16, 32, 48, 64}.  B*T == 0 is a no-op
+ * returning MLA_OK.
  * Alignment: every pointer 16-byte aligned.
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
  */
@@ -120,7 +121,7 @@ MLA_API size_t mla_latent_decode_workspace_size(int B, int H, int r, int max_len
  *   out       [B,H*d_v]
  *   workspace device buffer of >= mla_latent_decode_workspace_size(...) bytes,
  *             16-byte aligned, not used by any other call in flight
- * Supported: BF16 with r = 512, d_v = 128, 1 <= H <= 128.
+ * Supported: BF16 with r = 512, d_v = 128, 1 <= H <= 96.
  * A lens[b] outside [0, max_len] found on the device is clamped to that
  * range and reported as MLA_ERR_DEVICE_BOUNDS by mla_get_device_error().
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.

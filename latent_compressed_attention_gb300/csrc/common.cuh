@@ -358,4 +358,20 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
     return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Store one row of 32 fp32 values (times `mul`) as bf16 into a 128B-swizzled
+// K-major tile: columns [32*cc, 32*cc+32) of row `row`; each 64-column slab
+// of the tile is `slab_bytes` long.
+__device__ __forceinline__ void store_row32_bf16(uint32_t tile, uint32_t slab_bytes, uint32_t row, int cc,
+                                                 const float (&v)[32], float mul) {
+    const uint32_t slab = tile + static_cast<uint32_t>(cc >> 1) * slab_bytes;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t w0 = pack_bf16x2(v[8 * k + 0] * mul, v[8 * k + 1] * mul);
+        const uint32_t w1 = pack_bf16x2(v[8 * k + 2] * mul, v[8 * k + 3] * mul);
+        const uint32_t w2 = pack_bf16x2(v[8 * k + 4] * mul, v[8 * k + 5] * mul);
+        const uint32_t w3 = pack_bf16x2(v[8 * k + 6] * mul, v[8 * k + 7] * mul);
+        st_shared_v4(slab + sw128_offset(row, static_cast<uint32_t>((cc & 1) * 4 + k)), w0, w1, w2, w3);
+    }
+}
+
 }  // namespace mla

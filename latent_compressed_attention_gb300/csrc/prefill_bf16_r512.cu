@@ -107,21 +107,6 @@ __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
     return v;
 }
 
-// Store one row of 32 fp32 values (times `mul`) as bf16 into a 128B-swizzled
-// K-major tile: columns [32*cc, 32*cc+32) of row `row`, 64 columns per slab.
-__device__ __forceinline__ void store_row32_bf16(uint32_t tile, uint32_t row, int cc, const float (&v)[32],
-                                                 float mul) {
-    const uint32_t slab = tile + static_cast<uint32_t>(cc >> 1) * kSlab;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t w0 = pack_bf16x2(v[8 * k + 0] * mul, v[8 * k + 1] * mul);
-        const uint32_t w1 = pack_bf16x2(v[8 * k + 2] * mul, v[8 * k + 3] * mul);
-        const uint32_t w2 = pack_bf16x2(v[8 * k + 4] * mul, v[8 * k + 5] * mul);
-        const uint32_t w3 = pack_bf16x2(v[8 * k + 6] * mul, v[8 * k + 7] * mul);
-        st_shared_v4(slab + sw128_offset(row, static_cast<uint32_t>((cc & 1) * 4 + k)), w0, w1, w2, w3);
-    }
-}
-
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_r512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
                         const __grid_constant__ CUtensorMap tm_wuk, const __grid_constant__ CUtensorMap tm_wuv,
@@ -259,7 +244,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     float v[32];
                     tmem_ld32(trow + cc * 32, v);
                     tmem_wait_ld();
-                    store_row32_bf16(base + S_QABS, row, cc, v, p.qk_scale_log2);
+                    store_row32_bf16(base + S_QABS, kSlab, row, cc, v, p.qk_scale_log2);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -319,7 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (named_bar_or(1, 128, fail)) { ok = false; break; }
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) store_row32_bf16(base + S_QP, row, c4, s[c4], 1.f);
+                for (int c4 = 0; c4 < 4; ++c4) store_row32_bf16(base + S_QP, kSlab, row, c4, s[c4], 1.f);
                 st_shared_v2f(base + S_ROWINFO + row * 8, factor, l_run);
                 fence_proxy_async_smem();
                 const bool any = named_bar_or(1, 128, factor != 1.f);
@@ -477,7 +462,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     float v[32];
                     tmem_ld32(trow + kh * 256 + cc * 32, v);
                     tmem_wait_ld();
-                    store_row32_bf16(base + O_P, row, cc, v, inv_l);
+                    store_row32_bf16(base + O_P, kSlab, row, cc, v, inv_l);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();

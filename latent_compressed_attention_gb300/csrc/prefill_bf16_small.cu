@@ -1,6 +1,382 @@
-// bf16 absorbed prefill for small latent ranks (tcgen05).  Under construction.
+// bf16 causal absorbed Gated-MLA prefill for small latent ranks (r = 32 or
+// 64, d_q and d_v in {16, 32, 48, 64}) on the sm_103a tensor cores, one fused
+// kernel; the toy sizes of the course notes (r = 32, d = 16) are the target.
+//
+// Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）", steps 2-4, as in
+// the r = 512 kernel: W_UK absorb prologue, scores against the latent c,
+// causal online softmax, latent weighting by the same c tile, W_UV^T and gate
+// epilogue.  At these ranks the tensor work per score is tiny (4r FLOPs) and
+// the exponentials bound the kernel, so the design aims at many softmax warps
+// per SM: one CTA per 128-token tile, 256 TMEM columns and about 100 KB of
+// shared memory, two CTAs per SM.
+//
+// Narrow rows (r = 32: 64 bytes; d = 16: 32 bytes) are widened to the 128-byte
+// swizzled layout by TMA's zero fill past the tensor's inner extent: every
+// operand is a [rows x 64] bf16 tile, the padding columns are zero, and they
+// add nothing to any product.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
 #include "internal.h"
+
 namespace mla {
-bool prefill_bf16_small_supports(int, int, int) { return false; }
-cudaError_t launch_prefill_bf16_small(const PrefillArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kBM = 128;        // tokens per tile
+constexpr int kBN = 128;        // keys per block
+constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;
+
+constexpr uint32_t kTile = 16384;   // [128 rows x 64 bf16], 128B swizzle
+constexpr uint32_t QT = 0;          // q tile, then q_abs, then the epilogue's o_lat
+constexpr uint32_t WK = QT + kTile;             // W_UK[h] [d_q rows x 64]
+constexpr uint32_t WV = WK + 8192;              // W_UV[h] [d_v rows x 64]
+constexpr uint32_t RING = WV + 8192;            // c tiles
+constexpr int kStages = 2;
+constexpr uint32_t PT = RING + kStages * kTile; // P [128 rows x 128 keys] = 2 tiles
+constexpr uint32_t BARS = PT + 2 * kTile;
+constexpr uint32_t kSmemBytes = BARS + 256 + 1024;
+static_assert(RING % 1024 == 0 && PT % 1024 == 0, "alignment");
+
+constexpr uint32_t S_COL = 0, O_COL = 128;
+
+struct Bars {
+    uint64_t pro_full, absorb_done, qabs_ready;
+    uint64_t c_full[kStages], c_empty[kStages];
+    uint64_t s_full, s_free, p_full, pv_done, olat_ready, ep_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+struct Params {
+    const __nv_bfloat16 *gate;
+    __nv_bfloat16 *out;
+    int *err;
+    int T, H, d_q, d_v, n_qtiles, bh_count;
+    float qk_scale_log2;
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+    prefill_small_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
+                         const __grid_constant__ CUtensorMap tm_wuk, const __grid_constant__ CUtensorMap tm_wuv,
+                         const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    Bars *bars = reinterpret_cast<Bars *>(smem_raw + (base - raw) + BARS);
+    volatile int *abort_flag = &bars->abort;
+    auto B_ = [](uint64_t &b) { return smem_u32(&b); };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qt = p.n_qtiles - 1 - static_cast<int>(blockIdx.x) / p.bh_count;   // heaviest tiles first
+    const int bh = static_cast<int>(blockIdx.x) % p.bh_count;
+    const int b = bh / p.H, h = bh % p.H;
+    const int t0 = qt * kBM;
+    const int nkv = qt + 1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(B_(bars->pro_full), 1);
+        mbar_init(B_(bars->absorb_done), 1);
+        mbar_init(B_(bars->qabs_ready), 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(B_(bars->c_full[i]), 1);
+            mbar_init(B_(bars->c_empty[i]), 1);
+        }
+        mbar_init(B_(bars->s_full), 1);
+        mbar_init(B_(bars->s_free), 128);
+        mbar_init(B_(bars->p_full), 1);
+        mbar_init(B_(bars->pv_done), 1);
+        mbar_init(B_(bars->olat_ready), 1);
+        mbar_init(B_(bars->ep_done), 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&bars->tmem_base), 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_c);
+        const uint32_t pro = B_(bars->pro_full);
+        mbar_arrive_expect_tx(pro, kTile + (p.d_q + p.d_v) * 128u);
+        tma_load_4d(base + QT, &tm_q, pro, 0, h, t0, b);
+        tma_load_2d(base + WK, &tm_wuk, pro, 0, h * p.d_q);
+        tma_load_2d(base + WV, &tm_wuv, pro, 0, h * p.d_v);
+        bool ok = true;
+        int j = 0;
+        for (; ok && j < nkv; ++j) {
+            const int st = j % kStages;
+            if (j >= kStages &&
+                !(ok = mbar_wait(B_(bars->c_empty[st]), ((j / kStages) - 1) & 1, p.err, abort_flag)))
+                break;
+            mbar_arrive_expect_tx(B_(bars->c_full[st]), kTile);
+            tma_load_3d(base + RING + st * kTile, &tm_c, B_(bars->c_full[st]), 0, j * kBN, b);
+        }
+        if (!ok) *abort_flag = 1;
+        mbar_wait(pro, 0, p.err);
+        for (int k = (j > kStages ? j - kStages : 0); k < j; ++k)
+            mbar_wait(B_(bars->c_full[k % kStages]), (k / kStages) & 1, p.err);
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer
+        const uint32_t id_absorb = make_idesc_bf16(128, 64, 0, 1);
+        const uint32_t id_qk = make_idesc_bf16(128, kBN, 0, 0);
+        const uint32_t id_pv = make_idesc_bf16(128, 64, 0, 1);
+        const uint32_t id_ep = make_idesc_bf16(128, p.d_v, 0, 0);
+        bool ok = mbar_wait(B_(bars->pro_full), 0, p.err, abort_flag);
+        if (ok) {
+            tc_fence_after();
+            for (int kk = 0; kk < p.d_q / 16; ++kk)
+                umma_bf16(tmem + O_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
+                          make_smem_desc(base + WK + kk * 2048, 8192, 1024), id_absorb, kk > 0);
+            umma_commit(B_(bars->absorb_done));
+            ok = mbar_wait(B_(bars->qabs_ready), 0, p.err, abort_flag);
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+            const int st = j % kStages;
+            if (!(ok = mbar_wait(B_(bars->c_full[st]), (j / kStages) & 1, p.err, abort_flag))) break;
+            if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free), (j - 1) & 1, p.err, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
+                          make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, kk > 0);
+            umma_commit(B_(bars->s_full));
+            if (!(ok = mbar_wait(B_(bars->p_full), j & 1, p.err, abort_flag))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                umma_bf16(tmem + O_COL, make_smem_desc(base + PT + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024),
+                          make_smem_desc(base + RING + st * kTile + kk * 2048, 8192, 1024), id_pv,
+                          (j > 0 || kk > 0));
+            umma_commit(B_(bars->c_empty[st]));
+            umma_commit(B_(bars->pv_done));
+        }
+        if (ok && (ok = mbar_wait(B_(bars->olat_ready), 0, p.err, abort_flag))) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
+                          make_smem_desc(base + WV + kk * 32, 16, 1024), id_ep, kk > 0);
+            umma_commit(B_(bars->ep_done));
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 2) {
+        // ---- softmax / epilogue: thread `row` owns TMEM lane `row`
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const int t = t0 + row;
+        bool fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
+        bool ok = !named_bar_or(1, 128, fail);
+        if (ok) {   // q_abs (fp32 TMEM) -> q_abs * scale * log2(e), bf16, into the q tile
+            tc_fence_after();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                float v[32];
+                tmem_ld32(trow + O_COL + cc * 32, v);
+                tmem_wait_ld();
+                store_row32_bf16(base + QT, kTile, row, cc, v, p.qk_scale_log2);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+        }
+        named_bar_sync(1, 128);
+        if (row == 0 && ok) mbar_arrive(B_(bars->qabs_ready));
+
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int j = 0; ok && j < nkv; ++j) {
+            fail = !mbar_wait(B_(bars->s_full), j & 1, p.err, abort_flag);
+            if (named_bar_or(1, 128, fail)) { ok = false; break; }
+            tc_fence_after();
+            float s[4][32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_COL + c4 * 32, s[c4]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(B_(bars->s_free));
+            if (j == nkv - 1) {   // diagonal block: keys after the query or past the sequence
+                const int lim = min(t, p.T - 1) - j * kBN;
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[c4][i]);
+            float factor = 1.f;
+            if (mx > m_run + kRescaleLog2) {
+                factor = fast_exp2(m_run - mx);
+                m_run = mx;
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    s[c4][i] = fast_exp2(s[c4][i] - m_run);
+                    sum += s[c4][i];
+                }
+            l_run = l_run * factor + sum;
+            if (j > 0) {   // P and o_lat are free once the previous block's product completed
+                fail = !mbar_wait(B_(bars->pv_done), (j - 1) & 1, p.err, abort_flag);
+                if (named_bar_or(1, 128, fail)) { ok = false; break; }
+                if (named_bar_or(1, 128, factor != 1.f)) {
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, factor != 1.f)) {
+#pragma unroll
+                        for (int cc = 0; cc < 2; ++cc) {
+                            float v[32];
+                            tmem_ld32(trow + O_COL + cc * 32, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] *= factor;
+                            tmem_st32(trow + O_COL + cc * 32, v);
+                        }
+                        tmem_wait_st();
+                    }
+                    tc_fence_before();
+                }
+            }
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) store_row32_bf16(base + PT, kTile, row, c4, s[c4], 1.f);
+            fence_proxy_async_smem();
+            named_bar_sync(1, 128);
+            if (row == 0) mbar_arrive(B_(bars->p_full));
+        }
+        if (ok) {   // o_lat / l -> bf16 into the (now free) q tile for the W_UV product
+            fail = !mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag);
+            ok = !named_bar_or(1, 128, fail);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = 1.f / l_run;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                float v[32];
+                tmem_ld32(trow + O_COL + cc * 32, v);
+                tmem_wait_ld();
+                store_row32_bf16(base + QT, kTile, row, cc, v, inv_l);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_sync(1, 128);
+            if (row == 0) mbar_arrive(B_(bars->olat_ready));
+            fail = !mbar_wait(B_(bars->ep_done), 0, p.err, abort_flag);
+            ok = !named_bar_or(1, 128, fail);
+        }
+        if (ok) {
+            tc_fence_after();
+            const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.H + h) * p.d_v;
+            for (int v16 = 0; v16 < p.d_v / 16; ++v16) {
+                float o[16];
+                tmem_ld16(trow + S_COL + v16 * 16, o);
+                tmem_wait_ld();
+                if (t < p.T) {
+                    if (p.gate) {
+                        const uint4 *g4 = reinterpret_cast<const uint4 *>(p.gate + off + v16 * 16);
+#pragma unroll
+                        for (int q2 = 0; q2 < 2; ++q2) {
+                            const uint4 gv = __ldg(g4 + q2);
+                            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                o[8 * q2 + 2 * k] *=
+                                    __fdividef(1.f, 1.f + fast_exp2(-__uint_as_float(gw[k] << 16) * kLog2e));
+                                o[8 * q2 + 2 * k + 1] *=
+                                    __fdividef(1.f, 1.f + fast_exp2(-__uint_as_float(gw[k] & 0xFFFF0000u) * kLog2e));
+                            }
+                        }
+                    }
+                    uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off + v16 * 16);
+                    o4[0] = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                       pack_bf16x2(o[6], o[7]));
+                    o4[1] = make_uint4(pack_bf16x2(o[8], o[9]), pack_bf16x2(o[10], o[11]),
+                                       pack_bf16x2(o[12], o[13]), pack_bf16x2(o[14], o[15]));
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                    const cuuint32_t *box) {
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+bool dim_ok(int d) { return d == 16 || d == 32 || d == 48 || d == 64; }
+
+}  // namespace
+
+bool prefill_bf16_small_supports(int r, int d_q, int d_v) { return (r == 32 || r == 64) && dim_ok(d_q) && dim_ok(d_v); }
+
+cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s) {
+    if (!prefill_bf16_small_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
+    const cuuint64_t B = a.B, T = a.T, H = a.H, dq = a.d_q, dv = a.d_v, r = a.r;
+    CUtensorMap tm_q, tm_c, tm_wuk, tm_wuv;
+    {
+        const cuuint64_t dims[4] = {dq, H, T, B};
+        const cuuint64_t strides[3] = {dq * 2, H * dq * 2, T * H * dq * 2};
+        const cuuint32_t box[4] = {64, 1, kBM, 1};
+        if (encode_map(&tm_q, a.q, 4, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {r, T, B};
+        const cuuint64_t strides[2] = {r * 2, T * r * 2};
+        const cuuint32_t box[3] = {64, kBN, 1};
+        if (encode_map(&tm_c, a.c, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {r, H * dq};
+        const cuuint64_t strides[1] = {r * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(dq)};
+        if (encode_map(&tm_wuk, a.w_uk, 2, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {r, H * dv};
+        const cuuint64_t strides[1] = {r * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(dv)};
+        if (encode_map(&tm_wuv, a.w_uv, 2, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    Params p;
+    p.gate = static_cast<const __nv_bfloat16 *>(a.gate);
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.err = a.dev_err;
+    p.T = a.T;
+    p.H = a.H;
+    p.d_q = a.d_q;
+    p.d_v = a.d_v;
+    p.n_qtiles = (a.T + kBM - 1) / kBM;
+    p.bh_count = a.B * a.H;
+    p.qk_scale_log2 = a.scale * kLog2e;
+    cudaError_t e = cudaFuncSetAttribute(prefill_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    const long long n = static_cast<long long>(p.n_qtiles) * p.bh_count;
+    if (n > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    prefill_small_kernel<<<static_cast<unsigned>(n), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_wuk, tm_wuv, p);
+    return cudaGetLastError();
+}
+
 }  // namespace mla

@@ -73,7 +73,8 @@ def test_prefill_bad_dtype(lib):
 
 
 @pytest.mark.parametrize("kw", [dict(r=65), dict(dq=100), dict(dtype=BF16, r=48, dq=16, dv=16),
-                                dict(dtype=BF16, r=512, dq=64, dv=128)])
+                                dict(dtype=BF16, r=512, dq=64, dv=128), dict(dtype=BF16, r=32, dq=8, dv=16),
+                                dict(dtype=BF16, r=64, dq=16, dv=80)])
 def test_prefill_unsupported_shape(lib, kw):
     assert prefill(lib, **kw) == ERR_UNSUPPORTED
 
