@@ -12,14 +12,16 @@
 // A work tile is 128 consecutive tokens of one (batch, head).  Its fp32
 // latent accumulator o_lat is 128 x 512 = all 512 TMEM columns of an SM, so
 // the tile runs on a cluster of two CTAs:
-//   rank 0, the score CTA: absorbs W_UK into q (tcgen05, fp32 in TMEM),
-//     stores q_abs * scale * log2(e) as bf16 in smem, computes S = q_abs c^T
-//     per 128-key block into a double-buffered TMEM accumulator, and runs the
-//     online softmax (one thread per row).  P (bf16) and per-row (rescale
-//     factor, running sum) go to the value CTA by a DSMEM bulk copy.
+//   rank 0, the score CTA: absorbs W_UK into q (tcgen05, fp32 in TMEM), packs
+//     q_abs * scale * log2(e) as bf16 into TMEM columns 0-255, where it is the
+//     A operand of S = q_abs c^T; S is double-buffered in columns 256-511.
+//     Two warpgroups run the online softmax (64 columns of each row each; the
+//     row maximum is exchanged through smem).  P (bf16) and per-row (rescale
+//     factor, partial sums) are staged in double-buffered smem and shipped to
+//     the value CTA by asynchronous DSMEM bulk copies.
 //   rank 1, the value CTA: accumulates o_lat += P . c in TMEM (512 columns),
 //     rescales o_lat when a row maximum grew (lazily: only when it grew by
-//     more than 2^8), then divides by the row sum, projects with W_UV^T on
+//     more than 2^16), then divides by the row sum, projects with W_UV^T on
 //     the tensor cores and applies the sigmoid gate.
 // Each CTA loads its own c tiles (no multicast); both read them from L2.
 // Every wait is bounded; a CTA that gives up records an error, stops issuing
@@ -36,35 +38,42 @@ namespace {
 constexpr int kR = 512;      // latent rank
 constexpr int kD = 128;      // d_q = d_v
 constexpr int kBM = 128;     // query tokens per tile
-constexpr int kBN = 128;     // keys per block
-constexpr int kThreads = 256;
+constexpr int kBN = 128;     // keys per value-CTA unit
+constexpr int kBS = 256;     // keys per score block (two units)
+constexpr int kThreads = 384;   // warps 0 TMA, 1 MMA, 2 relay (value CTA), 4-7 and 8-11: two row warpgroups
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleLog2 = 8.0f;  // keep a stale row maximum until the new one exceeds it by this
+// Keep a stale row maximum until the new one exceeds it by this (log2 units):
+// p <= 2^16, far inside the fp32 range of the row sums and the accumulator.
+constexpr float kRescaleLog2 = 16.0f;
 
 constexpr uint32_t kSlab = 16384;  // [128 rows x 64 bf16] with 128-byte swizzle
 // score CTA
-constexpr uint32_t S_QABS = 0;                       // 8 slabs: W_UK during the absorb, then q_abs
-constexpr uint32_t S_QP = 8 * kSlab;                 // 2 slabs: q tile, then the P staging tile
-constexpr uint32_t S_RING = S_QP + 2 * kSlab;        // c ring
+constexpr uint32_t kSStage = 2 * kSlab;              // c ring stage: [256 keys x 64 latent columns]
+constexpr uint32_t S_RING = 0;                       // W_UK fills the ring for the absorb
 constexpr int kSStages = 4;
-constexpr uint32_t S_ROWINFO = S_RING + kSStages * kSlab;
-constexpr uint32_t kRowInfoBytes = kBM * 8 + 16;     // (factor, l) per row + block rescale flag
-constexpr uint32_t kRowInfoStride = 1056;
+constexpr uint32_t kPBytes = 2 * kSlab;              // one unit of P: [128 rows x 128 keys]
+constexpr uint32_t kRowInfoBytes = kBM * 8;          // {rescale factor, running sum} per row
+constexpr uint32_t kPUnit = kPBytes + kRowInfoBytes; // staging per warpgroup (the first also holds the q tile)
+constexpr uint32_t S_PST = S_RING + kSStages * kSStage;
 // value CTA
 constexpr uint32_t O_RING = 0;
 constexpr int kOStages = 2;
 constexpr uint32_t kOStage = 4 * kSlab;              // 256 latent columns x 128 keys
 constexpr uint32_t O_P = kOStages * kOStage;         // 2 P tiles (also the epilogue's o_lat staging)
-constexpr uint32_t kPBytes = 2 * kSlab;
-constexpr uint32_t O_ROWINFO = O_P + 2 * kPBytes;
-constexpr uint32_t BARS = S_ROWINFO + kRowInfoStride;
-constexpr uint32_t kSmemBytes = BARS + 512 + 1024;   // + barriers + alignment slack
-
-static_assert(O_ROWINFO + 2 * kRowInfoStride <= BARS, "value-CTA layout overlaps the barriers");
+constexpr uint32_t O_ROWINFO = O_P + 2 * kPBytes;    // 2 row-info blocks
+constexpr uint32_t BARS = S_PST + 2 * kPUnit;
+constexpr uint32_t PMAX = BARS + 512;                // [2 parities][2 warpgroups][128 rows] partial maxima
+constexpr uint32_t kSmemUsed = PMAX + 2 * 2 * kBM * 4;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
+// TMEM columns of the score CTA
+constexpr uint32_t S_QCOL = 0;     // packed bf16 q_abs: K step ks (16 latent columns) at columns 8 ks .. 8 ks + 7
+constexpr uint32_t S_SCOL = 256;   // S for one 256-key block
+static_assert(O_ROWINFO + 2 * kRowInfoBytes <= BARS, "value-CTA layout overlaps the barriers");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit");
+static_assert(S_PST % 1024 == 0 && (S_PST + kPUnit) % 1024 == 0 && O_P % 1024 == 0, "alignment");
 
 constexpr uint32_t kIdescAbsorb = make_idesc_bf16(128, 256, 0, 1);  // q (K-major) x W_UK (MN-major)
-constexpr uint32_t kIdescQK = make_idesc_bf16(128, 128, 0, 0);      // q_abs (K-major) x c (K-major)
+constexpr uint32_t kIdescQK = make_idesc_bf16(128, 256, 0, 0);      // q_abs (TMEM) x c (K-major), 256 keys
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);      // P (K-major) x c (MN-major)
 constexpr uint32_t kIdescEp = make_idesc_bf16(128, 128, 0, 0);      // o_lat (K-major) x W_UV (K-major)
 
@@ -82,6 +91,23 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
+// Opt-in wait accounting (build with MLA_NVCC_FLAGS=-DMLA_TRACE): cycles each
+// role spends at its waits and in its loop, summed over all CTAs.
+enum TraceSlot {
+    TR_S_MMA_LOOP, TR_S_MMA_SFREE, TR_S_MMA_SCFULL, TR_S_SM_LOOP, TR_S_SM_SFULL, TR_S_SM_XBAR, TR_S_SM_PFREE,
+    TR_S_SM_STORE, TR_O_MMA_LOOP, TR_O_MMA_PFULL, TR_O_MMA_OCFULL, TR_O_MMA_CORR, TR_O_COR_LOOP, TR_S_PROD_EMPTY,
+    TR_O_PROD_EMPTY, TR_TILES, TR_BLOCKS, TR_CORRECTIONS, TR_S_PROLOGUE, TR_O_EPILOGUE, TR_S_TOTAL, TR_O_TOTAL,
+    TR_S_SM_RELEASE, TR_COUNT
+};
+#ifdef MLA_TRACE
+__device__ unsigned long long g_trace[TR_COUNT];
+#define TR(...) __VA_ARGS__
+#define TR_ADD(slot, v) atomicAdd(&g_trace[slot], static_cast<unsigned long long>(v))
+#else
+#define TR(...)
+#define TR_ADD(slot, v) (void)0
+#endif
+
 struct Params {
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
@@ -90,27 +116,69 @@ struct Params {
     float qk_scale_log2;
 };
 
-__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
-    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 __device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
     float2 v;
     asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
+__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// Pairwise (tree) reductions over 64 values: short dependency chains.
+__device__ __forceinline__ float tree_max64(const float (&s)[2][32]) {
+    float m[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i] = fmaxf(s[0][i], s[1][i]);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+__device__ __forceinline__ float tree_max128(const float (&s)[4][32]) {
+    float m[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i] = fmaxf(fmaxf(s[0][i], s[1][i]), fmaxf(s[2][i], s[3][i]));
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+__device__ __forceinline__ float tree_sum128(const float (&s)[4][32]) {
+    float m[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i] = (s[0][i] + s[1][i]) + (s[2][i] + s[3][i]);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] += m[i + w];
+    return m[0];
+}
+__device__ __forceinline__ float tree_sum64(const float (&s)[2][32]) {
+    float m[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i] = s[0][i] + s[1][i];
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] += m[i + w];
+    return m[0];
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_r512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-                        const __grid_constant__ CUtensorMap tm_wuk, const __grid_constant__ CUtensorMap tm_wuv,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tm_c256, const __grid_constant__ CUtensorMap tm_wuk,
+                        const __grid_constant__ CUtensorMap tm_wuv, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -125,7 +193,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int bh = cluster_id % p.bh_count;
     const int b = bh / p.H, h = bh % p.H;
     const int t0 = qt * kBM;
-    const int nkv = qt + 1;   // 128-key blocks covering keys [0, min(T, t0 + 128))
+    const int nblk = (qt + 2) / 2;   // 256-key score blocks covering keys [0, min(T, t0 + 128))
+    const int nkv = 2 * nblk;        // 128-key value units (the last may be entirely masked)
 
     if (threadIdx.x == 0) {
         mbar_init(B_(bars->pro_full), 1);
@@ -137,11 +206,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(B_(bars->s_full[i]), 1);
-            mbar_init(B_(bars->s_free[i]), 128);
+            mbar_init(B_(bars->s_free[i]), 256);
             mbar_init(B_(bars->p_free[i]), 1);
-            mbar_init(B_(bars->p_full[i]), 1);
+            mbar_init(B_(bars->p_full[i]), 1);   // the value CTA's expect-tx arrival
             mbar_init(B_(bars->pv_done[i]), 1);
-            mbar_init(B_(bars->ri_read[i]), 128);
+            mbar_init(B_(bars->ri_read[i]), 256);
             mbar_init(B_(bars->olat_ready[i]), 1);
             mbar_init(B_(bars->ep_done[i]), 1);
         }
@@ -149,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(B_(bars->oc_full[i]), 1);
             mbar_init(B_(bars->oc_empty[i]), 1);
         }
-        mbar_init(B_(bars->corr_done), 128);
+        mbar_init(B_(bars->corr_done), 256);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -158,168 +227,204 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync_all();   // both CTAs' barriers exist before any remote arrival or copy
+    cluster_sync_all();   // both CTAs' barriers exist before any remote arrival or store
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    TR(const long long t_start = clock64();)
 
     if (rank == 0) {
         // =========================================================== score CTA
         if (warp == 0 && lane == 0) {
-            // ---- TMA producer: q tile + W_UK[h], then the c ring
+            // ---- TMA producer: q tile + W_UK[h] (ring uses 0-3), then c tiles [256 keys x 64]
             tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_c);
+            tma_prefetch_desc(&tm_c256);
             tma_prefetch_desc(&tm_wuk);
             const uint32_t pro = B_(bars->pro_full);
-            mbar_arrive_expect_tx(pro, 10 * kSlab);
-            for (int s = 0; s < 2; ++s) tma_load_4d(base + S_QP + s * kSlab, &tm_q, pro, s * 64, h, t0, b);
-            for (int s = 0; s < 8; ++s) tma_load_2d(base + S_QABS + s * kSlab, &tm_wuk, pro, s * 64, h * kD);
-            int it = 0;
+            mbar_arrive_expect_tx(pro, 2 * kSlab);
+            for (int s = 0; s < 2; ++s) tma_load_4d(base + S_PST + s * kSlab, &tm_q, pro, s * 64, h, t0, b);
+            for (int s = 0; s < kSStages; ++s) {
+                mbar_arrive_expect_tx(B_(bars->sc_full[s]), kSStage);
+                for (int i = 0; i < 2; ++i)
+                    tma_load_2d(base + S_RING + s * kSStage + i * kSlab, &tm_wuk, B_(bars->sc_full[s]),
+                                (2 * s + i) * 64, h * kD);
+            }
+            int it = kSStages;
             bool ok = true;
-            for (int j = 0; ok && j < nkv; ++j) {
+            for (int j = 0; ok && j < nblk; ++j) {
                 for (int kc = 0; kc < 8; ++kc, ++it) {
                     const int st = it % kSStages;
-                    if (it >= kSStages &&
-                        !(ok = mbar_wait(B_(bars->sc_empty[st]), ((it / kSStages) - 1) & 1, p.err, abort_flag)))
+                    TR(const long long _a = clock64();)
+                    if (!(ok = mbar_wait(B_(bars->sc_empty[st]), ((it / kSStages) - 1) & 1, p.err, abort_flag)))
                         break;
-                    mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSlab);
-                    tma_load_3d(base + S_RING + st * kSlab, &tm_c, B_(bars->sc_full[st]), kc * 64, j * kBN, b);
+                    TR(TR_ADD(TR_S_PROD_EMPTY, clock64() - _a);)
+                    mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSStage);
+                    tma_load_3d(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, j * kBS, b);
                 }
             }
             if (!ok) *abort_flag = 1;
             // no load may still be landing when the CTA exits
             mbar_wait(pro, 0, p.err);
-            for (int k = (it > kSStages ? it - kSStages : 0); k < it; ++k)
+            for (int k = it - kSStages; k < it; ++k)
                 mbar_wait(B_(bars->sc_full[k % kSStages]), (k / kSStages) & 1, p.err);
         } else if (warp == 1 && lane == 0) {
-            // ---- MMA issuer: absorb, then S = q_abs . c^T per key block
+            // ---- MMA issuer: absorb, then S = q_abs . c^T per 256-key block (q_abs from TMEM, N = 256)
             bool ok = mbar_wait(B_(bars->pro_full), 0, p.err, abort_flag);
+            for (int s = 0; ok && s < kSStages; ++s) ok = mbar_wait(B_(bars->sc_full[s]), 0, p.err, abort_flag);
             if (ok) {
                 tc_fence_after();
 #pragma unroll 1
                 for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = make_smem_desc(base + S_QP + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = make_smem_desc(base + S_PST + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
 #pragma unroll
                     for (int nh = 0; nh < 2; ++nh) {
-                        const uint64_t bd = make_smem_desc(base + S_QABS + nh * 4 * kSlab + kk * 2048, kSlab, 1024);
+                        const uint64_t bd = make_smem_desc(base + S_RING + nh * 2 * kSStage + kk * 2048, kSlab, 1024);
                         umma_bf16(tmem + nh * 256, a, bd, kIdescAbsorb, kk > 0);
                     }
                 }
                 umma_commit(B_(bars->absorb_done));
+                for (int s = 0; s < kSStages; ++s) umma_commit(B_(bars->sc_empty[s]));   // W_UK's slots are free
                 ok = mbar_wait(B_(bars->qabs_ready), 0, p.err, abort_flag);
             }
-            int it = 0;
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int sb = j & 1;
-                if (j >= 2 && !(ok = mbar_wait(B_(bars->s_free[sb]), ((j >> 1) - 1) & 1, p.err, abort_flag))) break;
+            int it = kSStages;
+            TR(long long tl0 = clock64(), w_free = 0, w_full = 0;)
+            for (int j = 0; ok && j < nblk; ++j) {
+                TR(long long _a = clock64();)
+                if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free[0]), (j - 1) & 1, p.err, abort_flag))) break;
+                TR(w_free += clock64() - _a;)
                 tc_fence_after();
                 for (int kc = 0; kc < 8; ++kc, ++it) {
                     const int st = it % kSStages;
+                    TR(long long _b = clock64();)
                     if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
+                    TR(w_full += clock64() - _b;)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t a = make_smem_desc(base + S_QABS + kc * kSlab + kk * 32, 16, 1024);
-                        const uint64_t bd = make_smem_desc(base + S_RING + st * kSlab + kk * 32, 16, 1024);
-                        umma_bf16(tmem + sb * kBN, a, bd, kIdescQK, (kc | kk) != 0);
+                        const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
+                        umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
+                                         (kc | kk) != 0);
                     }
                     umma_commit(B_(bars->sc_empty[st]));
                 }
                 if (!ok) break;
-                umma_commit(B_(bars->s_full[sb]));
+                umma_commit(B_(bars->s_full[0]));
             }
+            TR(TR_ADD(TR_S_MMA_LOOP, clock64() - tl0); TR_ADD(TR_S_MMA_SFREE, w_free); TR_ADD(TR_S_MMA_SCFULL, w_full);)
             if (!ok) *abort_flag = 1;
         } else if (warp >= 4) {
-            // ---- softmax warpgroup: thread `row` owns TMEM lane `row`
-            const int row = threadIdx.x - 128;
+            // ---- softmax: warpgroup `wg` owns keys [128 wg, 128 wg + 128) of each 256-key block, i.e. the
+            // value CTA's unit 2j + wg; thread `row` owns TMEM lane `row`
+            const int wg = (warp - 4) >> 2;
+            const int row = (warp & 3) * 32 + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             const int t = t0 + row;
-            bool fail = false;
-            fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
-            bool ok = !named_bar_or(1, 128, fail);
-            if (ok) {
-                // q_abs (fp32, TMEM) -> q_abs * scale * log2(e) as bf16 into the q_abs tile
+            const bool issuer = (threadIdx.x & 127) == 0;   // issues this warpgroup's bulk copies
+            bool fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
+            bool ok = !named_bar_or(1, 256, fail);
+            if (ok && wg == 0) {
+                // q_abs (fp32, TMEM columns 0-511) -> q_abs * scale * log2(e) packed as bf16 pairs into
+                // columns 0-255; chunk k (64 latent columns) lands in 32k..32k+31, which this thread has
+                // already read, so the compaction is in place, chunk by chunk in increasing order
                 tc_fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < kR / 32; ++cc) {
-                    float v[32];
-                    tmem_ld32(trow + cc * 32, v);
+                for (int k = 0; k < kR / 64; ++k) {
+                    float v[2][32], w[32];
+                    tmem_ld32(trow + k * 64, v[0]);
+                    tmem_ld32(trow + k * 64 + 32, v[1]);
                     tmem_wait_ld();
-                    store_row32_bf16(base + S_QABS, kSlab, row, cc, v, p.qk_scale_log2);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        w[i] = __uint_as_float(pack_bf16x2(v[i >> 4][2 * (i & 15)] * p.qk_scale_log2,
+                                                           v[i >> 4][2 * (i & 15) + 1] * p.qk_scale_log2));
+                    tmem_st32(trow + S_QCOL + k * 32, w);
+                    tmem_wait_st();
                 }
-                fence_proxy_async_smem();
                 tc_fence_before();
             }
-            named_bar_sync(1, 128);
-            if (row == 0 && ok) mbar_arrive(B_(bars->qabs_ready));
+            named_bar_sync(1, 256);
+            if (threadIdx.x == 128 && ok) mbar_arrive(B_(bars->qabs_ready));
+            TR(if (threadIdx.x == 128) TR_ADD(TR_S_PROLOGUE, clock64() - t_start);)
+            TR(long long tl0 = clock64(), w_sfull = 0, w_xbar = 0, w_pfree = 0, w_store = 0, w_rel = 0;)
 
-            float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int sb = j & 1, pb = j & 1;
-                fail = false;
-                fail = !mbar_wait(B_(bars->s_full[sb]), (j >> 1) & 1, p.err, abort_flag);
-                if (named_bar_or(1, 128, fail)) { ok = false; break; }
-                tc_fence_after();
+            const uint32_t ptile = base + S_PST + wg * kPUnit;   // this warpgroup's staging unit
+            const uint32_t ri = ptile + kPBytes;
+            float m_run = -INFINITY, l_part = 0.f;
+            for (int j = 0; ok && j < nblk; ++j) {
+                TR(long long _a = clock64();)
+                fail = fail || !mbar_wait(B_(bars->s_full[0]), j & 1, p.err, abort_flag);
+                TR(w_sfull += clock64() - _a;)
                 float s[4][32];
+                if (!fail) {
+                    tc_fence_after();
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + sb * kBN + c4 * 32, s[c4]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(B_(bars->s_free[sb]));
-
-                const int key0 = j * kBN;
-                if (j == nkv - 1) {   // the diagonal block: mask keys after the query and past the sequence
-                    const int lim = min(t, p.T - 1) - key0;   // last visible column
+                    for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_SCOL + wg * 128 + c4 * 32, s[c4]);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(B_(bars->s_free[0]));
+                    if (j == nblk - 1) {   // the last block: keys after the query or past the sequence
+                        const int lim = min(t, p.T - 1) - j * kBS - wg * 128;   // last visible column of this unit
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
+                        for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
+                            for (int i = 0; i < 32; ++i)
+                                if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
+                    }
+                    st_shared_f32(base + PMAX + ((j & 1) * 2 + wg) * kBM * 4 + row * 4, tree_max128(s));
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[c4][i]);
+                TR(long long _x = clock64();)
+                if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
+                TR(w_xbar += clock64() - _x;)
+                const float mx = fmaxf(ld_shared_f32(base + PMAX + ((j & 1) * 2 + 0) * kBM * 4 + row * 4),
+                                       ld_shared_f32(base + PMAX + ((j & 1) * 2 + 1) * kBM * 4 + row * 4));
                 float factor = 1.f;
                 if (mx > m_run + kRescaleLog2) {
                     factor = fast_exp2(m_run - mx);
                     m_run = mx;
                 }
-                float sum = 0.f;
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        s[c4][i] = fast_exp2(s[c4][i] - m_run);
-                        sum += s[c4][i];
-                    }
-                l_run = l_run * factor + sum;
+                    for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(s[c4][i] - m_run);
+                l_part = l_part * factor + tree_sum128(s);
 
-                // the staging tile is free once the previous copy has read it, and the
-                // value CTA's P buffer `pb` once its block j-2 product completed
-                fail = false;
-                if (row == 0) {
-                    bulk_wait_read_all();
-                    if (j >= 2) fail = !mbar_wait<true>(B_(bars->p_free[pb]), ((j >> 1) - 1) & 1, p.err, abort_flag);
-                }
-                if (named_bar_or(1, 128, fail)) { ok = false; break; }
+                TR(long long _s = clock64();)
+                // the staging unit is free once this warpgroup's previous copy has read it
+                if (issuer) bulk_wait_read_all();
+                named_bar_sync(2 + wg, 128);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) store_row32_bf16(base + S_QP, kSlab, row, c4, s[c4], 1.f);
-                st_shared_v2f(base + S_ROWINFO + row * 8, factor, l_run);
+                for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float *v = &s[c4][8 * k];
+                        st_shared_v4(ptile + (c4 >> 1) * kSlab + sw128_offset(row, (c4 & 1) * 4 + k),
+                                     pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                     pack_bf16x2(v[6], v[7]));
+                    }
+                // unit 2j carries the block's rescale factor; unit 2j+1 shares its maximum (factor 1)
+                st_shared_v2f(ri + row * 8, wg == 0 ? factor : 1.f, l_part);
                 fence_proxy_async_smem();
-                const bool any = named_bar_or(1, 128, factor != 1.f);
-                if (row == 0) {
-                    st_shared_u32(base + S_ROWINFO + kBM * 8, any ? 1u : 0u);
-                    fence_proxy_async_smem();
-                    const uint32_t dst_bar = mapa_shared(B_(bars->p_full[pb]), 1);
-                    bulk_copy_s2cluster(mapa_shared(base + O_P + pb * kPBytes, 1), base + S_QP, kPBytes, dst_bar);
-                    bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + pb * kRowInfoStride, 1), base + S_ROWINFO,
-                                        kRowInfoBytes, dst_bar);
-                    bulk_commit_group();
+                named_bar_sync(2 + wg, 128);
+                TR(w_store += clock64() - _s;)
+                if (issuer) {
+                    // the value CTA's P buffer `wg` is free once the product of unit 2(j-1) + wg completed
+                    TR(long long _f = clock64();)
+                    if (j >= 1) fail = !mbar_wait<true>(B_(bars->p_free[wg]), (j - 1) & 1, p.err, abort_flag);
+                    TR(w_pfree += clock64() - _f;)
+                    if (!fail) {
+                        const uint32_t dst_bar = mapa_shared(B_(bars->p_full[wg]), 1);
+                        bulk_copy_s2cluster(mapa_shared(base + O_P + wg * kPBytes, 1), ptile, kPBytes, dst_bar);
+                        bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + wg * kRowInfoBytes, 1), ri,
+                                            kRowInfoBytes, dst_bar);
+                        bulk_commit_group();
+                    }
                 }
             }
-            if (!ok) *abort_flag = 1;
-            if (row == 0) bulk_wait_all();
+            TR(if (threadIdx.x == 128) {
+                TR_ADD(TR_S_SM_LOOP, clock64() - tl0); TR_ADD(TR_S_SM_SFULL, w_sfull); TR_ADD(TR_S_SM_XBAR, w_xbar);
+                TR_ADD(TR_S_SM_PFREE, w_pfree); TR_ADD(TR_S_SM_STORE, w_store); TR_ADD(TR_S_SM_RELEASE, w_rel);
+            })
+            if (issuer) bulk_wait_all();
+            if (!ok || fail) *abort_flag = 1;
         }
     } else {
         // =========================================================== value CTA
@@ -332,9 +437,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < nkv + 1; ++j) {   // j == nkv: the W_UV tile
                 for (int nh = 0; nh < 2; ++nh, ++it) {
                     const int st = it % kOStages;
+                    TR(const long long _a = clock64();)
                     if (it >= kOStages &&
                         !(ok = mbar_wait(B_(bars->oc_empty[st]), ((it / kOStages) - 1) & 1, p.err, abort_flag)))
                         break;
+                    TR(TR_ADD(TR_O_PROD_EMPTY, clock64() - _a);)
                     const uint32_t full = B_(bars->oc_full[st]);
                     mbar_arrive_expect_tx(full, kOStage);
                     for (int q4 = 0; q4 < 4; ++q4) {
@@ -349,52 +456,78 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) *abort_flag = 1;
             for (int k = (it > kOStages ? it - kOStages : 0); k < it; ++k)
                 mbar_wait(B_(bars->oc_full[k % kOStages]), (k / kOStages) & 1, p.err);
-        } else if (warp == 1 && lane == 0) {
-            // ---- MMA issuer: o_lat += P . c, then o = o_lat . W_UV^T
+        } else if (warp == 1) {
+            // ---- MMA warp: o_lat += P . c, then o = o_lat . W_UV^T; lane 0 issues
+            const bool leader = lane == 0;
+            auto wait_all = [&](uint64_t &bar, uint32_t parity, bool cluster) {
+                return __all_sync(0xffffffffu, cluster ? mbar_wait<true>(B_(bar), parity, p.err, abort_flag)
+                                                       : mbar_wait(B_(bar), parity, p.err, abort_flag));
+            };
             int it = 0, ncorr = 0;
             bool ok = true;
+            TR(long long tl0 = clock64(), w_pfull = 0, w_oc = 0, w_corr = 0;)
             for (int j = 0; ok && j < nkv; ++j) {
                 const int pb = j & 1;
-                mbar_arrive_expect_tx(B_(bars->p_full[pb]), kPBytes + kRowInfoBytes);
-                if (!(ok = mbar_wait<true>(B_(bars->p_full[pb]), (j >> 1) & 1, p.err, abort_flag))) break;
-                const uint32_t flag = ld_shared_u32(base + O_ROWINFO + pb * kRowInfoStride + kBM * 8);
-                if (j > 0 && flag) {
-                    if (!(ok = mbar_wait(B_(bars->corr_done), ncorr & 1, p.err, abort_flag))) break;
+                TR(long long _a = clock64();)
+                if (leader) mbar_arrive_expect_tx(B_(bars->p_full[pb]), kPBytes + kRowInfoBytes);
+                if (!(ok = wait_all(bars->p_full[pb], (j >> 1) & 1, true))) break;
+                TR(w_pfull += clock64() - _a;)
+                // any row whose maximum grew needs o_lat rescaled before this block's product
+                const uint32_t ri = base + O_ROWINFO + pb * kRowInfoBytes;
+                bool grew = false;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) grew |= ld_shared_f32(ri + (lane + 32 * k) * 8) != 1.f;
+                if (j > 0 && __any_sync(0xffffffffu, grew)) {
+                    TR(long long _c = clock64();)
+                    if (!(ok = wait_all(bars->corr_done, ncorr & 1, false))) break;
+                    TR(w_corr += clock64() - _c;)
                     ++ncorr;
                 }
                 tc_fence_after();
                 for (int nh = 0; nh < 2; ++nh, ++it) {
                     const int st = it % kOStages;
-                    if (!(ok = mbar_wait(B_(bars->oc_full[st]), (it / kOStages) & 1, p.err, abort_flag))) break;
+                    TR(long long _o = clock64();)
+                    if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
+                    TR(w_oc += clock64() - _o;)
                     tc_fence_after();
+                    if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t a =
-                            make_smem_desc(base + O_P + pb * kPBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd = make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
-                        umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (j > 0 || kk > 0));
+                        for (int kk = 0; kk < kBN / 16; ++kk) {
+                            const uint64_t a = make_smem_desc(
+                                base + O_P + pb * kPBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                            const uint64_t bd = make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
+                            umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (j > 0 || kk > 0));
+                        }
+                        umma_commit(B_(bars->oc_empty[st]));
                     }
-                    umma_commit(B_(bars->oc_empty[st]));
+                    __syncwarp();
                 }
                 if (!ok) break;
-                umma_commit(B_(bars->pv_done[pb]));
+                if (leader) umma_commit(B_(bars->pv_done[pb]));
             }
+            TR(if (leader) {
+                TR_ADD(TR_O_MMA_LOOP, clock64() - tl0); TR_ADD(TR_O_MMA_PFULL, w_pfull); TR_ADD(TR_O_MMA_OCFULL, w_oc);
+                TR_ADD(TR_O_MMA_CORR, w_corr); TR_ADD(TR_CORRECTIONS, ncorr);
+            })
             for (int kh = 0; ok && kh < 2; ++kh, ++it) {
-                if (!(ok = mbar_wait(B_(bars->olat_ready[kh]), 0, p.err, abort_flag))) break;
+                if (!(ok = wait_all(bars->olat_ready[kh], 0, false))) break;
                 const int st = it % kOStages;
-                if (!(ok = mbar_wait(B_(bars->oc_full[st]), (it / kOStages) & 1, p.err, abort_flag))) break;
+                if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
                 tc_fence_after();
+                if (leader) {
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk) {
-                    const uint64_t a = make_smem_desc(base + O_P + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                    const uint64_t bd =
-                        make_smem_desc(base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                    umma_bf16(tmem, a, bd, kIdescEp, (kh > 0 || kk > 0));
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const uint64_t a = make_smem_desc(base + O_P + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                        const uint64_t bd =
+                            make_smem_desc(base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                        umma_bf16(tmem, a, bd, kIdescEp, (kh > 0 || kk > 0));
+                    }
+                    umma_commit(B_(bars->oc_empty[st]));
+                    umma_commit(B_(bars->ep_done[kh]));
                 }
-                umma_commit(B_(bars->oc_empty[st]));
-                umma_commit(B_(bars->ep_done[kh]));
+                __syncwarp();
             }
-            if (!ok) *abort_flag = 1;
+            if (!ok && leader) *abort_flag = 1;
         } else if (warp == 2 && lane == 0) {
             // ---- relay: P buffer pb is free again once its product completed and its row info was read
             for (int j = 0; j < nkv; ++j) {
@@ -407,36 +540,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 mbar_arrive_remote(B_(bars->p_free[pb]), 0);
             }
         } else if (warp >= 4) {
-            // ---- correction + epilogue warpgroup: thread `row` owns TMEM lane `row`
-            const int row = threadIdx.x - 128;
+            // ---- correction + epilogue: thread `row` of warpgroup `wg` owns TMEM lane `row`,
+            // latent columns [256 wg, 256 wg + 256) for rescaling
+            const int wg = (warp - 4) >> 2;
+            const int row = (warp & 3) * 32 + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             const int t = t0 + row;
-            float l_fin = 1.f;
+            float l_even = 0.f, l_odd = 0.f;
             bool ok = true, fail;
+            TR(long long tl0 = clock64();)
             for (int j = 0; j < nkv; ++j) {
                 const int pb = j & 1;
-                fail = false;
                 fail = !mbar_wait<true>(B_(bars->p_full[pb]), (j >> 1) & 1, p.err, abort_flag);
-                if (named_bar_or(2, 128, fail)) { ok = false; break; }
-                const uint32_t ri = base + O_ROWINFO + pb * kRowInfoStride;
-                const float2 fl = ld_shared_v2f(ri + row * 8);
-                const uint32_t flag = ld_shared_u32(ri + kBM * 8);
+                if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                const float2 fl = ld_shared_v2f(base + O_ROWINFO + pb * kRowInfoBytes + row * 8);
                 mbar_arrive(B_(bars->ri_read[pb]));
-                l_fin = fl.y;
-                if (j > 0 && flag) {
-                    fail = false;
+                // the two warpgroups of the score CTA keep separate sums (even and odd units)
+                if (j & 1)
+                    l_odd = fl.y;
+                else
+                    l_even = fl.y;
+                if (named_bar_or(4, 256, j > 0 && fl.x != 1.f)) {
                     fail = !mbar_wait(B_(bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, p.err, abort_flag);
-                    if (named_bar_or(2, 128, fail)) { ok = false; break; }
+                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, fl.x != 1.f)) {
 #pragma unroll 1
-                        for (int cc = 0; cc < kR / 32; ++cc) {
+                        for (int cc = 0; cc < 8; ++cc) {
                             float v[32];
-                            tmem_ld32(trow + cc * 32, v);
+                            const uint32_t ta = trow + wg * 256 + cc * 32;
+                            tmem_ld32(ta, v);
                             tmem_wait_ld();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] *= fl.x;
-                            tmem_st32(trow + cc * 32, v);
+                            tmem_st32(ta, v);
                         }
                         tmem_wait_st();
                     }
@@ -445,20 +582,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             }
             if (ok) {
-                fail = false;
                 fail = !mbar_wait(B_(bars->pv_done[(nkv - 1) & 1]), ((nkv - 1) >> 1) & 1, p.err, abort_flag);
-                ok = !named_bar_or(2, 128, fail);
+                ok = !named_bar_or(4, 256, fail);
             }
-            const float inv_l = 1.f / l_fin;
+            TR(long long t_ep = clock64(); if (threadIdx.x == 128) TR_ADD(TR_O_COR_LOOP, t_ep - tl0);)
+            const float inv_l = 1.f / (l_even + l_odd);
             for (int kh = 0; ok && kh < 2; ++kh) {
                 if (kh == 1) {   // the staging tile is free once the first half's product completed
-                    fail = false;
                     fail = !mbar_wait(B_(bars->ep_done[0]), 0, p.err, abort_flag);
-                    if (named_bar_or(2, 128, fail)) { ok = false; break; }
+                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int i = 0; i < 4; ++i) {
+                    const int cc = wg * 4 + i;   // 32-column chunk within this 256-column half
                     float v[32];
                     tmem_ld32(trow + kh * 256 + cc * 32, v);
                     tmem_wait_ld();
@@ -466,26 +603,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                named_bar_sync(2, 128);
-                if (row == 0) mbar_arrive(B_(bars->olat_ready[kh]));
+                named_bar_sync(4, 256);
+                if (threadIdx.x == 128) mbar_arrive(B_(bars->olat_ready[kh]));
             }
             if (ok) {
-                fail = false;
                 fail = !mbar_wait(B_(bars->ep_done[1]), 0, p.err, abort_flag);
-                ok = !named_bar_or(2, 128, fail);
+                ok = !named_bar_or(4, 256, fail);
             }
             if (ok) {
                 tc_fence_after();
-                float o[4][32];
+                float o[2][32];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + c4 * 32, o[c4]);
+                for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + wg * 64 + c2 * 32, o[c2]);
                 tmem_wait_ld();
                 if (t < p.T) {
-                    const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD;
+                    const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + wg * 64;
                     const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
                     uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
 #pragma unroll
-                    for (int v8 = 0; v8 < kD / 8; ++v8) {
+                    for (int v8 = 0; v8 < 8; ++v8) {
                         float y[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) y[i] = o[(v8 * 8 + i) >> 5][(v8 * 8 + i) & 31];
@@ -505,6 +641,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            TR(if (threadIdx.x == 128) TR_ADD(TR_O_EPILOGUE, clock64() - t_ep);)
             if (!ok) *abort_flag = 1;
         }
     }
@@ -512,6 +649,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    TR(if (threadIdx.x == 0) {
+        TR_ADD(rank == 0 ? TR_S_TOTAL : TR_O_TOTAL, clock64() - t_start);
+        if (rank == 0) { TR_ADD(TR_TILES, 1); TR_ADD(TR_BLOCKS, nkv); }
+    })
     if (warp == 1) tmem_dealloc(tmem, 512);
     cluster_sync_all();   // the partner no longer touches this CTA's shared memory
 }
@@ -530,10 +671,24 @@ CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t 
 
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v) { return r == kR && d_q == kD && d_v == kD; }
 
+#ifdef MLA_TRACE
+// Diagnostic build only: copy (and optionally clear) the wait-accounting slots.
+extern "C" __attribute__((visibility("default"))) int mla_debug_prefill_trace(unsigned long long *host, int n,
+                                                                                int clear) {
+    if (n > TR_COUNT) n = TR_COUNT;
+    if (cudaMemcpyFromSymbol(host, g_trace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+    if (clear) {
+        static const unsigned long long zeros[TR_COUNT] = {};
+        if (cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+    }
+    return n;
+}
+#endif
+
 cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_bf16_r512_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
     const cuuint64_t B = a.B, T = a.T, H = a.H;
-    CUtensorMap tm_q, tm_c, tm_wuk, tm_wuv;
+    CUtensorMap tm_q, tm_c, tm_c256, tm_wuk, tm_wuv;
     {
         const cuuint64_t dims[4] = {kD, H, T, B};
         const cuuint64_t strides[3] = {kD * 2, H * kD * 2, T * H * kD * 2};
@@ -545,6 +700,8 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
         const cuuint64_t strides[2] = {kR * 2, T * kR * 2};
         const cuuint32_t box[3] = {64, kBN, 1};
         if (encode_map(&tm_c, a.c, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint32_t box256[3] = {64, kBS, 1};
+        if (encode_map(&tm_c256, a.c, 3, dims, strides, box256) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[2] = {kR, H * kD};
@@ -567,7 +724,7 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const long long n_ctas = 2LL * p.n_qtiles * p.bh_count;
     if (n_ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    prefill_r512_kernel<<<static_cast<unsigned>(n_ctas), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_wuk, tm_wuv, p);
+    prefill_r512_kernel<<<static_cast<unsigned>(n_ctas), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk, tm_wuv, p);
     return cudaGetLastError();
 }
 
