@@ -435,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------------------------- merge
 constexpr int kMRows = 64;                          // sequences per merge CTA
+constexpr int kMergeThreads = 512;
 constexpr uint32_t kASlab = kMRows * 128;           // o_lat tile [64 rows x 64 latent columns]
 constexpr uint32_t MA_OFF = 0;
 constexpr uint32_t MA_BYTES = 7 * kASlab + kSlab;   // an M=128 operand read of the last slab stays inside
@@ -452,7 +453,7 @@ struct MergeParams {
     int B, H, max_len, G;
 };
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kMergeThreads, 1)
     decode_merge_kernel(const __grid_constant__ CUtensorMap tm_wuv, const MergeParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -498,8 +499,11 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     const long long total = s_total;
 
-    // log-sum-exp combine of the segments of each sequence; o_lat -> bf16 tile row
-    for (int i = warp; i < kMRows; i += 4) {
+    // log-sum-exp combine of the segments of each sequence; o_lat -> bf16 tile row.
+    // A warp takes a row at a time: lane i fetches segment i's (m, l), the warp
+    // reduces them with shuffles, then every lane accumulates its 16 latent
+    // columns over the segments, issuing a segment's loads together.
+    for (int i = warp; i < kMRows; i += kMergeThreads / 32) {
         const int b = b0 + i;
         float o[16];
 #pragma unroll
@@ -507,29 +511,44 @@ __global__ void __launch_bounds__(128, 1)
         const long long r0 = s_pre[i], r1 = s_pre[i + 1];
         if (b < p.B && r1 > r0) {
             const int G = p.G;
-            int c_first = static_cast<int>(((r0 + 1) * G - 1) / total);
-            c_first = min(c_first, G - 1);
+            const int c_first = min(static_cast<int>(((r0 + 1) * G - 1) / total), G - 1);
             // CTA c wrote slot c + b iff its share [lo_c, lo_c+1) overlaps [r0, r1)
             auto overlaps = [&](int c) {
-                return min(share_lo(total, c + 1, G), r1) > max(share_lo(total, c, G), r0);
+                return c < G && min(share_lo(total, c + 1, G), r1) > max(share_lo(total, c, G), r0);
             };
-            float M = -INFINITY;
-            for (int c = c_first; c < G && share_lo(total, c, G) < r1; ++c)
-                if (overlaps(c)) M = fmaxf(M, __ldg(p.ws_m + static_cast<size_t>(c + b) * H + h));
-            float L = 0.f;
-            for (int c = c_first; c < G && share_lo(total, c, G) < r1; ++c) {
+            int n_seg = 0;   // consecutive CTAs from c_first whose shares start before r1
+            while (c_first + n_seg < G && share_lo(total, c_first + n_seg, G) < r1) ++n_seg;
+            float M = -INFINITY, L = 0.f;
+            for (int s0 = 0; s0 < n_seg; s0 += 32) {
+                const int c = c_first + s0 + lane;
+                const bool has = s0 + lane < n_seg && overlaps(c);
+                const size_t slot = static_cast<size_t>(c + b);
+                const float m = has ? __ldg(p.ws_m + slot * H + h) : -INFINITY;
+                float mw = m;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
+                const float M_new = fmaxf(M, mw);
+                float lw = has ? fast_exp2(m - M_new) * __ldg(p.ws_l + slot * H + h) : 0.f;
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
+                L = (M == -INFINITY ? 0.f : L * fast_exp2(M - M_new)) + lw;
+                M = M_new;
+            }
+            for (int si = 0; si < n_seg; ++si) {
+                const int c = c_first + si;
                 if (!overlaps(c)) continue;
                 const size_t slot = static_cast<size_t>(c + b);
                 const float w = fast_exp2(__ldg(p.ws_m + slot * H + h) - M);
-                L += w * __ldg(p.ws_l + slot * H + h);
                 const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (slot * H + h) * kR + lane * 16);
+                float4 v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) v[q4] = __ldg(src + q4);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
-                    const float4 v = __ldg(src + q4);
-                    o[4 * q4 + 0] += w * v.x;
-                    o[4 * q4 + 1] += w * v.y;
-                    o[4 * q4 + 2] += w * v.z;
-                    o[4 * q4 + 3] += w * v.w;
+                    o[4 * q4 + 0] += w * v[q4].x;
+                    o[4 * q4 + 1] += w * v[q4].y;
+                    o[4 * q4 + 2] += w * v[q4].z;
+                    o[4 * q4 + 3] += w * v[q4].w;
                 }
             }
             const float inv = 1.f / L;
@@ -566,21 +585,22 @@ __global__ void __launch_bounds__(128, 1)
     if (warp < 2 && __all_sync(0xffffffffu, done)) {
         const int i = warp * 32 + lane;
         const int b = b0 + i;
-        float o[4][32];
+        const size_t off = (static_cast<size_t>(b) * H + h) * kDV;
+        const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
+        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
+#pragma unroll 1
+        for (int c4 = 0; c4 < kDV / 32; ++c4) {   // 32 output columns at a time
+            float o[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c4 * 32, o);
+            tmem_wait_ld();
+            if (b >= p.B) continue;
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c4 * 32, o[c4]);
-        tmem_wait_ld();
-        if (b < p.B) {
-            const size_t off = (static_cast<size_t>(b) * H + h) * kDV;
-            const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
-            uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
-#pragma unroll
-            for (int v8 = 0; v8 < kDV / 8; ++v8) {
+            for (int v8 = 0; v8 < 4; ++v8) {
                 float y[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) y[k] = o[(v8 * 8 + k) >> 5][(v8 * 8 + k) & 31];
+                for (int k = 0; k < 8; ++k) y[k] = o[v8 * 8 + k];
                 if (g4) {
-                    const uint4 gv = __ldg(g4 + v8);
+                    const uint4 gv = __ldg(g4 + c4 * 4 + v8);
                     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -588,8 +608,8 @@ __global__ void __launch_bounds__(128, 1)
                         y[2 * k + 1] *= __fdividef(1.f, 1.f + fast_exp2(-__uint_as_float(gw[k] & 0xFFFF0000u) * kLog2e));
                     }
                 }
-                o4[v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                                    pack_bf16x2(y[6], y[7]));
+                o4[c4 * 4 + v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                             pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
             }
         }
     }
@@ -718,7 +738,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     mp.max_len = a.max_len;
     mp.G = G;
     const dim3 grid(a.H, (a.B + kMRows - 1) / kMRows);
-    decode_merge_kernel<<<grid, 128, kSmemMerge, s>>>(tm_wuv, mp);
+    decode_merge_kernel<<<grid, kMergeThreads, kSmemMerge, s>>>(tm_wuv, mp);
     return cudaGetLastError();
 }
 
