@@ -137,6 +137,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Prefetch the box at {x, y, z} of a 3-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte aligned address into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
+                 : "memory");
+}
+
 // Make this thread's generic-proxy smem writes visible to the async proxy
 // (tensor core / TMA reads that follow a barrier).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -208,6 +222,28 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // All but the most recent bulk group of this thread have finished reading their source.
 __device__ __forceinline__ void bulk_wait_read_all_but_newest() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ programmatic dependent launch
+// Let the next kernel in the stream (launched with programmatic stream
+// serialisation) be scheduled; it still waits for this grid in grid_dependency_wait.
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid has completed and its memory operations are visible.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ------------------------------------------------------------------ register split
+// Warpgroup-wide change of the per-thread register budget.  Every warp of the
+// warpgroup executes the same call; the increases of all warpgroups must fit
+// in what the block was launched with (threads x registers per thread).
+template <uint32_t N>
+__device__ __forceinline__ void regs_release() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_acquire() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------------------ named barriers

@@ -7,23 +7,29 @@
 // section "完整计算流（四步）" follow: scores against c itself, softmax, the
 // latent weighting by c itself, W_UV^T, gate.
 //
-// Split kernel (one CTA per SM, persistent): the concatenation of all
-// sequences' cache rows is cut into one contiguous, equal share per CTA, so
-// ragged lengths balance by construction.  A CTA walks its share as segments
-// (one per sequence it touches) in blocks of 128 rows:
-//   S  = q_abs[b] . c_blk^T          M = 128 (heads, zero-padded), N = 128 rows, K = r
-//   O^T += c_blk^T . P^T             M = r (4 x 128), N = heads, K = 128 rows
-// Heads are rows of S, so the online softmax is one thread per head; the
-// latent accumulator is kept transposed (TMEM lanes = latent index, columns =
-// heads: 4 x 96 columns), which leaves 128 TMEM columns for S.  Each cache
-// row is read from HBM once for all heads; the value product re-reads the
-// block's tiles from L2.  Per segment the CTA writes (O^T, running max, sum).
+// Pair kernel (persistent, one cluster of two CTAs per SM pair): the
+// concatenation of all sequences' cache rows is cut into one contiguous,
+// equal share per cluster, so ragged lengths balance by construction.  A
+// cluster walks its share as segments (one per sequence it touches) in blocks
+// of 256 rows.  Heads are the M = 128 rows of every product (zero-padded):
+//   rank 0, the score CTA: q_abs[b] sits in TMEM as packed bf16 (columns
+//     0-255) and is the A operand of S = q_abs . c_blk^T (N = 256 cache rows,
+//     K = r) into columns 256-511.  Two warpgroups run the online softmax, one
+//     per 128-row half of the block (thread = head); P (bf16) and per-head
+//     (rescale factor, partial sum) go to the value CTA by DSMEM bulk copies.
+//   rank 1, the value CTA: o_lat += P . c_unit (M = heads, N = 2 x 256 latent
+//     columns, K = 128 cache rows), fp32 in all 512 TMEM columns, rescaled
+//     lazily when a head's maximum grew by more than 2^16.
+// Per segment the cluster writes (o_lat unnormalised, running max, sum) to a
+// workspace slot.  Each cache row is read from HBM once (the score CTA's copy,
+// prefetched into L2 a block ahead); the value CTA re-reads it from L2.
 // Merge kernel: one CTA per (head, 64 sequences) combines the segments of a
 // sequence with the log-sum-exp rule, rounds o_lat to bf16 and applies W_UV^T
 // on the tensor cores, then the sigmoid gate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -34,63 +40,137 @@ namespace {
 
 constexpr int kR = 512;
 constexpr int kDV = 128;
-constexpr int kBN = 128;      // cache rows per block
+constexpr int kBS = 256;      // cache rows per score block
+constexpr int kBN = 128;      // cache rows per value unit (two per block)
 constexpr int kHMax = 96;
-constexpr int kThreads = 256;
-constexpr float kRescaleLog2 = 8.0f;
+constexpr int kThreads = 384;   // warps 0 TMA, 1 MMA, 2 relay (value CTA), 4-7 and 8-11: two warpgroups
+// Register split: the control warpgroup (warps 0-3) gives registers to the two
+// math warpgroups.  4 x 32 x 56 + 8 x 32 x 216 = 62,464 <= 384 x 168 launched.
+#ifndef MLA_TRACE
+constexpr uint32_t kRegsCtl = 56, kRegsMath = 216, kRegsLaunch = 168;
+#else   // the wait accounting needs more registers in the control warps
+constexpr uint32_t kRegsCtl = 88, kRegsMath = 200, kRegsLaunch = 168;
+#endif
+static_assert(128 * kRegsCtl + 256 * kRegsMath <= kThreads * kRegsLaunch, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
+// Keep a stale maximum until the new one exceeds it by this (log2 units):
+// p <= 2^16, far inside the fp32 range of the sums and the accumulator.
+constexpr float kRescaleLog2 = 16.0f;
+// The score CTA's producer prefetches the cache rows this many 256-row blocks
+// ahead of its loads into L2.
+#ifndef MLA_DECODE_PREFETCH_BLOCKS
+#define MLA_DECODE_PREFETCH_BLOCKS 0
+#endif
+constexpr int kPrefetchBlocks = MLA_DECODE_PREFETCH_BLOCKS;
 // Largest scratch the no-alloc decode entry point can use (48 MiB: the K3 decode
-// workload, B = 64 and H = 96 on 152 SMs, needs 42.6 MB).
+// workload, B = 64 and H = 96 on 152 SMs, needs 27.6 MB).
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 
-constexpr uint32_t kSlab = 16384;            // c tile [128 rows x 64 latent columns], 128B swizzle
-constexpr uint32_t kQSlab = kHMax * 128;     // q_abs tile [96 heads x 64 latent columns]
-constexpr uint32_t kPSlab = kHMax * 128;     // P^T tile [96 heads x 64 cache rows]
-constexpr uint32_t Q_OFF = 0;
-constexpr uint32_t Q_BYTES = 7 * kQSlab + kSlab;   // an M=128 operand read of the last slab stays inside
-constexpr uint32_t RING_OFF = Q_BYTES;
-constexpr int kUnits = 3;                    // ring of units, 2 tiles each
-constexpr uint32_t kUnit = 2 * kSlab;
-constexpr uint32_t P_OFF = RING_OFF + kUnits * kUnit;
-constexpr uint32_t FAC_OFF = P_OFF + 2 * kPSlab;
-constexpr uint32_t BAR_OFF = FAC_OFF + 128 * 4;
-constexpr uint32_t kSmemSplit = BAR_OFF + 256 + 1024;
-static_assert(kSmemSplit <= 232448, "split kernel exceeds shared memory");
-static_assert(RING_OFF % 1024 == 0 && P_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+constexpr uint32_t kSlab = 16384;                    // [128 rows x 64 bf16] with 128-byte swizzle
+// P travels compactly: only the H <= 96 head rows of each [128 x 64] swizzled
+// slab are stored and copied.  The value CTA's M = 128 operand read of a slab
+// runs 4 KB into the following memory; those rows (heads >= H) only feed
+// accumulator rows nobody reads.
+constexpr uint32_t kPSlab = kHMax * 128;             // compact P slab: [96 heads x 64 rows]
+constexpr uint32_t kPBytes = 2 * kPSlab;             // one unit of P: [96 heads x 128 rows]
+constexpr uint32_t kRowInfoBytes = 128 * 8;          // {rescale factor, running sum} per head
+// score CTA
+constexpr uint32_t kSStage = 2 * kSlab;              // c ring stage: [256 rows x 64 latent columns]
+#ifndef MLA_DECODE_SCORE_STAGES
+#define MLA_DECODE_SCORE_STAGES 5
+#endif
+constexpr int kSStages = MLA_DECODE_SCORE_STAGES;
+constexpr uint32_t S_RING = 0;
+constexpr uint32_t kPUnit = kPBytes + kRowInfoBytes; // staging per warpgroup
+constexpr uint32_t S_PST = S_RING + kSStages * kSStage;
+constexpr uint32_t S_END = S_PST + 2 * kPUnit;
+// value CTA
+constexpr uint32_t O_RING = 0;
+constexpr int kOStages = 2;
+constexpr uint32_t kOStage = 4 * kSlab;              // 256 latent columns x 128 rows
+constexpr int kPBufs = 3;                            // P units in flight to the value CTA
+constexpr uint32_t O_P = kOStages * kOStage;         // kPBufs P tiles, then the operand over-read pad
+constexpr uint32_t O_ROWINFO = O_P + kPBufs * kPBytes + (kSlab - kPSlab);
+constexpr uint32_t O_END = O_ROWINFO + kPBufs * kRowInfoBytes;
+constexpr uint32_t BARS = S_END > O_END ? S_END : O_END;
+constexpr uint32_t PMAX = BARS + 512;                // [2 parities][2 warpgroups][128 heads] partial maxima
+constexpr uint32_t kSmemPair = PMAX + 2 * 2 * 128 * 4 + 1024;   // + alignment slack
+static_assert(BARS % 16 == 0, "barrier alignment");
+static_assert(kSmemPair <= 232448, "pair kernel exceeds shared memory");
+static_assert(S_PST % 1024 == 0 && kPUnit % 1024 == 0 && kPSlab % 1024 == 0 && O_P % 1024 == 0, "alignment");
+// TMEM columns of the score CTA
+constexpr uint32_t S_QCOL = 0;     // packed bf16 q_abs: K step ks (16 latent columns) at columns 8 ks .. 8 ks + 7
+constexpr uint32_t S_SCOL = 256;   // S for one 256-row block
 
-constexpr uint32_t S_COL = 0;     // TMEM columns of S
-constexpr uint32_t O_COL = 128;   // TMEM columns of O^T (4 blocks x Hp)
+constexpr uint32_t kIdescQK = make_idesc_bf16(128, 256, 0, 0);   // q_abs (TMEM) x c (K-major), 256 rows
+constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);   // P (K-major) x c (MN-major)
 
-struct SplitBars {
-    uint64_t q_full, q_free;
-    uint64_t u_full[kUnits], u_empty[kUnits];
-    uint64_t s_full, s_free, p_full, pv_done, o_drained;
+struct PairBars {
+    uint64_t qabs_ready;                              // score CTA
+    uint64_t sc_full[kSStages], sc_empty[kSStages];
+    uint64_t s_full, s_free;
+    uint64_t p_free[kPBufs];                          // arrivals from the value CTA
+    uint64_t oc_full[kOStages], oc_empty[kOStages];   // value CTA
+    uint64_t p_full[kPBufs];                          // bulk-copy transactions from the score CTA
+    uint64_t pv_done[kPBufs], ri_read[kPBufs], corr_done, o_drained;
     uint32_t tmem_base;
     int abort;
 };
-static_assert(sizeof(SplitBars) <= 256, "barrier block too large");
+static_assert(sizeof(PairBars) <= 512, "barrier block too large");
 
-struct SplitParams {
+// Opt-in wait accounting (build with MLA_NVCC_FLAGS=-DMLA_TRACE): cycles each
+// role spends at its waits and in its loop, summed over all CTAs.
+enum DecodeTraceSlot {
+    DT_S_MMA_LOOP, DT_S_MMA_SFREE, DT_S_MMA_SCFULL, DT_S_MMA_QREADY, DT_S_SM_LOOP, DT_S_SM_SFULL, DT_S_SM_XBAR,
+    DT_S_SM_PFREE, DT_S_SM_QLOAD, DT_O_MMA_LOOP, DT_O_MMA_PFULL, DT_O_MMA_OCFULL, DT_O_MMA_CORR, DT_O_MMA_DRAINED,
+    DT_O_COR_LOOP, DT_O_DRAIN, DT_S_PROD_EMPTY, DT_O_PROD_EMPTY, DT_SEGMENTS, DT_BLOCKS, DT_CORRECTIONS,
+    DT_S_TOTAL, DT_O_TOTAL, DT_COUNT
+};
+#ifdef MLA_TRACE
+__device__ unsigned long long g_dtrace[DT_COUNT];
+#define TR(...) __VA_ARGS__
+#define TR_ADD(slot, v) atomicAdd(&g_dtrace[slot], static_cast<unsigned long long>(v))
+// Per-block event times (cycles since the start barrier) of one cluster, for timelines.
+constexpr int kTLMax = 256, kTLEvents = 14, kTLCluster = 10;
+__device__ long long g_dtl[kTLEvents][kTLMax];
+__device__ long long g_dclu[2][512];   // per cluster: value CTA's total cycles, segments
+__device__ long long g_mtrace[6][1024];   // per merge CTA: phase end times (cycles since its start)
+#define MT(ph) do { if (threadIdx.x == 0) { const int _c = blockIdx.y * gridDim.x + blockIdx.x; \
+    if (_c < 1024) g_mtrace[ph][_c] = clock64() - mt0; } } while (0)
+#define TL(ev, idx, val) \
+    do { if (cl == kTLCluster && static_cast<int>(idx) < kTLMax) g_dtl[ev][idx] = (val); } while (0)
+#else
+#define TR(...)
+#define TR_ADD(slot, v) (void)0
+#define MT(ph) (void)0
+#endif
+
+struct PairParams {
     const int *lens;
+    const __nv_bfloat16 *q_abs;
     float *ws_o;   // [slots][H][r]
     float *ws_m;   // [slots][H]
     float *ws_l;   // [slots][H]
     int *err;
-    int B, H, Hp, max_len;
+    int B, H, max_len;
     float qk_scale_log2;
 };
 
 __device__ __forceinline__ int clamp_len(int x, int max_len) { return min(max(x, 0), max_len); }
 
-// The share of the concatenated cache rows that CTA c of G owns: [lo, hi).
+// Work is split on a virtual row axis: each non-empty sequence occupies
+// kSeqOverhead virtual rows (the cost of starting a segment: loading its
+// query, draining its accumulator, refilling the pipeline) followed by its
+// cache rows.  Cluster c of G owns the virtual rows [share_lo(c), share_lo(c+1)).
+constexpr long long kSeqOverhead = 1024;
 __device__ __forceinline__ long long share_lo(long long total, int c, int G) { return (total * c) / G; }
 
-// Walks the (sequence, [k0, k1)) segments of one CTA's share in order.  All
-// roles of the CTA run the same walk, so their ring and barrier counters agree.
+// Walks the (sequence, [k0, k1)) segments of one cluster's share in order.
+// Every role of both CTAs runs the same walk, so their counters agree.
 struct SegWalk {
     const int *lens;
     int B, max_len;
-    long long lo, hi, pre;   // pre = first concatenated row of sequence b
+    long long lo, hi, pre;   // pre = first virtual row of sequence b
     int b;
     __device__ void init(const int *lens_, int B_, int max_len_, long long lo_, long long hi_) {
         lens = lens_;
@@ -105,10 +185,10 @@ struct SegWalk {
     __device__ bool next(int &seq, int &k0, int &k1) {
         while (b < B && pre < hi) {
             const int len = clamp_len(__ldg(lens + b), max_len);
-            const long long s0 = max(pre, lo), s1 = min(pre + len, hi);
-            const long long base = pre;
+            const long long base = pre + kSeqOverhead;   // virtual row of cache row 0
+            const long long s0 = max(base, lo), s1 = min(base + len, hi);
             const int cur = b;
-            pre += len;
+            if (len > 0) pre = base + len;
             ++b;
             if (s1 > s0) {
                 seq = cur;
@@ -121,42 +201,136 @@ struct SegWalk {
     }
 };
 
+// The 256-row blocks of a share in walk order, for the L2 prefetch that runs ahead of the loads.
+struct BlockCursor {
+    SegWalk w;
+    int seq, key, k1;
+    bool valid;
+    __device__ void init(const SegWalk &from) {
+        w = from;
+        valid = w.next(seq, key, k1);
+    }
+    __device__ void advance() {
+        key += kBS;
+        if (key >= k1) valid = w.next(seq, key, k1);
+    }
+};
+
 __device__ __forceinline__ long long total_rows(const int *lens, int B, int max_len, int *err, bool report) {
     long long t = 0;
     for (int b = 0; b < B; ++b) {
         const int x = __ldg(lens + b);
         if (report && (x < 0 || x > max_len)) record_error(err, kDevErrBounds);
-        t += clamp_len(x, max_len);
+        const int len = clamp_len(x, max_len);
+        if (len > 0) t += kSeqOverhead + len;
     }
     return t;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
-                        const SplitParams p) {
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(a), "f"(b) : "memory");
+}
+
+// Reductions over 128 values as 8 interleaved chains: short dependency chains
+// without holding 32 extra temporaries next to the 128 values.
+__device__ __forceinline__ float max128(const float (&s)[4][32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = s[0][i];
+#pragma unroll
+    for (int k = 8; k < 128; ++k) m[k & 7] = fmaxf(m[k & 7], s[k >> 5][k & 31]);
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+__device__ __forceinline__ float min128(const float (&s)[4][32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = s[0][i];
+#pragma unroll
+    for (int k = 8; k < 128; ++k) m[k & 7] = fminf(m[k & 7], s[k >> 5][k & 31]);
+    return fminf(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])), fminf(fminf(m[4], m[5]), fminf(m[6], m[7])));
+}
+__device__ __forceinline__ float sum128(const float (&s)[4][32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = s[0][i];
+#pragma unroll
+    for (int k = 8; k < 128; ++k) m[k & 7] = m[k & 7] + s[k >> 5][k & 31];
+    return ((m[0] + m[1]) + (m[2] + m[3])) + ((m[4] + m[5]) + (m[6] + m[7]));
+}
+
+// Absorbed-query rows into TMEM: a head's packed bf16 pairs are its row's
+// 32-bit words in memory order.  Warpgroup wg owns latent columns
+// [256 wg, 256 wg + 256) of head `row` (zeros for padding heads), in two
+// halves of 16 x 16 bytes.
+__device__ __forceinline__ void q_issue(const __nv_bfloat16 *q_abs, int sq, int H, int row, bool head, int wg, int half,
+                                        uint4 (&v)[16]) {
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(q_abs + (static_cast<size_t>(sq) * H + (head ? row : 0)) * kR) + wg * 32 +
+        half * 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = head ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void q_store(uint32_t trow, int wg, int half, const uint4 (&v)[16]) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w[4 * i + 0] = __uint_as_float(v[8 * k + i].x);
+            w[4 * i + 1] = __uint_as_float(v[8 * k + i].y);
+            w[4 * i + 2] = __uint_as_float(v[8 * k + i].z);
+            w[4 * i + 3] = __uint_as_float(v[8 * k + i].w);
+        }
+        tmem_st32(trow + S_QCOL + wg * 128 + (half * 2 + k) * 32, w);
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_pair_kernel(const __grid_constant__ CUtensorMap tm_c256, const __grid_constant__ CUtensorMap tm_c,
+                       const PairParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    uint8_t *gbase = smem_raw + (base - raw);
-    SplitBars *bars = reinterpret_cast<SplitBars *>(gbase + BAR_OFF);
-    float *fac = reinterpret_cast<float *>(gbase + FAC_OFF);
+    PairBars *bars = reinterpret_cast<PairBars *>(smem_raw + (base - raw) + BARS);
     volatile int *abort_flag = &bars->abort;
     auto B_ = [](uint64_t &b) { return smem_u32(&b); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = gridDim.x, cta = blockIdx.x;
-    const int H = p.H, Hp = p.Hp;
+    const uint32_t rank = cluster_ctarank();
+    const int G = static_cast<int>(gridDim.x >> 1), cl = static_cast<int>(blockIdx.x >> 1);
+    const int H = p.H;
 
     if (threadIdx.x == 0) {
-        mbar_init(B_(bars->q_full), 1);
-        mbar_init(B_(bars->q_free), 1);
-        for (int i = 0; i < kUnits; ++i) {
-            mbar_init(B_(bars->u_full[i]), 1);
-            mbar_init(B_(bars->u_empty[i]), 1);
+        mbar_init(B_(bars->qabs_ready), 1);
+        for (int i = 0; i < kSStages; ++i) {
+            mbar_init(B_(bars->sc_full[i]), 1);
+            mbar_init(B_(bars->sc_empty[i]), 1);
         }
         mbar_init(B_(bars->s_full), 1);
-        mbar_init(B_(bars->s_free), 128);
-        mbar_init(B_(bars->p_full), 1);
-        mbar_init(B_(bars->pv_done), 1);
+        mbar_init(B_(bars->s_free), 256);
+        for (int i = 0; i < kPBufs; ++i) {
+            mbar_init(B_(bars->p_free[i]), 1);
+            mbar_init(B_(bars->p_full[i]), 1);   // the value CTA's expect-tx arrival
+            mbar_init(B_(bars->pv_done[i]), 1);
+            mbar_init(B_(bars->ri_read[i]), 256);
+        }
+        for (int i = 0; i < kOStages; ++i) {
+            mbar_init(B_(bars->oc_full[i]), 1);
+            mbar_init(B_(bars->oc_empty[i]), 1);
+        }
+        mbar_init(B_(bars->corr_done), 256);
         mbar_init(B_(bars->o_drained), 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -166,277 +340,483 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync_all();   // both CTAs' barriers exist before any remote arrival or copy
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    TR(const long long t_start = clock64();)
+    grid_launch_dependents();   // the merge may take SMs as clusters finish; it waits for the whole grid
 
-    const long long total = total_rows(p.lens, p.B, p.max_len, p.err, cta == 0 && threadIdx.x == 0);
-    const long long lo = share_lo(total, cta, G), hi = share_lo(total, cta + 1, G);
+    const long long total = total_rows(p.lens, p.B, p.max_len, p.err, cl == 0 && rank == 0 && threadIdx.x == 0);
     SegWalk walk;
-    walk.init(p.lens, p.B, p.max_len, lo, hi);
+    walk.init(p.lens, p.B, p.max_len, share_lo(total, cl, G), share_lo(total, cl + 1, G));
     int seq, k0, k1;
 
-    if (warp == 0 && lane == 0) {
-        // ---- producer: q_abs per segment, then ring units in consumption order
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_c);
-        uint32_t u = 0, nq = 0;
-        bool ok = true;
-        while (ok && walk.next(seq, k0, k1)) {
-            const int nblk = (k1 - k0 + kBN - 1) / kBN;
-            if (nq > 0 && !(ok = mbar_wait(B_(bars->q_free), (nq - 1) & 1, p.err, abort_flag))) break;
-            mbar_arrive_expect_tx(B_(bars->q_full), 8u * H * 128u);
-            for (int s = 0; s < 8; ++s) tma_load_3d(base + Q_OFF + s * kQSlab, &tm_q, B_(bars->q_full), s * 64, 0, seq);
-            ++nq;
-            for (int step = 0; ok && step <= nblk; ++step) {
-                for (int pass = 0; ok && pass < 2; ++pass) {
-                    const bool value = pass == 1;
-                    const int blk = value ? step - 1 : step;
-                    if (blk < 0 || blk >= nblk) continue;
-                    const int key = k0 + blk * kBN;
-                    for (int un = 0; un < 4; ++un, ++u) {
-                        const int st = u % kUnits;
-                        if (u >= kUnits &&
-                            !(ok = mbar_wait(B_(bars->u_empty[st]), ((u / kUnits) - 1) & 1, p.err, abort_flag)))
-                            break;
-                        mbar_arrive_expect_tx(B_(bars->u_full[st]), kUnit);
-                        for (int i = 0; i < 2; ++i)
-                            tma_load_3d(base + RING_OFF + st * kUnit + i * kSlab, &tm_c, B_(bars->u_full[st]),
-                                        (2 * un + i) * 64, key, seq);
+    if (warp < 4) {
+        regs_release<kRegsCtl>();
+        if (rank == 0) {
+            // =========================================================== score CTA
+            if (warp == 0 && lane == 0) {
+                // ---- TMA producer: c tiles [256 rows x 64 latent columns]; blocks ahead (and the next
+                // segment's absorbed query) are prefetched into L2 while this one streams in
+                tma_prefetch_desc(&tm_c256);
+                uint32_t it = 0;
+                bool ok = true;
+                BlockCursor pf;
+                pf.init(walk);
+                for (int i = 0; i < kPrefetchBlocks && pf.valid; ++i, pf.advance())
+                    for (int kc = 0; kc < 8; ++kc) tma_prefetch_l2_3d(&tm_c256, kc * 64, pf.key, pf.seq);
+                while (ok && walk.next(seq, k0, k1)) {
+                    const int nblk = (k1 - k0 + kBS - 1) / kBS;
+                    SegWalk nx = walk;
+                    int n_seq, n_k0, n_k1;
+                    const bool has_next = nx.next(n_seq, n_k0, n_k1);
+                    for (int j = 0; ok && j < nblk; ++j) {
+                        const int key = k0 + j * kBS;
+                        if (has_next && j + 2 >= nblk)   // the softmax loads it one to two blocks from now
+                            bulk_prefetch_l2(p.q_abs + static_cast<size_t>(n_seq) * H * kR, static_cast<uint32_t>(H) * kR * 2);
+                        if (pf.valid) {
+                            for (int kc = 0; kc < 8; ++kc) tma_prefetch_l2_3d(&tm_c256, kc * 64, pf.key, pf.seq);
+                            pf.advance();
+                        }
+                        for (int kc = 0; kc < 8; ++kc, ++it) {
+                            const int st = it % kSStages;
+                            TR(const long long _a = clock64();)
+                            if (it >= kSStages &&
+                                !(ok = mbar_wait(B_(bars->sc_empty[st]), ((it / kSStages) - 1) & 1, p.err, abort_flag)))
+                                break;
+                            TR(TR_ADD(DT_S_PROD_EMPTY, clock64() - _a);)
+                            mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSStage);
+                            tma_load_3d(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, key, seq);
+                        }
                     }
                 }
-            }
-        }
-        if (!ok) *abort_flag = 1;
-        for (uint32_t k = (u > kUnits ? u - kUnits : 0); k < u; ++k)
-            mbar_wait(B_(bars->u_full[k % kUnits]), (k / kUnits) & 1, p.err);
-        if (nq > 0) mbar_wait(B_(bars->q_full), (nq - 1) & 1, p.err);
-    } else if (warp == 1) {
-        // ---- MMA warp: lane 0 issues the tensor-core work; all 32 lanes wait on the
-        // ring and, in a sequence's last block, zero the cache rows at or past lens[b]
-        // in the value tiles (those rows may hold anything; p = 0 times them must stay 0)
-        const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);
-        const uint32_t idesc_o = make_idesc_bf16(128, Hp, 1, 0);
-        const bool leader = lane == 0;
-        uint32_t u = 0, nq = 0, ns = 0, np = 0, nseg = 0;
-        bool ok = true;
-        auto wait_all = [&](uint64_t &bar, uint32_t parity) {
-            return __all_sync(0xffffffffu, mbar_wait(B_(bar), parity, p.err, abort_flag));
-        };
-        while (ok && walk.next(seq, k0, k1)) {
-            const int nblk = (k1 - k0 + kBN - 1) / kBN;
-            const int len = clamp_len(__ldg(p.lens + seq), p.max_len);
-            if (!(ok = wait_all(bars->q_full, nq & 1))) break;
-            ++nq;
-            tc_fence_after();
-            for (int step = 0; ok && step <= nblk; ++step) {
-                if (step < nblk) {   // S = q_abs . c_blk^T
-                    if (ns > 0 && !(ok = wait_all(bars->s_free, (ns - 1) & 1))) break;
-                    tc_fence_after();
-                    for (int un = 0; ok && un < 4; ++un, ++u) {
-                        const int st = u % kUnits;
-                        if (!(ok = wait_all(bars->u_full[st], (u / kUnits) & 1))) break;
+                if (!ok) *abort_flag = 1;
+                // no load may still be landing when the CTA exits
+                for (uint32_t k = (it > kSStages ? it - kSStages : 0); k < it; ++k)
+                    mbar_wait(B_(bars->sc_full[k % kSStages]), (k / kSStages) & 1, p.err);
+            } else if (warp == 1 && lane == 0) {
+                // ---- MMA issuer: S = q_abs . c^T per 256-row block (q_abs from TMEM, N = 256)
+                uint32_t it = 0, jb = 0, nseg = 0;
+                bool ok = true;
+                TR(long long tl0 = clock64(), w_free = 0, w_full = 0, w_q = 0;)
+                while (ok && walk.next(seq, k0, k1)) {
+                    const int nblk = (k1 - k0 + kBS - 1) / kBS;
+                    TR(long long _q = clock64();)
+                    if (!(ok = mbar_wait(B_(bars->qabs_ready), nseg & 1, p.err, abort_flag))) break;
+                    TR(w_q += clock64() - _q; TL(13, jb, clock64() - t_start);)
+                    ++nseg;
+                    for (int j = 0; ok && j < nblk; ++j, ++jb) {
+                        TR(long long _a = clock64();)
+                        if (jb >= 1 && !(ok = mbar_wait(B_(bars->s_free), (jb - 1) & 1, p.err, abort_flag))) break;
+                        TR(w_free += clock64() - _a; TL(0, jb, clock64() - t_start); long long w_blk = 0;)
                         tc_fence_after();
-                        if (leader) {
-#pragma unroll
-                            for (int i = 0; i < 2; ++i) {
-                                const int kc = 2 * un + i;
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t a = make_smem_desc(base + Q_OFF + kc * kQSlab + kk * 32, 16, 1024);
-                                    const uint64_t bd =
-                                        make_smem_desc(base + RING_OFF + st * kUnit + i * kSlab + kk * 32, 16, 1024);
-                                    umma_bf16(tmem + S_COL, a, bd, idesc_s, (kc | kk) != 0);
-                                }
+                        for (int kc = 0; kc < 8; ++kc, ++it) {
+                            const int st = it % kSStages;
+                            TR(long long _b = clock64();)
+                            if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
+                            TR(w_full += clock64() - _b; w_blk += clock64() - _b;)
+                            tc_fence_after();
+    #pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
+                                umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
+                                                 (kc | kk) != 0);
                             }
-                            umma_commit(B_(bars->u_empty[st]));
+                            umma_commit(B_(bars->sc_empty[st]));
                         }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
-                    if (leader) {
+                        if (!ok) break;
                         umma_commit(B_(bars->s_full));
-                        if (step == nblk - 1) umma_commit(B_(bars->q_free));
+                        TR(TL(1, jb, clock64() - t_start); TL(7, jb, w_blk);)
                     }
-                    ++ns;
                 }
-                if (step >= 1) {   // O^T += c_blk^T . P^T for block step-1
-                    const int blk = step - 1;
-                    const int nvalid = len - (k0 + blk * kBN);   // rows of this block inside the sequence
-                    if (step == 1 && nseg > 0 &&   // the previous segment's O^T has been drained
-                        !(ok = wait_all(bars->o_drained, (nseg - 1) & 1)))
-                        break;
-                    if (!(ok = wait_all(bars->p_full, np & 1))) break;
-                    ++np;
-                    tc_fence_after();
-                    for (int rb = 0; ok && rb < 4; ++rb, ++u) {
-                        const int st = u % kUnits;
-                        if (!(ok = wait_all(bars->u_full[st], (u / kUnits) & 1))) break;
-                        if (nvalid < kBN) {
-                            for (int i = 0; i < 2; ++i) {
-                                const uint32_t tile = base + RING_OFF + st * kUnit + i * kSlab;
-                                for (int row = nvalid + lane; row < kBN; row += 32)
-#pragma unroll
-                                    for (int ch = 0; ch < 8; ++ch)
-                                        st_shared_v4(tile + (row >> 3) * 1024 + (row & 7) * 128 + ch * 16, 0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
+                TR(TR_ADD(DT_S_MMA_LOOP, clock64() - tl0); TR_ADD(DT_S_MMA_SFREE, w_free);
+                   TR_ADD(DT_S_MMA_SCFULL, w_full); TR_ADD(DT_S_MMA_QREADY, w_q);)
+                if (!ok) *abort_flag = 1;
+            }
+        } else {
+            // =========================================================== value CTA
+            if (warp == 0 && lane == 0) {
+                // ---- TMA producer: c tiles as the MN-major value operand, 2 x [128 rows x 256 latent columns] a unit
+                tma_prefetch_desc(&tm_c);
+                uint32_t it = 0;
+                bool ok = true;
+                while (ok && walk.next(seq, k0, k1)) {
+                    const int nunits = 2 * ((k1 - k0 + kBS - 1) / kBS);
+                    for (int u = 0; ok && u < nunits; ++u) {
+                        const int key = k0 + u * kBN;
+                        if (key >= k1) continue;   // a unit past the segment's end: nothing to load
+                        for (int nh = 0; nh < 2; ++nh, ++it) {
+                            const int st = it % kOStages;
+                            TR(const long long _a = clock64();)
+                            if (it >= kOStages &&
+                                !(ok = mbar_wait(B_(bars->oc_empty[st]), ((it / kOStages) - 1) & 1, p.err, abort_flag)))
+                                break;
+                            TR(TR_ADD(DT_O_PROD_EMPTY, clock64() - _a);)
+                            const uint32_t full = B_(bars->oc_full[st]);
+                            mbar_arrive_expect_tx(full, kOStage);
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                tma_load_3d(base + O_RING + st * kOStage + q4 * kSlab, &tm_c, full, (nh * 4 + q4) * 64, key,
+                                            seq);
                         }
-                        tc_fence_after();
-                        if (leader) {
-#pragma unroll
-                            for (int kk = 0; kk < kBN / 16; ++kk) {
-                                const uint64_t a =
-                                    make_smem_desc(base + RING_OFF + st * kUnit + kk * 2048, kSlab, 1024);
-                                const uint64_t bd =
-                                    make_smem_desc(base + P_OFF + (kk >> 2) * kPSlab + (kk & 3) * 32, 16, 1024);
-                                umma_bf16(tmem + O_COL + rb * Hp, a, bd, idesc_o, (blk > 0 || kk > 0));
-                            }
-                            umma_commit(B_(bars->u_empty[st]));
-                        }
-                        __syncwarp();
                     }
-                    if (!ok) break;
-                    if (leader) umma_commit(B_(bars->pv_done));
+                }
+                if (!ok) *abort_flag = 1;
+                for (uint32_t k = (it > kOStages ? it - kOStages : 0); k < it; ++k)
+                    mbar_wait(B_(bars->oc_full[k % kOStages]), (k / kOStages) & 1, p.err);
+            } else if (warp == 1) {
+                // ---- MMA warp: o_lat += P . c; lane 0 issues.  All lanes zero the cache rows at or past
+                // lens[b] in a sequence's last unit (those rows may hold anything; p = 0 times them must stay 0).
+                const bool leader = lane == 0;
+                auto wait_all = [&](uint64_t &bar, uint32_t parity, bool cluster) {
+                    return __all_sync(0xffffffffu, cluster ? mbar_wait<true>(B_(bar), parity, p.err, abort_flag)
+                                                           : mbar_wait(B_(bar), parity, p.err, abort_flag));
+                };
+                uint32_t it = 0, jj = 0, ncorr = 0, nseg = 0;
+                bool ok = true;
+                TR(long long tl0 = clock64(), w_pfull = 0, w_oc = 0, w_corr = 0, w_dr = 0;)
+                while (ok && walk.next(seq, k0, k1)) {
+                    const int nunits = 2 * ((k1 - k0 + kBS - 1) / kBS);
+                    const int len = clamp_len(__ldg(p.lens + seq), p.max_len);
+                    for (int u = 0; ok && u < nunits; ++u, ++jj) {
+                        const uint32_t pb = jj % kPBufs;
+                        TR(long long _a = clock64();)
+                        if (leader) mbar_arrive_expect_tx(B_(bars->p_full[pb]), 2u * H * 128u + kRowInfoBytes);
+                        if (!(ok = wait_all(bars->p_full[pb], (jj / kPBufs) & 1, true))) break;
+                        TR(w_pfull += clock64() - _a; if (leader) TL(8, jj, clock64() - t_start); long long w_u = 0;)
+                        if (u == 0 && nseg > 0) {   // the previous segment's o_lat has been drained
+                            TR(long long _d = clock64();)
+                            if (!(ok = wait_all(bars->o_drained, (nseg - 1) & 1, false))) break;
+                            TR(w_dr += clock64() - _d;)
+                        }
+                        // any head whose maximum grew needs o_lat rescaled before this unit's product
+                        const uint32_t ri = base + O_ROWINFO + pb * kRowInfoBytes;
+                        bool grew = false;
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k) grew |= ld_shared_f32(ri + (lane + 32 * k) * 8) != 1.f;
+                        if (u > 0 && __any_sync(0xffffffffu, grew)) {
+                            TR(long long _c = clock64();)
+                            if (!(ok = wait_all(bars->corr_done, ncorr & 1, false))) break;
+                            TR(w_corr += clock64() - _c;)
+                            ++ncorr;
+                        }
+                        const int key = k0 + u * kBN;
+                        if (key < k1) {
+                            const int nvalid = len - key;   // >= 1: rows of this unit inside the sequence
+                            for (int nh = 0; ok && nh < 2; ++nh, ++it) {
+                                const int st = it % kOStages;
+                                TR(long long _o = clock64();)
+                                if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
+                                TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
+                                if (nvalid < kBN) {
+                                    for (int sl = 0; sl < 4; ++sl) {
+                                        const uint32_t tile = base + O_RING + st * kOStage + sl * kSlab;
+                                        for (int r = nvalid + lane; r < kBN; r += 32)
+    #pragma unroll
+                                            for (int ch = 0; ch < 8; ++ch)
+                                                st_shared_v4(tile + (r >> 3) * 1024 + (r & 7) * 128 + ch * 16, 0, 0, 0, 0);
+                                    }
+                                    fence_proxy_async_smem();
+                                    __syncwarp();
+                                }
+                                tc_fence_after();
+                                if (leader) {
+    #pragma unroll
+                                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                                        const uint64_t a = make_smem_desc(
+                                            base + O_P + pb * kPBytes + (kk >> 2) * kPSlab + (kk & 3) * 32, 16, 1024);
+                                        const uint64_t bd =
+                                            make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
+                                        umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (u > 0 || kk > 0));
+                                    }
+                                    umma_commit(B_(bars->oc_empty[st]));
+                                }
+                                __syncwarp();
+                            }
+                            if (!ok) break;
+                        }
+                        if (leader) umma_commit(B_(bars->pv_done[pb]));
+                        TR(if (leader) { TL(9, jj, clock64() - t_start); TL(10, jj, w_u); })
+                    }
+                    ++nseg;
+                }
+                TR(if (leader) {
+                    TR_ADD(DT_O_MMA_LOOP, clock64() - tl0); TR_ADD(DT_O_MMA_PFULL, w_pfull); TR_ADD(DT_O_MMA_OCFULL, w_oc);
+                    TR_ADD(DT_O_MMA_CORR, w_corr); TR_ADD(DT_O_MMA_DRAINED, w_dr); TR_ADD(DT_CORRECTIONS, ncorr);
+                    TR_ADD(DT_SEGMENTS, nseg);
+                    if (cl < 512) g_dclu[1][cl] = nseg;
+                })
+                if (!ok && leader) *abort_flag = 1;
+            } else if (warp == 2 && lane == 0) {
+                // ---- relay: P buffer pb is free again once its product completed and its row info was read
+                uint32_t jj = 0;
+                bool ok = true;
+                while (ok && walk.next(seq, k0, k1)) {
+                    const int nunits = 2 * ((k1 - k0 + kBS - 1) / kBS);
+                    for (int u = 0; u < nunits; ++u, ++jj) {
+                        const uint32_t pb = jj % kPBufs;
+                        if (!mbar_wait(B_(bars->pv_done[pb]), (jj / kPBufs) & 1, p.err, abort_flag) ||
+                            !mbar_wait(B_(bars->ri_read[pb]), (jj / kPBufs) & 1, p.err, abort_flag)) {
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(B_(bars->p_free[pb]), 0);
+                        TR(TL(11, jj, clock64() - t_start);)
+                    }
                 }
             }
-            ++nseg;
         }
-        if (!ok && leader) *abort_flag = 1;
-    } else if (warp >= 4) {
-        // ---- softmax (thread = head row of S) / correction and drain (thread = TMEM lane of O^T)
-        const int tid = threadIdx.x - 128;
-        const uint32_t tq = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const bool head = tid < H;
-        uint32_t ns = 0, npv = 0, nseg = 0;
-        bool ok = true;
-        const int slot_base = cta;   // segment slot = cta + sequence index
-        while (ok && walk.next(seq, k0, k1)) {
-            const int nblk = (k1 - k0 + kBN - 1) / kBN;
-            float m_run = -INFINITY, l_run = 0.f;
-            for (int j = 0; j < nblk; ++j) {
-                bool fail = !mbar_wait(B_(bars->s_full), ns & 1, p.err, abort_flag);
-                if (named_bar_or(1, 128, fail)) { ok = false; break; }
-                ++ns;
-                tc_fence_after();
-                float s[4][32];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(tmem + tq + S_COL + c4 * 32, s[c4]);
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(B_(bars->s_free));
-
-                const int lim = k1 - (k0 + j * kBN);   // columns < lim are inside the segment
-                float factor = 1.f;
-                if (head) {
-                    float mx = -INFINITY;
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            s[c4][i] = c4 * 32 + i < lim ? s[c4][i] * p.qk_scale_log2 : -INFINITY;
-                            mx = fmaxf(mx, s[c4][i]);
+    } else {
+        regs_acquire<kRegsMath>();
+        if (rank == 0) {
+            // ---- softmax: warpgroup `wg` owns rows [128 wg, 128 wg + 128) of each 256-row block, i.e. the
+            // value CTA's unit 2j + wg; thread `row` owns TMEM lane `row`, which is head `row`
+            const int wg = (warp - 4) >> 2;
+            const int row = (warp & 3) * 32 + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const bool head = row < H;
+            const uint32_t ptile = base + S_PST + wg * kPUnit;
+            const uint32_t ri = ptile + kPBytes;
+            const float c_log2 = p.qk_scale_log2;
+            uint32_t jb = 0;
+            bool ok = true, fail = false;
+            TR(long long tl0 = clock64(), w_sfull = 0, w_xbar = 0, w_pfree = 0, w_q = 0;)
+            // q_abs[sq] -> TMEM columns 0-255: a head's packed bf16 pairs are its row's 32-bit words in
+            // memory order.  Warpgroup wg owns latent columns [256 wg, 256 wg + 256); its loads are all
+            // issued at once, and the stores wait until the previous segment's score products completed.
+            bool first = true;
+            while (ok && walk.next(seq, k0, k1)) {
+                const int nblk = (k1 - k0 + kBS - 1) / kBS;
+                if (first) {   // later segments' queries are stored during the previous segment's last block
+                    TR(long long _q = clock64();)
+                    uint4 v[16], v2[16];
+                    q_issue(p.q_abs, seq, H, row, head, wg, 0, v);
+                    q_issue(p.q_abs, seq, H, row, head, wg, 1, v2);
+                    q_store(trow, wg, 0, v);
+                    q_store(trow, wg, 1, v2);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    named_bar_sync(1, 256);
+                    if (threadIdx.x == 128) mbar_arrive(B_(bars->qabs_ready));
+                    first = false;
+                    TR(w_q += clock64() - _q;)
+                }
+                float m_run = -INFINITY, l_part = 0.f;
+                for (int j = 0; j < nblk; ++j, ++jb) {
+                    // in the segment's last block the next segment's query goes into TMEM as soon as this
+                    // block's score products have completed, so its first products overlap this softmax
+                    bool q_next = false;
+                    int n_seq = 0;
+                    if (j == nblk - 1) {
+                        SegWalk nx = walk;
+                        int n_k0, n_k1;
+                        q_next = nx.next(n_seq, n_k0, n_k1);
+                    }
+                    TR(long long _a = clock64();)
+                    if (q_next) {
+                        uint4 qv[16];   // half the query rides across the wait (registers allow no more)
+                        q_issue(p.q_abs, n_seq, H, row, head, wg, 0, qv);
+                        fail = fail || !mbar_wait(B_(bars->s_full), jb & 1, p.err, abort_flag);
+                        if (!fail) {
+                            tc_fence_after();
+                            q_store(trow, wg, 0, qv);
+                            q_issue(p.q_abs, n_seq, H, row, head, wg, 1, qv);
+                            q_store(trow, wg, 1, qv);
+                            tmem_wait_st();
                         }
+                    } else {
+                        fail = fail || !mbar_wait(B_(bars->s_full), jb & 1, p.err, abort_flag);
+                    }
+                    TR(w_sfull += clock64() - _a; if ((threadIdx.x & 127) == 0) TL(2 + 3 * wg, jb, clock64() - t_start);)
+                    float s[4][32];
+                    const int lim = k1 - (k0 + j * kBS + wg * 128);   // columns < lim are inside the segment
+                    if (!fail) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_SCOL + wg * 128 + c4 * 32, s[c4]);
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        mbar_arrive(B_(bars->s_free));
+                        // rows at or past the segment's end are masked (only the segment's last block has
+                        // any).  The scale multiplies inside the exponent: max(c s) = c max(s) for c >= 0,
+                        // c min(s) otherwise.  Padding heads (q_abs = 0) compute finite values nobody reads.
+                        if (lim < 128) {
+                            const float fill = c_log2 >= 0.f ? -INFINITY : INFINITY;
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (c4 * 32 + i >= lim) s[c4][i] = fill;
+                        }
+                        const float mraw = c_log2 >= 0.f ? max128(s) : min128(s);
+                        st_shared_f32(base + PMAX + ((jb & 1) * 2 + wg) * 512 + row * 4,
+                                      fabsf(mraw) == INFINITY ? -INFINITY : c_log2 * mraw);
+                    }
+                    TR(long long _x = clock64();)
+                    if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
+                    TR(w_xbar += clock64() - _x; if (threadIdx.x == 128) TL(3, jb, clock64() - t_start);)
+                    if (q_next && threadIdx.x == 128) {
+                        mbar_arrive(B_(bars->qabs_ready));
+                        TR(TL(12, jb, clock64() - t_start);)
+                    }
+                    const float mx = fmaxf(ld_shared_f32(base + PMAX + ((jb & 1) * 2 + 0) * 512 + row * 4),
+                                           ld_shared_f32(base + PMAX + ((jb & 1) * 2 + 1) * 512 + row * 4));
+                    float factor = 1.f;
                     if (mx > m_run + kRescaleLog2) {
                         factor = fast_exp2(m_run - mx);
                         m_run = mx;
                     }
-                    float sum = 0.f;
+                    const float neg_m = -m_run;
+                    if (lim < 128) {
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
+                        for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            s[c4][i] = fast_exp2(s[c4][i] - m_run);
-                            sum += s[c4][i];
-                        }
-                    l_run = l_run * factor + sum;
-                } else {
+                            for (int i = 0; i < 32; ++i)
+                                s[c4][i] = c4 * 32 + i < lim ? fast_exp2(fmaf(s[c4][i], c_log2, neg_m)) : 0.f;
+                    } else {
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4)
+                        for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) s[c4][i] = 0.f;
-                }
-                // P^T and O^T are free once the previous block's value product completed
-                if (j > 0) {
-                    fail = !mbar_wait(B_(bars->pv_done), npv & 1, p.err, abort_flag);
-                    ++npv;
-                }
-                fac[tid] = factor;
-                if (named_bar_or(1, 128, fail)) { ok = false; break; }
-                const bool any = named_bar_or(1, 128, j > 0 && factor != 1.f);
-                if (any) {   // rescale columns h of O^T by fac[h]
-                    tc_fence_after();
-                    for (int rb = 0; rb < 4; ++rb)
-                        for (int hc = 0; hc < Hp / 16; ++hc) {
-                            float v[16];
-                            const uint32_t ta = tmem + tq + O_COL + rb * Hp + hc * 16;
-                            tmem_ld16(ta, v);
-                            tmem_wait_ld();
+                            for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(fmaf(s[c4][i], c_log2, neg_m));
+                    }
+                    l_part = l_part * factor + sum128(s);
+
+                    // the staging unit is free once this warpgroup's previous copy has read it
+                    if ((threadIdx.x & 127) == 0) bulk_wait_read_all();
+                    named_bar_sync(2 + wg, 128);
+                    if (head)
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) v[i] *= fac[hc * 16 + i];
-                            tmem_st16(ta, v);
-                        }
-                    tmem_wait_st();
-                    tc_fence_before();
-                }
-                if (tid < Hp) {   // P^T row `tid` (zeros for padding heads)
+                        for (int c4 = 0; c4 < 4; ++c4)
 #pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) {
-                        const uint32_t slab = base + P_OFF + (c4 >> 1) * kPSlab;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const float *v = &s[c4][8 * k];
-                            st_shared_v4(slab + sw128_offset(tid, (c4 & 1) * 4 + k), pack_bf16x2(v[0], v[1]),
-                                         pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                            for (int k = 0; k < 4; ++k) {
+                                const float *v = &s[c4][8 * k];
+                                st_shared_v4(ptile + (c4 >> 1) * kPSlab + sw128_offset(row, (c4 & 1) * 4 + k),
+                                             pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                            }
+                    // unit 2j carries the block's rescale factor; unit 2j+1 shares its maximum (factor 1)
+                    st_shared_v2f(ri + row * 8, wg == 0 ? factor : 1.f, l_part);
+                    fence_proxy_async_smem();
+                    named_bar_sync(2 + wg, 128);
+                    if ((threadIdx.x & 127) == 0) {
+                        // unit u = 2 jb + wg goes to the value CTA's P buffer u mod 3, free once the product
+                        // of unit u - 3 completed
+                        const uint32_t u = 2 * jb + wg, pb = u % kPBufs;
+                        TR(long long _f = clock64();)
+                        if (u >= kPBufs)
+                            fail = !mbar_wait<true>(B_(bars->p_free[pb]), (u / kPBufs - 1) & 1, p.err, abort_flag);
+                        TR(w_pfree += clock64() - _f;)
+                        if (!fail) {
+                            const uint32_t p_rows_bytes = static_cast<uint32_t>(H) * 128;
+                            const uint32_t dst_bar = mapa_shared(B_(bars->p_full[pb]), 1);
+                            const uint32_t dst = mapa_shared(base + O_P + pb * kPBytes, 1);
+                            bulk_copy_s2cluster(dst, ptile, p_rows_bytes, dst_bar);
+                            bulk_copy_s2cluster(dst + kPSlab, ptile + kPSlab, p_rows_bytes, dst_bar);
+                            bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + pb * kRowInfoBytes, 1), ri,
+                                                kRowInfoBytes, dst_bar);
+                            bulk_commit_group();
+                            TR(TL(wg == 0 ? 4 : 6, jb, clock64() - t_start);)
                         }
                     }
                 }
-                fence_proxy_async_smem();
-                named_bar_sync(1, 128);
-                if (tid == 0) mbar_arrive(B_(bars->p_full));
+                if (!ok) break;
+                if (wg == 0 && head) p.ws_m[static_cast<size_t>(cl + seq) * H + row] = m_run;
             }
-            if (!ok) break;
-            // segment end: drain O^T and (m, l) into the workspace slot
-            bool fail = !mbar_wait(B_(bars->pv_done), npv & 1, p.err, abort_flag);
-            ++npv;
-            if (named_bar_or(1, 128, fail)) { ok = false; break; }
-            tc_fence_after();
-            const size_t slot = static_cast<size_t>(slot_base + seq);
-            float *wo = p.ws_o + slot * H * kR;
-            for (int rb = 0; rb < 4; ++rb)
-                for (int hc = 0; hc < Hp / 16; ++hc) {
-                    float v[16];
-                    tmem_ld16(tmem + tq + O_COL + rb * Hp + hc * 16, v);
+            TR(if (threadIdx.x == 128) {
+                TR_ADD(DT_S_SM_LOOP, clock64() - tl0); TR_ADD(DT_S_SM_SFULL, w_sfull); TR_ADD(DT_S_SM_XBAR, w_xbar);
+                TR_ADD(DT_S_SM_PFREE, w_pfree); TR_ADD(DT_S_SM_QLOAD, w_q); TR_ADD(DT_BLOCKS, jb);
+            })
+            if ((threadIdx.x & 127) == 0) bulk_wait_all();
+            if (!ok || fail) *abort_flag = 1;
+        } else {
+            // ---- correction + drain: thread `row` of warpgroup `wg` owns TMEM lane `row` (head `row`),
+            // latent columns [256 wg, 256 wg + 256)
+            const int wg = (warp - 4) >> 2;
+            const int row = (warp & 3) * 32 + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const bool head = row < H;
+            uint32_t jj = 0;
+            bool ok = true, fail;
+            TR(long long tl0 = clock64(), w_drain = 0;)
+            while (ok && walk.next(seq, k0, k1)) {
+                const int nunits = 2 * ((k1 - k0 + kBS - 1) / kBS);
+                float l_even = 0.f, l_odd = 0.f;
+                for (int u = 0; u < nunits; ++u, ++jj) {
+                    const uint32_t pb = jj % kPBufs;
+                    fail = !mbar_wait<true>(B_(bars->p_full[pb]), (jj / kPBufs) & 1, p.err, abort_flag);
+                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                    const float2 fl = ld_shared_v2f(base + O_ROWINFO + pb * kRowInfoBytes + row * 8);
+                    mbar_arrive(B_(bars->ri_read[pb]));
+                    // the two warpgroups of the score CTA keep separate sums (even and odd units)
+                    if (u & 1)
+                        l_odd = fl.y;
+                    else
+                        l_even = fl.y;
+                    if (named_bar_or(4, 256, u > 0 && fl.x != 1.f)) {
+                        const uint32_t prev = jj - 1;
+                        fail = !mbar_wait(B_(bars->pv_done[prev % kPBufs]), (prev / kPBufs) & 1, p.err, abort_flag);
+                        if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                        tc_fence_after();
+                        if (__any_sync(0xffffffffu, fl.x != 1.f)) {
+#pragma unroll 1
+                            for (int cc = 0; cc < 8; ++cc) {
+                                float v[32];
+                                const uint32_t ta = trow + wg * 256 + cc * 32;
+                                tmem_ld32(ta, v);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) v[i] *= fl.x;
+                                tmem_st32(ta, v);
+                            }
+                            tmem_wait_st();
+                        }
+                        tc_fence_before();
+                        mbar_arrive(B_(bars->corr_done));
+                    }
+                }
+                if (!ok) break;
+                // segment end: o_lat (unnormalised) and the sum into the workspace slot
+                TR(long long _d = clock64();)
+                const uint32_t last = jj - 1;
+                fail = !mbar_wait(B_(bars->pv_done[last % kPBufs]), (last / kPBufs) & 1, p.err, abort_flag);
+                if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                tc_fence_after();
+                const size_t slot = static_cast<size_t>(cl + seq);
+                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * H + (head ? row : 0)) * kR + wg * 256);
+#pragma unroll 1
+                for (int cc = 0; cc < 8; ++cc) {
+                    float v[32];
+                    tmem_ld32(trow + wg * 256 + cc * 32, v);
                     tmem_wait_ld();
+                    if (head)
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int h = hc * 16 + i;
-                        if (h < H) wo[static_cast<size_t>(h) * kR + rb * 128 + tid] = v[i];
-                    }
+                        for (int q = 0; q < 8; ++q)
+                            dst[cc * 8 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
-            if (head) {
-                p.ws_m[slot * H + tid] = m_run;
-                p.ws_l[slot * H + tid] = l_run;
+                if (wg == 0 && head) p.ws_l[slot * H + row] = l_even + l_odd;
+                tc_fence_before();
+                named_bar_sync(4, 256);
+                if (threadIdx.x == 128) mbar_arrive(B_(bars->o_drained));
+                TR(w_drain += clock64() - _d;)
             }
-            tc_fence_before();
-            named_bar_sync(1, 128);
-            if (tid == 0) mbar_arrive(B_(bars->o_drained));
-            ++nseg;
+            TR(if (threadIdx.x == 128) { TR_ADD(DT_O_COR_LOOP, clock64() - tl0); TR_ADD(DT_O_DRAIN, w_drain); })
+            if (!ok) *abort_flag = 1;
         }
-        if (!ok) *abort_flag = 1;
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    TR(if (threadIdx.x == 0) TR_ADD(rank == 0 ? DT_S_TOTAL : DT_O_TOTAL, clock64() - t_start);
+       if (threadIdx.x == 0 && rank == 1 && cl < 512) g_dclu[0][cl] = clock64() - t_start;)
     if (warp == 1) tmem_dealloc(tmem, 512);
+    cluster_sync_all();   // the partner no longer touches this CTA's shared memory or barriers
 }
 
 // ----------------------------------------------------------------------------- merge
-constexpr int kMRows = 64;                          // sequences per merge CTA
+constexpr int kMRows = 32;                          // sequences per merge CTA
 constexpr int kMergeThreads = 512;
-constexpr uint32_t kASlab = kMRows * 128;           // o_lat tile [64 rows x 64 latent columns]
+constexpr uint32_t kASlab = kMRows * 128;           // o_lat tile [32 rows x 64 latent columns]
 constexpr uint32_t MA_OFF = 0;
 constexpr uint32_t MA_BYTES = 7 * kASlab + kSlab;   // an M=128 operand read of the last slab stays inside
 constexpr uint32_t MW_OFF = MA_BYTES;               // W_UV[h]: 8 tiles [128 x 64]
@@ -467,6 +847,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, b0 = blockIdx.y * kMRows;
     const int H = p.H;
+    TR(const long long mt0 = clock64();)
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(w_full), 1);
@@ -485,19 +866,25 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
         tma_prefetch_desc(&tm_wuv);
         mbar_arrive_expect_tx(smem_u32(w_full), 8 * kSlab);
         for (int s = 0; s < 8; ++s) tma_load_2d(base + MW_OFF + s * kSlab, &tm_wuv, smem_u32(w_full), s * 64, h * kDV);
-        // row offsets of this CTA's sequences in the concatenated cache
+        // virtual row offsets of this CTA's sequences (the split kernel's work axis)
         long long total = 0;
         for (int b = 0; b < p.B; ++b) {
             const int x = __ldg(p.lens + b);
             if (x < 0 || x > p.max_len) record_error(p.err, kDevErrBounds);
             if (b >= b0 && b <= b0 + kMRows) s_pre[b - b0] = total;
-            total += clamp_len(x, p.max_len);
+            const int len = clamp_len(x, p.max_len);
+            if (len > 0) total += kSeqOverhead + len;
         }
         for (int b = max(p.B, b0); b <= b0 + kMRows; ++b) s_pre[b - b0] = total;
         s_total = total;
     }
     __syncthreads();
     const long long total = s_total;
+    // launched as a programmatic dependent of the split kernel: everything above overlapped its
+    // tail; its workspace writes are complete and visible after this
+    MT(0);
+    grid_dependency_wait();
+    MT(1);
 
     // log-sum-exp combine of the segments of each sequence; o_lat -> bf16 tile row.
     // A warp takes a row at a time: lane i fetches segment i's (m, l), the warp
@@ -508,7 +895,8 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
         float o[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) o[k] = 0.f;
-        const long long r0 = s_pre[i], r1 = s_pre[i + 1];
+        // the sequence's cache rows on the virtual axis (none for an empty sequence)
+        const long long r0 = s_pre[i] + kSeqOverhead, r1 = s_pre[i + 1];
         if (b < p.B && r1 > r0) {
             const int G = p.G;
             const int c_first = min(static_cast<int>(((r0 + 1) * G - 1) / total), G - 1);
@@ -566,8 +954,10 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    MT(2);
     if (threadIdx.x == 0) {
         if (mbar_wait(smem_u32(w_full), 0, p.err)) {
+            MT(3);
             tc_fence_after();
             const uint32_t idesc = make_idesc_bf16(128, kDV, 0, 0);
 #pragma unroll 1
@@ -582,7 +972,9 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     __syncwarp();
     const bool done = mbar_wait(smem_u32(mma_done), 0, p.err);
     tc_fence_after();
-    if (warp < 2 && __all_sync(0xffffffffu, done)) {
+    MT(4);
+    static_assert(kMRows % 32 == 0, "epilogue warps own 32 rows each");
+    if (warp < kMRows / 32 && __all_sync(0xffffffffu, done)) {
         const int i = warp * 32 + lane;
         const int b = b0 + i;
         const size_t off = (static_cast<size_t>(b) * H + h) * kDV;
@@ -615,6 +1007,7 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    MT(5);
     if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
@@ -669,35 +1062,99 @@ cudaError_t decode_noalloc_scratch(void **ptr) {
     return cudaSuccess;
 }
 
+
 bool decode_bf16_supports(int H, int d_v, int r) { return r == kR && d_v == kDV && H >= 1 && H <= kHMax; }
+
+namespace {
+// Clusters of the pair kernel that run at once on this device, at most one per
+// two SMs (a GPC with an odd SM count leaves one SM out).  Queried once per device.
+int pair_clusters(int num_sms) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> cached[kMaxDev];
+    const int cap = num_sms / 2 > 0 ? num_sms / 2 : 1;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) dev = -1;
+    if (dev >= 0) {
+        const int v = cached[dev].load();
+        if (v > 0) return v < cap ? v : cap;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * cap);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemPair;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        n = cap;
+    }
+    if (n > cap) n = cap;
+    if (dev >= 0) cached[dev].store(n);
+    return n;
+}
+}  // namespace
 
 size_t decode_bf16_workspace_bytes(int B, int H, int r, int, int num_sms) {
     if (r != kR || H < 1 || H > kHMax || B < 1 || num_sms < 1) return 0;
-    const size_t slots = slot_count(B, num_sms);
+    const size_t slots = slot_count(B, num_sms / 2 > 0 ? num_sms / 2 : 1);
     return slots * static_cast<size_t>(H) * (kR + 2) * sizeof(float);
 }
 
+#ifdef MLA_TRACE
+// Diagnostic build only: copy (and optionally clear) the decode wait-accounting slots.
+extern "C" __attribute__((visibility("default"))) int mla_debug_decode_trace(unsigned long long *host, int n,
+                                                                               int clear) {
+    if (n > DT_COUNT) n = DT_COUNT;
+    if (cudaMemcpyFromSymbol(host, g_dtrace, n * sizeof(unsigned long long)) != cudaSuccess) return -1;
+    if (clear) {
+        static const unsigned long long zeros[DT_COUNT] = {};
+        if (cudaMemcpyToSymbol(g_dtrace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
+    }
+    return n;
+}
+// Diagnostic build only: copy the per-block event times of the traced cluster.
+extern "C" __attribute__((visibility("default"))) int mla_debug_decode_timeline(long long *host) {
+    if (cudaMemcpyFromSymbol(host, g_dtl, sizeof(g_dtl)) != cudaSuccess) return -1;
+    return kTLEvents * kTLMax;
+}
+extern "C" __attribute__((visibility("default"))) int mla_debug_decode_merge(long long *host) {
+    if (cudaMemcpyFromSymbol(host, g_mtrace, sizeof(g_mtrace)) != cudaSuccess) return -1;
+    return 6 * 1024;
+}
+extern "C" __attribute__((visibility("default"))) int mla_debug_decode_clusters(long long *host) {
+    if (cudaMemcpyFromSymbol(host, g_dclu, sizeof(g_dclu)) != cudaSuccess) return -1;
+    return 1024;
+}
+#endif
+
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     if (!decode_bf16_supports(a.H, a.d_v, a.r)) return cudaErrorInvalidValue;
-    const int G = a.num_sms;
+    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemPair));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemMerge));
+    if (e != cudaSuccess) return e;
+    {   // the kernel's register split assumes this launch budget
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, decode_pair_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
+    }
+    const int G = pair_clusters(a.num_sms);
     const size_t slots = slot_count(a.B, G);
+    if (slots * static_cast<size_t>(a.H) * (kR + 2) * sizeof(float) > a.workspace_bytes) return cudaErrorInvalidValue;
     float *ws_o = static_cast<float *>(a.workspace);
     float *ws_m = ws_o + slots * a.H * kR;
     float *ws_l = ws_m + slots * a.H;
-    CUtensorMap tm_q, tm_c, tm_wuv;
+    CUtensorMap tm_c256, tm_c, tm_wuv;
     {
-        const cuuint64_t dims[3] = {kR, static_cast<cuuint64_t>(a.H), static_cast<cuuint64_t>(a.B)};
-        const cuuint64_t strides[2] = {kR * 2, static_cast<cuuint64_t>(a.H) * kR * 2};
-        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a.H), 1};
-        if (encode_map(&tm_q, a.q_abs, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    }
-    {
-        const cuuint64_t dims[3] = {kR, static_cast<cuuint64_t>(a.max_len > 0 ? a.max_len : 1),
-                                    static_cast<cuuint64_t>(a.B)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_cache) * 2,
-                                       static_cast<cuuint64_t>(a.max_len > 0 ? a.max_len : 1) * a.ld_cache * 2};
-        const cuuint32_t box[3] = {64, kBN, 1};
-        if (encode_map(&tm_c, a.c_cache, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint64_t rows = static_cast<cuuint64_t>(a.max_len > 0 ? a.max_len : 1);
+        const cuuint64_t dims[3] = {kR, rows, static_cast<cuuint64_t>(a.B)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_cache) * 2, rows * a.ld_cache * 2};
+        const cuuint32_t box256[3] = {64, kBS, 1};
+        if (encode_map(&tm_c256, a.c_cache, 3, dims, strides, box256) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint32_t box128[3] = {64, kBN, 1};
+        if (encode_map(&tm_c, a.c_cache, 3, dims, strides, box128) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[2] = {kR, static_cast<cuuint64_t>(a.H) * kDV};
@@ -705,24 +1162,18 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
         const cuuint32_t box[2] = {64, kDV};
         if (encode_map(&tm_wuv, a.w_uv, 2, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    SplitParams sp;
-    sp.lens = a.lens;
-    sp.ws_o = ws_o;
-    sp.ws_m = ws_m;
-    sp.ws_l = ws_l;
-    sp.err = a.dev_err;
-    sp.B = a.B;
-    sp.H = a.H;
-    sp.Hp = (a.H + 15) / 16 * 16;
-    sp.max_len = a.max_len;
-    sp.qk_scale_log2 = a.scale * kLog2e;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemSplit));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemMerge));
-    if (e != cudaSuccess) return e;
-    decode_split_kernel<<<G, kThreads, kSmemSplit, s>>>(tm_q, tm_c, sp);
+    PairParams pp;
+    pp.lens = a.lens;
+    pp.q_abs = static_cast<const __nv_bfloat16 *>(a.q_abs);
+    pp.ws_o = ws_o;
+    pp.ws_m = ws_m;
+    pp.ws_l = ws_l;
+    pp.err = a.dev_err;
+    pp.B = a.B;
+    pp.H = a.H;
+    pp.max_len = a.max_len;
+    pp.qk_scale_log2 = a.scale * kLog2e;
+    decode_pair_kernel<<<2 * G, kThreads, kSmemPair, s>>>(tm_c256, tm_c, pp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     MergeParams mp;
@@ -737,9 +1188,17 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     mp.H = a.H;
     mp.max_len = a.max_len;
     mp.G = G;
-    const dim3 grid(a.H, (a.B + kMRows - 1) / kMRows);
-    decode_merge_kernel<<<grid, kMergeThreads, kSmemMerge, s>>>(tm_wuv, mp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.H, (a.B + kMRows - 1) / kMRows);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = kSmemMerge;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel, tm_wuv, mp);
 }
 
 }  // namespace mla
