@@ -151,6 +151,36 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *ptr, uint32_t bytes
                  : "memory");
 }
 
+// L2 cache policies for the .L2::cache_hint forms: lines filled or touched
+// with evict_first leave L2 before normal lines; evict_last ones stay longer.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_3d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int x, int y, int z,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(policy)
+        : "memory");
+}
+
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_v4_hint(float4 *ptr, float4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+
 // Make this thread's generic-proxy smem writes visible to the async proxy
 // (tensor core / TMA reads that follow a barrier).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -359,6 +359,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 // ---- TMA producer: c tiles [256 rows x 64 latent columns]; blocks ahead (and the next
                 // segment's absorbed query) are prefetched into L2 while this one streams in
                 tma_prefetch_desc(&tm_c256);
+                const uint64_t keep = l2_policy_evict_last();   // the value CTA reads these rows again
                 uint32_t it = 0;
                 bool ok = true;
                 BlockCursor pf;
@@ -386,7 +387,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 break;
                             TR(TR_ADD(DT_S_PROD_EMPTY, clock64() - _a);)
                             mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSStage);
-                            tma_load_3d(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, key, seq);
+                            tma_load_3d_hint(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, key,
+                                             seq, keep);
                         }
                     }
                 }
@@ -438,6 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (warp == 0 && lane == 0) {
                 // ---- TMA producer: c tiles as the MN-major value operand, 2 x [128 rows x 256 latent columns] a unit
                 tma_prefetch_desc(&tm_c);
+                const uint64_t done_with = l2_policy_evict_first();   // the last read of these rows
                 uint32_t it = 0;
                 bool ok = true;
                 while (ok && walk.next(seq, k0, k1)) {
@@ -455,8 +458,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const uint32_t full = B_(bars->oc_full[st]);
                             mbar_arrive_expect_tx(full, kOStage);
                             for (int q4 = 0; q4 < 4; ++q4)
-                                tma_load_3d(base + O_RING + st * kOStage + q4 * kSlab, &tm_c, full, (nh * 4 + q4) * 64, key,
-                                            seq);
+                                tma_load_3d_hint(base + O_RING + st * kOStage + q4 * kSlab, &tm_c, full,
+                                                 (nh * 4 + q4) * 64, key, seq, done_with);
                         }
                     }
                 }
@@ -783,6 +786,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const size_t slot = static_cast<size_t>(cl + seq);
                 float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * H + (head ? row : 0)) * kR + wg * 256);
+                const uint64_t ws_keep = l2_policy_evict_last();   // the merge reads it right after this kernel
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
                     float v[32];
@@ -791,7 +795,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (head)
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            dst[cc * 8 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                            st_global_v4_hint(dst + cc * 8 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
+                                              ws_keep);
                 }
                 if (wg == 0 && head) p.ws_l[slot * H + row] = l_even + l_odd;
                 tc_fence_before();
