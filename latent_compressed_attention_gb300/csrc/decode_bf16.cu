@@ -795,8 +795,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (head)
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            st_global_v4_hint(dst + cc * 8 + q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]),
-                                              ws_keep);
+                            st_global_v4_hint(dst + cc * 8 + q,
+                                              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]), ws_keep);
                 }
                 if (wg == 0 && head) p.ws_l[slot * H + row] = l_even + l_odd;
                 tc_fence_before();
