@@ -19,6 +19,7 @@ rank runs its own replica (the path needs no exchange: weak scaling).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -295,7 +296,7 @@ def run_decode(torch, lca, dev, stream, flush, args, pk):
     gbs = cache_bytes / (ms * 1e-3) / 1e9
     return {"workload": DECODE.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "cache_bytes_per_step": cache_bytes, "sum_lens": int(d["lens_np"].sum()),
-            "roofline": {"kernel": "decode (split + merge)", "bound": "hbm", "achieved": round(gbs, 1),
+            "roofline": {"kernel": "decode (pair + merge)", "bound": "hbm", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "peak_source": pk["source"],
                          "traffic": committed_traffic("decode", DECODE_SRC)},
@@ -382,11 +383,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")
+    ap.add_argument("--decode-batch", type=int, default=W.K3_DECODE_BF16.B,
+                    help="sequences of the decode workload (64 is the benchmark; fewer is for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    global PREFILL
+    global PREFILL, DECODE
     PREFILL = W.WORKLOADS[args.workload]
+    if args.decode_batch != DECODE.B:
+        DECODE = dataclasses.replace(DECODE, B=args.decode_batch, name=f"{DECODE.name}_b{args.decode_batch}")
     if args.impl == "reference":
         run_reference(args)
     else:

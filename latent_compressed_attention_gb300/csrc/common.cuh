@@ -137,14 +137,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
-// Prefetch the box at {x, y, z} of a 3-D tensor map into L2 (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(x), "r"(y), "r"(z)
-                 : "memory");
-}
-
 // Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte aligned address into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *ptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)

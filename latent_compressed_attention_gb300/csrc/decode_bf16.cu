@@ -8,8 +8,9 @@
 // latent weighting by c itself, W_UV^T, gate.
 //
 // Pair kernel (persistent, one cluster of two CTAs per SM pair): the
-// concatenation of all sequences' cache rows is cut into one contiguous,
-// equal share per cluster, so ragged lengths balance by construction.  A
+// concatenation of all sequences' cache rows (plus a fixed charge per
+// sequence start) is cut into one contiguous, equal share per cluster, so
+// ragged lengths balance by construction.  A
 // cluster walks its share as segments (one per sequence it touches) in blocks
 // of 256 rows.  Heads are the M = 128 rows of every product (zero-padded):
 //   rank 0, the score CTA: q_abs[b] sits in TMEM as packed bf16 (columns
@@ -21,11 +22,13 @@
 //     columns, K = 128 cache rows), fp32 in all 512 TMEM columns, rescaled
 //     lazily when a head's maximum grew by more than 2^16.
 // Per segment the cluster writes (o_lat unnormalised, running max, sum) to a
-// workspace slot.  Each cache row is read from HBM once (the score CTA's copy,
-// prefetched into L2 a block ahead); the value CTA re-reads it from L2.
-// Merge kernel: one CTA per (head, 64 sequences) combines the segments of a
-// sequence with the log-sum-exp rule, rounds o_lat to bf16 and applies W_UV^T
-// on the tensor cores, then the sigmoid gate.
+// workspace slot.  Each cache row is read from HBM once by the score CTA,
+// which keeps it in L2 (evict_last) for the value CTA's second read
+// (evict_first).
+// Merge kernel: one CTA per (head, 32 sequences), launched as a programmatic
+// dependent of the pair kernel, combines the segments of a sequence with the
+// log-sum-exp rule, rounds o_lat to bf16 and applies W_UV^T on the tensor
+// cores, then the sigmoid gate.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -56,12 +59,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Keep a stale maximum until the new one exceeds it by this (log2 units):
 // p <= 2^16, far inside the fp32 range of the sums and the accumulator.
 constexpr float kRescaleLog2 = 16.0f;
-// The score CTA's producer prefetches the cache rows this many 256-row blocks
-// ahead of its loads into L2.
-#ifndef MLA_DECODE_PREFETCH_BLOCKS
-#define MLA_DECODE_PREFETCH_BLOCKS 0
-#endif
-constexpr int kPrefetchBlocks = MLA_DECODE_PREFETCH_BLOCKS;
 // Largest scratch the no-alloc decode entry point can use (48 MiB: the K3 decode
 // workload, B = 64 and H = 96 on 152 SMs, needs 27.6 MB).
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
@@ -76,10 +73,7 @@ constexpr uint32_t kPBytes = 2 * kPSlab;             // one unit of P: [96 heads
 constexpr uint32_t kRowInfoBytes = 128 * 8;          // {rescale factor, running sum} per head
 // score CTA
 constexpr uint32_t kSStage = 2 * kSlab;              // c ring stage: [256 rows x 64 latent columns]
-#ifndef MLA_DECODE_SCORE_STAGES
-#define MLA_DECODE_SCORE_STAGES 5
-#endif
-constexpr int kSStages = MLA_DECODE_SCORE_STAGES;
+constexpr int kSStages = 5;
 constexpr uint32_t S_RING = 0;
 constexpr uint32_t kPUnit = kPBytes + kRowInfoBytes; // staging per warpgroup
 constexpr uint32_t S_PST = S_RING + kSStages * kSStage;
@@ -198,21 +192,6 @@ struct SegWalk {
             }
         }
         return false;
-    }
-};
-
-// The 256-row blocks of a share in walk order, for the L2 prefetch that runs ahead of the loads.
-struct BlockCursor {
-    SegWalk w;
-    int seq, key, k1;
-    bool valid;
-    __device__ void init(const SegWalk &from) {
-        w = from;
-        valid = w.next(seq, key, k1);
-    }
-    __device__ void advance() {
-        key += kBS;
-        if (key >= k1) valid = w.next(seq, key, k1);
     }
 };
 
@@ -356,16 +335,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0) {
             // =========================================================== score CTA
             if (warp == 0 && lane == 0) {
-                // ---- TMA producer: c tiles [256 rows x 64 latent columns]; blocks ahead (and the next
-                // segment's absorbed query) are prefetched into L2 while this one streams in
+                // ---- TMA producer: c tiles [256 rows x 64 latent columns]; the next segment's absorbed
+                // query is prefetched into L2 near the end of this one
                 tma_prefetch_desc(&tm_c256);
                 const uint64_t keep = l2_policy_evict_last();   // the value CTA reads these rows again
                 uint32_t it = 0;
                 bool ok = true;
-                BlockCursor pf;
-                pf.init(walk);
-                for (int i = 0; i < kPrefetchBlocks && pf.valid; ++i, pf.advance())
-                    for (int kc = 0; kc < 8; ++kc) tma_prefetch_l2_3d(&tm_c256, kc * 64, pf.key, pf.seq);
                 while (ok && walk.next(seq, k0, k1)) {
                     const int nblk = (k1 - k0 + kBS - 1) / kBS;
                     SegWalk nx = walk;
@@ -375,10 +350,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int key = k0 + j * kBS;
                         if (has_next && j + 2 >= nblk)   // the softmax loads it one to two blocks from now
                             bulk_prefetch_l2(p.q_abs + static_cast<size_t>(n_seq) * H * kR, static_cast<uint32_t>(H) * kR * 2);
-                        if (pf.valid) {
-                            for (int kc = 0; kc < 8; ++kc) tma_prefetch_l2_3d(&tm_c256, kc * 64, pf.key, pf.seq);
-                            pf.advance();
-                        }
                         for (int kc = 0; kc < 8; ++kc, ++it) {
                             const int st = it % kSStages;
                             TR(const long long _a = clock64();)
