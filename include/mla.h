@@ -146,7 +146,7 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
  *
  * - Sizes whose scratch need (mla_latent_decode_workspace_size) exceeds
  *   48 MiB return MLA_ERR_WORKSPACE and launch nothing.  The K3 decode
- *   workload (B = 64, H = 96, r = 512 on a 152-SM GB300) needs 42.6 MB.
+ *   workload (B = 64, H = 96, r = 512 on a 152-SM GB300) needs 13.9 MB.
  * - The call allocates and frees nothing, on the host or the device.
  * - The first call on a device looks up the scratch array's device address
  *   on that device (cudaGetSymbolAddress); make that first call before any

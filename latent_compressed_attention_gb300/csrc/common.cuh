@@ -137,6 +137,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, uint
         : "memory");
 }
 
+// Prefetch the box at {x, y} of a 2-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void *tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // Prefetch `bytes` (a multiple of 16) of global memory at a 16-byte aligned address into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *ptr, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(ptr)), "r"(bytes)
@@ -167,9 +175,9 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap,
 }
 
 // 16-byte global store with an L2 cache policy.
-__device__ __forceinline__ void st_global_v4_hint(float4 *ptr, float4 v, uint64_t policy) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "f"(v.x), "f"(v.y),
-                 "f"(v.z), "f"(v.w), "l"(policy)
+__device__ __forceinline__ void st_global_v4_hint(uint4 *ptr, uint4 v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
                  : "memory");
 }
 

@@ -60,7 +60,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // p <= 2^16, far inside the fp32 range of the sums and the accumulator.
 constexpr float kRescaleLog2 = 16.0f;
 // Largest scratch the no-alloc decode entry point can use (48 MiB: the K3 decode
-// workload, B = 64 and H = 96 on 152 SMs, needs 27.6 MB).
+// workload, B = 64 and H = 96 on 152 SMs, needs 13.9 MB).
 constexpr size_t kNoAllocScratchBytes = size_t(48) << 20;
 
 constexpr uint32_t kSlab = 16384;                    // [128 rows x 64 bf16] with 128-byte swizzle
@@ -128,7 +128,7 @@ __device__ unsigned long long g_dtrace[DT_COUNT];
 constexpr int kTLMax = 256, kTLEvents = 14, kTLCluster = 10;
 __device__ long long g_dtl[kTLEvents][kTLMax];
 __device__ long long g_dclu[2][512];   // per cluster: value CTA's total cycles, segments
-__device__ long long g_mtrace[6][1024];   // per merge CTA: phase end times (cycles since its start)
+__device__ long long g_mtrace[8][1024];   // per merge CTA: phase end times (cycles since its start)
 #define MT(ph) do { if (threadIdx.x == 0) { const int _c = blockIdx.y * gridDim.x + blockIdx.x; \
     if (_c < 1024) g_mtrace[ph][_c] = clock64() - mt0; } } while (0)
 #define TL(ev, idx, val) \
@@ -142,7 +142,7 @@ __device__ long long g_mtrace[6][1024];   // per merge CTA: phase end times (cyc
 struct PairParams {
     const int *lens;
     const __nv_bfloat16 *q_abs;
-    float *ws_o;   // [slots][H][r]
+    __nv_bfloat16 *ws_o;   // [slots][H][r], unnormalised o_lat rounded to bf16
     float *ws_m;   // [slots][H]
     float *ws_l;   // [slots][H]
     int *err;
@@ -756,7 +756,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (named_bar_or(4, 256, fail)) { ok = false; break; }
                 tc_fence_after();
                 const size_t slot = static_cast<size_t>(cl + seq);
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + (slot * H + (head ? row : 0)) * kR + wg * 256);
+                uint4 *dst = reinterpret_cast<uint4 *>(p.ws_o + (slot * H + (head ? row : 0)) * kR + wg * 256);
                 const uint64_t ws_keep = l2_policy_evict_last();   // the merge reads it right after this kernel
 #pragma unroll 1
                 for (int cc = 0; cc < 8; ++cc) {
@@ -765,9 +765,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     tmem_wait_ld();
                     if (head)
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            st_global_v4_hint(dst + cc * 8 + q,
-                                              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]), ws_keep);
+                        for (int q = 0; q < 4; ++q)
+                            st_global_v4_hint(dst + cc * 4 + q,
+                                              make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                                                         pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                                         pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                                                         pack_bf16x2(v[8 * q + 6], v[8 * q + 7])),
+                                              ws_keep);
                 }
                 if (wg == 0 && head) p.ws_l[slot * H + row] = l_even + l_odd;
                 tc_fence_before();
@@ -792,42 +796,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------- merge
 constexpr int kMRows = 32;                          // sequences per merge CTA
 constexpr int kMergeThreads = 512;
+constexpr int kMaxClusters = 128;                   // share boundaries the merge keeps in shared memory
 constexpr uint32_t kASlab = kMRows * 128;           // o_lat tile [32 rows x 64 latent columns]
 constexpr uint32_t MA_OFF = 0;
 constexpr uint32_t MA_BYTES = 7 * kASlab + kSlab;   // an M=128 operand read of the last slab stays inside
-constexpr uint32_t MW_OFF = MA_BYTES;               // W_UV[h]: 8 tiles [128 x 64]
-constexpr uint32_t MBAR_OFF = MW_OFF + 8 * kSlab;
-constexpr uint32_t kSmemMerge = MBAR_OFF + 64 + 1024;
+constexpr uint32_t MW_OFF = MA_BYTES;               // W_UV[h] ring: 2 stages x [128 x 128 latent] (2 slabs)
+constexpr uint32_t kWStage = 2 * kSlab;
+constexpr uint32_t MBAR_OFF = MW_OFF + 2 * kWStage;
+constexpr uint32_t kSmemMerge = MBAR_OFF + 64 + 1024;   // two CTAs fit on an SM
 static_assert(MW_OFF % 1024 == 0, "alignment");
 
 struct MergeParams {
     const int *lens;
-    const float *ws_o, *ws_m, *ws_l;
+    const __nv_bfloat16 *ws_o;
+    const float *ws_m, *ws_l;
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
     int *err;
     int B, H, max_len, G;
 };
 
-__global__ void __launch_bounds__(kMergeThreads, 1)
+__global__ void __launch_bounds__(kMergeThreads, 2)
     decode_merge_kernel(const __grid_constant__ CUtensorMap tm_wuv, const MergeParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    uint64_t *w_full = reinterpret_cast<uint64_t *>(gbase + MBAR_OFF);
-    uint64_t *mma_done = w_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(w_full + 2);
+    uint64_t *w_full = reinterpret_cast<uint64_t *>(gbase + MBAR_OFF);   // [2]
+    uint64_t *w_empty = w_full + 2;                                      // [2]
+    uint64_t *mma_done = w_full + 4;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(w_full + 5);
     __shared__ long long s_pre[kMRows + 1];
+    __shared__ long long s_lo[kMaxClusters + 1];
     __shared__ long long s_total;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.x, b0 = blockIdx.y * kMRows;
-    const int H = p.H;
+    const int H = p.H, G = p.G;
     TR(const long long mt0 = clock64();)
 
     if (threadIdx.x == 0) {
-        mbar_init(smem_u32(w_full), 1);
-        mbar_init(smem_u32(mma_done), 1);
+        for (int i = 0; i < 5; ++i) mbar_init(smem_u32(w_full + i), 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -838,34 +846,53 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    auto load_w_chunk = [&](int k) {   // latent columns [128 k, 128 k + 128) of W_UV[h] into stage k % 2
+        const uint32_t bar = smem_u32(w_full + (k & 1));
+        mbar_arrive_expect_tx(bar, kWStage);
+        for (int sl = 0; sl < 2; ++sl)
+            tma_load_2d(base + MW_OFF + (k & 1) * kWStage + sl * kSlab, &tm_wuv, bar, k * 128 + sl * 64, h * kDV);
+    };
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tm_wuv);
-        mbar_arrive_expect_tx(smem_u32(w_full), 8 * kSlab);
-        for (int s = 0; s < 8; ++s) tma_load_2d(base + MW_OFF + s * kSlab, &tm_wuv, smem_u32(w_full), s * 64, h * kDV);
-        // virtual row offsets of this CTA's sequences (the split kernel's work axis)
-        long long total = 0;
-        for (int b = 0; b < p.B; ++b) {
-            const int x = __ldg(p.lens + b);
+        load_w_chunk(0);
+        load_w_chunk(1);
+        for (int k = 2; k < 4; ++k)
+            for (int sl = 0; sl < 2; ++sl) tma_prefetch_l2_2d(&tm_wuv, k * 128 + sl * 64, h * kDV);
+    }
+    if (warp == 1) {
+        // virtual row offsets of this CTA's sequences (the pair kernel's work axis): a warp-wide scan
+        long long run = 0;
+        for (int c0 = 0; c0 < p.B; c0 += 32) {
+            const int b = c0 + lane;
+            const int x = b < p.B ? __ldg(p.lens + b) : 0;
             if (x < 0 || x > p.max_len) record_error(p.err, kDevErrBounds);
-            if (b >= b0 && b <= b0 + kMRows) s_pre[b - b0] = total;
             const int len = clamp_len(x, p.max_len);
-            if (len > 0) total += kSeqOverhead + len;
+            long long v = len > 0 ? kSeqOverhead + len : 0, incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const long long n = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += n;
+            }
+            const long long excl = run + incl - v;   // virtual start of sequence b
+            if (b < p.B && b >= b0 && b <= b0 + kMRows) s_pre[b - b0] = excl;
+            run += __shfl_sync(0xffffffffu, incl, 31);
         }
-        for (int b = max(p.B, b0); b <= b0 + kMRows; ++b) s_pre[b - b0] = total;
-        s_total = total;
+        for (int b = max(p.B, b0) + lane; b <= b0 + kMRows; b += 32) s_pre[b - b0] = run;
+        if (lane == 0) s_total = run;
     }
     __syncthreads();
     const long long total = s_total;
-    // launched as a programmatic dependent of the split kernel: everything above overlapped its
+    for (int c = threadIdx.x; c <= G && c <= kMaxClusters; c += kMergeThreads) s_lo[c] = share_lo(total, c, G);
+    __syncthreads();
+    // launched as a programmatic dependent of the pair kernel: everything above overlapped its
     // tail; its workspace writes are complete and visible after this
     MT(0);
     grid_dependency_wait();
     MT(1);
 
     // log-sum-exp combine of the segments of each sequence; o_lat -> bf16 tile row.
-    // A warp takes a row at a time: lane i fetches segment i's (m, l), the warp
-    // reduces them with shuffles, then every lane accumulates its 16 latent
-    // columns over the segments, issuing a segment's loads together.
+    // A warp takes a row at a time: lane j holds segment j's (m, l) and weight;
+    // every lane accumulates its 16 latent columns, two segments' loads in flight.
     for (int i = warp; i < kMRows; i += kMergeThreads / 32) {
         const int b = b0 + i;
         float o[16];
@@ -874,50 +901,69 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
         // the sequence's cache rows on the virtual axis (none for an empty sequence)
         const long long r0 = s_pre[i] + kSeqOverhead, r1 = s_pre[i + 1];
         if (b < p.B && r1 > r0) {
-            const int G = p.G;
             const int c_first = min(static_cast<int>(((r0 + 1) * G - 1) / total), G - 1);
-            // CTA c wrote slot c + b iff its share [lo_c, lo_c+1) overlaps [r0, r1)
-            auto overlaps = [&](int c) {
-                return c < G && min(share_lo(total, c + 1, G), r1) > max(share_lo(total, c, G), r0);
-            };
-            int n_seg = 0;   // consecutive CTAs from c_first whose shares start before r1
-            while (c_first + n_seg < G && share_lo(total, c_first + n_seg, G) < r1) ++n_seg;
-            float M = -INFINITY, L = 0.f;
+            // cluster c wrote slot c + b iff its share [lo_c, lo_c+1) overlaps [r0, r1)
+            auto overlaps = [&](int c) { return c < G && min(s_lo[c + 1], r1) > max(s_lo[c], r0); };
+            int n_seg = 0;   // consecutive clusters from c_first whose shares start before r1
+            while (c_first + n_seg < G && s_lo[c_first + n_seg] < r1) ++n_seg;
+            float M = -INFINITY, L = 0.f, wl = 0.f;
             for (int s0 = 0; s0 < n_seg; s0 += 32) {
                 const int c = c_first + s0 + lane;
                 const bool has = s0 + lane < n_seg && overlaps(c);
                 const size_t slot = static_cast<size_t>(c + b);
                 const float m = has ? __ldg(p.ws_m + slot * H + h) : -INFINITY;
+                const float l = has ? __ldg(p.ws_l + slot * H + h) : 0.f;
                 float mw = m;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, off));
                 const float M_new = fmaxf(M, mw);
-                float lw = has ? fast_exp2(m - M_new) * __ldg(p.ws_l + slot * H + h) : 0.f;
+                float lw = has ? fast_exp2(m - M_new) * l : 0.f;
 #pragma unroll
                 for (int off = 16; off >= 1; off >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, off);
                 L = (M == -INFINITY ? 0.f : L * fast_exp2(M - M_new)) + lw;
                 M = M_new;
+                wl = has ? fast_exp2(m - M) : 0.f;   // final when all segments fit one pass
             }
-            for (int si = 0; si < n_seg; ++si) {
-                const int c = c_first + si;
-                if (!overlaps(c)) continue;
-                const size_t slot = static_cast<size_t>(c + b);
-                const float w = fast_exp2(__ldg(p.ws_m + slot * H + h) - M);
-                const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + (slot * H + h) * kR + lane * 16);
-                float4 v[4];
+            if (i == 0) MT(6);
+            for (int s0 = 0; s0 < n_seg; s0 += 32) {
+                if (n_seg > 32) {   // more segments than lanes: weights against the final maximum
+                    const int c = c_first + s0 + lane;
+                    const bool has = s0 + lane < n_seg && overlaps(c);
+                    wl = has ? fast_exp2(__ldg(p.ws_m + static_cast<size_t>(c + b) * H + h) - M) : 0.f;
+                }
+                const int cnt = min(32, n_seg - s0);
+                for (int j = 0; j < cnt; j += 2) {
+                    const bool two = j + 1 < cnt;
+                    const float w0 = __shfl_sync(0xffffffffu, wl, j);
+                    const float w1 = __shfl_sync(0xffffffffu, wl, two ? j + 1 : j);
+                    const size_t slot0 = static_cast<size_t>(c_first + s0 + j + b);
+                    // a segment with weight 0 (empty share) is not read; its slot may hold anything
+                    const uint4 *src0 = reinterpret_cast<const uint4 *>(p.ws_o + (slot0 * H + h) * kR + lane * 16);
+                    const uint4 *src1 = src0 + static_cast<size_t>(H) * kR / 8;
+                    uint4 v0[2], v1[2];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) v[q4] = __ldg(src + q4);
+                    for (int q = 0; q < 2; ++q) {
+                        v0[q] = w0 != 0.f ? __ldg(src0 + q) : make_uint4(0, 0, 0, 0);
+                        v1[q] = two && w1 != 0.f ? __ldg(src1 + q) : make_uint4(0, 0, 0, 0);
+                    }
+                    const float u1 = two ? w1 : 0.f;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    o[4 * q4 + 0] += w * v[q4].x;
-                    o[4 * q4 + 1] += w * v[q4].y;
-                    o[4 * q4 + 2] += w * v[q4].z;
-                    o[4 * q4 + 3] += w * v[q4].w;
+                    for (int q = 0; q < 2; ++q) {
+                        const uint32_t a[4] = {v0[q].x, v0[q].y, v0[q].z, v0[q].w};
+                        const uint32_t c[4] = {v1[q].x, v1[q].y, v1[q].z, v1[q].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {   // bf16 pair -> two fp32: the bits are the upper half
+                            o[8 * q + 2 * k] += w0 * __uint_as_float(a[k] << 16) + u1 * __uint_as_float(c[k] << 16);
+                            o[8 * q + 2 * k + 1] +=
+                                w0 * __uint_as_float(a[k] & 0xFFFF0000u) + u1 * __uint_as_float(c[k] & 0xFFFF0000u);
+                        }
+                    }
                 }
             }
             const float inv = 1.f / L;
 #pragma unroll
             for (int k = 0; k < 16; ++k) o[k] *= inv;
+            if (i == 0) MT(7);
         }
         const uint32_t slab = base + MA_OFF + (lane >> 2) * kASlab;
 #pragma unroll
@@ -932,18 +978,34 @@ __global__ void __launch_bounds__(kMergeThreads, 1)
     __syncthreads();
     MT(2);
     if (threadIdx.x == 0) {
-        if (mbar_wait(smem_u32(w_full), 0, p.err)) {
-            MT(3);
+        // o = o_lat . W_UV^T over four 128-column chunks of the latent, two in flight
+        const uint32_t idesc = make_idesc_bf16(128, kDV, 0, 0);
+        bool ok = true;
+        int loaded = 2;   // chunks whose loads were issued
+        for (int k = 0; ok && k < 4; ++k) {
+            const int st = k & 1;
+            if (!(ok = mbar_wait(smem_u32(w_full + st), (k >> 1) & 1, p.err))) break;
+            if (k == 0) MT(3);
             tc_fence_after();
-            const uint32_t idesc = make_idesc_bf16(128, kDV, 0, 0);
-#pragma unroll 1
-            for (int kk = 0; kk < kR / 16; ++kk) {
-                const uint64_t a = make_smem_desc(base + MA_OFF + (kk >> 2) * kASlab + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd = make_smem_desc(base + MW_OFF + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                umma_bf16(tmem, a, bd, idesc, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const int ks = 8 * k + kk;   // K step of 16 latent columns
+                const uint64_t a = make_smem_desc(base + MA_OFF + (ks >> 2) * kASlab + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd =
+                    make_smem_desc(base + MW_OFF + st * kWStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                umma_bf16(tmem, a, bd, idesc, ks > 0);
             }
-            umma_commit(smem_u32(mma_done));
+            umma_commit(smem_u32(w_empty + st));
+            if (k + 2 < 4) {   // the stage is refilled once its products completed
+                if (!(ok = mbar_wait(smem_u32(w_empty + st), 0, p.err))) break;
+                load_w_chunk(k + 2);
+                ++loaded;
+            }
         }
+        if (ok) umma_commit(smem_u32(mma_done));
+        // no load may still be landing when the CTA exits
+        if (!ok)
+            for (int k = 0; k < loaded; ++k) mbar_wait(smem_u32(w_full + (k & 1)), (k >> 1) & 1, p.err);
     }
     __syncwarp();
     const bool done = mbar_wait(smem_u32(mma_done), 0, p.err);
@@ -1072,7 +1134,7 @@ int pair_clusters(int num_sms) {
 size_t decode_bf16_workspace_bytes(int B, int H, int r, int, int num_sms) {
     if (r != kR || H < 1 || H > kHMax || B < 1 || num_sms < 1) return 0;
     const size_t slots = slot_count(B, num_sms / 2 > 0 ? num_sms / 2 : 1);
-    return slots * static_cast<size_t>(H) * (kR + 2) * sizeof(float);
+    return slots * static_cast<size_t>(H) * (kR * sizeof(__nv_bfloat16) + 2 * sizeof(float));
 }
 
 #ifdef MLA_TRACE
@@ -1094,7 +1156,7 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_decode_timeline(
 }
 extern "C" __attribute__((visibility("default"))) int mla_debug_decode_merge(long long *host) {
     if (cudaMemcpyFromSymbol(host, g_mtrace, sizeof(g_mtrace)) != cudaSuccess) return -1;
-    return 6 * 1024;
+    return 8 * 1024;
 }
 extern "C" __attribute__((visibility("default"))) int mla_debug_decode_clusters(long long *host) {
     if (cudaMemcpyFromSymbol(host, g_dclu, sizeof(g_dclu)) != cudaSuccess) return -1;
@@ -1117,10 +1179,12 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
         if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
     const int G = pair_clusters(a.num_sms);
+    if (G > kMaxClusters) return cudaErrorInvalidConfiguration;
     const size_t slots = slot_count(a.B, G);
-    if (slots * static_cast<size_t>(a.H) * (kR + 2) * sizeof(float) > a.workspace_bytes) return cudaErrorInvalidValue;
-    float *ws_o = static_cast<float *>(a.workspace);
-    float *ws_m = ws_o + slots * a.H * kR;
+    if (slots * static_cast<size_t>(a.H) * (kR * sizeof(__nv_bfloat16) + 2 * sizeof(float)) > a.workspace_bytes)
+        return cudaErrorInvalidValue;
+    __nv_bfloat16 *ws_o = static_cast<__nv_bfloat16 *>(a.workspace);
+    float *ws_m = reinterpret_cast<float *>(ws_o + slots * a.H * kR);
     float *ws_l = ws_m + slots * a.H;
     CUtensorMap tm_c256, tm_c, tm_wuv;
     {
