@@ -80,8 +80,10 @@ constexpr uint32_t S_PST = S_RING + kSStages * kSStage;
 constexpr uint32_t S_END = S_PST + 2 * kPUnit;
 // value CTA
 constexpr uint32_t O_RING = 0;
-constexpr int kOStages = 2;
-constexpr uint32_t kOStage = 4 * kSlab;              // 256 latent columns x 128 rows
+constexpr int kVRows = 64;                           // cache rows per value ring stage (half a unit)
+constexpr uint32_t kVSlab = kVRows * 128;            // [64 rows x 64 latent columns], 128-byte swizzle
+constexpr int kOStages = 4;
+constexpr uint32_t kOStage = 4 * kVSlab;             // 256 latent columns x 64 rows
 constexpr int kPBufs = 3;                            // P units in flight to the value CTA
 constexpr uint32_t O_P = kOStages * kOStage;         // kPBufs P tiles, then the operand over-read pad
 constexpr uint32_t O_ROWINFO = O_P + kPBufs * kPBytes + (kSlab - kPSlab);
@@ -409,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
             // =========================================================== value CTA
             if (warp == 0 && lane == 0) {
-                // ---- TMA producer: c tiles as the MN-major value operand, 2 x [128 rows x 256 latent columns] a unit
+                // ---- TMA producer: c tiles as the MN-major value operand, 4 x [64 rows x 256 latent columns] a unit
                 tma_prefetch_desc(&tm_c);
                 const uint64_t done_with = l2_policy_evict_first();   // the last read of these rows
                 uint32_t it = 0;
@@ -419,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int u = 0; ok && u < nunits; ++u) {
                         const int key = k0 + u * kBN;
                         if (key >= k1) continue;   // a unit past the segment's end: nothing to load
-                        for (int nh = 0; nh < 2; ++nh, ++it) {
+                        for (int nq = 0; ok && nq < 4; ++nq, ++it) {   // latent half nq >> 1, row half nq & 1
                             const int st = it % kOStages;
                             TR(const long long _a = clock64();)
                             if (it >= kOStages &&
@@ -429,8 +431,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             const uint32_t full = B_(bars->oc_full[st]);
                             mbar_arrive_expect_tx(full, kOStage);
                             for (int q4 = 0; q4 < 4; ++q4)
-                                tma_load_3d_hint(base + O_RING + st * kOStage + q4 * kSlab, &tm_c, full,
-                                                 (nh * 4 + q4) * 64, key, seq, done_with);
+                                tma_load_3d_hint(base + O_RING + st * kOStage + q4 * kVSlab, &tm_c, full,
+                                                 ((nq >> 1) * 4 + q4) * 64, key + (nq & 1) * kVRows, seq, done_with);
                         }
                     }
                 }
@@ -475,17 +477,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         }
                         const int key = k0 + u * kBN;
                         if (key < k1) {
-                            const int nvalid = len - key;   // >= 1: rows of this unit inside the sequence
-                            for (int nh = 0; ok && nh < 2; ++nh, ++it) {
-                                const int st = it % kOStages;
+                            for (int nq = 0; ok && nq < 4; ++nq, ++it) {   // latent half nq >> 1, row half nq & 1
+                                const int st = it % kOStages, hr = nq & 1;
+                                const int nvalid = len - key - hr * kVRows;   // rows of this stage inside the sequence
                                 TR(long long _o = clock64();)
                                 if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
                                 TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
-                                if (nvalid < kBN) {
+                                if (nvalid < kVRows) {
                                     for (int sl = 0; sl < 4; ++sl) {
-                                        const uint32_t tile = base + O_RING + st * kOStage + sl * kSlab;
-                                        for (int r = nvalid + lane; r < kBN; r += 32)
-    #pragma unroll
+                                        const uint32_t tile = base + O_RING + st * kOStage + sl * kVSlab;
+                                        for (int r = max(nvalid, 0) + lane; r < kVRows; r += 32)
+#pragma unroll
                                             for (int ch = 0; ch < 8; ++ch)
                                                 st_shared_v4(tile + (r >> 3) * 1024 + (r & 7) * 128 + ch * 16, 0, 0, 0, 0);
                                     }
@@ -494,13 +496,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 }
                                 tc_fence_after();
                                 if (leader) {
-    #pragma unroll
-                                    for (int kk = 0; kk < kBN / 16; ++kk) {
+#pragma unroll
+                                    for (int j = 0; j < kVRows / 16; ++j) {
+                                        const int kk = hr * 4 + j;   // K step within the unit's 128 rows
                                         const uint64_t a = make_smem_desc(
-                                            base + O_P + pb * kPBytes + (kk >> 2) * kPSlab + (kk & 3) * 32, 16, 1024);
+                                            base + O_P + pb * kPBytes + hr * kPSlab + j * 32, 16, 1024);
                                         const uint64_t bd =
-                                            make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
-                                        umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (u > 0 || kk > 0));
+                                            make_smem_desc(base + O_RING + st * kOStage + j * 2048, kVSlab, 1024);
+                                        umma_bf16(tmem + (nq >> 1) * 256, a, bd, kIdescPV, (u > 0 || kk > 0));
                                     }
                                     umma_commit(B_(bars->oc_empty[st]));
                                 }
@@ -1193,8 +1196,8 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
         const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_cache) * 2, rows * a.ld_cache * 2};
         const cuuint32_t box256[3] = {64, kBS, 1};
         if (encode_map(&tm_c256, a.c_cache, 3, dims, strides, box256) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-        const cuuint32_t box128[3] = {64, kBN, 1};
-        if (encode_map(&tm_c, a.c_cache, 3, dims, strides, box128) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint32_t box64[3] = {64, kVRows, 1};
+        if (encode_map(&tm_c, a.c_cache, 3, dims, strides, box64) != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[2] = {kR, static_cast<cuuint64_t>(a.H) * kDV};
