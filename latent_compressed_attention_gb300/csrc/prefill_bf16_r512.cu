@@ -103,6 +103,11 @@ enum TraceSlot {
 __device__ unsigned long long g_trace[TR_COUNT];
 #define TR(...) __VA_ARGS__
 #define TR_ADD(slot, v) atomicAdd(&g_trace[slot], static_cast<unsigned long long>(v))
+// Per-block event times (cycles since the start barrier) of the first cluster (the heaviest tile).
+constexpr int kTLMax = 128, kTLEvents = 12;
+__device__ long long g_ptl[kTLEvents][kTLMax];
+#define TL(ev, idx, val) \
+    do { if (cluster_id == 0 && static_cast<int>(idx) < kTLMax) g_ptl[ev][idx] = (val); } while (0)
 #else
 #define TR(...)
 #define TR_ADD(slot, v) (void)0
@@ -290,13 +295,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < nblk; ++j) {
                 TR(long long _a = clock64();)
                 if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free[0]), (j - 1) & 1, p.err, abort_flag))) break;
-                TR(w_free += clock64() - _a;)
+                TR(w_free += clock64() - _a; TL(0, j, clock64() - t_start); long long w_blk = 0;)
                 tc_fence_after();
                 for (int kc = 0; kc < 8; ++kc, ++it) {
                     const int st = it % kSStages;
                     TR(long long _b = clock64();)
                     if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
-                    TR(w_full += clock64() - _b;)
+                    TR(w_full += clock64() - _b; w_blk += clock64() - _b;)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -308,6 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 umma_commit(B_(bars->s_full[0]));
+                TR(TL(1, j, clock64() - t_start); TL(7, j, w_blk);)
             }
             TR(TR_ADD(TR_S_MMA_LOOP, clock64() - tl0); TR_ADD(TR_S_MMA_SFREE, w_free); TR_ADD(TR_S_MMA_SCFULL, w_full);)
             if (!ok) *abort_flag = 1;
@@ -352,7 +358,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int j = 0; ok && j < nblk; ++j) {
                 TR(long long _a = clock64();)
                 fail = fail || !mbar_wait(B_(bars->s_full[0]), j & 1, p.err, abort_flag);
-                TR(w_sfull += clock64() - _a;)
+                TR(w_sfull += clock64() - _a; if ((threadIdx.x & 127) == 0) TL(2 + 3 * wg, j, clock64() - t_start);)
                 float s[4][32];
                 if (!fail) {
                     tc_fence_after();
@@ -373,7 +379,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 TR(long long _x = clock64();)
                 if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
-                TR(w_xbar += clock64() - _x;)
+                TR(w_xbar += clock64() - _x; if (threadIdx.x == 128) TL(3, j, clock64() - t_start);)
                 const float mx = fmaxf(ld_shared_f32(base + PMAX + ((j & 1) * 2 + 0) * kBM * 4 + row * 4),
                                        ld_shared_f32(base + PMAX + ((j & 1) * 2 + 1) * kBM * 4 + row * 4));
                 float factor = 1.f;
@@ -416,6 +422,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + wg * kRowInfoBytes, 1), ri,
                                             kRowInfoBytes, dst_bar);
                         bulk_commit_group();
+                        TR(TL(wg == 0 ? 4 : 6, j, clock64() - t_start);)
                     }
                 }
             }
@@ -471,7 +478,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 TR(long long _a = clock64();)
                 if (leader) mbar_arrive_expect_tx(B_(bars->p_full[pb]), kPBytes + kRowInfoBytes);
                 if (!(ok = wait_all(bars->p_full[pb], (j >> 1) & 1, true))) break;
-                TR(w_pfull += clock64() - _a;)
+                TR(w_pfull += clock64() - _a; if (leader) TL(8, j, clock64() - t_start); long long w_u = 0;)
                 // any row whose maximum grew needs o_lat rescaled before this block's product
                 const uint32_t ri = base + O_ROWINFO + pb * kRowInfoBytes;
                 bool grew = false;
@@ -488,7 +495,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int st = it % kOStages;
                     TR(long long _o = clock64();)
                     if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
-                    TR(w_oc += clock64() - _o;)
+                    TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
                     tc_fence_after();
                     if (leader) {
 #pragma unroll
@@ -504,6 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 if (leader) umma_commit(B_(bars->pv_done[pb]));
+                TR(if (leader) { TL(9, j, clock64() - t_start); TL(10, j, w_u); })
             }
             TR(if (leader) {
                 TR_ADD(TR_O_MMA_LOOP, clock64() - tl0); TR_ADD(TR_O_MMA_PFULL, w_pfull); TR_ADD(TR_O_MMA_OCFULL, w_oc);
@@ -682,6 +690,11 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_prefill_trace(un
         if (cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros)) != cudaSuccess) return -1;
     }
     return n;
+}
+// Diagnostic build only: copy the per-block event times of the traced cluster.
+extern "C" __attribute__((visibility("default"))) int mla_debug_prefill_timeline(long long *host) {
+    if (cudaMemcpyFromSymbol(host, g_ptl, sizeof(g_ptl)) != cudaSuccess) return -1;
+    return kTLEvents * kTLMax;
 }
 #endif
 
