@@ -5,7 +5,8 @@ d_q=d_v=128, r=512, bf16, scale 1): the W_UK absorb, the latent scores, the
 causal softmax, the latent weighting, the W_UV up-projection and the gate, all
 in the library's fused kernel.  The cached-latent decode (B=64, cache lengths
 uniform in [1024, 32768], H=96, r=512) is timed in the same run and reported
-under "decode".
+under "decode", and the whole layer at the prefill's size (step-1 projections
+with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -242,6 +243,7 @@ def run_ours(args):
         e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
     decode = run_decode(torch, lca, dev, stream, flush, args, pk) if not args.no_decode else None
+    layer_line = run_layer(torch, lca, dev, stream, flush, args, pk) if not args.no_layer else None
     if lca.mla_get_device_error() != 0:
         raise RuntimeError("device error word set after the timed region")
 
@@ -268,6 +270,8 @@ def run_ours(args):
         }
         if decode is not None:
             line["decode"] = decode
+        if layer_line is not None:
+            line["layer"] = layer_line
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -302,6 +306,46 @@ def run_decode(torch, lca, dev, stream, flush, args, pk):
                          "peak_source": pk["source"],
                          "traffic": committed_traffic("decode", DECODE_SRC)},
             "gpu_launches": 2 * args.steps}
+
+
+def layer_flops(w) -> dict:
+    """Algorithmic FLOPs of the whole layer: the five projections plus the absorbed attention."""
+    M = w.B * w.T
+    gemm = 2 * M * (w.D * w.r_q + w.r_q * w.H * w.d_q + w.D * w.r + w.D * w.H * w.d_v + w.H * w.d_v * w.D)
+    attn = w.B * w.H * (2 * w.r * w.T * (w.T + 1) + 2 * w.T * w.r * (w.d_q + w.d_v))
+    return {"gemm": gemm, "attention": attn, "total": gemm + attn}
+
+
+def run_layer(torch, lca, dev, stream, flush, args, pk):
+    """The whole layer (x -> y through step 1, the attention and W_o) at the prefill workload's size."""
+    w = PREFILL
+    p = W.draw_layer(w, seed=0)
+    to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
+    t = {k: to(v) for k, v in p.items()}
+    del p
+    ws_bytes = lca.mla_gated_layer_workspace_size(w.B, w.T, w.D, w.H, w.d_q, w.d_v, w.r, w.r_q, torch.bfloat16)
+    if ws_bytes == 0:
+        return {"unavailable": "layer shape not supported"}
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    y = torch.empty((w.B, w.T, w.D), dtype=torch.bfloat16, device=dev)
+    step = lambda: lca.mla_gated_layer_fwd(t["x"], t["q_down"], t["q_up"], t["kv_down"], t["kv_up"],  # noqa: E731
+                                           t["gate"], t["o_proj"], w.H, w.d_q, w.d_v, w.scale, out=y, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = statistics.mean(timed_steps(torch, step, args.steps, flush, stream))
+    fl = layer_flops(w)
+    tf = fl["total"] / (ms * 1e-3) / 1e12
+    return {"workload": w.name.replace("prefill", "layer"), "value": round(tf, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "flops_per_step": fl["total"], "gemm_flops": fl["gemm"],
+            "attention_flops": fl["attention"],
+            "config": {"B": w.B, "T": w.T, "D": w.D, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "r_q": w.r_q,
+                       "inputs": "x ~ N(0,1), weights ~ N(0, 0.02^2), bf16"},
+            "roofline": {"kernel": "layer (5 tensor-core GEMMs + prefill_r512_kernel)", "bound": "tensor",
+                         "achieved": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tf / pk["bf16_tflops"], 4), "peak_source": pk["source"] + " (burst bf16)",
+                         "traffic": None},
+            "gpu_launches": 6 * args.steps}
 
 
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
@@ -382,6 +426,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")
     ap.add_argument("--decode-batch", type=int, default=W.K3_DECODE_BF16.B,

@@ -161,6 +161,48 @@ MLA_API int mla_latent_decode_noalloc(const void *q_abs, const void *c_cache, lo
                                       int B, int H, int d_v, int r, int dtype, void *stream);
 
 /*
+ * mla_gated_layer_workspace_size - bytes of device workspace mla_gated_layer_fwd
+ * needs for these sizes (0 if the shape or dtype is not supported).
+ */
+MLA_API size_t mla_gated_layer_workspace_size(int B, int T, int D, int H, int d_q, int d_v, int r, int r_q,
+                                              int dtype);
+
+/*
+ * mla_gated_layer_fwd - the whole Gated-MLA layer (page "Gated MLA（矩阵吸收版）",
+ * section "完整计算流（四步）", steps 1-4, plus the output projection of the
+ * listing in section "代码对照"):
+ *
+ *   c   = RMSNorm(x . w_kv_down^T)                         [B,T,r]
+ *   q   = RMSNorm(x . w_q_down^T) . w_q_up^T                 [B,T,H,d_q]
+ *   g   = x . w_gate^T                                       [B,T,H*d_v]
+ *   o   = mla_absorbed_attn_fwd(q, c, W_UK, W_UV, g, scale)  [B,T,H*d_v]
+ *   y   = o . w_o^T                                          [B,T,D]
+ *
+ * RMSNorm: z / sqrt(mean(z^2) + 1e-6), unit gain.  No biases.  Weights are
+ * nn.Linear weights [out_features, in_features], row-major:
+ *   w_q_down [r_q, D]   w_q_up [H*d_q, r_q]   w_kv_down [r, D]
+ *   w_kv_up  [H*(d_q+d_v), r]: all heads' W_UK rows first (W_UK = w_kv_up as
+ *            [H,d_q,r]), then all heads' W_UV rows ([H,d_v,r])
+ *   w_gate   [H*d_v, D]   w_o [D, H*d_v]
+ * x [B,T,D] and y [B,T,D], row-major.  All tensors share `dtype`.
+ *
+ * Supported: MLA_DTYPE_F32 with r, d_q, d_v <= 64 (SIMT fp32, no TF32);
+ * MLA_DTYPE_BF16 with r = 512, d_q = d_v = 128, H even, D and r_q multiples of
+ * 256 (tensor-core GEMMs, fp32 accumulation, bf16 intermediate results).
+ *
+ *   workspace  device buffer of >= mla_gated_layer_workspace_size(...) bytes,
+ *              16-byte aligned, caller-owned.  On return (in stream order) it
+ *              holds, each part starting on a 256-byte boundary and in the
+ *              input dtype: q [B*T, H*d_q], c [B*T, r], g [B*T, H*d_v] and o
+ *              [B*T, H*d_v], followed by internal scratch.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
+                                const void *w_kv_up, const void *w_gate, const void *w_o, float scale, void *y,
+                                int B, int T, int D, int H, int d_q, int d_v, int r, int r_q, int dtype,
+                                void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * mla_get_device_error - synchronise `stream`, then read and clear the current
  * device's error word.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT,
  * MLA_ERR_DEVICE_BOUNDS, or MLA_ERR_CUDA if the synchronisation itself failed.

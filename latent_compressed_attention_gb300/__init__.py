@@ -22,7 +22,7 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error", "mla_status_string", "mla_version",
-           "DTYPE_BF16", "DTYPE_F32"]
+           "mla_gated_layer_fwd", "mla_gated_layer_workspace_size", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
@@ -59,6 +59,10 @@ def library():
             lib.mla_latent_decode.restype = i
             lib.mla_latent_decode_noalloc.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp]
             lib.mla_latent_decode_noalloc.restype = i
+            lib.mla_gated_layer_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
+            lib.mla_gated_layer_workspace_size.restype = sz
+            lib.mla_gated_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, f, vp] + [i] * 9 + [vp, sz, vp]
+            lib.mla_gated_layer_fwd.restype = i
             lib.mla_get_device_error.argtypes = [vp]
             lib.mla_get_device_error.restype = i
             lib.mla_status_string.argtypes = [i]
@@ -141,6 +145,68 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
                                          B, T, H, d_q, d_v, r, _dtype_code(q), _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_absorbed_attn_fwd")
+    return out
+
+
+def mla_gated_layer_workspace_size(B: int, T: int, D: int, H: int, d_q: int, d_v: int, r: int, r_q: int,
+                                   dtype) -> int:
+    """Workspace bytes of mla_gated_layer_fwd (0: shape or dtype unsupported); dtype a torch dtype."""
+    torch = _torch()
+    code = DTYPE_BF16 if dtype == torch.bfloat16 else DTYPE_F32 if dtype == torch.float32 else -1
+    return int(library().mla_gated_layer_workspace_size(B, T, D, H, d_q, d_v, r, r_q, code))
+
+
+def layer_workspace_views(workspace, B: int, T: int, H: int, d_q: int, d_v: int, r: int, dtype):
+    """The intermediate results mla_gated_layer_fwd leaves in its workspace: q, c, g, o."""
+    torch = _torch()
+    es = torch.tensor([], dtype=dtype).element_size()
+    M = B * T
+    align = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    offs, sizes = [], [M * H * d_q, M * r, M * H * d_v, M * H * d_v]
+    o = 0
+    for n in sizes:
+        offs.append(o)
+        o += align(n * es)
+    flat = workspace.view(torch.uint8)
+    return tuple(flat[off:off + n * es].view(dtype) for off, n in zip(offs, sizes))
+
+
+def mla_gated_layer_fwd(x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, H: int, d_q: int, d_v: int,
+                        scale: float = 1.0, out=None, workspace=None, stream=None):
+    """The whole Gated-MLA layer: x [B,T,D] -> y [B,T,D] (allocated if not given).
+
+    Weights are nn.Linear weights [out, in]: w_q_down [r_q,D], w_q_up [H*d_q,r_q], w_kv_down [r,D],
+    w_kv_up [H*(d_q+d_v),r] (W_UK rows, then W_UV rows), w_gate [H*d_v,D], w_o [D,H*d_v].
+    A workspace (uint8 CUDA tensor) is allocated when not given; after the call it holds q, c, g
+    and the gated attention output (``layer_workspace_views``).
+    """
+    torch = _torch()
+    B, T, D = x.shape
+    r_q, r = w_q_down.shape[0], w_kv_down.shape[0]
+    dev, dt = x.device, x.dtype
+    _check(x, "x", dt, dev)
+    _check(w_q_down, "w_q_down", dt, dev, (r_q, D))
+    _check(w_q_up, "w_q_up", dt, dev, (H * d_q, r_q))
+    _check(w_kv_down, "w_kv_down", dt, dev, (r, D))
+    _check(w_kv_up, "w_kv_up", dt, dev, (H * (d_q + d_v), r))
+    _check(w_gate, "w_gate", dt, dev, (H * d_v, D))
+    _check(w_o, "w_o", dt, dev, (D, H * d_v))
+    if out is None:
+        out = torch.empty((B, T, D), dtype=dt, device=dev)
+    _check(out, "out", dt, dev, (B, T, D))
+    lib = library()
+    code = _dtype_code(x)
+    need = int(lib.mla_gated_layer_workspace_size(B, T, D, H, d_q, d_v, r, r_q, code))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_gated_layer_fwd(x.data_ptr(), w_q_down.data_ptr(), w_q_up.data_ptr(), w_kv_down.data_ptr(),
+                                 w_kv_up.data_ptr(), w_gate.data_ptr(), w_o.data_ptr(), float(scale),
+                                 out.data_ptr(), B, T, D, H, d_q, d_v, r, r_q, code, ws_ptr, ws_bytes,
+                                 _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_gated_layer_fwd")
     return out
 
 

@@ -182,6 +182,45 @@ MLA_API int mla_latent_decode_noalloc(const void *q_abs, const void *c_cache, lo
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+MLA_API size_t mla_gated_layer_workspace_size(int B, int T, int D, int H, int d_q, int d_v, int r, int r_q,
+                                              int dtype) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return 0;
+    if (B < 0 || T < 0) return 0;
+    const bool f32 = dtype == MLA_DTYPE_F32;
+    if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32)) return 0;
+    const long long M = static_cast<long long>(B) * T;
+    if (M > INT_MAX) return 0;
+    return gated_layer_workspace_bytes(M, H, d_q, d_v, r, r_q, f32);
+}
+
+MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
+                                const void *w_kv_up, const void *w_gate, const void *w_o, float scale, void *y,
+                                int B, int T, int D, int H, int d_q, int d_v, int r, int r_q, int dtype,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || T < 0 || D <= 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0 || r_q <= 0) return MLA_ERR_SHAPE;
+    const long long M = static_cast<long long>(B) * T;
+    const long long widest = static_cast<long long>(H) * (d_q + d_v) > D ? static_cast<long long>(H) * (d_q + d_v)
+                                                                          : static_cast<long long>(D);
+    if (M > INT_MAX || !mul_fits(M, widest > r_q ? widest : r_q, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (!x || !w_q_down || !w_q_up || !w_kv_down || !w_kv_up || !w_gate || !w_o || !y) return MLA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_q_down) || !aligned16(w_q_up) || !aligned16(w_kv_down) ||
+        !aligned16(w_kv_up) || !aligned16(w_gate) || !aligned16(w_o) || !aligned16(y))
+        return MLA_ERR_ALIGN;
+    const bool f32 = dtype == MLA_DTYPE_F32;
+    if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32)) return MLA_ERR_UNSUPPORTED;
+    if (M == 0) return MLA_OK;
+    const size_t need = gated_layer_workspace_bytes(M, H, d_q, d_v, r, r_q, f32);
+    if (!workspace || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    LayerArgs a{x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, y, scale, B, T, D, H, d_q, d_v, r, r_q,
+                f32, workspace, workspace_bytes, dev->err_word, dev->num_sms};
+    const cudaError_t e = launch_gated_layer(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API int mla_get_device_error(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
     DeviceInfo *dev = nullptr;

@@ -52,6 +52,39 @@ bool decode_bf16_supports(int H, int d_v, int r);
 size_t decode_noalloc_scratch_capacity();
 cudaError_t decode_noalloc_scratch(void **ptr);
 
+// bf16 tensor-core GEMM C[M,N] = A[M,K] . B[N,K]^T (both row-major, K-major operands), fp32
+// accumulation, bf16 output, with the epilogues the layer's projections need.
+enum GemmEpilogue { kGemmPlain = 0, kGemmSumSq = 1, kGemmRowScale = 2, kGemmRmsNorm = 3 };
+struct GemmArgs {
+    const void *A, *B;
+    void *C;
+    float *ss;   // row sums of squares: accumulated (kGemmSumSq) or read (kGemmRowScale)
+    int M, N, K;
+    long long lda, ldb, ldc;   // elements
+    int epilogue;
+    float n_norm, eps;         // RMSNorm divisor (columns of the normalised row) and epsilon
+    int *dev_err;
+    int num_sms;
+};
+bool gemm_bf16_supports(int N, int K, int epilogue);
+cudaError_t launch_gemm_bf16(const GemmArgs &g, cudaStream_t s);
+
+// The whole Gated-MLA layer: step-1 projections, the absorbed attention, W_o.
+struct LayerArgs {
+    const void *x, *w_q_down, *w_q_up, *w_kv_down, *w_kv_up, *w_gate, *w_o;
+    void *y;
+    float scale;
+    int B, T, D, H, d_q, d_v, r, r_q;
+    bool f32;
+    void *workspace;
+    size_t workspace_bytes;
+    int *dev_err;
+    int num_sms;
+};
+bool gated_layer_supports(int D, int H, int d_q, int d_v, int r, int r_q, bool f32);
+size_t gated_layer_workspace_bytes(long long M, int H, int d_q, int d_v, int r, int r_q, bool f32);
+cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s);
+
 // Driver entry point for cuTensorMapEncodeTiled, resolved once through the runtime.
 void *tensor_map_encode_fn();
 

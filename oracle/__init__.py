@@ -8,7 +8,8 @@ library.
 * ``prefill`` / ``decode`` call the plain C loops in ``mla_oracle.c`` (steps
   2-4 of the page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）").
 * ``layer`` holds step 1 (the low-rank latent and query paths) and the output
-  projection of step 4, in numpy fp64, used to build full-layer inputs.
+  projection of step 4, in numpy fp64, used to build full-layer inputs;
+  ``layer_forward`` composes them with ``prefill`` into the whole layer.
 
 Parity status of each function is stated in its docstring; the pins live in
 ``tests/test_oracle.py``.
@@ -113,6 +114,35 @@ def prefill(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, rows=None, lib=None
     if rc != 0:
         raise ValueError(f"oracle prefill rejected its arguments (code {rc})")
     return out
+
+
+def layer_forward(x, p, H: int, d_q: int, d_v: int, scale: float = 1.0, rows=None) -> np.ndarray:
+    """The whole Gated-MLA layer in fp64: x [B,T,D] -> y, for all rows or the flattened rows ``rows``.
+
+    Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）": step 1 (``layer``:
+    c = RMSNorm(x W_kv_down^T), q = RMSNorm(x W_q_down^T) W_q_up^T, g = x W_gate^T), steps
+    2-4 (``prefill``), then y = o W_o^T (``layer.output_projection``).  ``p`` holds the
+    weights as nn.Linear weights under the keys of ``workloads.draw_layer``: q_down, q_up,
+    kv_down, kv_up, gate, o_proj.  Only the requested rows' q, g and o are formed; c is
+    formed for every row (each row's attention reads all earlier latents).
+    Returns [B,T,D], or [len(rows), D].
+    Parity: a composition of pinned parts (tests/test_oracle.py checks it against the
+    all-rows composition of ``layer.step1``, ``prefill`` and ``layer.output_projection``).
+    """
+    from . import layer
+    x = _f64(x)
+    B, T, D = x.shape
+    flat = x.reshape(B * T, D)
+    sel = np.arange(B * T) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    c = layer.rmsnorm(flat @ _f64(p["kv_down"]).T).reshape(B, T, -1)
+    q = np.zeros((B * T, H * d_q))
+    q[sel] = layer.rmsnorm(flat[sel] @ _f64(p["q_down"]).T) @ _f64(p["q_up"]).T
+    g = np.zeros((B * T, H * d_v))
+    g[sel] = flat[sel] @ _f64(p["gate"]).T
+    w_uk, w_uv = layer.split_kv_up(_f64(p["kv_up"]), H, d_q, d_v)
+    o = prefill(q.reshape(B, T, H, d_q), c, w_uk, w_uv, g.reshape(B, T, H * d_v), scale, rows=sel)
+    y = layer.output_projection(o, p["o_proj"])
+    return y.reshape(B, T, D) if rows is None else y
 
 
 def decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0) -> np.ndarray:

@@ -125,3 +125,51 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 4, 2, 16)
     with pytest.raises(ValueError, match="CUDA tensor"):
         lca.mla_absorbed_attn_fwd(x, torch.zeros(1, 4, 32), torch.zeros(2, 16, 32), torch.zeros(2, 16, 32))
+
+
+# ----------------------------------------------------------------------------- whole layer
+def layer(lib, x=FAKE, wqd=FAKE, wqu=FAKE, wkvd=FAKE, wkvu=FAKE, wg=FAKE, wo=FAKE, y=FAKE, B=1, T=16, D=256, H=2,
+          dq=128, dv=128, r=512, rq=256, dtype=BF16, ws=FAKE, ws_bytes=1 << 40):
+    return lib.mla_gated_layer_fwd(x, wqd, wqu, wkvd, wkvu, wg, wo, 1.0, y, B, T, D, H, dq, dv, r, rq, dtype, ws,
+                                   ws_bytes, None)
+
+
+@pytest.mark.parametrize("field", ["x", "wqd", "wqu", "wkvd", "wkvu", "wg", "wo", "y"])
+def test_layer_null_pointer(lib, field):
+    assert layer(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("field", ["x", "wo", "y", "ws"])
+def test_layer_misaligned(lib, field):
+    assert layer(lib, **{field: FAKE + 8}) == ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(D=0), dict(H=0), dict(rq=0), dict(B=1 << 20, T=1 << 20)])
+def test_layer_bad_shape(lib, kw):
+    assert layer(lib, **kw) == ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(H=3), dict(D=320), dict(rq=320), dict(r=256), dict(dq=64),
+                                dict(dtype=F32, r=128, dq=16, dv=16)])
+def test_layer_unsupported(lib, kw):
+    assert layer(lib, **kw) == ERR_UNSUPPORTED
+
+
+def test_layer_workspace_checked_before_launch(lib):
+    need = lib.mla_gated_layer_workspace_size(1, 16, 256, 2, 128, 128, 512, 256, BF16)
+    assert need > 0
+    assert layer(lib, ws=None) == ERR_WORKSPACE
+    assert layer(lib, ws_bytes=need - 1) == ERR_WORKSPACE
+    assert layer(lib, dtype=9) == ERR_DTYPE
+    assert layer(lib, T=0) == OK
+
+
+def test_layer_workspace_size(lib):
+    # q, c, g, o, the low-rank query and the row sums, each on a 256-byte boundary
+    B, T, D, H, d, r, rq = 2, 128, 256, 8, 16, 32, 64
+    M = B * T
+    parts = [M * H * d * 4, M * r * 4, M * H * d * 4, M * H * d * 4, M * rq * 4, M * 4]
+    assert lib.mla_gated_layer_workspace_size(B, T, D, H, d, d, r, rq, F32) == sum((p + 255) // 256 * 256
+                                                                                   for p in parts)
+    assert lib.mla_gated_layer_workspace_size(1, 16, 256, 3, 128, 128, 512, 256, BF16) == 0
+    assert lib.mla_gated_layer_workspace_size(1, 16, 256, 2, 128, 128, 512, 256, 5) == 0

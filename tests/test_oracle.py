@@ -87,6 +87,22 @@ def test_absorbed_equals_decompressed_toy_layer(oracle):
     assert rel_err(y, ref @ p["o_proj"].T) < 1e-12
 
 
+def test_layer_forward_is_the_composition_of_its_steps(oracle):
+    """layer_forward (all rows, and a row sample) == step 1, prefill, W_o composed by hand, with the
+    attention replaced by its explicit-decompression form, so a slip in the composition fails here."""
+    w = W.TOY_LAYER_F32
+    p = W.draw_layer(w, T=48, B=2)
+    q, c, g = layer.step1(p["x"], p["kv_down"], p["q_down"], p["q_up"], p["gate"], w.H, w.d_q)
+    w_uk, w_uv = layer.split_kv_up(p["kv_up"], w.H, w.d_q, w.d_v)
+    ref = decompressed(q, c, w_uk, w_uv, g, 0.7) @ p["o_proj"].T
+    full = oracle.layer_forward(p["x"], p, w.H, w.d_q, w.d_v, 0.7)
+    assert full.shape == (2, 48, w.D)
+    assert rel_err(full, ref) < 1e-12
+    rows = np.array([0, 5, 47, 48, 70, 95])
+    part = oracle.layer_forward(p["x"], p, w.H, w.d_q, w.d_v, 0.7, rows=rows)
+    assert rel_err(part, ref.reshape(96, w.D)[rows]) < 1e-12
+
+
 def test_peaky_attention_equals_decompressed(oracle):
     """Stress case: W_UK ~ N(0,1) makes attention nearly one-hot; the identity still holds."""
     rng = np.random.default_rng(7)
