@@ -244,6 +244,8 @@ def run_ours(args):
 
     decode = run_decode(torch, lca, dev, stream, flush, args, pk) if not args.no_decode else None
     layer_line = run_layer(torch, lca, dev, stream, flush, args, pk) if not args.no_layer else None
+    layer_dec = run_layer_decode(torch, lca, dev, stream, flush, args, pk) \
+        if not (args.no_layer or args.no_decode) else None
     if lca.mla_get_device_error() != 0:
         raise RuntimeError("device error word set after the timed region")
 
@@ -272,6 +274,8 @@ def run_ours(args):
             line["decode"] = decode
         if layer_line is not None:
             line["layer"] = layer_line
+        if layer_dec is not None:
+            line["layer_decode"] = layer_dec
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -346,6 +350,45 @@ def run_layer(torch, lca, dev, stream, flush, args, pk):
                          "frac": round(tf / pk["bf16_tflops"], 4), "peak_source": pk["source"] + " (burst bf16)",
                          "traffic": None},
             "gpu_launches": 6 * args.steps}
+
+
+def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
+    """One decode step of the whole layer (step 1, latent append, cached-latent attention, W_o) for the
+    decode workload's sequences, with the prefill workload's layer sizes."""
+    w = PREFILL
+    dw = DECODE
+    p = W.draw_layer(dataclasses.replace(w, B=dw.B, T=1), seed=1)
+    to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
+    t = {k: to(v) for k, v in p.items()}
+    del p
+    x = t["x"].reshape(dw.B, w.D)
+    d = decode_inputs(torch, dev)
+    lens = d["lens"].clone()
+    ok = lens < dw.max_len            # a sequence at the cache's end keeps its length (no free row)
+    lens = torch.where(ok, lens, lens - 1).to(torch.int32)
+    y = torch.empty((dw.B, w.D), dtype=torch.bfloat16, device=dev)
+    need = lca.library().mla_gated_layer_decode_workspace_size(dw.B, w.D, w.H, w.d_q, w.d_v, w.r, w.r_q,
+                                                               dw.max_len, lca.DTYPE_BF16)
+    if need == 0:
+        return {"unavailable": "layer decode shape not supported"}
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    step = lambda: lca.mla_gated_layer_decode(x, t["q_down"], t["q_up"], t["kv_down"], t["kv_up"],  # noqa: E731
+                                              t["gate"], t["o_proj"], d["cache"], lens, w.H, w.d_q, w.d_v,
+                                              dw.scale, out=y, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = statistics.mean(timed_steps(torch, step, args.steps, flush, stream))
+    cache_bytes = int((lens.to(torch.int64) + 1).sum().item()) * w.r * 2
+    weight_bytes = sum(int(v.numel()) * 2 for k, v in t.items() if k != "x")
+    gbs = (cache_bytes + weight_bytes) / (ms * 1e-3) / 1e9
+    return {"workload": "k3_layer_decode_bf16", "value": round(dw.B / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(ms, 4), "tokens_per_step": dw.B, "cache_bytes_per_step": cache_bytes,
+            "weight_bytes_per_step": weight_bytes,
+            "roofline": {"kernel": "layer decode step (6 GEMMs with M = B, append, absorb, pair + merge)",
+                         "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"], "traffic": None},
+            "gpu_launches": 9 * args.steps}
 
 
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)

@@ -203,6 +203,44 @@ MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void 
                                 void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * mla_gated_layer_decode_workspace_size - bytes of device workspace
+ * mla_gated_layer_decode needs on the CURRENT device (0 if unsupported).
+ */
+MLA_API size_t mla_gated_layer_decode_workspace_size(int B, int D, int H, int d_q, int d_v, int r, int r_q,
+                                                     int max_len, int dtype);
+
+/*
+ * mla_gated_layer_decode - one decode step of the whole layer with the
+ * latent-cache append (page "Gated MLA（矩阵吸收版）": only the latent c is
+ * cached, section "低秩压缩"; steps 1-4 of section "完整计算流（四步）"; W_o).
+ * For each sequence b, the new token x[b] (position lens[b]):
+ *
+ *   c_cache[b, lens[b], :] = RMSNorm(x[b] . w_kv_down^T)          (the append)
+ *   q_abs = (RMSNorm(x[b] . w_q_down^T) . w_q_up^T) . W_UK          per head
+ *   o     = mla_latent_decode(q_abs, c_cache, lens[b] + 1 rows, W_UV, g = x[b] . w_gate^T, scale)
+ *   y[b]  = o . w_o^T
+ *
+ *   x [B, D], y [B, D]; weights as in mla_gated_layer_fwd.
+ *   c_cache    [B, max_len, r] with row stride ld_cache (elements, multiple of
+ *              8, >= r); row lens[b] of each sequence is written.
+ *   lens       int32 [B] on the device: the new token's position, in
+ *              [0, max_len).  Read only; the caller advances it after the
+ *              step.  A position outside the range is reported as
+ *              MLA_ERR_DEVICE_BOUNDS (mla_get_device_error) and that row is
+ *              not written.
+ *   workspace  >= mla_gated_layer_decode_workspace_size(...) bytes, 16-byte
+ *              aligned.
+ * Supported: MLA_DTYPE_BF16 with r = 512, d_q = d_v = 128, 1 <= H <= 96 and
+ * even, D and r_q multiples of 256.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
+                                   const void *w_kv_up, const void *w_gate, const void *w_o, float scale, void *y,
+                                   void *c_cache, long long ld_cache, const int *lens, int max_len, int B, int D,
+                                   int H, int d_q, int d_v, int r, int r_q, int dtype, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * mla_get_device_error - synchronise `stream`, then read and clear the current
  * device's error word.  Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT,
  * MLA_ERR_DEVICE_BOUNDS, or MLA_ERR_CUDA if the synchronisation itself failed.

@@ -22,7 +22,7 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error", "mla_status_string", "mla_version",
-           "mla_gated_layer_fwd", "mla_gated_layer_workspace_size", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
+           "mla_gated_layer_fwd", "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
@@ -63,6 +63,10 @@ def library():
             lib.mla_gated_layer_workspace_size.restype = sz
             lib.mla_gated_layer_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, f, vp] + [i] * 9 + [vp, sz, vp]
             lib.mla_gated_layer_fwd.restype = i
+            lib.mla_gated_layer_decode_workspace_size.argtypes = [i] * 9
+            lib.mla_gated_layer_decode_workspace_size.restype = sz
+            lib.mla_gated_layer_decode.argtypes = [vp] * 7 + [f, vp, vp, ll, vp] + [i] * 9 + [vp, sz, vp]
+            lib.mla_gated_layer_decode.restype = i
             lib.mla_get_device_error.argtypes = [vp]
             lib.mla_get_device_error.restype = i
             lib.mla_status_string.argtypes = [i]
@@ -207,6 +211,47 @@ def mla_gated_layer_fwd(x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, H:
                                  _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_gated_layer_fwd")
+    return out
+
+
+def mla_gated_layer_decode(x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, c_cache, lens, H: int, d_q: int,
+                           d_v: int, scale: float = 1.0, out=None, workspace=None, stream=None):
+    """One decode step of the whole layer: x [B,D] (the new tokens) -> y [B,D].
+
+    Appends each token's latent to c_cache [B,max_len,r] (unit inner stride) at row lens[b]
+    (int32 [B] on the device, read only: advance it after the step), then attends to rows
+    [0, lens[b]].  Weights as in ``mla_gated_layer_fwd``.  bf16 only.
+    """
+    torch = _torch()
+    B, D = x.shape
+    r_q, r = w_q_down.shape[0], w_kv_down.shape[0]
+    dev, dt = x.device, x.dtype
+    _check(x, "x", dt, dev)
+    for name, t, shape in (("w_q_down", w_q_down, (r_q, D)), ("w_q_up", w_q_up, (H * d_q, r_q)),
+                           ("w_kv_down", w_kv_down, (r, D)), ("w_kv_up", w_kv_up, (H * (d_q + d_v), r)),
+                           ("w_gate", w_gate, (H * d_v, D)), ("w_o", w_o, (D, H * d_v))):
+        _check(t, name, dt, dev, shape)
+    max_len = c_cache.shape[1]
+    if c_cache.dtype != dt or c_cache.device != dev or c_cache.dim() != 3 or c_cache.shape[0] != B \
+            or c_cache.shape[2] != r or c_cache.stride(2) != 1 or c_cache.stride(0) != max_len * c_cache.stride(1):
+        raise ValueError("c_cache must be [B,max_len,r] with unit inner stride and batch stride max_len*row_stride")
+    _check(lens, "lens", torch.int32, dev, (B,))
+    if out is None:
+        out = torch.empty((B, D), dtype=dt, device=dev)
+    _check(out, "out", dt, dev, (B, D))
+    lib = library()
+    code = _dtype_code(x)
+    need = int(lib.mla_gated_layer_decode_workspace_size(B, D, H, d_q, d_v, r, r_q, max_len, code))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_gated_layer_decode(x.data_ptr(), w_q_down.data_ptr(), w_q_up.data_ptr(), w_kv_down.data_ptr(),
+                                    w_kv_up.data_ptr(), w_gate.data_ptr(), w_o.data_ptr(), float(scale),
+                                    out.data_ptr(), c_cache.data_ptr(), c_cache.stride(1), lens.data_ptr(), max_len,
+                                    B, D, H, d_q, d_v, r, r_q, code, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_gated_layer_decode")
     return out
 
 

@@ -221,6 +221,44 @@ MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void 
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+MLA_API size_t mla_gated_layer_decode_workspace_size(int B, int D, int H, int d_q, int d_v, int r, int r_q,
+                                                     int max_len, int dtype) {
+    if (dtype != MLA_DTYPE_BF16 || B <= 0 || max_len < 0) return 0;
+    if (!gated_layer_decode_supports(D, H, d_q, d_v, r, r_q)) return 0;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return 0;
+    return gated_layer_decode_workspace_bytes(B, H, d_q, d_v, r, r_q, max_len, dev->num_sms);
+}
+
+MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
+                                   const void *w_kv_up, const void *w_gate, const void *w_o, float scale, void *y,
+                                   void *c_cache, long long ld_cache, const int *lens, int max_len, int B, int D,
+                                   int H, int d_q, int d_v, int r, int r_q, int dtype, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || D <= 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0 || r_q <= 0 || max_len < 0 || ld_cache < r)
+        return MLA_ERR_SHAPE;
+    if (!mul_fits(static_cast<long long>(B) * max_len, ld_cache, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (!x || !w_q_down || !w_q_up || !w_kv_down || !w_kv_up || !w_gate || !w_o || !y || !c_cache || !lens)
+        return MLA_ERR_NULL;
+    if (!aligned16(x) || !aligned16(w_q_down) || !aligned16(w_q_up) || !aligned16(w_kv_down) ||
+        !aligned16(w_kv_up) || !aligned16(w_gate) || !aligned16(w_o) || !aligned16(y) || !aligned16(c_cache) ||
+        !aligned16(lens) || (ld_cache % 8) != 0)
+        return MLA_ERR_ALIGN;
+    if (dtype != MLA_DTYPE_BF16 || !gated_layer_decode_supports(D, H, d_q, d_v, r, r_q)) return MLA_ERR_UNSUPPORTED;
+    if (B == 0) return MLA_OK;
+    if (!workspace) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (workspace_bytes < gated_layer_decode_workspace_bytes(B, H, d_q, d_v, r, r_q, max_len, dev->num_sms))
+        return MLA_ERR_WORKSPACE;
+    LayerDecodeArgs a{x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, y, c_cache, ld_cache, lens, max_len,
+                      scale, B, D, H, d_q, d_v, r, r_q, workspace, workspace_bytes, dev->err_word, dev->num_sms};
+    const cudaError_t e = launch_gated_layer_decode(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API int mla_get_device_error(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MLA_ERR_CUDA;
     DeviceInfo *dev = nullptr;

@@ -85,6 +85,27 @@ bool gated_layer_supports(int D, int H, int d_q, int d_v, int r, int r_q, bool f
 size_t gated_layer_workspace_bytes(long long M, int H, int d_q, int d_v, int r, int r_q, bool f32);
 cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s);
 
+// One decode step of the whole layer: the new token's latent is appended to the cache at
+// row lens[b], then the sequence attends to rows [0, lens[b]].
+struct LayerDecodeArgs {
+    const void *x, *w_q_down, *w_q_up, *w_kv_down, *w_kv_up, *w_gate, *w_o;
+    void *y;
+    void *c_cache;
+    long long ld_cache;
+    const int *lens;
+    int max_len;
+    float scale;
+    int B, D, H, d_q, d_v, r, r_q;
+    void *workspace;
+    size_t workspace_bytes;
+    int *dev_err;
+    int num_sms;
+};
+bool gated_layer_decode_supports(int D, int H, int d_q, int d_v, int r, int r_q);
+size_t gated_layer_decode_workspace_bytes(int B, int H, int d_q, int d_v, int r, int r_q, int max_len,
+                                          int num_sms);
+cudaError_t launch_gated_layer_decode(const LayerDecodeArgs &a, cudaStream_t s);
+
 // Driver entry point for cuTensorMapEncodeTiled, resolved once through the runtime.
 void *tensor_map_encode_fn();
 

@@ -173,3 +173,32 @@ def test_layer_workspace_size(lib):
                                                                                    for p in parts)
     assert lib.mla_gated_layer_workspace_size(1, 16, 256, 3, 128, 128, 512, 256, BF16) == 0
     assert lib.mla_gated_layer_workspace_size(1, 16, 256, 2, 128, 128, 512, 256, 5) == 0
+
+
+def layer_decode(lib, x=FAKE, y=FAKE, cache=FAKE, ld=512, lens=FAKE, max_len=64, B=2, D=256, H=2, r=512, rq=256,
+                 dtype=BF16, ws=FAKE, ws_bytes=1 << 40):
+    return lib.mla_gated_layer_decode(x, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1.0, y, cache, ld, lens, max_len, B, D,
+                                      H, 128, 128, r, rq, dtype, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [dict(x=None), dict(y=None), dict(cache=None), dict(lens=None)])
+def test_layer_decode_null_pointer(lib, kw):
+    assert layer_decode(lib, **kw) == ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(ld=100), dict(max_len=-1), dict(B=-1), dict(D=0)])
+def test_layer_decode_bad_shape(lib, kw):
+    assert layer_decode(lib, **kw) == ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=F32), dict(H=3), dict(H=98), dict(rq=128), dict(r=256, ld=256)])
+def test_layer_decode_unsupported(lib, kw):
+    assert layer_decode(lib, **kw) == ERR_UNSUPPORTED
+
+
+def test_layer_decode_checks_before_launch(lib):
+    assert layer_decode(lib, lens=FAKE + 4) == ERR_ALIGN
+    assert layer_decode(lib, ld=520 + 4) == ERR_ALIGN
+    assert layer_decode(lib, ws=None) == ERR_WORKSPACE
+    assert layer_decode(lib, B=0) == OK
+    assert layer_decode(lib, dtype=4) == ERR_DTYPE
