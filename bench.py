@@ -166,8 +166,12 @@ def decode_inputs(torch, dev):
 
 
 def timed_steps(torch, fn, steps, flush, stream):
-    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step (outside the events)."""
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step (outside the events),
+    and the number of kernels the library launched over the steps (its own launch counter)."""
+    import latent_compressed_attention_gb300 as lca
+
     times = []
+    first = lca.mla_kernel_launches()
     for _ in range(steps):
         flush.zero_()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -176,7 +180,7 @@ def timed_steps(torch, fn, steps, flush, stream):
         e.record(stream)
         e.synchronize()
         times.append(s.elapsed_time(e))
-    return times
+    return times, lca.mla_kernel_launches() - first
 
 
 def run_ours(args):
@@ -210,7 +214,7 @@ def run_ours(args):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        times = timed_steps(torch, step, args.steps, flush, stream)
+        times, launches = timed_steps(torch, step, args.steps, flush, stream)
     torch.cuda.synchronize()
     barrier(world)
     total_ms = max_over_ranks(sum(times), world)
@@ -238,7 +242,7 @@ def run_ours(args):
         for _ in range(2):
             e2e_step()
         torch.cuda.synchronize()
-        e2e_times = timed_steps(torch, e2e_step, max(3, args.steps // 2), flush, stream)
+        e2e_times, _ = timed_steps(torch, e2e_step, max(3, args.steps // 2), flush, stream)
         e2e_ms = max_over_ranks(statistics.mean(e2e_times), world)
         e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
@@ -267,7 +271,7 @@ def run_ours(args):
                          "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
                          "peak_source": pk["source"] + " (burst bf16)",
                          "traffic": committed_traffic("prefill_r512_kernel", KERNEL_SRC)},
-            "gpu_launches": args.steps,
+            "gpu_launches": launches,
             "clocks": clk.summary(),
         }
         if decode is not None:
@@ -299,7 +303,7 @@ def run_decode(torch, lca, dev, stream, flush, args, pk):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    times = timed_steps(torch, step, args.steps, flush, stream)
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
     ms = statistics.mean(times)
     cache_bytes = int(d["lens_np"].astype(np.int64).sum()) * DECODE.r * 2
     gbs = cache_bytes / (ms * 1e-3) / 1e9
@@ -309,7 +313,7 @@ def run_decode(torch, lca, dev, stream, flush, args, pk):
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "peak_source": pk["source"],
                          "traffic": committed_traffic("decode", DECODE_SRC)},
-            "gpu_launches": 2 * args.steps}
+            "gpu_launches": launches}
 
 
 def layer_flops(w) -> dict:
@@ -337,7 +341,8 @@ def run_layer(torch, lca, dev, stream, flush, args, pk):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    ms = statistics.mean(timed_steps(torch, step, args.steps, flush, stream))
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
     fl = layer_flops(w)
     tf = fl["total"] / (ms * 1e-3) / 1e12
     return {"workload": w.name.replace("prefill", "layer"), "value": round(tf, 2), "unit": "TFLOP/s",
@@ -349,7 +354,7 @@ def run_layer(torch, lca, dev, stream, flush, args, pk):
                          "achieved": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tf / pk["bf16_tflops"], 4), "peak_source": pk["source"] + " (burst bf16)",
                          "traffic": None},
-            "gpu_launches": 6 * args.steps}
+            "gpu_launches": launches}
 
 
 def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
@@ -378,7 +383,8 @@ def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    ms = statistics.mean(timed_steps(torch, step, args.steps, flush, stream))
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
     cache_bytes = int((lens.to(torch.int64) + 1).sum().item()) * w.r * 2
     weight_bytes = sum(int(v.numel()) * 2 for k, v in t.items() if k != "x")
     gbs = (cache_bytes + weight_bytes) / (ms * 1e-3) / 1e9
@@ -388,7 +394,7 @@ def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
             "roofline": {"kernel": "layer decode step (6 GEMMs with M = B, append, absorb, pair + merge)",
                          "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"], "traffic": None},
-            "gpu_launches": 9 * args.steps}
+            "gpu_launches": launches}
 
 
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)

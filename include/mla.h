@@ -253,6 +253,12 @@ MLA_API const char *mla_status_string(int status);
 /* mla_version - library version as major*10000 + minor*100 + patch. */
 MLA_API int mla_version(void);
 
+/*
+ * mla_kernel_launches - kernels this library has launched in this process
+ * (every entry point, device and stream; a diagnostic counter, never reset).
+ */
+MLA_API unsigned long long mla_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

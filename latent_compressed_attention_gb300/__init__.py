@@ -21,8 +21,10 @@ import threading
 from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
-           "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error", "mla_status_string", "mla_version",
-           "mla_gated_layer_fwd", "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
+           "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
+           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_gated_layer_fwd",
+           "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16",
+           "DTYPE_F32"]
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
@@ -73,6 +75,8 @@ def library():
             lib.mla_status_string.restype = ctypes.c_char_p
             lib.mla_version.argtypes = []
             lib.mla_version.restype = i
+            lib.mla_kernel_launches.argtypes = []
+            lib.mla_kernel_launches.restype = ctypes.c_ulonglong
             _lib = lib
     return _lib
 
@@ -86,6 +90,11 @@ def mla_status_string(status: int) -> str:
 
 def mla_version() -> int:
     return int(library().mla_version())
+
+
+def mla_kernel_launches() -> int:
+    """Kernels the library has launched in this process (a diagnostic counter)."""
+    return int(library().mla_kernel_launches())
 
 
 # ----------------------------------------------------------------------------- torch marshalling

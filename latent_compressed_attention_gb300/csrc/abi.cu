@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <mutex>
@@ -26,6 +27,7 @@ struct DeviceInfo {
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_mutex;
+std::atomic<unsigned long long> g_launches{0};
 
 cudaError_t device_info(DeviceInfo *&out) {
     int dev = 0;
@@ -54,6 +56,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool mul_fits(long long a, long long b, long long limit) { return a == 0 || b <= limit / a; }
 
 }  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void *tensor_map_encode_fn() {
     static void *fn = nullptr;
@@ -92,6 +96,8 @@ MLA_API const char *mla_status_string(int status) {
 }
 
 MLA_API int mla_version(void) { return 100; }
+
+MLA_API unsigned long long mla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
                                   const void *gate, float scale, void *out, int B, int T, int H, int d_q,
@@ -190,7 +196,7 @@ MLA_API size_t mla_gated_layer_workspace_size(int B, int T, int D, int H, int d_
     if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32)) return 0;
     const long long M = static_cast<long long>(B) * T;
     if (M > INT_MAX) return 0;
-    return gated_layer_workspace_bytes(M, H, d_q, d_v, r, r_q, f32);
+    return gated_layer_workspace_bytes(M, D, H, d_q, d_v, r, r_q, f32);
 }
 
 MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
@@ -210,7 +216,7 @@ MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void 
     const bool f32 = dtype == MLA_DTYPE_F32;
     if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32)) return MLA_ERR_UNSUPPORTED;
     if (M == 0) return MLA_OK;
-    const size_t need = gated_layer_workspace_bytes(M, H, d_q, d_v, r, r_q, f32);
+    const size_t need = gated_layer_workspace_bytes(M, D, H, d_q, d_v, r, r_q, f32);
     if (!workspace || workspace_bytes < need) return MLA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     DeviceInfo *dev = nullptr;
@@ -227,7 +233,7 @@ MLA_API size_t mla_gated_layer_decode_workspace_size(int B, int D, int H, int d_
     if (!gated_layer_decode_supports(D, H, d_q, d_v, r, r_q)) return 0;
     DeviceInfo *dev = nullptr;
     if (device_info(dev) != cudaSuccess) return 0;
-    return gated_layer_decode_workspace_bytes(B, H, d_q, d_v, r, r_q, max_len, dev->num_sms);
+    return gated_layer_decode_workspace_bytes(B, D, H, d_q, d_v, r, r_q, max_len, dev->num_sms);
 }
 
 MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const void *w_q_up, const void *w_kv_down,
@@ -251,7 +257,7 @@ MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const vo
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     DeviceInfo *dev = nullptr;
     if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (workspace_bytes < gated_layer_decode_workspace_bytes(B, H, d_q, d_v, r, r_q, max_len, dev->num_sms))
+    if (workspace_bytes < gated_layer_decode_workspace_bytes(B, D, H, d_q, d_v, r, r_q, max_len, dev->num_sms))
         return MLA_ERR_WORKSPACE;
     LayerDecodeArgs a{x, w_q_down, w_q_up, w_kv_down, w_kv_up, w_gate, w_o, y, c_cache, ld_cache, lens, max_len,
                       scale, B, D, H, d_q, d_v, r, r_q, workspace, workspace_bytes, dev->err_word, dev->num_sms};

@@ -1217,6 +1217,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     pp.max_len = a.max_len;
     pp.qk_scale_log2 = a.scale * kLog2e;
     decode_pair_kernel<<<2 * G, kThreads, kSmemPair, s>>>(tm_c256, tm_c, pp);
+    note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     MergeParams mp;
@@ -1241,6 +1242,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    note_launch();
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel, tm_wuv, mp);
 }
 

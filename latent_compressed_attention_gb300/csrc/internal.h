@@ -65,8 +65,11 @@ struct GemmArgs {
     float n_norm, eps;         // RMSNorm divisor (columns of the normalised row) and epsilon
     int *dev_err;
     int num_sms;
+    // Split K (few row tiles): zeroed scratch of gemm_bf16_split_bytes() bytes, or NULL = never split
+    float *split_acc;
 };
 bool gemm_bf16_supports(int N, int K, int epilogue);
+size_t gemm_bf16_split_bytes(const GemmArgs &g);   // 0: this product does not split
 cudaError_t launch_gemm_bf16(const GemmArgs &g, cudaStream_t s);
 
 // The whole Gated-MLA layer: step-1 projections, the absorbed attention, W_o.
@@ -82,7 +85,12 @@ struct LayerArgs {
     int num_sms;
 };
 bool gated_layer_supports(int D, int H, int d_q, int d_v, int r, int r_q, bool f32);
-size_t gated_layer_workspace_bytes(long long M, int H, int d_q, int d_v, int r, int r_q, bool f32);
+// The layer's five bf16 projections in the order they run, and the zeroed split-K
+// scratch each reserves: slice i is [off[i], off[i + 1]) (empty = never splits), sized
+// for any device of up to 256 SMs; off[kLayerGemms] is the total.
+enum LayerGemm { kQDown = 0, kQUp, kKvDown, kGate, kOProj, kLayerGemms };
+size_t layer_split_plan(long long M, int D, int H, int d_q, int d_v, int r, int r_q, size_t off[kLayerGemms + 1]);
+size_t gated_layer_workspace_bytes(long long M, int D, int H, int d_q, int d_v, int r, int r_q, bool f32);
 cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s);
 
 // One decode step of the whole layer: the new token's latent is appended to the cache at
@@ -102,11 +110,14 @@ struct LayerDecodeArgs {
     int num_sms;
 };
 bool gated_layer_decode_supports(int D, int H, int d_q, int d_v, int r, int r_q);
-size_t gated_layer_decode_workspace_bytes(int B, int H, int d_q, int d_v, int r, int r_q, int max_len,
+size_t gated_layer_decode_workspace_bytes(int B, int D, int H, int d_q, int d_v, int r, int r_q, int max_len,
                                           int num_sms);
 cudaError_t launch_gated_layer_decode(const LayerDecodeArgs &a, cudaStream_t s);
 
 // Driver entry point for cuTensorMapEncodeTiled, resolved once through the runtime.
 void *tensor_map_encode_fn();
+
+// Count one kernel launch of this library (read by mla_kernel_launches).
+void note_launch();
 
 }  // namespace mla

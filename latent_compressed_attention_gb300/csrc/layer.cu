@@ -18,8 +18,9 @@
 //
 // Workspace, in this order, each part starting on a 256-byte boundary:
 // q [M, H d_q], c [M, r], g [M, H d_v], o [M, H d_v] (the layer's intermediate
-// results, in the input dtype), then the low-rank query [M, r_q] (input dtype)
-// and the row sums of squares [M] (fp32); M = B T.
+// results, in the input dtype), then the low-rank query [M, r_q] (input dtype),
+// the row sums of squares [M] (fp32) and (bf16) the fp32 split-K scratch of the
+// projections with too few row tiles to fill the GPU; M = B T.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -33,10 +34,31 @@ constexpr float kRmsEps = 1e-6f;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t q, c, g, o, yq, ss, end;
+    size_t q, c, g, o, yq, ss, acc, end;
 };
 
-Layout layout(long long M, int H, int d_q, int d_v, int r, int r_q, size_t es) {
+}  // namespace
+
+size_t layer_split_plan(long long M, int D, int H, int d_q, int d_v, int r, int r_q, size_t off[kLayerGemms + 1]) {
+    const int n[kLayerGemms] = {r_q, H * d_q, r, H * d_v, D};
+    const int k[kLayerGemms] = {D, r_q, D, D, H * d_v};
+    const int epi[kLayerGemms] = {kGemmSumSq, kGemmRowScale, kGemmRmsNorm, kGemmPlain, kGemmPlain};
+    off[0] = 0;
+    for (int i = 0; i < kLayerGemms; ++i) {
+        GemmArgs g{};
+        g.M = static_cast<int>(M);
+        g.N = n[i];
+        g.K = k[i];
+        g.epilogue = epi[i];
+        g.num_sms = 256;
+        off[i + 1] = off[i] + gemm_bf16_split_bytes(g);
+    }
+    return off[kLayerGemms];
+}
+
+namespace {
+
+Layout layout(long long M, int D, int H, int d_q, int d_v, int r, int r_q, size_t es) {
     Layout L;
     L.q = 0;
     L.c = L.q + align256(static_cast<size_t>(M) * H * d_q * es);
@@ -44,7 +66,9 @@ Layout layout(long long M, int H, int d_q, int d_v, int r, int r_q, size_t es) {
     L.o = L.g + align256(static_cast<size_t>(M) * H * d_v * es);
     L.yq = L.o + align256(static_cast<size_t>(M) * H * d_v * es);
     L.ss = L.yq + align256(static_cast<size_t>(M) * r_q * es);
-    L.end = L.ss + align256(static_cast<size_t>(M) * sizeof(float));
+    L.acc = L.ss + align256(static_cast<size_t>(M) * sizeof(float));   // split-K scratch, right after ss
+    size_t off[kLayerGemms + 1];
+    L.end = L.acc + (es == 2 ? layer_split_plan(M, D, H, d_q, d_v, r, r_q, off) : 0);
     return L;
 }
 
@@ -85,12 +109,14 @@ __global__ void rmsnorm_rows_f32_kernel(float *Z, int M, int N, float eps) {
 
 cudaError_t gemm_f32(const void *A, const void *B, void *C, long long M, int N, int K, cudaStream_t s) {
     const dim3 grid((N + kT - 1) / kT, static_cast<unsigned>((M + kT - 1) / kT));
+    note_launch();
     gemm_f32_kernel<<<grid, kT * kT, 0, s>>>(static_cast<const float *>(A), static_cast<const float *>(B),
                                                static_cast<float *>(C), static_cast<int>(M), N, K);
     return cudaGetLastError();
 }
 
 cudaError_t rmsnorm_f32(void *Z, long long M, int N, cudaStream_t s) {
+    note_launch();
     rmsnorm_rows_f32_kernel<<<static_cast<unsigned>((M + 7) / 8), 256, 0, s>>>(static_cast<float *>(Z),
                                                                               static_cast<int>(M), N, kRmsEps);
     return cudaGetLastError();
@@ -106,14 +132,14 @@ bool gated_layer_supports(int D, int H, int d_q, int d_v, int r, int r_q, bool f
            gemm_bf16_supports(H * d_v, D, kGemmPlain) && gemm_bf16_supports(D, H * d_v, kGemmPlain);
 }
 
-size_t gated_layer_workspace_bytes(long long M, int H, int d_q, int d_v, int r, int r_q, bool f32) {
-    return layout(M, H, d_q, d_v, r, r_q, f32 ? 4 : 2).end;
+size_t gated_layer_workspace_bytes(long long M, int D, int H, int d_q, int d_v, int r, int r_q, bool f32) {
+    return layout(M, D, H, d_q, d_v, r, r_q, f32 ? 4 : 2).end;
 }
 
 cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s) {
     const long long M = static_cast<long long>(a.B) * a.T;
     const size_t es = a.f32 ? 4 : 2;
-    const Layout L = layout(M, a.H, a.d_q, a.d_v, a.r, a.r_q, es);
+    const Layout L = layout(M, a.D, a.H, a.d_q, a.d_v, a.r, a.r_q, es);
     if (a.workspace_bytes < L.end) return cudaErrorInvalidValue;
     char *ws = static_cast<char *>(a.workspace);
     void *q = ws + L.q, *c = ws + L.c, *g = ws + L.g, *o = ws + L.o, *yq = ws + L.yq;
@@ -129,13 +155,16 @@ cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s) {
         if ((e = rmsnorm_f32(c, M, a.r, s)) != cudaSuccess) return e;
         if ((e = gemm_f32(a.x, a.w_gate, g, M, Hv, a.D, s)) != cudaSuccess) return e;
     } else {
-        if ((e = cudaMemsetAsync(ss, 0, static_cast<size_t>(M) * sizeof(float), s)) != cudaSuccess) return e;
+        // one memset zeroes the row sums of squares and every split-K slice
+        if ((e = cudaMemsetAsync(ss, 0, L.end - L.ss, s)) != cudaSuccess) return e;
+        size_t off[kLayerGemms + 1];
+        layer_split_plan(M, a.D, a.H, a.d_q, a.d_v, a.r, a.r_q, off);
         GemmArgs gm{};
         gm.M = static_cast<int>(M);
         gm.dev_err = a.dev_err;
         gm.num_sms = a.num_sms;
         gm.eps = kRmsEps;
-        auto run = [&](const void *A, long long lda, const void *B, void *C, int N, int K, int epi,
+        auto run = [&](int which, const void *A, long long lda, const void *B, void *C, int N, int K, int epi,
                        float n_norm) {
             gm.A = A;
             gm.lda = lda;
@@ -148,14 +177,20 @@ cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s) {
             gm.epilogue = epi;
             gm.ss = ss;
             gm.n_norm = n_norm;
+            gm.split_acc = nullptr;
+            const size_t need = gemm_bf16_split_bytes(gm);
+            if (need != 0 && need <= off[which + 1] - off[which])
+                gm.split_acc = reinterpret_cast<float *>(ws + L.acc + off[which]);
             return launch_gemm_bf16(gm, s);
         };
-        if ((e = run(a.x, a.D, a.w_q_down, yq, a.r_q, a.D, kGemmSumSq, 0.f)) != cudaSuccess) return e;
-        if ((e = run(yq, a.r_q, a.w_q_up, q, Hq, a.r_q, kGemmRowScale, static_cast<float>(a.r_q))) != cudaSuccess)
+        if ((e = run(kQDown, a.x, a.D, a.w_q_down, yq, a.r_q, a.D, kGemmSumSq, 0.f)) != cudaSuccess) return e;
+        if ((e = run(kQUp, yq, a.r_q, a.w_q_up, q, Hq, a.r_q, kGemmRowScale, static_cast<float>(a.r_q))) !=
+            cudaSuccess)
             return e;
-        if ((e = run(a.x, a.D, a.w_kv_down, c, a.r, a.D, kGemmRmsNorm, static_cast<float>(a.r))) != cudaSuccess)
+        if ((e = run(kKvDown, a.x, a.D, a.w_kv_down, c, a.r, a.D, kGemmRmsNorm, static_cast<float>(a.r))) !=
+            cudaSuccess)
             return e;
-        if ((e = run(a.x, a.D, a.w_gate, g, Hv, a.D, kGemmPlain, 0.f)) != cudaSuccess) return e;
+        if ((e = run(kGate, a.x, a.D, a.w_gate, g, Hv, a.D, kGemmPlain, 0.f)) != cudaSuccess) return e;
     }
     PrefillArgs pa{q, c, a.w_kv_up, w_uv, g, o, a.scale, a.B, a.T, a.H, a.d_q, a.d_v, a.r, a.dev_err, a.num_sms};
     e = a.f32 ? launch_prefill_f32_simt(pa, s) : launch_prefill_bf16_r512(pa, s);
@@ -174,6 +209,11 @@ cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s) {
     go.epilogue = kGemmPlain;
     go.dev_err = a.dev_err;
     go.num_sms = a.num_sms;
+    size_t off[kLayerGemms + 1];
+    layer_split_plan(M, a.D, a.H, a.d_q, a.d_v, a.r, a.r_q, off);
+    const size_t need = gemm_bf16_split_bytes(go);
+    if (need != 0 && need <= off[kOProj + 1] - off[kOProj])
+        go.split_acc = reinterpret_cast<float *>(ws + L.acc + off[kOProj]);
     return launch_gemm_bf16(go, s);
 }
 

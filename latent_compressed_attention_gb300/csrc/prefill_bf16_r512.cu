@@ -737,6 +737,7 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const long long n_ctas = 2LL * p.n_qtiles * p.bh_count;
     if (n_ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    note_launch();
     prefill_r512_kernel<<<static_cast<unsigned>(n_ctas), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk, tm_wuv, p);
     return cudaGetLastError();
 }

@@ -375,6 +375,7 @@ cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const long long n = static_cast<long long>(p.n_qtiles) * p.bh_count;
     if (n > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    note_launch();
     prefill_small_kernel<<<static_cast<unsigned>(n), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_wuk, tm_wuv, p);
     return cudaGetLastError();
 }

@@ -115,6 +115,7 @@ bool prefill_f32_simt_supports(int r, int d_q, int d_v) {
 cudaError_t launch_prefill_f32_simt(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_f32_simt_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
     const dim3 grid((a.T + kRows - 1) / kRows, a.H, a.B);
+    note_launch();
     prefill_f32_kernel<<<grid, kRows, 0, s>>>(
         static_cast<const float *>(a.q), static_cast<const float *>(a.c), static_cast<const float *>(a.w_uk),
         static_cast<const float *>(a.w_uv), static_cast<const float *>(a.gate), static_cast<float *>(a.out),

@@ -82,19 +82,17 @@ def test_decode_step_equals_prefill_row(env):
     assert rel_err(got, ref) <= TOL
 
 
-def test_decode_step_full_size_dims(env):
-    """D=7168, H=96, r_q=1536 (the K3 layer's sizes), four sequences of ragged synthetic caches."""
+def decode_against_oracle(env, w, B, max_len, seed):
+    """One step for B sequences at random positions, against the oracle's composition."""
     torch, lca, oracle = env
-    w = W.K3_PREFILL_BF16
-    B, max_len = 4, 4096
-    p = {k: W.round_bf16(v) for k, v in W.draw_layer(dataclasses.replace(w, B=B, T=1), seed=9).items()}
+    p = {k: W.round_bf16(v) for k, v in W.draw_layer(dataclasses.replace(w, B=B, T=1), seed=seed).items()}
     x_t = p["x"].reshape(B, w.D)
-    rng = np.random.default_rng(9)
-    pos = rng.integers(100, max_len - 1, B)
+    rng = np.random.default_rng(seed)
+    pos = rng.integers(0, max_len - 1, B)
     dec = dataclasses.replace(W.K3_DECODE_BF16, B=B)
     cache_np = np.zeros((B, max_len, w.r))
     for b in range(B):
-        cache_np[b, :pos[b]] = W.decode_cache_rows(dec, b, int(pos[b]), seed=9)
+        cache_np[b, :pos[b]] = W.decode_cache_rows(dec, b, int(pos[b]), seed=seed)
     cache = bf(torch, cache_np)
     lens = torch.tensor(pos, dtype=torch.int32, device="cuda")
     y = lca.mla_gated_layer_decode(bf(torch, x_t), *weights(torch, p), cache, lens, w.H, w.d_q, w.d_v, w.scale)
@@ -114,6 +112,17 @@ def test_decode_step_full_size_dims(env):
     assert rel_err(y.float().double().cpu().numpy(), ref) <= TOL
     got_rows = np.stack([cache[b, pos[b]].float().cpu().numpy() for b in range(B)])
     assert rel_err(got_rows, c_t) <= TOL
+
+
+def test_decode_step_full_size_dims(env):
+    """D=7168, H=96, r_q=1536 (the K3 layer's sizes), four sequences of ragged synthetic caches."""
+    decode_against_oracle(env, W.K3_PREFILL_BF16, B=4, max_len=4096, seed=9)
+
+
+def test_decode_step_batch_past_one_row_tile(env):
+    """130 sequences: two 128-row tiles in every projection and in the query absorption."""
+    w = dataclasses.replace(W.MID_PREFILL_BF16, D=512, H=2, r_q=256, scale=1.0 / np.sqrt(128.0))
+    decode_against_oracle(env, w, B=130, max_len=96, seed=4)
 
 
 def test_decode_step_position_out_of_range_is_reported(env):
