@@ -42,6 +42,9 @@ PREFILL = W.K3_PREFILL_BF16
 DECODE = W.K3_DECODE_BF16
 KERNEL_SRC = os.path.join(ROOT, "latent_compressed_attention_gb300", "csrc", "prefill_bf16_r512.cu")
 DECODE_SRC = os.path.join(ROOT, "latent_compressed_attention_gb300", "csrc", "decode_bf16.cu")
+_CSRC = os.path.join(ROOT, "latent_compressed_attention_gb300", "csrc")
+LAYER_SRCS = [os.path.join(_CSRC, f) for f in ("gemm_bf16.cu", "layer.cu", "prefill_bf16_r512.cu")]
+LAYER_DECODE_SRCS = [os.path.join(_CSRC, f) for f in ("gemm_bf16.cu", "layer_decode.cu", "decode_bf16.cu")]
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 L2_FLUSH_BYTES = 512 << 20   # > 129 MB L2
 
@@ -56,13 +59,17 @@ def peaks():
     return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
 
 
-def src_hash(path):
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(paths):
+    """First 16 hex digits of the SHA-256 of the files' bytes, concatenated in order."""
+    h = hashlib.sha256()
+    for path in ([paths] if isinstance(paths, str) else paths):
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, src: str):
-    """DRAM bytes per launch from a committed ncu capture, if the kernel source is unchanged since."""
+def committed_traffic(kernel: str, src):
+    """DRAM bytes per launch (or per call) from a committed ncu capture, if the sources are unchanged since."""
     try:
         with open(PROFILE_TRAFFIC) as f:
             d = json.load(f)[kernel]
@@ -350,10 +357,10 @@ def run_layer(torch, lca, dev, stream, flush, args, pk):
             "attention_flops": fl["attention"],
             "config": {"B": w.B, "T": w.T, "D": w.D, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "r_q": w.r_q,
                        "inputs": "x ~ N(0,1), weights ~ N(0, 0.02^2), bf16"},
-            "roofline": {"kernel": "layer (5 tensor-core GEMMs + prefill_r512_kernel)", "bound": "tensor",
-                         "achieved": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "roofline": {"kernel": "layer (5 tensor-core GEMMs, the latent's row pass, prefill_r512_kernel)",
+                         "bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": round(tf / pk["bf16_tflops"], 4), "peak_source": pk["source"] + " (burst bf16)",
-                         "traffic": None},
+                         "traffic": committed_traffic("layer", LAYER_SRCS)},
             "gpu_launches": launches}
 
 
@@ -391,9 +398,11 @@ def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
     return {"workload": "k3_layer_decode_bf16", "value": round(dw.B / (ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(ms, 4), "tokens_per_step": dw.B, "cache_bytes_per_step": cache_bytes,
             "weight_bytes_per_step": weight_bytes,
-            "roofline": {"kernel": "layer decode step (6 GEMMs with M = B, append, absorb, pair + merge)",
+            "roofline": {"kernel": "layer decode step (5 GEMMs with M = B and their row passes, append, absorb, "
+                                   "pair + merge)",
                          "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"], "traffic": None},
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"],
+                         "traffic": committed_traffic("layer_decode", LAYER_DECODE_SRCS)},
             "gpu_launches": launches}
 
 
