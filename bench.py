@@ -6,7 +6,10 @@ causal softmax, the latent weighting, the W_UV up-projection and the gate, all
 in the library's fused kernel.  The cached-latent decode (B=64, cache lengths
 uniform in [1024, 32768], H=96, r=512) is timed in the same run and reported
 under "decode", and the whole layer at the prefill's size (step-1 projections
-with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".
+with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".  The two
+small configurations run under "small_prefill" (r=32 at T=2048, bf16, bound by
+the exponential unit) and "toy_layer" (the fp32 toy layer, bound by launch
+latency).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -257,6 +260,8 @@ def run_ours(args):
     layer_line = run_layer(torch, lca, dev, stream, flush, args, pk) if not args.no_layer else None
     layer_dec = run_layer_decode(torch, lca, dev, stream, flush, args, pk) \
         if not (args.no_layer or args.no_decode) else None
+    small = run_small_prefill(torch, lca, dev, stream, flush, args) if not args.no_small else None
+    toy = run_toy_layer(torch, lca, dev, stream, flush, args) if not args.no_small else None
     if lca.mla_get_device_error() != 0:
         raise RuntimeError("device error word set after the timed region")
 
@@ -287,6 +292,10 @@ def run_ours(args):
             line["layer"] = layer_line
         if layer_dec is not None:
             line["layer_decode"] = layer_dec
+        if small is not None:
+            line["small_prefill"] = small
+        if toy is not None:
+            line["toy_layer"] = toy
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -406,6 +415,73 @@ def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
             "gpu_launches": launches}
 
 
+# Exponentials per clock per SM on the multi-function unit (ex2, fp32), and fp32 FMA lanes per SM.
+MUFU_EX2_PER_CLK_SM = 16
+FP32_LANES_SM = 128
+SM_MAX_MHZ = 2070.0
+
+
+def run_small_prefill(torch, lca, dev, stream, flush, args):
+    """The small-rank prefill (r = 32, d = 16, T = 2048, bf16): one exponential per causal score and only
+    4 r = 128 tensor-core FLOPs per exponential, so the exponential unit bounds it."""
+    w = W.TOY_LONG_BF16
+    d = W.draw_prefill_direct(w, seed=0)
+    t = {k: torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(dev) for k, v in d.items() if v is not None}
+    out = torch.empty((w.B, w.T, w.H * w.d_v), dtype=torch.bfloat16, device=dev)
+    step = lambda: lca.mla_absorbed_attn_fwd(t["q"], t["c"], t["w_uk"], t["w_uv"], t["gate"], w.scale,  # noqa: E731
+                                             out=out)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
+    exps = w.B * w.H * w.T * (w.T + 1) // 2
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = MUFU_EX2_PER_CLK_SM * sms * SM_MAX_MHZ * 1e6 / 1e9   # G ex2/s
+    achieved = exps / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "value": round(w.prefill_flops() / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 5), "flops_per_step": w.prefill_flops(), "exp_per_step": exps,
+            "config": {"B": w.B, "T": w.T, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "scale": w.scale,
+                       "l2": "flushed between steps"},
+            "roofline": {"kernel": "prefill_small_kernel", "bound": "alu", "achieved": round(achieved, 1),
+                         "peak": round(peak, 1), "unit": "G ex2/s", "frac": round(achieved / peak, 4),
+                         "peak_source": f"derived: {MUFU_EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {SM_MAX_MHZ:.0f} MHz",
+                         "traffic": None},
+            "gpu_launches": launches}
+
+
+def run_toy_layer(torch, lca, dev, stream, flush, args):
+    """The fp32 toy layer (B=2, T=128, D=256, H=8, d=16, r=32, r_q=64) through step 1, the attention and W_o:
+    2.1e7 attention FLOPs, so launch latency bounds it."""
+    w = W.TOY_LAYER_F32
+    p = W.draw_layer(w, seed=0)
+    t = {k: torch.from_numpy(v.astype(np.float32)).to(dev) for k, v in p.items()}
+    ws = torch.empty(lca.mla_gated_layer_workspace_size(w.B, w.T, w.D, w.H, w.d_q, w.d_v, w.r, w.r_q, torch.float32),
+                     dtype=torch.uint8, device=dev)
+    y = torch.empty((w.B, w.T, w.D), dtype=torch.float32, device=dev)
+    step = lambda: lca.mla_gated_layer_fwd(t["x"], t["q_down"], t["q_up"], t["kv_down"], t["kv_up"],  # noqa: E731
+                                           t["gate"], t["o_proj"], w.H, w.d_q, w.d_v, w.scale, out=y, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
+    fl = layer_flops(w)["total"]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = 2 * FP32_LANES_SM * sms * SM_MAX_MHZ * 1e6 / 1e12
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": round(ms * 1e3, 2), "unit": "us/call", "higher_is_better": False,
+            "ms_per_step": round(ms, 5), "flops_per_step": fl, "kernels_per_call": launches // max(args.steps, 1),
+            "config": {"B": w.B, "T": w.T, "D": w.D, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "r_q": w.r_q,
+                       "dtype": "f32 (fp32 FMAs, no TF32)", "l2": "flushed between steps"},
+            "roofline": {"kernel": "toy layer (fp32 SIMT kernels)", "bound": "alu", "achieved": round(tf, 4),
+                         "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tf / peak, 5),
+                         "peak_source": f"derived: fp32 FMA {FP32_LANES_SM} lanes/SM x 2 x {sms} SMs x "
+                                        f"{SM_MAX_MHZ:.0f} MHz; the call is launch-latency bound",
+                         "traffic": None},
+            "gpu_launches": launches}
+
+
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
 def oracle_inputs():
     return W.draw_prefill_direct(PREFILL, seed=0)
@@ -485,6 +561,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-small", action="store_true", help="skip the small-rank prefill and the fp32 toy layer")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")
     ap.add_argument("--decode-batch", type=int, default=W.K3_DECODE_BF16.B,

@@ -2,13 +2,19 @@
 // TF32), for the toy layer sizes (r, d_q, d_v <= 64).
 //
 // Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）", steps 2-4, fused
-// into one kernel: each thread owns one (b, t, h) query row, absorbs W_UK into
-// its query (step 2), streams the latent rows u <= t through shared memory
-// with an online softmax (scores and the latent weighting of step 3 share the
-// same c rows), then applies W_UV^T and the sigmoid gate (step 4).
-//
-// One CTA = one (b, h) and 128 consecutive tokens.  Work per token grows with
-// t, so the grid is ordered heaviest tile first.
+// into one kernel.  One CTA = one (b, h) and 128 consecutive tokens; each of
+// its 8 warps owns 16 of those query rows (interleaved, so every warp gets
+// early and late rows).  Per row the warp
+//   absorbs W_UK into the query (step 2, lane j computes latent column j),
+//   walks the latent rows u <= t in chunks of 32 that the CTA stages in
+//   shared memory: lane u scores key u against q_abs (step 2), the warp takes
+//   the chunk maximum and the sum with shuffles (online softmax, step 2),
+//   and lane j adds sum_u p_u c[u, j] to its latent column (step 3, the same c
+//   rows as the scores),
+//   then applies W_UV^T and the sigmoid gate (steps 3-4, lane v computes
+//   output column v).
+// Short dependency chains per lane and no bank conflicts (the staged rows are
+// padded to r + 1 floats) keep the warps busy; heavy tiles launch first.
 #include "common.cuh"
 #include "internal.h"
 
@@ -16,93 +22,136 @@ namespace mla {
 namespace {
 
 constexpr int kMaxDim = 64;   // r, d_q, d_v limit of this kernel
-constexpr int kRows = 128;    // tokens per CTA (one per thread)
-constexpr int kKeys = 64;     // latent rows staged per shared-memory tile
+constexpr int kRows = 128;    // tokens per CTA
+constexpr int kWarps = 8;
+constexpr int kRowsPerWarp = kRows / kWarps;
+constexpr int kKeys = 32;     // latent rows staged per chunk: one per lane
+constexpr int kPad = kMaxDim + 1;
 
-__global__ void __launch_bounds__(kRows) prefill_f32_kernel(const float *__restrict__ q,
-                                                            const float *__restrict__ c,
-                                                            const float *__restrict__ w_uk,
-                                                            const float *__restrict__ w_uv,
-                                                            const float *__restrict__ gate,
-                                                            float *__restrict__ out, float scale, int T,
-                                                            int H, int d_q, int d_v, int r) {
-    __shared__ float s_wuk[kMaxDim * kMaxDim];
-    __shared__ float s_wuv[kMaxDim * kMaxDim];
-    __shared__ float s_c[kKeys * kMaxDim];
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *__restrict__ q,
+                                                                  const float *__restrict__ c,
+                                                                  const float *__restrict__ w_uk,
+                                                                  const float *__restrict__ w_uv,
+                                                                  const float *__restrict__ gate,
+                                                                  float *__restrict__ out, float scale, int T,
+                                                                  int H, int d_q, int d_v, int r) {
+    __shared__ float s_c[kKeys * kPad];                         // staged latent rows, padded
+    __shared__ float s_qa[kWarps][kRowsPerWarp][kMaxDim];       // q_abs of each warp's rows
+    __shared__ float s_p[kWarps][kKeys];                        // one chunk's softmax weights
 
     const int n_tiles = (T + kRows - 1) / kRows;
     const int tile = n_tiles - 1 - static_cast<int>(blockIdx.x);   // heaviest first
     const int h = blockIdx.y, b = blockIdx.z;
-    const int t = tile * kRows + static_cast<int>(threadIdx.x);
-    const bool active = t < T;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t0 = tile * kRows;
+    const float *wuk = w_uk + static_cast<size_t>(h) * d_q * r;
+    const float *wuv = w_uv + static_cast<size_t>(h) * d_v * r;
 
-    for (int i = threadIdx.x; i < d_q * r; i += kRows) s_wuk[i] = w_uk[(size_t)h * d_q * r + i];
-    for (int i = threadIdx.x; i < d_v * r; i += kRows) s_wuv[i] = w_uv[(size_t)h * d_v * r + i];
-    __syncthreads();
-
-    // step 2: q_abs = q_h . W_UK,h
-    float qa[kMaxDim];
+    // step 2, absorb: q_abs[t, j] = sum_d q[b, t, h, d] W_UK[h, d, j]; lane j holds columns j and j + 32
+    float o[kRowsPerWarp][2], m[kRowsPerWarp], l[kRowsPerWarp];
 #pragma unroll
-    for (int j = 0; j < kMaxDim; ++j) qa[j] = 0.f;
-    if (active) {
-        const float *qrow = q + (((size_t)b * T + t) * H + h) * d_q;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int t = t0 + i * kWarps + warp;
+        o[i][0] = o[i][1] = 0.f;
+        m[i] = -INFINITY;
+        l[i] = 0.f;
+        if (t >= T) continue;
+        const float *qrow = q + ((static_cast<size_t>(b) * T + t) * H + h) * d_q;
+        float a0 = 0.f, a1 = 0.f;
         for (int d = 0; d < d_q; ++d) {
-            const float qd = qrow[d];
-#pragma unroll
-            for (int j = 0; j < kMaxDim; ++j)
-                if (j < r) qa[j] = fmaf(qd, s_wuk[d * r + j], qa[j]);
+            const float qd = __ldg(qrow + d);
+            if (lane < r) a0 = fmaf(qd, __ldg(wuk + d * r + lane), a0);
+            if (lane + 32 < r) a1 = fmaf(qd, __ldg(wuk + d * r + lane + 32), a1);
         }
+        s_qa[warp][i][lane] = a0;
+        s_qa[warp][i][lane + 32] = a1;
     }
+    __syncwarp();
 
-    float o[kMaxDim];
-#pragma unroll
-    for (int j = 0; j < kMaxDim; ++j) o[j] = 0.f;
-    float m = -INFINITY, l = 0.f;
-
-    const int last_key = min(T, (tile + 1) * kRows);   // keys this CTA needs: [0, last_key)
-    const float *cb = c + (size_t)b * T * r;
+    const int last_key = min(T, t0 + kRows);   // keys this CTA needs: [0, last_key)
+    const float *cb = c + static_cast<size_t>(b) * T * r;
     for (int k0 = 0; k0 < last_key; k0 += kKeys) {
-        const int nk = min(kKeys, last_key - k0);
         __syncthreads();
-        for (int i = threadIdx.x; i < nk * r; i += kRows) s_c[i] = cb[(size_t)k0 * r + i];
+        for (int i = threadIdx.x; i < kKeys * r; i += kWarps * 32) {
+            const int u = i / r, j = i - u * r;
+            s_c[u * kPad + j] = k0 + u < T ? __ldg(cb + static_cast<size_t>(k0 + u) * r + j) : 0.f;
+        }
         __syncthreads();
-        if (!active) continue;
-        const int n_vis = min(nk, t - k0 + 1);   // keys u <= t in this tile
-        for (int u = 0; u < n_vis; ++u) {
-            const float *cu = s_c + u * r;
-            float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < kMaxDim; ++j)
-                if (j < r) s = fmaf(qa[j], cu[j], s);
-            s *= scale;
-            if (s > m) {   // online softmax: rescale the running sums to the new maximum
-                const float corr = expf(m - s);
-                l *= corr;
-#pragma unroll
-                for (int j = 0; j < kMaxDim; ++j) o[j] *= corr;
-                m = s;
+        for (int i = 0; i < kRowsPerWarp; ++i) {
+            const int t = t0 + i * kWarps + warp;
+            if (t >= T || k0 > t) continue;   // warp-uniform
+            const int n_vis = min(kKeys, t - k0 + 1);   // keys u <= t of this chunk
+            // scores: lane u against key k0 + u
+            float s = -INFINITY;
+            if (lane < n_vis) {
+                float acc0 = 0.f, acc1 = 0.f;
+                const float *cu = s_c + lane * kPad;
+                const float *qa = s_qa[warp][i];
+                int j = 0;
+                for (; j + 1 < r; j += 2) {
+                    acc0 = fmaf(qa[j], cu[j], acc0);
+                    acc1 = fmaf(qa[j + 1], cu[j + 1], acc1);
+                }
+                if (j < r) acc0 = fmaf(qa[j], cu[j], acc0);
+                s = (acc0 + acc1) * scale;
             }
-            const float p = expf(s - m);
-            l += p;
-#pragma unroll
-            for (int j = 0; j < kMaxDim; ++j)
-                if (j < r) o[j] = fmaf(p, cu[j], o[j]);
+            // online softmax over the chunk
+            const float m_new = fmaxf(m[i], warp_max(s));
+            const float corr = expf(m[i] - m_new);   // 0 on the first chunk (m = -inf)
+            const float p = lane < n_vis ? expf(s - m_new) : 0.f;
+            l[i] = l[i] * corr + warp_sum(p);
+            m[i] = m_new;
+            s_p[warp][lane] = p;
+            __syncwarp();
+            // step 3, latent weighting: lane j adds sum_u p_u c[u, j]
+            float a0 = 0.f, a1 = 0.f;
+            for (int u = 0; u < n_vis; ++u) {
+                const float pu = s_p[warp][u];
+                a0 = fmaf(pu, s_c[u * kPad + lane], a0);
+                a1 = fmaf(pu, s_c[u * kPad + lane + 32], a1);
+            }
+            o[i][0] = fmaf(o[i][0], corr, a0);
+            o[i][1] = fmaf(o[i][1], corr, a1);
+            __syncwarp();
         }
     }
-    if (!active) return;
 
-    // step 3 (W_UV^T) and step 4 (gate)
-    const float inv_l = 1.f / l;
-    float *orow = out + ((size_t)b * T + t) * H * d_v + (size_t)h * d_v;
-    const float *grow = gate ? gate + ((size_t)b * T + t) * H * d_v + (size_t)h * d_v : nullptr;
-    for (int v = 0; v < d_v; ++v) {
-        float acc = 0.f;
+    // step 3 (W_UV^T) and step 4 (gate): lane v computes output columns v and v + 32
 #pragma unroll
-        for (int j = 0; j < kMaxDim; ++j)
-            if (j < r) acc = fmaf(o[j], s_wuv[v * r + j], acc);
-        acc *= inv_l;
-        if (grow) acc = acc / (1.f + expf(-grow[v]));
-        orow[v] = acc;
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int t = t0 + i * kWarps + warp;
+        if (t >= T) continue;
+        const float inv_l = 1.f / l[i];
+        float *ol = s_qa[warp][i];   // this row's q_abs is no longer needed: reuse it for o_lat / l
+        ol[lane] = o[i][0] * inv_l;
+        ol[lane + 32] = o[i][1] * inv_l;
+        __syncwarp();
+        float *orow = out + (static_cast<size_t>(b) * T + t) * H * d_v + static_cast<size_t>(h) * d_v;
+        const float *grow = gate ? gate + (static_cast<size_t>(b) * T + t) * H * d_v + static_cast<size_t>(h) * d_v
+                                 : nullptr;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int v = lane + 32 * half;
+            if (v >= d_v) continue;
+            const float *wv = wuv + static_cast<size_t>(v) * r;
+            float acc = 0.f;
+            for (int j = 0; j < r; ++j) acc = fmaf(ol[j], __ldg(wv + j), acc);
+            if (grow) acc = acc / (1.f + expf(-grow[v]));
+            orow[v] = acc;
+        }
+        __syncwarp();
     }
 }
 
@@ -116,7 +165,7 @@ cudaError_t launch_prefill_f32_simt(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_f32_simt_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
     const dim3 grid((a.T + kRows - 1) / kRows, a.H, a.B);
     note_launch();
-    prefill_f32_kernel<<<grid, kRows, 0, s>>>(
+    prefill_f32_kernel<<<grid, kWarps * 32, 0, s>>>(
         static_cast<const float *>(a.q), static_cast<const float *>(a.c), static_cast<const float *>(a.w_uk),
         static_cast<const float *>(a.w_uv), static_cast<const float *>(a.gate), static_cast<float *>(a.out),
         a.scale, a.T, a.H, a.d_q, a.d_v, a.r);
