@@ -8,7 +8,9 @@
 // epilogue.  At these ranks the tensor work per score is tiny (4r FLOPs) and
 // the exponentials bound the kernel, so the design aims at many softmax warps
 // per SM: one CTA per 128-token tile, 256 TMEM columns and about 100 KB of
-// shared memory, two CTAs per SM.
+// shared memory, two CTAs per SM, and two softmax threads per query row (each
+// owns 64 keys of a block; the row maximum and the row sums are exchanged
+// through shared memory), with tree reductions to keep dependency chains short.
 //
 // Narrow rows (r = 32: 64 bytes; d = 16: 32 bytes) are widened to the 128-byte
 // swizzled layout by TMA's zero fill past the tensor's inner extent: every
@@ -25,7 +27,8 @@ namespace {
 
 constexpr int kBM = 128;        // tokens per tile
 constexpr int kBN = 128;        // keys per block
-constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 softmax / epilogue
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-5 and 6-9: two softmax / epilogue groups
+constexpr int kMath = 256;      // softmax threads (two per query row)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -37,7 +40,9 @@ constexpr uint32_t RING = WV + 8192;            // c tiles
 constexpr int kStages = 2;
 constexpr uint32_t PT = RING + kStages * kTile; // P [128 rows x 128 keys] = 2 tiles
 constexpr uint32_t BARS = PT + 2 * kTile;
-constexpr uint32_t kSmemBytes = BARS + 256 + 1024;
+constexpr uint32_t PMAX = BARS + 256;            // [2 parities][2 groups][128 rows] partial row maxima
+constexpr uint32_t LSUM = PMAX + 2 * 2 * kBM * 4;   // [2 groups][128 rows] partial row sums
+constexpr uint32_t kSmemBytes = LSUM + 2 * kBM * 4 + 1024;   // + alignment slack
 static_assert(RING % 1024 == 0 && PT % 1024 == 0, "alignment");
 
 constexpr uint32_t S_COL = 0, O_COL = 128;
@@ -49,6 +54,36 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+
+// Pairwise (tree) reductions over 64 values: short dependency chains.
+__device__ __forceinline__ float tree_max64(const float (&s)[2][32]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = fmaxf(fmaxf(s[0][i], s[0][i + 16]), fmaxf(s[1][i], s[1][i + 16]));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+__device__ __forceinline__ float tree_sum64(const float (&s)[2][32]) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m[i] = (s[0][i] + s[0][i + 16]) + (s[1][i] + s[1][i + 16]);
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] += m[i + w];
+    return m[0];
+}
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
 
 struct Params {
     const __nv_bfloat16 *gate;
@@ -84,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(B_(bars->c_empty[i]), 1);
         }
         mbar_init(B_(bars->s_full), 1);
-        mbar_init(B_(bars->s_free), 128);
+        mbar_init(B_(bars->s_free), kMath);
         mbar_init(B_(bars->p_full), 1);
         mbar_init(B_(bars->pv_done), 1);
         mbar_init(B_(bars->olat_ready), 1);
@@ -139,18 +174,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             umma_commit(B_(bars->absorb_done));
             ok = mbar_wait(B_(bars->qabs_ready), 0, p.err, abort_flag);
         }
-        for (int j = 0; ok && j < nkv; ++j) {
+        // S(j + 1) is issued as soon as the softmax has read S(j) out of TMEM, so the next block's scores are
+        // ready when the softmax finishes block j; then P(j) . c(j)
+        auto issue_scores = [&](int j) {
             const int st = j % kStages;
-            if (!(ok = mbar_wait(B_(bars->c_full[st]), (j / kStages) & 1, p.err, abort_flag))) break;
-            if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free), (j - 1) & 1, p.err, abort_flag))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
                 umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
                           make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, kk > 0);
             umma_commit(B_(bars->s_full));
+        };
+        if (ok && (ok = mbar_wait(B_(bars->c_full[0]), 0, p.err, abort_flag))) issue_scores(0);
+        for (int j = 0; ok && j < nkv; ++j) {
+            if (j + 1 < nkv) {
+                const int sn = (j + 1) % kStages;
+                if (!(ok = mbar_wait(B_(bars->c_full[sn]), ((j + 1) / kStages) & 1, p.err, abort_flag))) break;
+                if (!(ok = mbar_wait(B_(bars->s_free), j & 1, p.err, abort_flag))) break;
+                issue_scores(j + 1);
+            }
             if (!(ok = mbar_wait(B_(bars->p_full), j & 1, p.err, abort_flag))) break;
             tc_fence_after();
+            const int st = j % kStages;
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 umma_bf16(tmem + O_COL, make_smem_desc(base + PT + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024),
@@ -169,116 +214,108 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (!ok) *abort_flag = 1;
     } else if (warp >= 2) {
-        // ---- softmax / epilogue: thread `row` owns TMEM lane `row`
+        // ---- softmax / epilogue: group g (warps 2-5 or 6-9) owns keys [64 g, 64 g + 64) of every block and
+        // 32-column chunk g of the 64-column q_abs / o_lat tiles; thread `row` owns TMEM lane `row`
+        const int g = (warp - 2) >> 2;
         const int row = (warp & 3) * 32 + lane;
         const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const int t = t0 + row;
+        const bool leader = threadIdx.x == 64;   // arrives on the barriers the MMA warp waits for
         bool fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
-        bool ok = !named_bar_or(1, 128, fail);
+        bool ok = !named_bar_or(1, kMath, fail);
         if (ok) {   // q_abs (fp32 TMEM) -> q_abs * scale * log2(e), bf16, into the q tile
             tc_fence_after();
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                float v[32];
-                tmem_ld32(trow + O_COL + cc * 32, v);
-                tmem_wait_ld();
-                store_row32_bf16(base + QT, kTile, row, cc, v, p.qk_scale_log2);
-            }
+            float v[32];
+            tmem_ld32(trow + O_COL + g * 32, v);
+            tmem_wait_ld();
+            store_row32_bf16(base + QT, kTile, row, g, v, p.qk_scale_log2);
             fence_proxy_async_smem();
             tc_fence_before();
         }
-        named_bar_sync(1, 128);
-        if (row == 0 && ok) mbar_arrive(B_(bars->qabs_ready));
+        named_bar_sync(1, kMath);
+        if (leader && ok) mbar_arrive(B_(bars->qabs_ready));
 
-        float m_run = -INFINITY, l_run = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;   // l_run: this group's part of the row sum
         for (int j = 0; ok && j < nkv; ++j) {
             fail = !mbar_wait(B_(bars->s_full), j & 1, p.err, abort_flag);
-            if (named_bar_or(1, 128, fail)) { ok = false; break; }
+            if (named_bar_or(1, kMath, fail)) { ok = false; break; }
             tc_fence_after();
-            float s[4][32];
+            float s[2][32];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_COL + c4 * 32, s[c4]);
+            for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + S_COL + g * 64 + c2 * 32, s[c2]);
             tmem_wait_ld();
             tc_fence_before();
             mbar_arrive(B_(bars->s_free));
             if (j == nkv - 1) {   // diagonal block: keys after the query or past the sequence
-                const int lim = min(t, p.T - 1) - j * kBN;
+                const int lim = min(t, p.T - 1) - j * kBN - g * 64;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
+                for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
+                        if (c2 * 32 + i > lim) s[c2][i] = -INFINITY;
             }
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[c4][i]);
+            st_shared_f32(base + PMAX + ((j & 1) * 2 + g) * kBM * 4 + row * 4, tree_max64(s));
+            named_bar_sync(1, kMath);   // publishes both groups' partial maxima
+            const float mx = fmaxf(ld_shared_f32(base + PMAX + ((j & 1) * 2 + 0) * kBM * 4 + row * 4),
+                                   ld_shared_f32(base + PMAX + ((j & 1) * 2 + 1) * kBM * 4 + row * 4));
             float factor = 1.f;
             if (mx > m_run + kRescaleLog2) {
                 factor = fast_exp2(m_run - mx);
                 m_run = mx;
             }
-            float sum = 0.f;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
+            for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[c4][i] = fast_exp2(s[c4][i] - m_run);
-                    sum += s[c4][i];
-                }
-            l_run = l_run * factor + sum;
+                for (int i = 0; i < 32; ++i) s[c2][i] = fast_exp2(s[c2][i] - m_run);
+            l_run = l_run * factor + tree_sum64(s);
             if (j > 0) {   // P and o_lat are free once the previous block's product completed
                 fail = !mbar_wait(B_(bars->pv_done), (j - 1) & 1, p.err, abort_flag);
-                if (named_bar_or(1, 128, fail)) { ok = false; break; }
-                if (named_bar_or(1, 128, factor != 1.f)) {
+                if (named_bar_or(1, kMath, fail)) { ok = false; break; }
+                if (named_bar_or(1, kMath, factor != 1.f)) {
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, factor != 1.f)) {
+                        float v[32];
+                        tmem_ld32(trow + O_COL + g * 32, v);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int cc = 0; cc < 2; ++cc) {
-                            float v[32];
-                            tmem_ld32(trow + O_COL + cc * 32, v);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] *= factor;
-                            tmem_st32(trow + O_COL + cc * 32, v);
-                        }
+                        for (int i = 0; i < 32; ++i) v[i] *= factor;
+                        tmem_st32(trow + O_COL + g * 32, v);
                         tmem_wait_st();
                     }
                     tc_fence_before();
                 }
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) store_row32_bf16(base + PT, kTile, row, c4, s[c4], 1.f);
+            for (int c2 = 0; c2 < 2; ++c2) store_row32_bf16(base + PT, kTile, row, 2 * g + c2, s[c2], 1.f);
             fence_proxy_async_smem();
-            named_bar_sync(1, 128);
-            if (row == 0) mbar_arrive(B_(bars->p_full));
-        }
-        if (ok) {   // o_lat / l -> bf16 into the (now free) q tile for the W_UV product
-            fail = !mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag);
-            ok = !named_bar_or(1, 128, fail);
+            named_bar_sync(1, kMath);
+            if (leader) mbar_arrive(B_(bars->p_full));
         }
         if (ok) {
+            fail = !mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag);
+            ok = !named_bar_or(1, kMath, fail);
+        }
+        // the row sum: both groups' parts
+        st_shared_f32(base + LSUM + g * kBM * 4 + row * 4, l_run);
+        named_bar_sync(1, kMath);
+        const float l_row = ld_shared_f32(base + LSUM + row * 4) + ld_shared_f32(base + LSUM + kBM * 4 + row * 4);
+        if (ok) {   // o_lat / l -> bf16 into the (now free) q tile for the W_UV product
             tc_fence_after();
-            const float inv_l = 1.f / l_run;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                float v[32];
-                tmem_ld32(trow + O_COL + cc * 32, v);
-                tmem_wait_ld();
-                store_row32_bf16(base + QT, kTile, row, cc, v, inv_l);
-            }
+            float v[32];
+            tmem_ld32(trow + O_COL + g * 32, v);
+            tmem_wait_ld();
+            store_row32_bf16(base + QT, kTile, row, g, v, 1.f / l_row);
             fence_proxy_async_smem();
             tc_fence_before();
-            named_bar_sync(1, 128);
-            if (row == 0) mbar_arrive(B_(bars->olat_ready));
+            named_bar_sync(1, kMath);
+            if (leader) mbar_arrive(B_(bars->olat_ready));
             fail = !mbar_wait(B_(bars->ep_done), 0, p.err, abort_flag);
-            ok = !named_bar_or(1, 128, fail);
+            ok = !named_bar_or(1, kMath, fail);
         }
         if (ok) {
             tc_fence_after();
             const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.H + h) * p.d_v;
-            for (int v16 = 0; v16 < p.d_v / 16; ++v16) {
+            for (int v16 = g; v16 < p.d_v / 16; v16 += 2) {
                 float o[16];
                 tmem_ld16(trow + S_COL + v16 * 16, o);
                 tmem_wait_ld();
