@@ -247,6 +247,19 @@ MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const vo
  */
 MLA_API int mla_get_device_error(void *stream);
 
+/*
+ * mla_debug_wait_timeout - exercise the device-side failure path.  The pages
+ * have no counterpart: this is a diagnostic of the library's own error
+ * handling.  Launches one thread on `stream` that waits, with the same bounded
+ * wait every kernel of this library uses, for an mbarrier phase that nothing
+ * completes; after `limit_us` microseconds (1 .. 2,000,000) the wait gives up
+ * and records MLA_ERR_DEVICE_TIMEOUT in the current device's error word, which
+ * mla_get_device_error() then returns.  Nothing faults or traps; the context
+ * stays usable.  Returns MLA_OK when launched, MLA_ERR_SHAPE for a limit out
+ * of range (nothing launched), MLA_ERR_CUDA if the launch failed.
+ */
+MLA_API int mla_debug_wait_timeout(unsigned int limit_us, void *stream);
+
 /* mla_status_string - static, NUL-terminated description of a status code. */
 MLA_API const char *mla_status_string(int status);
 

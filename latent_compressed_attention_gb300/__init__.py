@@ -22,7 +22,7 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
-           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_gated_layer_fwd",
+           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout", "mla_gated_layer_fwd",
            "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16",
            "DTYPE_F32"]
 
@@ -69,6 +69,8 @@ def library():
             lib.mla_gated_layer_decode_workspace_size.restype = sz
             lib.mla_gated_layer_decode.argtypes = [vp] * 7 + [f, vp, vp, ll, vp] + [i] * 9 + [vp, sz, vp]
             lib.mla_gated_layer_decode.restype = i
+            lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
+            lib.mla_debug_wait_timeout.restype = i
             lib.mla_get_device_error.argtypes = [vp]
             lib.mla_get_device_error.restype = i
             lib.mla_status_string.argtypes = [i]
@@ -342,6 +344,16 @@ def mla_latent_decode_noalloc(q_abs, c_cache, lens, w_uv, gate=None, scale: floa
     if rc != 0:
         raise MLAError(rc, "mla_latent_decode_noalloc")
     return out
+
+
+def mla_debug_wait_timeout(limit_us: int = 1000, stream=None, device=None) -> None:
+    """Make one device-side bounded wait give up after `limit_us` (a barrier nothing completes); the device
+    error word then holds MLA_ERR_DEVICE_TIMEOUT (read it with mla_get_device_error)."""
+    torch = _torch()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    rc = library().mla_debug_wait_timeout(int(limit_us), _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_debug_wait_timeout")
 
 
 def mla_get_device_error(stream=None, device=None) -> int:

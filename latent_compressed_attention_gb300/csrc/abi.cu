@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/mla.h"
+#include "common.cuh"
 #include "internal.h"
 
 namespace mla {
@@ -71,6 +72,17 @@ void *tensor_map_encode_fn() {
             fn = p;
     });
     return fn;
+}
+
+// One thread waits, with the library's bounded wait, for a barrier phase that
+// nothing completes: the wait gives up after `limit_ns` and records
+// kDevErrTimeout in the device error word, exactly as a stalled pipeline would.
+__global__ void wait_timeout_probe_kernel(int *err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    mbar_init(b, 1);
+    fence_mbar_init();
+    mbar_wait(b, 0, err, nullptr, limit_ns);
 }
 
 }  // namespace mla
@@ -263,6 +275,16 @@ MLA_API int mla_gated_layer_decode(const void *x, const void *w_q_down, const vo
                       scale, B, D, H, d_q, d_v, r, r_q, workspace, workspace_bytes, dev->err_word, dev->num_sms};
     const cudaError_t e = launch_gated_layer_decode(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_debug_wait_timeout(unsigned int limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 2000000u) return MLA_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    note_launch();
+    wait_timeout_probe_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(dev->err_word,
+                                                                             uint64_t(limit_us) * 1000u);
+    return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 MLA_API int mla_get_device_error(void *stream) {

@@ -90,18 +90,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false,
-// records kDevErrTimeout) after MLA_WAIT_LIMIT_NS, or at once when *abort is
-// set by another thread of the CTA that already gave up.
+// records kDevErrTimeout) after `limit_ns` (MLA_WAIT_LIMIT_NS unless given), or
+// at once when *abort is set by another thread of the CTA that already gave up.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err,
-                                          const volatile int *abort = nullptr) {
+                                          const volatile int *abort = nullptr,
+                                          uint64_t limit_ns = MLA_WAIT_LIMIT_NS) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (abort && *abort) return false;
-            if (globaltimer_ns() - t0 > MLA_WAIT_LIMIT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
 #ifdef MLA_TIMEOUT_PRINT
                 // diagnostic build only: which barrier (shared-memory offset) and phase gave up
                 if ((threadIdx.x & 31) == 0)

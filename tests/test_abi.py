@@ -202,3 +202,8 @@ def test_layer_decode_checks_before_launch(lib):
     assert layer_decode(lib, ws=None) == ERR_WORKSPACE
     assert layer_decode(lib, B=0) == OK
     assert layer_decode(lib, dtype=4) == ERR_DTYPE
+
+
+@pytest.mark.parametrize("limit_us", [0, 2000001])
+def test_wait_timeout_probe_rejects_limits_out_of_range(lib, limit_us):
+    assert lib.mla_debug_wait_timeout(limit_us, None) == ERR_SHAPE
