@@ -2,9 +2,9 @@
 // TF32), for the toy layer sizes (r, d_q, d_v <= 64).
 //
 // Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）", steps 2-4, fused
-// into one kernel.  One CTA = one (b, h) and 128 consecutive tokens; each of
-// its 8 warps owns 16 of those query rows (interleaved, so every warp gets
-// early and late rows).  Per row the warp
+// into one kernel.  One CTA = one (b, h) and 16 consecutive tokens (so even a
+// short sequence fills the GPU); each of its 8 warps owns 2 of those query
+// rows.  Per row the warp
 //   absorbs W_UK into the query (step 2, lane j computes latent column j),
 //   walks the latent rows u <= t in chunks of 32 that the CTA stages in
 //   shared memory: lane u scores key u against q_abs (step 2), the warp takes
@@ -22,7 +22,7 @@ namespace mla {
 namespace {
 
 constexpr int kMaxDim = 64;   // r, d_q, d_v limit of this kernel
-constexpr int kRows = 128;    // tokens per CTA
+constexpr int kRows = 16;     // tokens per CTA
 constexpr int kWarps = 8;
 constexpr int kRowsPerWarp = kRows / kWarps;
 constexpr int kKeys = 32;     // latent rows staged per chunk: one per lane
