@@ -41,6 +41,14 @@ constexpr int kBM = 128;     // query tokens per tile
 constexpr int kBN = 128;     // keys per value-CTA unit
 constexpr int kBS = 256;     // keys per score block (two units)
 constexpr int kThreads = 384;   // warps 0 TMA, 1 MMA, 2 relay (value CTA), 4-7 and 8-11: two row warpgroups
+// Register split: the control warpgroup (warps 0-3) gives registers to the two row warpgroups.
+// 4 x 32 x 72 + 8 x 32 x 208 = 62,464 <= 384 x 168 launched; the launcher checks the kernel's count.
+#ifndef MLA_TRACE
+constexpr uint32_t kRegsCtl = 72, kRegsMath = 208, kRegsLaunch = 168;
+#else   // the wait accounting needs more registers in the control warps
+constexpr uint32_t kRegsCtl = 88, kRegsMath = 200, kRegsLaunch = 168;
+#endif
+static_assert(128 * kRegsCtl + 256 * kRegsMath <= kThreads * kRegsLaunch, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 // Keep a stale row maximum until the new one exceeds it by this (log2 units):
 // p <= 2^16, far inside the fp32 range of the row sums and the accumulator.
@@ -78,14 +86,14 @@ constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);      // P (K-majo
 constexpr uint32_t kIdescEp = make_idesc_bf16(128, 128, 0, 0);      // o_lat (K-major) x W_UV (K-major)
 
 struct Bars {
-    uint64_t pro_full, absorb_done, qabs_ready;   // score CTA
+    uint64_t pro_full, absorb_done, qabs_ready, q_free;   // score CTA
     uint64_t sc_full[kSStages], sc_empty[kSStages];
     uint64_t s_full[2], s_free[2];
     uint64_t p_free[2];                           // arrivals from the value CTA
     uint64_t oc_full[kOStages], oc_empty[kOStages];  // value CTA
     uint64_t p_full[2];                           // bulk-copy transactions from the score CTA
     uint64_t pv_done[2], ri_read[2], corr_done;
-    uint64_t olat_ready[2], ep_done[2];
+    uint64_t olat_ready[2], ep_done[2], ep_read;
     uint32_t tmem_base;
     int abort;
 };
@@ -103,11 +111,11 @@ enum TraceSlot {
 __device__ unsigned long long g_trace[TR_COUNT];
 #define TR(...) __VA_ARGS__
 #define TR_ADD(slot, v) atomicAdd(&g_trace[slot], static_cast<unsigned long long>(v))
-// Per-block event times (cycles since the start barrier) of the first cluster (the heaviest tile).
+// Per-block event times (cycles since the start barrier) of cluster 0's first tile (the heaviest).
 constexpr int kTLMax = 128, kTLEvents = 12;
 __device__ long long g_ptl[kTLEvents][kTLMax];
 #define TL(ev, idx, val) \
-    do { if (cluster_id == 0 && static_cast<int>(idx) < kTLMax) g_ptl[ev][idx] = (val); } while (0)
+    do { if (static_cast<int>(idx) < kTLMax) g_ptl[ev][idx] = (val); } while (0)
 #else
 #define TR(...)
 #define TR_ADD(slot, v) (void)0
@@ -118,8 +126,28 @@ struct Params {
     __nv_bfloat16 *out;
     int *err;
     int T, H, n_qtiles, bh_count;
+    int n_tiles;   // n_qtiles * bh_count work tiles, numbered heaviest first
+    int G;         // clusters of the persistent grid
     float qk_scale_log2;
 };
+
+// Work tile `tile` (heaviest first): 128 query tokens of one (batch, head) and the key blocks they see.
+struct TileInfo {
+    int b, h, t0;
+    int nblk;   // 256-key score blocks covering keys [0, min(T, t0 + 128))
+    int nkv;    // 128-key value units (the last may be entirely masked)
+};
+__device__ __forceinline__ TileInfo tile_info(int tile, const Params &p) {
+    const int qt = p.n_qtiles - 1 - tile / p.bh_count;
+    const int bh = tile % p.bh_count;
+    TileInfo ti;
+    ti.b = bh / p.H;
+    ti.h = bh % p.H;
+    ti.t0 = qt * kBM;
+    ti.nblk = (qt + 2) / 2;
+    ti.nkv = 2 * ti.nblk;
+    return ti;
+}
 
 __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
@@ -139,16 +167,6 @@ __device__ __forceinline__ void st_shared_v2f(uint32_t addr, float a, float b) {
 }
 
 // Pairwise (tree) reductions over 64 values: short dependency chains.
-__device__ __forceinline__ float tree_max64(const float (&s)[2][32]) {
-    float m[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m[i] = fmaxf(s[0][i], s[1][i]);
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
-    return m[0];
-}
 __device__ __forceinline__ float tree_max128(const float (&s)[4][32]) {
     float m[32];
 #pragma unroll
@@ -169,16 +187,6 @@ __device__ __forceinline__ float tree_sum128(const float (&s)[4][32]) {
         for (int i = 0; i < w; ++i) m[i] += m[i + w];
     return m[0];
 }
-__device__ __forceinline__ float tree_sum64(const float (&s)[2][32]) {
-    float m[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m[i] = s[0][i] + s[1][i];
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) m[i] += m[i + w];
-    return m[0];
-}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_r512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_c,
@@ -193,18 +201,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
-    const int cluster_id = static_cast<int>(blockIdx.x >> 1);
-    const int qt = p.n_qtiles - 1 - cluster_id / p.bh_count;   // heaviest tiles first
-    const int bh = cluster_id % p.bh_count;
-    const int b = bh / p.H, h = bh % p.H;
-    const int t0 = qt * kBM;
-    const int nblk = (qt + 2) / 2;   // 256-key score blocks covering keys [0, min(T, t0 + 128))
-    const int nkv = 2 * nblk;        // 128-key value units (the last may be entirely masked)
+    const int cl = static_cast<int>(blockIdx.x >> 1);   // this cluster; it walks the tiles of tile_of(k)
+    // Tile k of this cluster: a snake over the heavy-first tile order, so every cluster's work adds up the same.
+    auto tile_of = [&](int k) { return k * p.G + ((k & 1) ? p.G - 1 - cl : cl); };
 
     if (threadIdx.x == 0) {
         mbar_init(B_(bars->pro_full), 1);
         mbar_init(B_(bars->absorb_done), 1);
         mbar_init(B_(bars->qabs_ready), 1);
+        mbar_init(B_(bars->q_free), 1);
         for (int i = 0; i < kSStages; ++i) {
             mbar_init(B_(bars->sc_full[i]), 1);
             mbar_init(B_(bars->sc_empty[i]), 1);
@@ -224,6 +229,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(B_(bars->oc_empty[i]), 1);
         }
         mbar_init(B_(bars->corr_done), 256);
+        mbar_init(B_(bars->ep_read), 256);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -236,431 +242,504 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     TR(const long long t_start = clock64();)
-
-    if (rank == 0) {
-        // =========================================================== score CTA
-        if (warp == 0 && lane == 0) {
-            // ---- TMA producer: q tile + W_UK[h] (ring uses 0-3), then c tiles [256 keys x 64]
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_c256);
-            tma_prefetch_desc(&tm_wuk);
-            const uint32_t pro = B_(bars->pro_full);
-            mbar_arrive_expect_tx(pro, 2 * kSlab);
-            for (int s = 0; s < 2; ++s) tma_load_4d(base + S_PST + s * kSlab, &tm_q, pro, s * 64, h, t0, b);
-            for (int s = 0; s < kSStages; ++s) {
-                mbar_arrive_expect_tx(B_(bars->sc_full[s]), kSStage);
-                for (int i = 0; i < 2; ++i)
-                    tma_load_2d(base + S_RING + s * kSStage + i * kSlab, &tm_wuk, B_(bars->sc_full[s]),
-                                (2 * s + i) * 64, h * kD);
-            }
-            int it = kSStages;
-            bool ok = true;
-            for (int j = 0; ok && j < nblk; ++j) {
-                for (int kc = 0; kc < 8; ++kc, ++it) {
-                    const int st = it % kSStages;
-                    TR(const long long _a = clock64();)
-                    if (!(ok = mbar_wait(B_(bars->sc_empty[st]), ((it / kSStages) - 1) & 1, p.err, abort_flag)))
-                        break;
-                    TR(TR_ADD(TR_S_PROD_EMPTY, clock64() - _a);)
-                    mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSStage);
-                    tma_load_3d(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, j * kBS, b);
-                }
-            }
-            if (!ok) *abort_flag = 1;
-            // no load may still be landing when the CTA exits
-            mbar_wait(pro, 0, p.err);
-            for (int k = it - kSStages; k < it; ++k)
-                mbar_wait(B_(bars->sc_full[k % kSStages]), (k / kSStages) & 1, p.err);
-        } else if (warp == 1 && lane == 0) {
-            // ---- MMA issuer: absorb, then S = q_abs . c^T per 256-key block (q_abs from TMEM, N = 256)
-            bool ok = mbar_wait(B_(bars->pro_full), 0, p.err, abort_flag);
-            for (int s = 0; ok && s < kSStages; ++s) ok = mbar_wait(B_(bars->sc_full[s]), 0, p.err, abort_flag);
-            if (ok) {
-                tc_fence_after();
-#pragma unroll 1
-                for (int kk = 0; kk < kD / 16; ++kk) {
-                    const uint64_t a = make_smem_desc(base + S_PST + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-#pragma unroll
-                    for (int nh = 0; nh < 2; ++nh) {
-                        const uint64_t bd = make_smem_desc(base + S_RING + nh * 2 * kSStage + kk * 2048, kSlab, 1024);
-                        umma_bf16(tmem + nh * 256, a, bd, kIdescAbsorb, kk > 0);
-                    }
-                }
-                umma_commit(B_(bars->absorb_done));
-                for (int s = 0; s < kSStages; ++s) umma_commit(B_(bars->sc_empty[s]));   // W_UK's slots are free
-                ok = mbar_wait(B_(bars->qabs_ready), 0, p.err, abort_flag);
-            }
-            int it = kSStages;
-            TR(long long tl0 = clock64(), w_free = 0, w_full = 0;)
-            for (int j = 0; ok && j < nblk; ++j) {
-                TR(long long _a = clock64();)
-                if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free[0]), (j - 1) & 1, p.err, abort_flag))) break;
-                TR(w_free += clock64() - _a; TL(0, j, clock64() - t_start); long long w_blk = 0;)
-                tc_fence_after();
-                for (int kc = 0; kc < 8; ++kc, ++it) {
-                    const int st = it % kSStages;
-                    TR(long long _b = clock64();)
-                    if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
-                    TR(w_full += clock64() - _b; w_blk += clock64() - _b;)
-                    tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
-                        umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
-                                         (kc | kk) != 0);
-                    }
-                    umma_commit(B_(bars->sc_empty[st]));
-                }
-                if (!ok) break;
-                umma_commit(B_(bars->s_full[0]));
-                TR(TL(1, j, clock64() - t_start); TL(7, j, w_blk);)
-            }
-            TR(TR_ADD(TR_S_MMA_LOOP, clock64() - tl0); TR_ADD(TR_S_MMA_SFREE, w_free); TR_ADD(TR_S_MMA_SCFULL, w_full);)
-            if (!ok) *abort_flag = 1;
-        } else if (warp >= 4) {
-            // ---- softmax: warpgroup `wg` owns keys [128 wg, 128 wg + 128) of each 256-key block, i.e. the
-            // value CTA's unit 2j + wg; thread `row` owns TMEM lane `row`
-            const int wg = (warp - 4) >> 2;
-            const int row = (warp & 3) * 32 + lane;
-            const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-            const int t = t0 + row;
-            const bool issuer = (threadIdx.x & 127) == 0;   // issues this warpgroup's bulk copies
-            bool fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
-            bool ok = !named_bar_or(1, 256, fail);
-            if (ok && wg == 0) {
-                // q_abs (fp32, TMEM columns 0-511) -> q_abs * scale * log2(e) packed as bf16 pairs into
-                // columns 0-255; chunk k (64 latent columns) lands in 32k..32k+31, which this thread has
-                // already read, so the compaction is in place, chunk by chunk in increasing order
-                tc_fence_after();
-#pragma unroll 1
-                for (int k = 0; k < kR / 64; ++k) {
-                    float v[2][32], w[32];
-                    tmem_ld32(trow + k * 64, v[0]);
-                    tmem_ld32(trow + k * 64 + 32, v[1]);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        w[i] = __uint_as_float(pack_bf16x2(v[i >> 4][2 * (i & 15)] * p.qk_scale_log2,
-                                                           v[i >> 4][2 * (i & 15) + 1] * p.qk_scale_log2));
-                    tmem_st32(trow + S_QCOL + k * 32, w);
-                    tmem_wait_st();
-                }
-                tc_fence_before();
-            }
-            named_bar_sync(1, 256);
-            if (threadIdx.x == 128 && ok) mbar_arrive(B_(bars->qabs_ready));
-            TR(if (threadIdx.x == 128) TR_ADD(TR_S_PROLOGUE, clock64() - t_start);)
-            TR(long long tl0 = clock64(), w_sfull = 0, w_xbar = 0, w_pfree = 0, w_store = 0, w_rel = 0;)
-
-            const uint32_t ptile = base + S_PST + wg * kPUnit;   // this warpgroup's staging unit
-            const uint32_t ri = ptile + kPBytes;
-            float m_run = -INFINITY, l_part = 0.f;
-            for (int j = 0; ok && j < nblk; ++j) {
-                TR(long long _a = clock64();)
-                fail = fail || !mbar_wait(B_(bars->s_full[0]), j & 1, p.err, abort_flag);
-                TR(w_sfull += clock64() - _a; if ((threadIdx.x & 127) == 0) TL(2 + 3 * wg, j, clock64() - t_start);)
-                float s[4][32];
-                if (!fail) {
-                    tc_fence_after();
-#pragma unroll
-                    for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_SCOL + wg * 128 + c4 * 32, s[c4]);
-                    tmem_wait_ld();
-                    tc_fence_before();
-                    mbar_arrive(B_(bars->s_free[0]));
-                    if (j == nblk - 1) {   // the last block: keys after the query or past the sequence
-                        const int lim = min(t, p.T - 1) - j * kBS - wg * 128;   // last visible column of this unit
-#pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
-                    }
-                    st_shared_f32(base + PMAX + ((j & 1) * 2 + wg) * kBM * 4 + row * 4, tree_max128(s));
-                }
-                TR(long long _x = clock64();)
-                if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
-                TR(w_xbar += clock64() - _x; if (threadIdx.x == 128) TL(3, j, clock64() - t_start);)
-                const float mx = fmaxf(ld_shared_f32(base + PMAX + ((j & 1) * 2 + 0) * kBM * 4 + row * 4),
-                                       ld_shared_f32(base + PMAX + ((j & 1) * 2 + 1) * kBM * 4 + row * 4));
-                float factor = 1.f;
-                if (mx > m_run + kRescaleLog2) {
-                    factor = fast_exp2(m_run - mx);
-                    m_run = mx;
-                }
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(s[c4][i] - m_run);
-                l_part = l_part * factor + tree_sum128(s);
-
-                TR(long long _s = clock64();)
-                // the staging unit is free once this warpgroup's previous copy has read it
-                if (issuer) bulk_wait_read_all();
-                named_bar_sync(2 + wg, 128);
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float *v = &s[c4][8 * k];
-                        st_shared_v4(ptile + (c4 >> 1) * kSlab + sw128_offset(row, (c4 & 1) * 4 + k),
-                                     pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                                     pack_bf16x2(v[6], v[7]));
-                    }
-                // unit 2j carries the block's rescale factor; unit 2j+1 shares its maximum (factor 1)
-                st_shared_v2f(ri + row * 8, wg == 0 ? factor : 1.f, l_part);
-                fence_proxy_async_smem();
-                named_bar_sync(2 + wg, 128);
-                TR(w_store += clock64() - _s;)
-                if (issuer) {
-                    // the value CTA's P buffer `wg` is free once the product of unit 2(j-1) + wg completed
-                    TR(long long _f = clock64();)
-                    if (j >= 1) fail = !mbar_wait<true>(B_(bars->p_free[wg]), (j - 1) & 1, p.err, abort_flag);
-                    TR(w_pfree += clock64() - _f;)
-                    if (!fail) {
-                        const uint32_t dst_bar = mapa_shared(B_(bars->p_full[wg]), 1);
-                        bulk_copy_s2cluster(mapa_shared(base + O_P + wg * kPBytes, 1), ptile, kPBytes, dst_bar);
-                        bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + wg * kRowInfoBytes, 1), ri,
-                                            kRowInfoBytes, dst_bar);
-                        bulk_commit_group();
-                        TR(TL(wg == 0 ? 4 : 6, j, clock64() - t_start);)
-                    }
-                }
-            }
-            TR(if (threadIdx.x == 128) {
-                TR_ADD(TR_S_SM_LOOP, clock64() - tl0); TR_ADD(TR_S_SM_SFULL, w_sfull); TR_ADD(TR_S_SM_XBAR, w_xbar);
-                TR_ADD(TR_S_SM_PFREE, w_pfree); TR_ADD(TR_S_SM_STORE, w_store); TR_ADD(TR_S_SM_RELEASE, w_rel);
-            })
-            if (issuer) bulk_wait_all();
-            if (!ok || fail) *abort_flag = 1;
-        }
-    } else {
-        // =========================================================== value CTA
-        if (warp == 0 && lane == 0) {
-            // ---- TMA producer: c tiles as the MN-major value operand, then W_UV[h]
-            tma_prefetch_desc(&tm_c);
-            tma_prefetch_desc(&tm_wuv);
-            int it = 0;
-            bool ok = true;
-            for (int j = 0; ok && j < nkv + 1; ++j) {   // j == nkv: the W_UV tile
-                for (int nh = 0; nh < 2; ++nh, ++it) {
-                    const int st = it % kOStages;
-                    TR(const long long _a = clock64();)
-                    if (it >= kOStages &&
-                        !(ok = mbar_wait(B_(bars->oc_empty[st]), ((it / kOStages) - 1) & 1, p.err, abort_flag)))
-                        break;
-                    TR(TR_ADD(TR_O_PROD_EMPTY, clock64() - _a);)
-                    const uint32_t full = B_(bars->oc_full[st]);
-                    mbar_arrive_expect_tx(full, kOStage);
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const uint32_t dst = base + O_RING + st * kOStage + q4 * kSlab;
-                        if (j < nkv)
-                            tma_load_3d(dst, &tm_c, full, (nh * 4 + q4) * 64, j * kBN, b);
-                        else
-                            tma_load_2d(dst, &tm_wuv, full, (nh * 4 + q4) * 64, h * kD);
-                    }
-                }
-            }
-            if (!ok) *abort_flag = 1;
-            for (int k = (it > kOStages ? it - kOStages : 0); k < it; ++k)
-                mbar_wait(B_(bars->oc_full[k % kOStages]), (k / kOStages) & 1, p.err);
-        } else if (warp == 1) {
-            // ---- MMA warp: o_lat += P . c, then o = o_lat . W_UV^T; lane 0 issues
-            const bool leader = lane == 0;
-            auto wait_all = [&](uint64_t &bar, uint32_t parity, bool cluster) {
-                return __all_sync(0xffffffffu, cluster ? mbar_wait<true>(B_(bar), parity, p.err, abort_flag)
-                                                       : mbar_wait(B_(bar), parity, p.err, abort_flag));
-            };
-            int it = 0, ncorr = 0;
-            bool ok = true;
-            TR(long long tl0 = clock64(), w_pfull = 0, w_oc = 0, w_corr = 0;)
-            for (int j = 0; ok && j < nkv; ++j) {
-                const int pb = j & 1;
-                TR(long long _a = clock64();)
-                if (leader) mbar_arrive_expect_tx(B_(bars->p_full[pb]), kPBytes + kRowInfoBytes);
-                if (!(ok = wait_all(bars->p_full[pb], (j >> 1) & 1, true))) break;
-                TR(w_pfull += clock64() - _a; if (leader) TL(8, j, clock64() - t_start); long long w_u = 0;)
-                // any row whose maximum grew needs o_lat rescaled before this block's product
-                const uint32_t ri = base + O_ROWINFO + pb * kRowInfoBytes;
-                bool grew = false;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) grew |= ld_shared_f32(ri + (lane + 32 * k) * 8) != 1.f;
-                if (j > 0 && __any_sync(0xffffffffu, grew)) {
-                    TR(long long _c = clock64();)
-                    if (!(ok = wait_all(bars->corr_done, ncorr & 1, false))) break;
-                    TR(w_corr += clock64() - _c;)
-                    ++ncorr;
-                }
-                tc_fence_after();
-                for (int nh = 0; nh < 2; ++nh, ++it) {
-                    const int st = it % kOStages;
-                    TR(long long _o = clock64();)
-                    if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
-                    TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
-                    tc_fence_after();
-                    if (leader) {
-#pragma unroll
-                        for (int kk = 0; kk < kBN / 16; ++kk) {
-                            const uint64_t a = make_smem_desc(
-                                base + O_P + pb * kPBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                            const uint64_t bd = make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
-                            umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (j > 0 || kk > 0));
+    if (warp < 4) {
+        regs_release<kRegsCtl>();   // warpgroup-uniform
+        if (rank == 0) {
+            // =========================================================== score CTA: control
+            if (warp == 0 && lane == 0) {
+                // ---- TMA producer.  Per tile: the q tile into the first P staging buffer, W_UK[h] into four ring
+                // positions, then c tiles [256 keys x 64] for every score block.  A tile takes 4 + 8 nblk ring
+                // positions, a multiple of the 4 stages, so W_UK always fills slots 0-3 in order.
+                tma_prefetch_desc(&tm_q);
+                tma_prefetch_desc(&tm_c256);
+                tma_prefetch_desc(&tm_wuk);
+                const uint32_t pro = B_(bars->pro_full);
+                int it = 0, k = 0;
+                bool ok = true;
+                for (; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    // the staging buffer takes the next q once the previous tile's last P copy has read it
+                    if (k >= 1 && !(ok = mbar_wait(B_(bars->q_free), (k - 1) & 1, p.err, abort_flag))) break;
+                    mbar_arrive_expect_tx(pro, 2 * kSlab);
+                    for (int s = 0; s < 2; ++s) tma_load_4d(base + S_PST + s * kSlab, &tm_q, pro, s * 64, ti.h, ti.t0, ti.b);
+                    const int n_pos = 4 + 8 * ti.nblk;
+                    for (int i = 0; i < n_pos; ++i, ++it) {
+                        const int st = it % kSStages;
+                        TR(const long long _a = clock64();)
+                        if (it >= kSStages &&
+                            !(ok = mbar_wait(B_(bars->sc_empty[st]), ((it / kSStages) - 1) & 1, p.err, abort_flag)))
+                            break;
+                        TR(TR_ADD(TR_S_PROD_EMPTY, clock64() - _a);)
+                        const uint32_t full = B_(bars->sc_full[st]);
+                        mbar_arrive_expect_tx(full, kSStage);
+                        if (i < 4) {
+                            for (int s = 0; s < 2; ++s)
+                                tma_load_2d(base + S_RING + st * kSStage + s * kSlab, &tm_wuk, full, (2 * i + s) * 64,
+                                            ti.h * kD);
+                        } else {
+                            const int q = i - 4;
+                            tma_load_3d(base + S_RING + st * kSStage, &tm_c256, full, (q & 7) * 64, (q >> 3) * kBS, ti.b);
                         }
-                        umma_commit(B_(bars->oc_empty[st]));
                     }
-                    __syncwarp();
                 }
-                if (!ok) break;
-                if (leader) umma_commit(B_(bars->pv_done[pb]));
-                TR(if (leader) { TL(9, j, clock64() - t_start); TL(10, j, w_u); })
-            }
-            TR(if (leader) {
-                TR_ADD(TR_O_MMA_LOOP, clock64() - tl0); TR_ADD(TR_O_MMA_PFULL, w_pfull); TR_ADD(TR_O_MMA_OCFULL, w_oc);
-                TR_ADD(TR_O_MMA_CORR, w_corr); TR_ADD(TR_CORRECTIONS, ncorr);
-            })
-            for (int kh = 0; ok && kh < 2; ++kh, ++it) {
-                if (!(ok = wait_all(bars->olat_ready[kh], 0, false))) break;
-                const int st = it % kOStages;
-                if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
-                tc_fence_after();
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const uint64_t a = make_smem_desc(base + O_P + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                        const uint64_t bd =
-                            make_smem_desc(base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                        umma_bf16(tmem, a, bd, kIdescEp, (kh > 0 || kk > 0));
-                    }
-                    umma_commit(B_(bars->oc_empty[st]));
-                    umma_commit(B_(bars->ep_done[kh]));
-                }
-                __syncwarp();
-            }
-            if (!ok && leader) *abort_flag = 1;
-        } else if (warp == 2 && lane == 0) {
-            // ---- relay: P buffer pb is free again once its product completed and its row info was read
-            for (int j = 0; j < nkv; ++j) {
-                const int pb = j & 1;
-                if (!mbar_wait(B_(bars->pv_done[pb]), (j >> 1) & 1, p.err, abort_flag) ||
-                    !mbar_wait(B_(bars->ri_read[pb]), (j >> 1) & 1, p.err, abort_flag)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                mbar_arrive_remote(B_(bars->p_free[pb]), 0);
-            }
-        } else if (warp >= 4) {
-            // ---- correction + epilogue: thread `row` of warpgroup `wg` owns TMEM lane `row`,
-            // latent columns [256 wg, 256 wg + 256) for rescaling
-            const int wg = (warp - 4) >> 2;
-            const int row = (warp & 3) * 32 + lane;
-            const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-            const int t = t0 + row;
-            float l_even = 0.f, l_odd = 0.f;
-            bool ok = true, fail;
-            TR(long long tl0 = clock64();)
-            for (int j = 0; j < nkv; ++j) {
-                const int pb = j & 1;
-                fail = !mbar_wait<true>(B_(bars->p_full[pb]), (j >> 1) & 1, p.err, abort_flag);
-                if (named_bar_or(4, 256, fail)) { ok = false; break; }
-                const float2 fl = ld_shared_v2f(base + O_ROWINFO + pb * kRowInfoBytes + row * 8);
-                mbar_arrive(B_(bars->ri_read[pb]));
-                // the two warpgroups of the score CTA keep separate sums (even and odd units)
-                if (j & 1)
-                    l_odd = fl.y;
-                else
-                    l_even = fl.y;
-                if (named_bar_or(4, 256, j > 0 && fl.x != 1.f)) {
-                    fail = !mbar_wait(B_(bars->pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, p.err, abort_flag);
-                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                if (!ok) *abort_flag = 1;
+                // no load may still be landing when the CTA exits
+                if (k > 0) mbar_wait(pro, (k - 1) & 1, p.err);
+                for (int q = (it > kSStages ? it - kSStages : 0); q < it; ++q)
+                    mbar_wait(B_(bars->sc_full[q % kSStages]), (q / kSStages) & 1, p.err);
+            } else if (warp == 1 && lane == 0) {
+                // ---- MMA issuer: per tile the absorb, then S = q_abs . c^T per 256-key block (q_abs from TMEM)
+                int it = 0, gb = 0;   // ring positions consumed, score blocks issued (all tiles)
+                bool ok = true;
+                TR(long long tl0 = clock64(), w_free = 0, w_full = 0;)
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    TR(const bool tl_on = cl == 0 && k == 0;)
+                    ok = mbar_wait(B_(bars->pro_full), k & 1, p.err, abort_flag);
+                    for (int i = 0; ok && i < 4; ++i)
+                        ok = mbar_wait(B_(bars->sc_full[(it + i) % kSStages]), ((it + i) / kSStages) & 1, p.err, abort_flag);
+                    // the absorb writes all 512 TMEM columns: the previous tile's last S must have been read
+                    if (ok && gb >= 1) ok = mbar_wait(B_(bars->s_free[0]), (gb - 1) & 1, p.err, abort_flag);
+                    if (!ok) break;
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, fl.x != 1.f)) {
-#pragma unroll 1
-                        for (int cc = 0; cc < 8; ++cc) {
-                            float v[32];
-                            const uint32_t ta = trow + wg * 256 + cc * 32;
-                            tmem_ld32(ta, v);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] *= fl.x;
-                            tmem_st32(ta, v);
+    #pragma unroll 1
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint64_t a = make_smem_desc(base + S_PST + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+    #pragma unroll
+                        for (int nh = 0; nh < 2; ++nh) {
+                            const uint64_t bd = make_smem_desc(base + S_RING + nh * 2 * kSStage + kk * 2048, kSlab, 1024);
+                            umma_bf16(tmem + nh * 256, a, bd, kIdescAbsorb, kk > 0);
                         }
-                        tmem_wait_st();
                     }
-                    tc_fence_before();
-                    mbar_arrive(B_(bars->corr_done));
+                    umma_commit(B_(bars->absorb_done));
+                    for (int i = 0; i < 4; ++i, ++it) umma_commit(B_(bars->sc_empty[it % kSStages]));   // W_UK's slots
+                    if (!(ok = mbar_wait(B_(bars->qabs_ready), k & 1, p.err, abort_flag))) break;
+                    for (int j = 0; ok && j < ti.nblk; ++j, ++gb) {
+                        TR(long long _a = clock64();)
+                        if (j >= 1 && !(ok = mbar_wait(B_(bars->s_free[0]), (gb - 1) & 1, p.err, abort_flag))) break;
+                        TR(w_free += clock64() - _a; if (tl_on) TL(0, j, clock64() - t_start); long long w_blk = 0;)
+                        tc_fence_after();
+                        for (int kc = 0; kc < 8; ++kc, ++it) {
+                            const int st = it % kSStages;
+                            TR(long long _b = clock64();)
+                            if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
+                            TR(w_full += clock64() - _b; w_blk += clock64() - _b;)
+                            tc_fence_after();
+    #pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
+                                umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
+                                                 (kc | kk) != 0);
+                            }
+                            umma_commit(B_(bars->sc_empty[st]));
+                        }
+                        if (!ok) break;
+                        umma_commit(B_(bars->s_full[0]));
+                        TR(if (tl_on) { TL(1, j, clock64() - t_start); TL(7, j, w_blk); })
+                    }
                 }
+                TR(TR_ADD(TR_S_MMA_LOOP, clock64() - tl0); TR_ADD(TR_S_MMA_SFREE, w_free); TR_ADD(TR_S_MMA_SCFULL, w_full);)
+                if (!ok) *abort_flag = 1;
             }
-            if (ok) {
-                fail = !mbar_wait(B_(bars->pv_done[(nkv - 1) & 1]), ((nkv - 1) >> 1) & 1, p.err, abort_flag);
-                ok = !named_bar_or(4, 256, fail);
-            }
-            TR(long long t_ep = clock64(); if (threadIdx.x == 128) TR_ADD(TR_O_COR_LOOP, t_ep - tl0);)
-            const float inv_l = 1.f / (l_even + l_odd);
-            for (int kh = 0; ok && kh < 2; ++kh) {
-                if (kh == 1) {   // the staging tile is free once the first half's product completed
-                    fail = !mbar_wait(B_(bars->ep_done[0]), 0, p.err, abort_flag);
-                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
-                    const int cc = wg * 4 + i;   // 32-column chunk within this 256-column half
-                    float v[32];
-                    tmem_ld32(trow + kh * 256 + cc * 32, v);
-                    tmem_wait_ld();
-                    store_row32_bf16(base + O_P, kSlab, row, cc, v, inv_l);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                named_bar_sync(4, 256);
-                if (threadIdx.x == 128) mbar_arrive(B_(bars->olat_ready[kh]));
-            }
-            if (ok) {
-                fail = !mbar_wait(B_(bars->ep_done[1]), 0, p.err, abort_flag);
-                ok = !named_bar_or(4, 256, fail);
-            }
-            if (ok) {
-                tc_fence_after();
-                float o[2][32];
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + wg * 64 + c2 * 32, o[c2]);
-                tmem_wait_ld();
-                if (t < p.T) {
-                    const size_t off = ((static_cast<size_t>(b) * p.T + t) * p.H + h) * kD + wg * 64;
-                    const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
-                    uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
-#pragma unroll
-                    for (int v8 = 0; v8 < 8; ++v8) {
-                        float y[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) y[i] = o[(v8 * 8 + i) >> 5][(v8 * 8 + i) & 31];
-                        if (g4) {
-                            const uint4 gv = __ldg(g4 + v8);
-                            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                const float g_lo = __uint_as_float(gw[i] << 16);
-                                const float g_hi = __uint_as_float(gw[i] & 0xFFFF0000u);
-                                y[2 * i] *= __fdividef(1.f, 1.f + fast_exp2(-g_lo * kLog2e));
-                                y[2 * i + 1] *= __fdividef(1.f, 1.f + fast_exp2(-g_hi * kLog2e));
+        } else {
+            // =========================================================== value CTA: control
+            if (warp == 0 && lane == 0) {
+                // ---- TMA producer: per tile, c tiles as the MN-major value operand for every unit, then W_UV[h]
+                tma_prefetch_desc(&tm_c);
+                tma_prefetch_desc(&tm_wuv);
+                int it = 0;
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    for (int j = 0; ok && j < ti.nkv + 1; ++j) {   // j == nkv: the W_UV tile
+                        for (int nh = 0; nh < 2; ++nh, ++it) {
+                            const int st = it % kOStages;
+                            TR(const long long _a = clock64();)
+                            if (it >= kOStages &&
+                                !(ok = mbar_wait(B_(bars->oc_empty[st]), ((it / kOStages) - 1) & 1, p.err, abort_flag)))
+                                break;
+                            TR(TR_ADD(TR_O_PROD_EMPTY, clock64() - _a);)
+                            const uint32_t full = B_(bars->oc_full[st]);
+                            mbar_arrive_expect_tx(full, kOStage);
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const uint32_t dst = base + O_RING + st * kOStage + q4 * kSlab;
+                                if (j < ti.nkv)
+                                    tma_load_3d(dst, &tm_c, full, (nh * 4 + q4) * 64, j * kBN, ti.b);
+                                else
+                                    tma_load_2d(dst, &tm_wuv, full, (nh * 4 + q4) * 64, ti.h * kD);
                             }
                         }
-                        o4[v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                            pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                    }
+                }
+                if (!ok) *abort_flag = 1;
+                for (int q = (it > kOStages ? it - kOStages : 0); q < it; ++q)
+                    mbar_wait(B_(bars->oc_full[q % kOStages]), (q / kOStages) & 1, p.err);
+            } else if (warp == 1) {
+                // ---- MMA warp: per tile o_lat += P . c, then o = o_lat . W_UV^T; lane 0 issues
+                const bool leader = lane == 0;
+                auto wait_all = [&](uint64_t &bar, uint32_t parity, bool cluster) {
+                    return __all_sync(0xffffffffu, cluster ? mbar_wait<true>(B_(bar), parity, p.err, abort_flag)
+                                                           : mbar_wait(B_(bar), parity, p.err, abort_flag));
+                };
+                int it = 0, ncorr = 0, gu = 0;   // ring positions, corrections, units (all tiles)
+                bool ok = true;
+                TR(long long tl0 = clock64(), w_pfull = 0, w_oc = 0, w_corr = 0;)
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    TR(const bool tl_on = cl == 0 && k == 0;)
+                    // o_lat's TMEM columns are free once the previous tile's epilogue has read its output
+                    if (k >= 1 && !(ok = wait_all(bars->ep_read, (k - 1) & 1, false))) break;
+                    for (int j = 0; ok && j < ti.nkv; ++j, ++gu) {
+                        const int pb = gu & 1;
+                        TR(long long _a = clock64();)
+                        if (leader) mbar_arrive_expect_tx(B_(bars->p_full[pb]), kPBytes + kRowInfoBytes);
+                        if (!(ok = wait_all(bars->p_full[pb], (gu >> 1) & 1, true))) break;
+                        TR(w_pfull += clock64() - _a; if (leader && tl_on) TL(8, j, clock64() - t_start); long long w_u = 0;)
+                        // any row whose maximum grew needs o_lat rescaled before this unit's product
+                        const uint32_t rinfo = base + O_ROWINFO + pb * kRowInfoBytes;
+                        bool grew = false;
+    #pragma unroll
+                        for (int q = 0; q < 4; ++q) grew |= ld_shared_f32(rinfo + (lane + 32 * q) * 8) != 1.f;
+                        if (j > 0 && __any_sync(0xffffffffu, grew)) {
+                            TR(long long _c = clock64();)
+                            if (!(ok = wait_all(bars->corr_done, ncorr & 1, false))) break;
+                            TR(w_corr += clock64() - _c;)
+                            ++ncorr;
+                        }
+                        tc_fence_after();
+                        for (int nh = 0; nh < 2; ++nh, ++it) {
+                            const int st = it % kOStages;
+                            TR(long long _o = clock64();)
+                            if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
+                            TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
+                            tc_fence_after();
+                            if (leader) {
+    #pragma unroll
+                                for (int kk = 0; kk < kBN / 16; ++kk) {
+                                    const uint64_t a = make_smem_desc(
+                                        base + O_P + pb * kPBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                                    const uint64_t bd =
+                                        make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
+                                    umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (j > 0 || kk > 0));
+                                }
+                                umma_commit(B_(bars->oc_empty[st]));
+                            }
+                            __syncwarp();
+                        }
+                        if (!ok) break;
+                        if (leader) umma_commit(B_(bars->pv_done[pb]));
+                        TR(if (leader && tl_on) { TL(9, j, clock64() - t_start); TL(10, j, w_u); })
+                    }
+                    for (int kh = 0; ok && kh < 2; ++kh, ++it) {
+                        if (!(ok = wait_all(bars->olat_ready[kh], k & 1, false))) break;
+                        const int st = it % kOStages;
+                        if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
+                        tc_fence_after();
+                        if (leader) {
+    #pragma unroll
+                            for (int kk = 0; kk < 16; ++kk) {
+                                const uint64_t a = make_smem_desc(base + O_P + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                                const uint64_t bd = make_smem_desc(
+                                    base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                                umma_bf16(tmem, a, bd, kIdescEp, (kh > 0 || kk > 0));
+                            }
+                            umma_commit(B_(bars->oc_empty[st]));
+                            umma_commit(B_(bars->ep_done[kh]));
+                        }
+                        __syncwarp();
+                    }
+                }
+                TR(if (leader) {
+                    TR_ADD(TR_O_MMA_LOOP, clock64() - tl0); TR_ADD(TR_O_MMA_PFULL, w_pfull); TR_ADD(TR_O_MMA_OCFULL, w_oc);
+                    TR_ADD(TR_O_MMA_CORR, w_corr); TR_ADD(TR_CORRECTIONS, ncorr);
+                })
+                if (!ok && leader) *abort_flag = 1;
+            } else if (warp == 2 && lane == 0) {
+                // ---- relay: P buffer pb is free again once its product completed and its row info was read; the
+                // buffers of a tile's last two units are also the epilogue's staging, free after its second product
+                int gu = 0;
+                bool ok = true;
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    for (int j = 0; j < ti.nkv; ++j, ++gu) {
+                        const int pb = gu & 1;
+                        if (!mbar_wait(B_(bars->pv_done[pb]), (gu >> 1) & 1, p.err, abort_flag) ||
+                            !mbar_wait(B_(bars->ri_read[pb]), (gu >> 1) & 1, p.err, abort_flag) ||
+                            (j >= ti.nkv - 2 && !mbar_wait(B_(bars->ep_done[1]), k & 1, p.err, abort_flag))) {
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_remote(B_(bars->p_free[pb]), 0);
                     }
                 }
             }
-            TR(if (threadIdx.x == 128) TR_ADD(TR_O_EPILOGUE, clock64() - t_ep);)
-            if (!ok) *abort_flag = 1;
+        }
+    } else {
+        regs_acquire<kRegsMath>();
+        if (rank == 0) {
+            // =========================================================== score CTA: softmax
+                // ---- softmax: warpgroup `wg` owns keys [128 wg, 128 wg + 128) of each 256-key block, i.e. the
+                // value CTA's unit 2j + wg; thread `row` owns TMEM lane `row`
+                const int wg = (warp - 4) >> 2;
+                const int row = (warp & 3) * 32 + lane;
+                const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+                const bool issuer = (threadIdx.x & 127) == 0;   // issues this warpgroup's bulk copies
+                const uint32_t ptile = base + S_PST + wg * kPUnit;   // this warpgroup's staging unit
+                const uint32_t ri = ptile + kPBytes;
+                int gb = 0, nu = 0;   // score blocks (all tiles), units this warpgroup has sent
+                bool ok = true, fail = false;
+                TR(long long tl0 = clock64(), w_sfull = 0, w_xbar = 0, w_pfree = 0, w_store = 0, w_rel = 0;)
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    TR(const bool tl_on = cl == 0 && k == 0;)
+                    const int t = ti.t0 + row;
+                    fail = fail || !mbar_wait(B_(bars->absorb_done), k & 1, p.err, abort_flag);
+                    if (named_bar_or(1, 256, fail)) { ok = false; break; }
+                    if (wg == 0) {
+                        // q_abs (fp32, TMEM columns 0-511) -> q_abs * scale * log2(e) packed as bf16 pairs into
+                        // columns 0-255; chunk k (64 latent columns) lands in 32k..32k+31, which this thread has
+                        // already read, so the compaction is in place, chunk by chunk in increasing order
+                        tc_fence_after();
+    #pragma unroll 1
+                        for (int kc = 0; kc < kR / 64; ++kc) {
+                            float v[2][32], w[32];
+                            tmem_ld32(trow + kc * 64, v[0]);
+                            tmem_ld32(trow + kc * 64 + 32, v[1]);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                w[i] = __uint_as_float(pack_bf16x2(v[i >> 4][2 * (i & 15)] * p.qk_scale_log2,
+                                                                   v[i >> 4][2 * (i & 15) + 1] * p.qk_scale_log2));
+                            tmem_st32(trow + S_QCOL + kc * 32, w);
+                            tmem_wait_st();
+                        }
+                        tc_fence_before();
+                    }
+                    named_bar_sync(1, 256);
+                    if (threadIdx.x == 128) mbar_arrive(B_(bars->qabs_ready));
+                    TR(if (threadIdx.x == 128) { TR_ADD(TR_S_PROLOGUE, clock64() - t_start); TR_ADD(TR_TILES, 1);
+                                                 TR_ADD(TR_BLOCKS, ti.nkv); })
+
+                    float m_run = -INFINITY, l_part = 0.f;
+                    for (int j = 0; j < ti.nblk; ++j, ++gb) {
+                        TR(long long _a = clock64();)
+                        fail = fail || !mbar_wait(B_(bars->s_full[0]), gb & 1, p.err, abort_flag);
+                        TR(w_sfull += clock64() - _a;
+                           if (tl_on && (threadIdx.x & 127) == 0) TL(2 + 3 * wg, j, clock64() - t_start);)
+                        float s[4][32];
+                        if (!fail) {
+                            tc_fence_after();
+    #pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) tmem_ld32(trow + S_SCOL + wg * 128 + c4 * 32, s[c4]);
+                            tmem_wait_ld();
+                            tc_fence_before();
+                            mbar_arrive(B_(bars->s_free[0]));
+                            if (j == ti.nblk - 1) {   // the last block: keys after the query or past the sequence
+                                const int lim = min(t, p.T - 1) - j * kBS - wg * 128;   // last visible column
+    #pragma unroll
+                                for (int c4 = 0; c4 < 4; ++c4)
+    #pragma unroll
+                                    for (int i = 0; i < 32; ++i)
+                                        if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
+                            }
+                            st_shared_f32(base + PMAX + ((gb & 1) * 2 + wg) * kBM * 4 + row * 4, tree_max128(s));
+                        }
+                        TR(long long _x = clock64();)
+                        if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
+                        TR(w_xbar += clock64() - _x; if (tl_on && threadIdx.x == 128) TL(3, j, clock64() - t_start);)
+                        const float mx = fmaxf(ld_shared_f32(base + PMAX + ((gb & 1) * 2 + 0) * kBM * 4 + row * 4),
+                                               ld_shared_f32(base + PMAX + ((gb & 1) * 2 + 1) * kBM * 4 + row * 4));
+                        float factor = 1.f;
+                        if (mx > m_run + kRescaleLog2) {
+                            factor = fast_exp2(m_run - mx);
+                            m_run = mx;
+                        }
+    #pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4)
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(s[c4][i] - m_run);
+                        l_part = l_part * factor + tree_sum128(s);
+
+                        TR(long long _s = clock64();)
+                        // the staging unit is free once this warpgroup's previous copy has read it
+                        if (issuer) bulk_wait_read_all();
+                        named_bar_sync(2 + wg, 128);
+    #pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4)
+    #pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                const float *v = &s[c4][8 * q4];
+                                st_shared_v4(ptile + (c4 >> 1) * kSlab + sw128_offset(row, (c4 & 1) * 4 + q4),
+                                             pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                                             pack_bf16x2(v[6], v[7]));
+                            }
+                        // unit 2j carries the block's rescale factor; unit 2j+1 shares its maximum (factor 1)
+                        st_shared_v2f(ri + row * 8, wg == 0 ? factor : 1.f, l_part);
+                        fence_proxy_async_smem();
+                        named_bar_sync(2 + wg, 128);
+                        TR(w_store += clock64() - _s;)
+                        if (issuer) {
+                            // the value CTA's P buffer `wg` is free once the product of this warpgroup's previous
+                            // unit completed (and, after a tile's last units, once the epilogue's staging is done)
+                            TR(long long _f = clock64();)
+                            if (nu >= 1) fail = !mbar_wait<true>(B_(bars->p_free[wg]), (nu - 1) & 1, p.err, abort_flag);
+                            TR(w_pfree += clock64() - _f;)
+                            if (!fail) {
+                                const uint32_t dst_bar = mapa_shared(B_(bars->p_full[wg]), 1);
+                                bulk_copy_s2cluster(mapa_shared(base + O_P + wg * kPBytes, 1), ptile, kPBytes, dst_bar);
+                                bulk_copy_s2cluster(mapa_shared(base + O_ROWINFO + wg * kRowInfoBytes, 1), ri,
+                                                    kRowInfoBytes, dst_bar);
+                                bulk_commit_group();
+                                TR(if (tl_on) TL(wg == 0 ? 4 : 6, j, clock64() - t_start);)
+                            }
+                        }
+                        ++nu;
+                    }
+                    if (!ok) break;
+                    // the first staging buffer takes the next tile's q tile once this tile's last copy has read it
+                    if (issuer) bulk_wait_read_all();
+                    if (issuer && wg == 0) mbar_arrive(B_(bars->q_free));
+                }
+                TR(if (threadIdx.x == 128) {
+                    TR_ADD(TR_S_SM_LOOP, clock64() - tl0); TR_ADD(TR_S_SM_SFULL, w_sfull); TR_ADD(TR_S_SM_XBAR, w_xbar);
+                    TR_ADD(TR_S_SM_PFREE, w_pfree); TR_ADD(TR_S_SM_STORE, w_store); TR_ADD(TR_S_SM_RELEASE, w_rel);
+                })
+                if (issuer) bulk_wait_all();
+                if (!ok || fail) *abort_flag = 1;
+        } else {
+            // =========================================================== value CTA: corrections, epilogue
+                // ---- correction + epilogue: thread `row` of warpgroup `wg` owns TMEM lane `row`,
+                // latent columns [256 wg, 256 wg + 256) for rescaling
+                const int wg = (warp - 4) >> 2;
+                const int row = (warp & 3) * 32 + lane;
+                const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+                int gu = 0;
+                bool ok = true, fail;
+                TR(long long tl0 = clock64();)
+                for (int k = 0; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    const int t = ti.t0 + row;
+                    float l_even = 0.f, l_odd = 0.f;
+                    for (int j = 0; j < ti.nkv; ++j, ++gu) {
+                        const int pb = gu & 1;
+                        fail = !mbar_wait<true>(B_(bars->p_full[pb]), (gu >> 1) & 1, p.err, abort_flag);
+                        if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                        const float2 fl = ld_shared_v2f(base + O_ROWINFO + pb * kRowInfoBytes + row * 8);
+                        mbar_arrive(B_(bars->ri_read[pb]));
+                        // the two warpgroups of the score CTA keep separate sums (even and odd units)
+                        if (j & 1)
+                            l_odd = fl.y;
+                        else
+                            l_even = fl.y;
+                        if (named_bar_or(4, 256, j > 0 && fl.x != 1.f)) {
+                            const int pu = gu - 1;
+                            fail = !mbar_wait(B_(bars->pv_done[pu & 1]), (pu >> 1) & 1, p.err, abort_flag);
+                            if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                            tc_fence_after();
+                            if (__any_sync(0xffffffffu, fl.x != 1.f)) {
+    #pragma unroll 1
+                                for (int cc = 0; cc < 8; ++cc) {
+                                    float v[32];
+                                    const uint32_t ta = trow + wg * 256 + cc * 32;
+                                    tmem_ld32(ta, v);
+                                    tmem_wait_ld();
+    #pragma unroll
+                                    for (int i = 0; i < 32; ++i) v[i] *= fl.x;
+                                    tmem_st32(ta, v);
+                                }
+                                tmem_wait_st();
+                            }
+                            tc_fence_before();
+                            mbar_arrive(B_(bars->corr_done));
+                        }
+                    }
+                    if (!ok) break;
+                    {
+                        const int pu = gu - 1;   // this tile's last unit
+                        fail = !mbar_wait(B_(bars->pv_done[pu & 1]), (pu >> 1) & 1, p.err, abort_flag);
+                        if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                    }
+                    TR(const long long t_ep = clock64();)
+                    const float inv_l = 1.f / (l_even + l_odd);
+                    for (int kh = 0; ok && kh < 2; ++kh) {
+                        if (kh == 1) {   // the staging tile is free once the first half's product completed
+                            fail = !mbar_wait(B_(bars->ep_done[0]), k & 1, p.err, abort_flag);
+                            if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                        }
+                        tc_fence_after();
+    #pragma unroll 1
+                        for (int i = 0; i < 4; ++i) {
+                            const int cc = wg * 4 + i;   // 32-column chunk within this 256-column half
+                            float v[32];
+                            tmem_ld32(trow + kh * 256 + cc * 32, v);
+                            tmem_wait_ld();
+                            store_row32_bf16(base + O_P, kSlab, row, cc, v, inv_l);
+                        }
+                        fence_proxy_async_smem();
+                        tc_fence_before();
+                        named_bar_sync(4, 256);
+                        if (threadIdx.x == 128) mbar_arrive(B_(bars->olat_ready[kh]));
+                    }
+                    if (!ok) break;
+                    fail = !mbar_wait(B_(bars->ep_done[1]), k & 1, p.err, abort_flag);
+                    if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                    tc_fence_after();
+                    float o[2][32];
+    #pragma unroll
+                    for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + wg * 64 + c2 * 32, o[c2]);
+                    tmem_wait_ld();
+                    tc_fence_before();
+                    mbar_arrive(B_(bars->ep_read));   // the next tile may overwrite these TMEM columns
+                    if (t < p.T) {
+                        const size_t off = ((static_cast<size_t>(ti.b) * p.T + t) * p.H + ti.h) * kD + wg * 64;
+                        const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
+                        uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
+    #pragma unroll
+                        for (int v8 = 0; v8 < 8; ++v8) {
+                            float y[8];
+    #pragma unroll
+                            for (int i = 0; i < 8; ++i) y[i] = o[(v8 * 8 + i) >> 5][(v8 * 8 + i) & 31];
+                            if (g4) {
+                                const uint4 gv = __ldg(g4 + v8);
+                                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    #pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float g_lo = __uint_as_float(gw[i] << 16);
+                                    const float g_hi = __uint_as_float(gw[i] & 0xFFFF0000u);
+                                    y[2 * i] *= __fdividef(1.f, 1.f + fast_exp2(-g_lo * kLog2e));
+                                    y[2 * i + 1] *= __fdividef(1.f, 1.f + fast_exp2(-g_hi * kLog2e));
+                                }
+                            }
+                            o4[v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                        }
+                    }
+                    TR(if (threadIdx.x == 128) TR_ADD(TR_O_EPILOGUE, clock64() - t_ep);)
+                }
+                TR(if (threadIdx.x == 128) TR_ADD(TR_O_COR_LOOP, clock64() - tl0);)
+                if (!ok) *abort_flag = 1;
         }
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    TR(if (threadIdx.x == 0) {
-        TR_ADD(rank == 0 ? TR_S_TOTAL : TR_O_TOTAL, clock64() - t_start);
-        if (rank == 0) { TR_ADD(TR_TILES, 1); TR_ADD(TR_BLOCKS, nkv); }
-    })
+    TR(if (threadIdx.x == 0) TR_ADD(rank == 0 ? TR_S_TOTAL : TR_O_TOTAL, clock64() - t_start);)
     if (warp == 1) tmem_dealloc(tmem, 512);
     cluster_sync_all();   // the partner no longer touches this CTA's shared memory
 }
@@ -732,13 +811,24 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     p.n_qtiles = (a.T + kBM - 1) / kBM;
     p.bh_count = a.B * a.H;
     p.qk_scale_log2 = a.scale * kLog2e;
+    const long long n_tiles = static_cast<long long>(p.n_qtiles) * p.bh_count;
+    if (n_tiles > 0x3FFFFFFFLL) return cudaErrorInvalidValue;
+    p.n_tiles = static_cast<int>(n_tiles);
+    // persistent grid: one cluster per SM pair, each walking its share of the tiles
+    p.G = static_cast<int>(n_tiles < a.num_sms / 2 ? n_tiles : (a.num_sms / 2 > 0 ? a.num_sms / 2 : 1));
     cudaError_t e = cudaFuncSetAttribute(prefill_r512_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    const long long n_ctas = 2LL * p.n_qtiles * p.bh_count;
-    if (n_ctas > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    if (n_tiles == 0) return cudaSuccess;
+    {   // the kernel's register split assumes this launch budget
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, prefill_r512_kernel);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
+    }
     note_launch();
-    prefill_r512_kernel<<<static_cast<unsigned>(n_ctas), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk, tm_wuv, p);
+    prefill_r512_kernel<<<static_cast<unsigned>(2 * p.G), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk,
+                                                                                    tm_wuv, p);
     return cudaGetLastError();
 }
 
