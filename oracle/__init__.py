@@ -10,6 +10,8 @@ library.
 * ``layer`` holds step 1 (the low-rank latent and query paths) and the output
   projection of step 4, in numpy fp64, used to build full-layer inputs;
   ``layer_forward`` composes them with ``prefill`` into the whole layer.
+* ``prefill_backward`` (module ``backward``) takes the chain rule back through
+  steps 2-4 in numpy fp64: the gradients of the prefill's inputs.
 
 Parity status of each function is stated in its docstring; the pins live in
 ``tests/test_oracle.py``.
@@ -143,6 +145,14 @@ def layer_forward(x, p, H: int, d_q: int, d_v: int, scale: float = 1.0, rows=Non
     o = prefill(q.reshape(B, T, H, d_q), c, w_uk, w_uv, g.reshape(B, T, H * d_v), scale, rows=sel)
     y = layer.output_projection(o, p["o_proj"])
     return y.reshape(B, T, D) if rows is None else y
+
+
+def prefill_backward(q, c, w_uk, w_uv, gate, scale: float, dout) -> dict:
+    """Gradients of sum(dout * prefill(...)) in fp64; see ``oracle.backward``.
+    Parity: pinned by finite differences of ``prefill`` (tests/test_oracle_backward.py).
+    """
+    from .backward import prefill_backward as _bwd
+    return _bwd(q, c, w_uk, w_uv, gate, scale, dout)
 
 
 def decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0) -> np.ndarray:
