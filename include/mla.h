@@ -91,6 +91,31 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
                                   int dtype, void *stream);
 
 /*
+ * mla_absorbed_attn_bwd - gradients of the attention (steps 2-4 of section
+ * "完整计算流（四步）" of the page "Gated MLA（矩阵吸收版）", which gives the forward
+ * only; this takes the chain rule back through it).  For
+ * L = sum(dout * out) with out = mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate,
+ * scale) it writes (all fp32, caller-owned device memory, overwritten):
+ *   dq     [B,T,H,d_q]   dL/dq
+ *   dc     [B,T,r]       dL/dc (summed over heads and over the queries that see each key)
+ *   dw_uk  [H,d_q,r]     dL/dW_UK (summed over batch and tokens)
+ *   dw_uv  [H,d_v,r]     dL/dW_UV
+ *   dgate  [B,T,H*d_v]   dL/dgate (the pre-sigmoid logits); NULL exactly when gate is NULL
+ * Inputs as for mla_absorbed_attn_fwd, plus dout [B,T,H*d_v].
+ * workspace: >= mla_absorbed_attn_bwd_workspace_size(...) bytes, 16-byte
+ * aligned (per-row q_abs, do_lat and softmax statistics between the kernels).
+ * Supported: MLA_DTYPE_F32 with r, d_q, d_v <= 64 (the toy sizes); anything
+ * else returns MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
+ * blocks formed with atomics, so their last bits may differ between calls.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype);
+MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate,
+                                  float scale, const void *dout, void *dq, void *dc, void *dw_uk, void *dw_uv,
+                                  void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * mla_latent_decode_workspace_size - bytes of device workspace mla_latent_decode
  * needs for these sizes on the CURRENT device (it depends on the SM count).
  * Returns 0 for sizes that are invalid or unsupported.

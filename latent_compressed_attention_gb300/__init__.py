@@ -22,7 +22,7 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
-           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout", "mla_gated_layer_fwd",
+           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout", "mla_absorbed_attn_bwd", "mla_gated_layer_fwd",
            "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16",
            "DTYPE_F32"]
 
@@ -69,6 +69,10 @@ def library():
             lib.mla_gated_layer_decode_workspace_size.restype = sz
             lib.mla_gated_layer_decode.argtypes = [vp] * 7 + [f, vp, vp, ll, vp] + [i] * 9 + [vp, sz, vp]
             lib.mla_gated_layer_decode.restype = i
+            lib.mla_absorbed_attn_bwd_workspace_size.argtypes = [i] * 7
+            lib.mla_absorbed_attn_bwd_workspace_size.restype = sz
+            lib.mla_absorbed_attn_bwd.argtypes = [vp] * 5 + [f] + [vp] * 6 + [i] * 7 + [vp, sz, vp]
+            lib.mla_absorbed_attn_bwd.restype = i
             lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
             lib.mla_debug_wait_timeout.restype = i
             lib.mla_get_device_error.argtypes = [vp]
@@ -160,6 +164,40 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
                                          B, T, H, d_q, d_v, r, _dtype_code(q), _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_absorbed_attn_fwd")
+    return out
+
+
+def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=None, stream=None) -> dict:
+    """Gradients of sum(dout * mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate, scale)): a dict with dq, dc, dw_uk,
+    dw_uv and dgate (None without a gate), allocated here.  fp32, r, d_q, d_v <= 64."""
+    torch = _torch()
+    B, T, H, d_q = q.shape
+    r = c.shape[-1]
+    d_v = w_uv.shape[1]
+    dev, dt = q.device, q.dtype
+    _check(q, "q", dt, dev)
+    _check(c, "c", dt, dev, (B, T, r))
+    _check(w_uk, "w_uk", dt, dev, (H, d_q, r))
+    _check(w_uv, "w_uv", dt, dev, (H, d_v, r))
+    _check(dout, "dout", dt, dev, (B, T, H * d_v))
+    if gate is not None:
+        _check(gate, "gate", dt, dev, (B, T, H * d_v))
+    lib = library()
+    code = _dtype_code(q)
+    out = dict(dq=torch.empty_like(q), dc=torch.empty_like(c), dw_uk=torch.empty_like(w_uk),
+               dw_uv=torch.empty_like(w_uv), dgate=None if gate is None else torch.empty_like(gate))
+    need = int(lib.mla_absorbed_attn_bwd_workspace_size(B, T, H, d_q, d_v, r, code))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    rc = lib.mla_absorbed_attn_bwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(), ptr(gate),
+                                   float(scale), dout.data_ptr(), out["dq"].data_ptr(), out["dc"].data_ptr(),
+                                   out["dw_uk"].data_ptr(), out["dw_uv"].data_ptr(), ptr(out["dgate"]),
+                                   B, T, H, d_q, d_v, r, code, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_absorbed_attn_bwd")
     return out
 
 

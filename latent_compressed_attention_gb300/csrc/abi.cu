@@ -144,6 +144,39 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype) {
+    if (dtype != MLA_DTYPE_F32 || B <= 0 || T <= 0 || H <= 0) return 0;
+    if (!backward_f32_supports(r, d_q, d_v)) return 0;
+    if (!mul_fits(static_cast<long long>(B) * T, static_cast<long long>(H) * (2 * r + 4), LLONG_MAX / 8)) return 0;
+    return backward_f32_workspace_bytes(B, T, H, r);
+}
+
+MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate,
+                                  float scale, const void *dout, void *dq, void *dc, void *dw_uk, void *dw_uv,
+                                  void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
+    if (B < 0 || T < 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0) return MLA_ERR_SHAPE;
+    const long long rows = static_cast<long long>(B) * T;
+    if (!mul_fits(rows, static_cast<long long>(H) * (2 * r + 4 > d_q + d_v ? 2 * r + 4 : d_q + d_v), LLONG_MAX / 8) ||
+        rows > INT_MAX)
+        return MLA_ERR_SHAPE;
+    if (!q || !c || !w_uk || !w_uv || !dout || !dq || !dc || !dw_uk || !dw_uv) return MLA_ERR_NULL;
+    if ((gate == nullptr) != (dgate == nullptr)) return MLA_ERR_NULL;   // a gate and its gradient go together
+    if (!aligned16(q) || !aligned16(c) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dc) || !aligned16(dw_uk) || !aligned16(dw_uv) || (gate && !aligned16(gate)) ||
+        (dgate && !aligned16(dgate)))
+        return MLA_ERR_ALIGN;
+    if (dtype != MLA_DTYPE_F32 || !backward_f32_supports(r, d_q, d_v)) return MLA_ERR_UNSUPPORTED;
+    if (rows == 0) return MLA_OK;
+    if (!workspace) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    if (workspace_bytes < backward_f32_workspace_bytes(B, T, H, r)) return MLA_ERR_WORKSPACE;
+    BackwardArgs a{q, c, w_uk, w_uv, gate, dout, dq, dc, dw_uk, dw_uv, dgate, scale, B, T, H, d_q, d_v, r, workspace};
+    const cudaError_t e = launch_backward_f32(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 MLA_API size_t mla_latent_decode_workspace_size(int B, int H, int r, int max_len) {
     if (B <= 0 || H <= 0 || r <= 0 || max_len < 0) return 0;
     if (!decode_bf16_supports(H, 128, r)) return 0;

@@ -31,6 +31,14 @@ struct DecodeArgs {
     int num_sms;
 };
 
+struct BackwardArgs {
+    const void *q, *c, *w_uk, *w_uv, *gate, *dout;
+    void *dq, *dc, *dw_uk, *dw_uv, *dgate;
+    float scale;
+    int B, T, H, d_q, d_v, r;
+    void *workspace;   // backward_f32_workspace_bytes(B, T, H, r)
+};
+
 // Each launcher validates nothing the ABI already checked; it returns a
 // cudaError_t from the launch (or cudaErrorInvalidValue for an internal
 // precondition) and never synchronises.
@@ -41,6 +49,11 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s);
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v);
 
 cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s);
+
+// fp32 gradients of the attention (steps 2-4); r, d_q, d_v <= 64.
+bool backward_f32_supports(int r, int d_q, int d_v);
+size_t backward_f32_workspace_bytes(long long B, long long T, long long H, int r);
+cudaError_t launch_backward_f32(const BackwardArgs &a, cudaStream_t s);
 bool prefill_bf16_small_supports(int r, int d_q, int d_v);
 
 size_t decode_bf16_workspace_bytes(int B, int H, int r, int max_len, int num_sms);

@@ -207,3 +207,50 @@ def test_layer_decode_checks_before_launch(lib):
 @pytest.mark.parametrize("limit_us", [0, 2000001])
 def test_wait_timeout_probe_rejects_limits_out_of_range(lib, limit_us):
     assert lib.mla_debug_wait_timeout(limit_us, None) == ERR_SHAPE
+
+
+# ----------------------------------------------------------------------------- backward
+def bwd_call(lib, **kw):
+    a = dict(q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=FAKE, dout=FAKE, dq=FAKE, dc=FAKE, dwuk=FAKE, dwuv=FAKE,
+             dgate=FAKE, B=2, T=128, H=8, dq_dim=16, dv=16, r=32, dtype=F32, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.mla_absorbed_attn_bwd(a["q"], a["c"], a["wuk"], a["wuv"], a["gate"], 1.0, a["dout"], a["dq"], a["dc"],
+                                     a["dwuk"], a["dwuv"], a["dgate"], a["B"], a["T"], a["H"], a["dq_dim"], a["dv"],
+                                     a["r"], a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("field", ["q", "c", "wuk", "wuv", "dout", "dq", "dc", "dwuk", "dwuv"])
+def test_backward_null_pointer(lib, field):
+    assert bwd_call(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(gate=None), dict(dgate=None)])
+def test_backward_gate_and_its_gradient_go_together(lib, kw):
+    assert bwd_call(lib, **kw) == ERR_NULL
+
+
+@pytest.mark.parametrize("field", ["q", "dout", "dc", "dgate", "ws"])
+def test_backward_misaligned(lib, field):
+    assert bwd_call(lib, **{field: FAKE + 4}) == ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=BF16), dict(r=65), dict(dq_dim=128), dict(dv=65)])
+def test_backward_unsupported(lib, kw):
+    assert bwd_call(lib, **kw) == ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(H=0), dict(r=0), dict(B=1 << 20, T=1 << 20)])
+def test_backward_bad_shape(lib, kw):
+    assert bwd_call(lib, **kw) == ERR_SHAPE
+
+
+def test_backward_workspace_checked_before_launch(lib):
+    assert bwd_call(lib, ws=None) == ERR_WORKSPACE
+    assert bwd_call(lib, ws_bytes=16) == ERR_WORKSPACE
+    assert bwd_call(lib, B=0) == OK   # nothing to do
+
+
+def test_backward_workspace_size(lib):
+    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, F32) == 2 * 128 * 8 * (2 * 32 + 4) * 4
+    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, BF16) == 0
+    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 65, F32) == 0
