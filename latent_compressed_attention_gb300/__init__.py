@@ -22,9 +22,9 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
-           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout", "mla_absorbed_attn_bwd", "mla_gated_layer_fwd",
-           "mla_gated_layer_workspace_size", "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16",
-           "DTYPE_F32"]
+           "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout",
+           "mla_absorbed_attn_bwd", "mla_gated_layer_fwd", "mla_gated_layer_workspace_size",
+           "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
 
 DTYPE_BF16 = 0
 DTYPE_F32 = 1
