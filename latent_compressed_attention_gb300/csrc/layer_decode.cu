@@ -27,7 +27,7 @@ namespace {
 
 constexpr float kRmsEps = 1e-6f;
 constexpr int kAbsThreads = 128;
-constexpr int kAbsTmemCols = 512;                 // fp32 accumulator columns: r <= 512
+constexpr int kAbsCols = 256;                     // latent columns (fp32 TMEM accumulator columns) per CTA
 constexpr uint32_t kAbsASlab = 128 * 128;         // [128 sequences x 64 d] bf16, 128-byte swizzle
 constexpr uint32_t kAbsWBox = 64 * 128;           // [64 d x 64 latent columns] bf16
 constexpr uint32_t kAbsIdesc = make_idesc_bf16(128, 256, 0, 1);   // q (K-major) x W_UK (MN-major)
@@ -73,18 +73,21 @@ __global__ void append_latent_kernel(const __nv_bfloat16 *c, __nv_bfloat16 *cach
 }
 
 // q_abs[b, h, :] = q[b, h, :] . W_UK[h] (d_q -> r) on the tensor cores, fp32
-// accumulation in TMEM, bf16 out.  A CTA takes one head and up to 128
-// sequences: A = the sequences' q rows of that head (K-major, rows past B read
-// as zeros), B = W_UK[h] [d_q, r] as stored (latent columns contiguous, so an
-// MN-major operand), D = [128, r] in r TMEM columns.  One thread issues every
-// copy and product; the four warps then drain their 32 TMEM lanes.
+// accumulation in TMEM, bf16 out.  A CTA takes one head, up to 128 sequences
+// and 256 of the latent columns (two CTAs per head at r = 512, so 192 CTAs
+// share the W_UK stream): A = the sequences' q rows of that head (K-major,
+// rows past B read as zeros), B = its 256 columns of W_UK[h] [d_q, r] as stored
+// (latent columns contiguous, so an MN-major operand), D = [128, 256] in 256
+// TMEM columns.  One thread issues every copy and product; the four warps then
+// drain their 32 TMEM lanes.
 __global__ void __launch_bounds__(kAbsThreads, 1)
     absorb_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_w,
                         __nv_bfloat16 *q_abs, int B, int H, int d_q, int r, int *err) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const int n_kh = d_q / 64, n_ns = r / 64;
+    const int n_kh = d_q / 64, n_ns = kAbsCols / 64;
+    const int nh = blockIdx.z;   // this CTA's 256 latent columns
     const uint32_t w_off = n_kh * kAbsASlab, bar_off = w_off + n_kh * n_ns * kAbsWBox;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem_raw + (base - raw) + bar_off);
     uint64_t *done = full + 1;
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(smem_u32(tmem_slot), kAbsTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), kAbsCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -112,19 +115,18 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
         for (int kh = 0; kh < n_kh; ++kh) {
             tma_load_3d(base + kh * kAbsASlab, &tm_q, bar, kh * 64, h, b0);
             for (int ns = 0; ns < n_ns; ++ns)
-                tma_load_3d(base + w_off + (kh * n_ns + ns) * kAbsWBox, &tm_w, bar, ns * 64, kh * 64, h);
+                tma_load_3d(base + w_off + (kh * n_ns + ns) * kAbsWBox, &tm_w, bar, (nh * n_ns + ns) * 64, kh * 64,
+                            h);
         }
         if (mbar_wait(bar, 0, err)) {
             tc_fence_after();
-            for (int nh = 0; nh < r / 256; ++nh)
-                for (int kh = 0; kh < n_kh; ++kh)
+            for (int kh = 0; kh < n_kh; ++kh)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {   // K steps of 16 within a 64-wide slab
-                        const uint64_t ad = make_smem_desc(base + kh * kAbsASlab + j * 32, 16, 1024);
-                        const uint64_t bd =
-                            make_smem_desc(base + w_off + (kh * n_ns + nh * 4) * kAbsWBox + j * 2048, kAbsWBox, 1024);
-                        umma_bf16(tmem + nh * 256, ad, bd, kAbsIdesc, (kh | j) != 0);
-                    }
+                for (int j = 0; j < 4; ++j) {   // K steps of 16 within a 64-wide slab
+                    const uint64_t ad = make_smem_desc(base + kh * kAbsASlab + j * 32, 16, 1024);
+                    const uint64_t bd = make_smem_desc(base + w_off + kh * n_ns * kAbsWBox + j * 2048, kAbsWBox, 1024);
+                    umma_bf16(tmem, ad, bd, kAbsIdesc, (kh | j) != 0);
+                }
             umma_commit(smem_u32(done));
         } else {
             *abort_flag = 1;
@@ -135,9 +137,9 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     if (ok) {   // warp-uniform: the TMEM loads below are warp-collective
         tc_fence_after();
         const int b = b0 + warp * 32 + lane;
-        uint4 *dst = reinterpret_cast<uint4 *>(q_abs + (static_cast<size_t>(b < B ? b : 0) * H + h) * r);
+        uint4 *dst = reinterpret_cast<uint4 *>(q_abs + (static_cast<size_t>(b < B ? b : 0) * H + h) * r + nh * kAbsCols);
 #pragma unroll 1
-        for (int cc = 0; cc < r / 32; ++cc) {
+        for (int cc = 0; cc < kAbsCols / 32; ++cc) {
             float v[32];
             tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cc * 32, v);
             tmem_wait_ld();
@@ -152,11 +154,12 @@ __global__ void __launch_bounds__(kAbsThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kAbsTmemCols);
+    if (warp == 0) tmem_dealloc(tmem, kAbsCols);
 }
 
 size_t absorb_smem_bytes(int d_q, int r) {
-    return static_cast<size_t>(d_q / 64) * (kAbsASlab + static_cast<size_t>(r / 64) * kAbsWBox) + 64 + 1024;
+    (void)r;   // each CTA takes 256 latent columns
+    return static_cast<size_t>(d_q / 64) * (kAbsASlab + static_cast<size_t>(kAbsCols / 64) * kAbsWBox) + 64 + 1024;
 }
 
 CUresult encode_bf16_3d(CUtensorMap *m, const void *ptr, const cuuint64_t *dims, const cuuint64_t *strides,
@@ -173,7 +176,7 @@ CUresult encode_bf16_3d(CUtensorMap *m, const void *ptr, const cuuint64_t *dims,
 
 bool gated_layer_decode_supports(int D, int H, int d_q, int d_v, int r, int r_q) {
     return gated_layer_supports(D, H, d_q, d_v, r, r_q, false) && decode_bf16_supports(H, d_v, r) &&
-           d_q % 64 == 0 && r % 256 == 0 && r <= kAbsTmemCols && absorb_smem_bytes(d_q, r) <= 227u * 1024;
+           d_q % 64 == 0 && r % kAbsCols == 0 && absorb_smem_bytes(d_q, r) <= 227u * 1024;
 }
 
 size_t gated_layer_decode_workspace_bytes(int B, int D, int H, int d_q, int d_v, int r, int r_q, int max_len,
@@ -256,8 +259,8 @@ cudaError_t launch_gated_layer_decode(const LayerDecodeArgs &a, cudaStream_t s) 
                                   static_cast<int>(asmem))) != cudaSuccess)
         return e;
     note_launch();
-    absorb_query_kernel<<<dim3(a.H, (a.B + 127) / 128), kAbsThreads, asmem, s>>>(tm_q, tm_w, qa, a.B, a.H, a.d_q,
-                                                                                 a.r, a.dev_err);
+    absorb_query_kernel<<<dim3(a.H, (a.B + 127) / 128, a.r / kAbsCols), kAbsThreads, asmem, s>>>(
+        tm_q, tm_w, qa, a.B, a.H, a.d_q, a.r, a.dev_err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     DecodeArgs da{qa, a.c_cache, w_uv, g, lens1, o, a.ld_cache, a.max_len, a.scale, a.B, a.H, a.d_v, a.r,
                   ws + L.dec, dec_bytes, a.dev_err, a.num_sms};
