@@ -247,23 +247,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (rank == 0) {
             // =========================================================== score CTA: control
             if (warp == 0 && lane == 0) {
-                // ---- TMA producer.  Per tile: the q tile into the first P staging buffer, W_UK[h] into four ring
-                // positions, then c tiles [256 keys x 64] for every score block.  A tile takes 4 + 8 nblk ring
-                // positions, a multiple of the 4 stages, so W_UK always fills slots 0-3 in order.
-                tma_prefetch_desc(&tm_q);
+                // ---- ring producer.  Per tile: W_UK[h] into four ring positions, then c tiles [256 keys x 64] for
+                // every score block, streaming on into the next tile as slots free up.  A tile takes 4 + 8 nblk
+                // ring positions, a multiple of the 4 stages, so W_UK always fills slots 0-3 in order.
                 tma_prefetch_desc(&tm_c256);
                 tma_prefetch_desc(&tm_wuk);
-                const uint32_t pro = B_(bars->pro_full);
                 int it = 0, k = 0;
                 bool ok = true;
                 for (; ok; ++k) {
                     const int tile = tile_of(k);
                     if (tile >= p.n_tiles) break;
                     const TileInfo ti = tile_info(tile, p);
-                    // the staging buffer takes the next q once the previous tile's last P copy has read it
-                    if (k >= 1 && !(ok = mbar_wait(B_(bars->q_free), (k - 1) & 1, p.err, abort_flag))) break;
-                    mbar_arrive_expect_tx(pro, 2 * kSlab);
-                    for (int s = 0; s < 2; ++s) tma_load_4d(base + S_PST + s * kSlab, &tm_q, pro, s * 64, ti.h, ti.t0, ti.b);
                     const int n_pos = 4 + 8 * ti.nblk;
                     for (int i = 0; i < n_pos; ++i, ++it) {
                         const int st = it % kSStages;
@@ -286,9 +280,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) *abort_flag = 1;
                 // no load may still be landing when the CTA exits
-                if (k > 0) mbar_wait(pro, (k - 1) & 1, p.err);
                 for (int q = (it > kSStages ? it - kSStages : 0); q < it; ++q)
                     mbar_wait(B_(bars->sc_full[q % kSStages]), (q / kSStages) & 1, p.err);
+            } else if (warp == 2 && lane == 0) {
+                // ---- q producer: each tile's q tile into the first P staging buffer, once the previous tile's last
+                // P copy has read it (apart from the ring, so the ring streams across tile boundaries)
+                tma_prefetch_desc(&tm_q);
+                const uint32_t pro = B_(bars->pro_full);
+                int k = 0;
+                bool ok = true;
+                for (; ok; ++k) {
+                    const int tile = tile_of(k);
+                    if (tile >= p.n_tiles) break;
+                    const TileInfo ti = tile_info(tile, p);
+                    if (k >= 1 && !(ok = mbar_wait(B_(bars->q_free), (k - 1) & 1, p.err, abort_flag))) break;
+                    mbar_arrive_expect_tx(pro, 2 * kSlab);
+                    for (int s = 0; s < 2; ++s) tma_load_4d(base + S_PST + s * kSlab, &tm_q, pro, s * 64, ti.h, ti.t0, ti.b);
+                }
+                if (!ok) *abort_flag = 1;
+                if (k > 0) mbar_wait(pro, (k - 1) & 1, p.err);   // no load may still be landing when the CTA exits
             } else if (warp == 1 && lane == 0) {
                 // ---- MMA issuer: per tile the absorb, then S = q_abs . c^T per 256-key block (q_abs from TMEM)
                 int it = 0, gb = 0;   // ring positions consumed, score blocks issued (all tiles)
