@@ -9,7 +9,8 @@ under "decode", and the whole layer at the prefill's size (step-1 projections
 with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".  The two
 small configurations run under "small_prefill" (r=32 at T=2048, bf16, bound by
 the exponential unit), "toy_layer" (the fp32 toy layer, bound by launch
-latency) and "toy_backward" (the gradients of the toy layer's attention, fp32).
+latency), "toy_backward" (the gradients of the toy layer's attention, fp32) and
+"small_backward" (the same at the toy long-context sizes with bf16 inputs).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -251,6 +252,7 @@ def run_ours(args):
     small = run_small_prefill(torch, lca, dev, stream, flush, args) if not args.no_small else None
     toy = run_toy_layer(torch, lca, dev, stream, flush, args) if not args.no_small else None
     toy_bwd = run_toy_backward(torch, lca, dev, stream, flush, args) if not args.no_small else None
+    small_bwd = run_toy_backward(torch, lca, dev, stream, flush, args, W.TOY_LONG_BF16) if not args.no_small else None
     if lca.mla_get_device_error() != 0:
         raise RuntimeError("device error word set after the timed region")
 
@@ -289,6 +291,8 @@ def run_ours(args):
             line["toy_layer"] = toy
         if toy_bwd is not None:
             line["toy_backward"] = toy_bwd
+        if small_bwd is not None:
+            line["small_backward"] = small_bwd
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -529,16 +533,19 @@ def backward_flops(w) -> float:
     return w.B * w.H * (12.0 * w.r * pairs + 6.0 * w.T * w.r * (w.d_q + w.d_v))
 
 
-def run_toy_backward(torch, lca, dev, stream, flush, args):
-    """Gradients of the attention at the toy layer's sizes (fp32, B=2, T=128, H=8, d=16, r=32) for a random
-    dout; q, c, W_UK, W_UV and the gate logits are the seeded direct draws of the toy workload."""
-    w = W.TOY_LAYER_F32
+def run_toy_backward(torch, lca, dev, stream, flush, args, w=None):
+    """Gradients of the attention for a random dout: at the toy layer's sizes (fp32, B=2, T=128, H=8, d=16,
+    r=32) or, given the toy long-context workload, at its sizes with bf16 inputs (B=4, T=2048); q, c, W_UK,
+    W_UV and the gate logits are the workload's seeded direct draws.  Gradients are fp32 either way."""
+    w = W.TOY_LAYER_F32 if w is None else w
     d = W.draw_prefill_direct(w, seed=0)
-    dout = np.random.default_rng(1).standard_normal((w.B, w.T, w.H * w.d_v))
-    t = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(dev)  # noqa: E731
+    dout = W.round_to(np.random.default_rng(1).standard_normal((w.B, w.T, w.H * w.d_v)), w.dtype)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(dt).to(dev)  # noqa: E731
     q, c, g, w_uk, w_uv, dout = (t(a) for a in (d["q"], d["c"], d["gate"], d["w_uk"], d["w_uv"], dout))
-    ws = torch.empty(lca.library().mla_absorbed_attn_bwd_workspace_size(w.B, w.T, w.H, w.d_q, w.d_v, w.r,
-                                                                         lca.DTYPE_F32), dtype=torch.uint8, device=dev)
+    code = lca.DTYPE_BF16 if w.dtype == "bf16" else lca.DTYPE_F32
+    ws = torch.empty(lca.library().mla_absorbed_attn_bwd_workspace_size(w.B, w.T, w.H, w.d_q, w.d_v, w.r, code),
+                     dtype=torch.uint8, device=dev)
     step = lambda: lca.mla_absorbed_attn_bwd(q, c, w_uk, w_uv, g, w.scale, dout, workspace=ws)  # noqa: E731
     for _ in range(args.warmup):
         step()
@@ -549,16 +556,19 @@ def run_toy_backward(torch, lca, dev, stream, flush, args):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     peak = 2 * FP32_LANES_SM * sms * SM_MAX_MHZ * 1e6 / 1e12
     tf = fl / (ms * 1e-3) / 1e12
-    return {"workload": "toy_backward_f32", "value": round(ms * 1e3, 2), "unit": "us/call", "higher_is_better": False,
+    return {"workload": w.name.replace("toy_layer_f32", "toy_backward_f32").replace("toy_long_bf16",
+                                                                                      "toy_long_backward_bf16"),
+            "value": round(ms * 1e3, 2), "unit": "us/call", "higher_is_better": False,
             "ms_per_step": round(ms, 5), "flops_per_step": fl, "kernels_per_call": launches // max(args.steps, 1),
             "config": {"B": w.B, "T": w.T, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r,
-                       "inputs": "direct draws of the toy workload, dout ~ N(0,1)", "dtype": "f32",
+                       "inputs": "direct draws of the workload, dout ~ N(0,1)",
+                       "dtype": f"{w.dtype} inputs, f32 arithmetic and gradients",
                        "l2": "flushed between steps"},
             "roofline": {"kernel": "bwd_query_kernel + bwd_key_kernel (fp32 SIMT)", "bound": "alu",
                          "achieved": round(tf, 4), "peak": round(peak, 1), "unit": "TFLOP/s",
                          "frac": round(tf / peak, 5),
                          "peak_source": f"derived: fp32 FMA {FP32_LANES_SM} lanes/SM x 2 x {sms} SMs x "
-                                        f"{SM_MAX_MHZ:.0f} MHz; the call is latency bound at this size",
+                                        f"{SM_MAX_MHZ:.0f} MHz" + ("; the call is latency bound at this size" if w.T <= 256 else ""),
                          "traffic": None},
             "gpu_launches": launches}
 

@@ -95,17 +95,19 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
  * "完整计算流（四步）" of the page "Gated MLA（矩阵吸收版）", which gives the forward
  * only; this takes the chain rule back through it).  For
  * L = sum(dout * out) with out = mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate,
- * scale) it writes (all fp32, caller-owned device memory, overwritten):
+ * scale) it writes (fp32 whatever the input dtype, caller-owned device memory,
+ * overwritten):
  *   dq     [B,T,H,d_q]   dL/dq
  *   dc     [B,T,r]       dL/dc (summed over heads and over the queries that see each key)
  *   dw_uk  [H,d_q,r]     dL/dW_UK (summed over batch and tokens)
  *   dw_uv  [H,d_v,r]     dL/dW_UV
  *   dgate  [B,T,H*d_v]   dL/dgate (the pre-sigmoid logits); NULL exactly when gate is NULL
- * Inputs as for mla_absorbed_attn_fwd, plus dout [B,T,H*d_v].
+ * Inputs as for mla_absorbed_attn_fwd, plus dout [B,T,H*d_v], all of dtype
+ * `dtype` (MLA_DTYPE_F32 or MLA_DTYPE_BF16; bf16 values are widened to fp32).
  * workspace: >= mla_absorbed_attn_bwd_workspace_size(...) bytes, 16-byte
  * aligned (per-row q_abs, do_lat and softmax statistics between the kernels).
- * Supported: MLA_DTYPE_F32 with r, d_q, d_v <= 64 (the toy sizes); anything
- * else returns MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
+ * Supported: r, d_q, d_v <= 64 (the toy sizes), fp32 arithmetic throughout;
+ * larger widths return MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
  * blocks formed with atomics, so their last bits may differ between calls.
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
  */

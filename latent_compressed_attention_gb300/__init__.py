@@ -169,7 +169,7 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
 
 def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=None, stream=None) -> dict:
     """Gradients of sum(dout * mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate, scale)): a dict with dq, dc, dw_uk,
-    dw_uv and dgate (None without a gate), allocated here.  fp32, r, d_q, d_v <= 64."""
+    dw_uv and dgate (None without a gate), allocated here as fp32.  Inputs fp32 or bf16; r, d_q, d_v <= 64."""
     torch = _torch()
     B, T, H, d_q = q.shape
     r = c.shape[-1]
@@ -184,8 +184,8 @@ def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=
         _check(gate, "gate", dt, dev, (B, T, H * d_v))
     lib = library()
     code = _dtype_code(q)
-    out = dict(dq=torch.empty_like(q), dc=torch.empty_like(c), dw_uk=torch.empty_like(w_uk),
-               dw_uv=torch.empty_like(w_uv), dgate=None if gate is None else torch.empty_like(gate))
+    f32 = lambda t: torch.empty(t.shape, dtype=torch.float32, device=dev)  # noqa: E731
+    out = dict(dq=f32(q), dc=f32(c), dw_uk=f32(w_uk), dw_uv=f32(w_uv), dgate=None if gate is None else f32(gate))
     need = int(lib.mla_absorbed_attn_bwd_workspace_size(B, T, H, d_q, d_v, r, code))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)

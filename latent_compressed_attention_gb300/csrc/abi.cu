@@ -145,7 +145,7 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
 }
 
 MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype) {
-    if (dtype != MLA_DTYPE_F32 || B <= 0 || T <= 0 || H <= 0) return 0;
+    if ((dtype != MLA_DTYPE_F32 && dtype != MLA_DTYPE_BF16) || B <= 0 || T <= 0 || H <= 0) return 0;
     if (!backward_f32_supports(r, d_q, d_v)) return 0;
     if (!mul_fits(static_cast<long long>(B) * T, static_cast<long long>(H) * (2 * r + 4), LLONG_MAX / 8)) return 0;
     return backward_f32_workspace_bytes(B, T, H, r);
@@ -167,12 +167,13 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
         !aligned16(dq) || !aligned16(dc) || !aligned16(dw_uk) || !aligned16(dw_uv) || (gate && !aligned16(gate)) ||
         (dgate && !aligned16(dgate)))
         return MLA_ERR_ALIGN;
-    if (dtype != MLA_DTYPE_F32 || !backward_f32_supports(r, d_q, d_v)) return MLA_ERR_UNSUPPORTED;
+    if (!backward_f32_supports(r, d_q, d_v)) return MLA_ERR_UNSUPPORTED;
     if (rows == 0) return MLA_OK;
     if (!workspace) return MLA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
     if (workspace_bytes < backward_f32_workspace_bytes(B, T, H, r)) return MLA_ERR_WORKSPACE;
-    BackwardArgs a{q, c, w_uk, w_uv, gate, dout, dq, dc, dw_uk, dw_uv, dgate, scale, B, T, H, d_q, d_v, r, workspace};
+    BackwardArgs a{q, c, w_uk, w_uv, gate, dout, dq, dc, dw_uk, dw_uv, dgate, scale, B, T, H, d_q, d_v, r, workspace,
+                   dtype == MLA_DTYPE_BF16};
     const cudaError_t e = launch_backward_f32(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

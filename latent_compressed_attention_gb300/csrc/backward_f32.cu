@@ -1,5 +1,6 @@
 // fp32 gradients of the causal absorbed Gated-MLA attention (steps 2-4) on the
-// CUDA cores (true fp32 FMA, no TF32), for the toy sizes (r, d_q, d_v <= 64).
+// CUDA cores (true fp32 FMA, no TF32), for the toy sizes (r, d_q, d_v <= 64);
+// inputs fp32 or bf16 (read and widened to fp32), gradients fp32.
 //
 // The page "Gated MLA（矩阵吸收版）" gives the forward (section "完整计算流（四步）":
 // q_abs = q W_UK, s = scale q_abs c^T masked to u <= t, a = softmax(s),
@@ -32,13 +33,17 @@ constexpr int kPerWarp = kRows / kWarps;   // 2
 constexpr int kChunk = 32;     // staged keys (query kernel) or queries (key kernel)
 constexpr int kPad = kMaxDim + 1;
 
+template <typename In>
 struct BwdParams {
-    const float *q, *c, *w_uk, *w_uv, *gate, *dout;
+    const In *q, *c, *w_uk, *w_uv, *gate, *dout;
     float *dq, *dc, *dw_uk, *dw_uv, *dgate;
     float *ws_qa, *ws_dol, *ws_st;   // [B,T,H,r], [B,T,H,r], [B,T,H,4] = (m, l, delta, 0)
     float scale;
     int B, T, H, d_q, d_v, r;
 };
+
+__device__ __forceinline__ float ld(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float ld(const __nv_bfloat16 *p) { return __bfloat162float(__ldg(p)); }
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -62,7 +67,8 @@ constexpr int kQDwuv = kQDwuk + kMaxDim * kMaxDim;            // [kMaxDim][kMaxD
 constexpr int kQFloats = kQDwuv + kMaxDim * kMaxDim;
 constexpr size_t kQSmem = kQFloats * sizeof(float);
 
-__global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams p) {
+template <typename In>
+__global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams<In> p) {
     extern __shared__ float sm[];
     float *s_c = sm + kQC, *s_qa = sm + kQQa, *s_dol = sm + kQDol, *s_vec = sm + kQVec, *s_p = sm + kQP;
     float *s_dwuk = sm + kQDwuk, *s_dwuv = sm + kQDwuv;
@@ -72,8 +78,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
     const int h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = tile * kRows;
-    const float *wuk = p.w_uk + static_cast<size_t>(h) * dq_dim * r;
-    const float *wuv = p.w_uv + static_cast<size_t>(h) * dv * r;
+    const In *wuk = p.w_uk + static_cast<size_t>(h) * dq_dim * r;
+    const In *wuv = p.w_uv + static_cast<size_t>(h) * dv * r;
     float *vec = s_vec + warp * kMaxDim;
     float *pw = s_p + warp * kChunk;
 
@@ -89,11 +95,11 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
         ol[i][0] = ol[i][1] = delta[i] = dqa[i][0] = dqa[i][1] = 0.f;
         float a0 = 0.f, a1 = 0.f;
         if (t < T) {
-            const float *qrow = p.q + ((static_cast<size_t>(b) * T + t) * H + h) * dq_dim;
+            const In *qrow = p.q + ((static_cast<size_t>(b) * T + t) * H + h) * dq_dim;
             for (int d = 0; d < dq_dim; ++d) {
-                const float qd = __ldg(qrow + d);
-                if (lane < r) a0 = fmaf(qd, __ldg(wuk + d * r + lane), a0);
-                if (lane + 32 < r) a1 = fmaf(qd, __ldg(wuk + d * r + lane + 32), a1);
+                const float qd = ld(qrow + d);
+                if (lane < r) a0 = fmaf(qd, ld(wuk + d * r + lane), a0);
+                if (lane + 32 < r) a1 = fmaf(qd, ld(wuk + d * r + lane + 32), a1);
             }
         }
         s_qa[(warp * kPerWarp + i) * kMaxDim + lane] = a0;
@@ -102,12 +108,12 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
     __syncwarp();
 
     const int last_key = min(T, t0 + kRows);   // keys this CTA needs: [0, last_key)
-    const float *cb = p.c + static_cast<size_t>(b) * T * r;
+    const In *cb = p.c + static_cast<size_t>(b) * T * r;
     auto stage = [&](int k0) {
         __syncthreads();
         for (int i = threadIdx.x; i < kChunk * r; i += kWarps * 32) {
             const int u = i / r, j = i - u * r;
-            s_c[u * kPad + j] = k0 + u < T ? __ldg(cb + static_cast<size_t>(k0 + u) * r + j) : 0.f;
+            s_c[u * kPad + j] = k0 + u < T ? ld(cb + static_cast<size_t>(k0 + u) * r + j) : 0.f;
         }
         __syncthreads();
     };
@@ -169,10 +175,10 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
             dov[half] = 0.f;
             if (v >= dv) continue;
             float o = 0.f;
-            for (int j = 0; j < r; ++j) o = fmaf(vec[j], __ldg(wuv + v * r + j), o);
-            const float dout = __ldg(p.dout + row * dv + v);
+            for (int j = 0; j < r; ++j) o = fmaf(vec[j], ld(wuv + v * r + j), o);
+            const float dout = ld(p.dout + row * dv + v);
             if (p.gate) {
-                const float sg = 1.f / (1.f + expf(-__ldg(p.gate + row * dv + v)));
+                const float sg = 1.f / (1.f + expf(-ld(p.gate + row * dv + v)));
                 p.dgate[row * dv + v] = dout * o * sg * (1.f - sg);
                 dov[half] = dout * sg;
             } else {
@@ -188,11 +194,11 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
         for (int v = 0; v < dv; ++v) {
             const float dv_ = vec[v];
             if (lane < r) {
-                dl0 = fmaf(dv_, __ldg(wuv + v * r + lane), dl0);
+                dl0 = fmaf(dv_, ld(wuv + v * r + lane), dl0);
                 atomicAdd(s_dwuv + v * kMaxDim + lane, dv_ * ol[i][0]);
             }
             if (lane + 32 < r) {
-                dl1 = fmaf(dv_, __ldg(wuv + v * r + lane + 32), dl1);
+                dl1 = fmaf(dv_, ld(wuv + v * r + lane + 32), dl1);
                 atomicAdd(s_dwuv + v * kMaxDim + lane + 32, dv_ * ol[i][1]);
             }
         }
@@ -255,17 +261,17 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_query_kernel(const BwdParams 
         vec[lane] = dqa[i][0];
         vec[lane + 32] = dqa[i][1];
         __syncwarp();
-        const float *qrow = p.q + row * dq_dim;
+        const In *qrow = p.q + row * dq_dim;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int d = lane + 32 * half;
             if (d >= dq_dim) continue;
             float acc = 0.f;
-            for (int j = 0; j < r; ++j) acc = fmaf(vec[j], __ldg(wuk + d * r + j), acc);
+            for (int j = 0; j < r; ++j) acc = fmaf(vec[j], ld(wuk + d * r + j), acc);
             p.dq[row * dq_dim + d] = acc;
         }
         for (int d = 0; d < dq_dim; ++d) {
-            const float qd = __ldg(qrow + d);
+            const float qd = ld(qrow + d);
             if (lane < r) atomicAdd(s_dwuk + d * kMaxDim + lane, qd * dqa[i][0]);
             if (lane + 32 < r) atomicAdd(s_dwuk + d * kMaxDim + lane + 32, qd * dqa[i][1]);
         }
@@ -294,7 +300,8 @@ constexpr int kKDs = kKA + kWarps * kChunk;              // [kWarps][kChunk] sca
 constexpr int kKFloats = kKDs + kWarps * kChunk;
 constexpr size_t kKSmem = kKFloats * sizeof(float);
 
-__global__ void __launch_bounds__(kWarps * 32) bwd_key_kernel(const BwdParams p) {
+template <typename In>
+__global__ void __launch_bounds__(kWarps * 32) bwd_key_kernel(const BwdParams<In> p) {
     extern __shared__ float sm[];
     float *s_ck = sm + kKC, *s_qa = sm + kKQa, *s_dol = sm + kKDol, *s_st = sm + kKSt;
     const int T = p.T, H = p.H, r = p.r;
@@ -302,10 +309,10 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_key_kernel(const BwdParams p)
     const int h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *pa = sm + kKA + warp * kChunk, *pds = sm + kKDs + warp * kChunk;
-    const float *cb = p.c + static_cast<size_t>(b) * T * r;
+    const In *cb = p.c + static_cast<size_t>(b) * T * r;
     for (int i = threadIdx.x; i < kRows * r; i += kWarps * 32) {
         const int u = i / r, j = i - u * r;
-        s_ck[u * kPad + j] = k0 + u < T ? __ldg(cb + static_cast<size_t>(k0 + u) * r + j) : 0.f;
+        s_ck[u * kPad + j] = k0 + u < T ? ld(cb + static_cast<size_t>(k0 + u) * r + j) : 0.f;
     }
     float acc[kPerWarp][2] = {};
     for (int tq0 = (k0 / kChunk) * kChunk; tq0 < T; tq0 += kChunk) {   // queries t >= k0, 32 at a time
@@ -373,15 +380,15 @@ size_t backward_f32_workspace_bytes(long long B, long long T, long long H, int r
     return static_cast<size_t>(B * T * H) * (2 * static_cast<size_t>(r) + 4) * sizeof(float);
 }
 
-cudaError_t launch_backward_f32(const BackwardArgs &a, cudaStream_t s) {
-    if (!backward_f32_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
-    BwdParams p;
-    p.q = static_cast<const float *>(a.q);
-    p.c = static_cast<const float *>(a.c);
-    p.w_uk = static_cast<const float *>(a.w_uk);
-    p.w_uv = static_cast<const float *>(a.w_uv);
-    p.gate = static_cast<const float *>(a.gate);
-    p.dout = static_cast<const float *>(a.dout);
+template <typename In>
+static cudaError_t launch_typed(const BackwardArgs &a, cudaStream_t s) {
+    BwdParams<In> p;
+    p.q = static_cast<const In *>(a.q);
+    p.c = static_cast<const In *>(a.c);
+    p.w_uk = static_cast<const In *>(a.w_uk);
+    p.w_uv = static_cast<const In *>(a.w_uv);
+    p.gate = static_cast<const In *>(a.gate);
+    p.dout = static_cast<const In *>(a.dout);
     p.dq = static_cast<float *>(a.dq);
     p.dc = static_cast<float *>(a.dc);
     p.dw_uk = static_cast<float *>(a.dw_uk);
@@ -405,16 +412,21 @@ cudaError_t launch_backward_f32(const BackwardArgs &a, cudaStream_t s) {
         return e;
     if ((e = cudaMemsetAsync(a.dw_uv, 0, static_cast<size_t>(a.H) * a.d_v * a.r * sizeof(float), s)) != cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(bwd_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(bwd_query_kernel<In>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kQSmem))) != cudaSuccess)
         return e;
     const unsigned tiles = static_cast<unsigned>((a.T + kRows - 1) / kRows);
     note_launch();
-    bwd_query_kernel<<<dim3(tiles, a.H, a.B), kWarps * 32, kQSmem, s>>>(p);
+    bwd_query_kernel<In><<<dim3(tiles, a.H, a.B), kWarps * 32, kQSmem, s>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch();
-    bwd_key_kernel<<<dim3(tiles, a.H, a.B), kWarps * 32, kKSmem, s>>>(p);
+    bwd_key_kernel<In><<<dim3(tiles, a.H, a.B), kWarps * 32, kKSmem, s>>>(p);
     return cudaGetLastError();
+}
+
+cudaError_t launch_backward_f32(const BackwardArgs &a, cudaStream_t s) {
+    if (!backward_f32_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
+    return a.bf16 ? launch_typed<__nv_bfloat16>(a, s) : launch_typed<float>(a, s);
 }
 
 }  // namespace mla

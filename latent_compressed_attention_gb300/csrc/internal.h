@@ -37,6 +37,7 @@ struct BackwardArgs {
     float scale;
     int B, T, H, d_q, d_v, r;
     void *workspace;   // backward_f32_workspace_bytes(B, T, H, r)
+    bool bf16;         // inputs bf16 (else fp32); the gradients are fp32 either way
 };
 
 // Each launcher validates nothing the ABI already checked; it returns a

@@ -234,7 +234,7 @@ def test_backward_misaligned(lib, field):
     assert bwd_call(lib, **{field: FAKE + 4}) == ERR_ALIGN
 
 
-@pytest.mark.parametrize("kw", [dict(dtype=BF16), dict(r=65), dict(dq_dim=128), dict(dv=65)])
+@pytest.mark.parametrize("kw", [dict(r=65), dict(dq_dim=128), dict(dv=65), dict(r=512, dq_dim=128, dv=128)])
 def test_backward_unsupported(lib, kw):
     assert bwd_call(lib, **kw) == ERR_UNSUPPORTED
 
@@ -242,6 +242,10 @@ def test_backward_unsupported(lib, kw):
 @pytest.mark.parametrize("kw", [dict(B=-1), dict(H=0), dict(r=0), dict(B=1 << 20, T=1 << 20)])
 def test_backward_bad_shape(lib, kw):
     assert bwd_call(lib, **kw) == ERR_SHAPE
+
+
+def test_backward_bad_dtype(lib):
+    assert bwd_call(lib, dtype=7) == ERR_DTYPE
 
 
 def test_backward_workspace_checked_before_launch(lib):
@@ -252,5 +256,6 @@ def test_backward_workspace_checked_before_launch(lib):
 
 def test_backward_workspace_size(lib):
     assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, F32) == 2 * 128 * 8 * (2 * 32 + 4) * 4
-    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, BF16) == 0
+    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, BF16) == 2 * 128 * 8 * (2 * 32 + 4) * 4
+    assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, 7) == 0
     assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 65, F32) == 0

@@ -103,3 +103,40 @@ def test_backward_repeatable(env):
     assert np.array_equal(a["dq"], b["dq"]) and np.array_equal(a["dgate"], b["dgate"])   # no atomics
     for k in ("dc", "dw_uk", "dw_uv"):   # sums over thread blocks in any order
         assert np.max(np.abs(a[k] - b[k])) <= 1e-5 * np.max(np.abs(a[k]))
+
+
+def case_bf16(B, T, H, dq, dv, r, seed, gate=True):
+    w = W.Workload(name="bwd16", kind="prefill", dtype="bf16", B=B, T=T, D=256, H=H, d_q=dq, d_v=dv, r=r,
+                   r_q=64, scale=1.0, gate=gate, q_std=1.0)
+    d = W.draw_prefill_direct(w, seed=seed)
+    rng = np.random.default_rng(seed + 2000)
+    d["dout"] = W.round_bf16(rng.standard_normal((B, T, H * dv)))
+    return d
+
+
+def run_bf16(env, d, scale):
+    torch, lca, oracle = env
+    t = lambda a: None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)  # noqa: E731
+    got = lca.mla_absorbed_attn_bwd(t(d["q"]), t(d["c"]), t(d["w_uk"]), t(d["w_uv"]), t(d["gate"]), scale,
+                                    t(d["dout"]))
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    assert got["dq"].dtype == torch.float32
+    ref = oracle.prefill_backward(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale, d["dout"])
+    return {k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref
+
+
+@pytest.mark.parametrize("B,T,H,dq,dv,r,gate", [(2, 5, 3, 16, 16, 32, True), (1, 300, 2, 16, 16, 32, False),
+                                                (1, 130, 2, 64, 32, 64, True)])
+def test_backward_bf16_inputs(env, B, T, H, dq, dv, r, gate):
+    """bf16 inputs are widened to fp32: the gradients meet the fp32 bar on the rounded inputs."""
+    d = case_bf16(B, T, H, dq, dv, r, seed=T + H, gate=gate)
+    got, ref = run_bf16(env, d, 1.0)
+    check(got, ref)
+
+
+def test_backward_toy_long_context_full(env):
+    """The toy long-context configuration (B=4, T=2048, H=8, d=16, r=32, bf16 inputs), every gradient."""
+    d = case_bf16(4, 2048, 8, 16, 16, 32, seed=1)
+    got, ref = run_bf16(env, d, 1.0)
+    check(got, ref)
