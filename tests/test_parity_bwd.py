@@ -140,3 +140,12 @@ def test_backward_toy_long_context_full(env):
     d = case_bf16(4, 2048, 8, 16, 16, 32, seed=1)
     got, ref = run_bf16(env, d, 1.0)
     check(got, ref)
+
+
+@pytest.mark.parametrize("B,T,H,dq,dv,r", [(2, 65, 2, 16, 16, 16), (1, 70, 2, 8, 12, 20), (1, 150, 1, 33, 17, 40),
+                                           (1, 64, 3, 5, 3, 1), (1, 129, 1, 64, 64, 63)])
+def test_backward_padded_widths(env, B, T, H, dq, dv, r):
+    """Widths that the 16-, 32- and 64-column tilings pad with zeros, and tile-edge sequence lengths."""
+    d = case(B, T, H, dq, dv, r, seed=3 * T + r)
+    got, ref = run(env, d, 0.7)
+    check(got, ref)
