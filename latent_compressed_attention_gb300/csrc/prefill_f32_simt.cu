@@ -14,7 +14,7 @@
 //   then applies W_UV^T and the sigmoid gate (steps 3-4, lane v computes
 //   output column v).
 // Short dependency chains per lane and no bank conflicts (the staged rows are
-// padded to r + 1 floats) keep the warps busy; heavy tiles launch first.
+// padded to r + 1 floats) keep the warps busy; heavy tiles launch first, over all heads.
 #include "common.cuh"
 #include "internal.h"
 
@@ -51,8 +51,8 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *_
     __shared__ float s_p[kWarps][kKeys];                        // one chunk's softmax weights
 
     const int n_tiles = (T + kRows - 1) / kRows;
-    const int tile = n_tiles - 1 - static_cast<int>(blockIdx.x);   // heaviest first
-    const int h = blockIdx.y, b = blockIdx.z;
+    const int tile = n_tiles - 1 - static_cast<int>(blockIdx.y);   // heaviest first, over all heads
+    const int b = static_cast<int>(blockIdx.x) / H, h = static_cast<int>(blockIdx.x) % H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t0 = tile * kRows;
     const float *wuk = w_uk + static_cast<size_t>(h) * d_q * r;
@@ -163,7 +163,10 @@ bool prefill_f32_simt_supports(int r, int d_q, int d_v) {
 
 cudaError_t launch_prefill_f32_simt(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_f32_simt_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
-    const dim3 grid((a.T + kRows - 1) / kRows, a.H, a.B);
+    // (b, h) is the fastest grid index, so the heaviest tiles of every head are dispatched first
+    const unsigned tiles = static_cast<unsigned>((a.T + kRows - 1) / kRows);
+    if (tiles > 65535u) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.H), tiles);
     note_launch();
     prefill_f32_kernel<<<grid, kWarps * 32, 0, s>>>(
         static_cast<const float *>(a.q), static_cast<const float *>(a.c), static_cast<const float *>(a.w_uk),
