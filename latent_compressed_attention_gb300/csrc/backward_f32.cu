@@ -14,7 +14,7 @@
 //   query kernel: one CTA per (b, h, 64 query rows).  Pass 1 recomputes q_abs, the softmax statistics
 //     and o_lat over the keys u <= t (32 keys staged at a time); the per-row epilogue forms o, dgate, do,
 //     do_lat, delta and this CTA's part of dW_UV.  Pass 2 walks the keys again for dq_abs, and the
-//     epilogue forms dq and this CTA's part of dW_UK.  q_abs, do_lat and (m, l, delta) go to the
+//     epilogue forms dq and this CTA's part of dW_UK.  q_abs, do_lat and (m, 1/l, delta) go to the
 //     workspace for the key kernel.
 //   key kernel: one CTA per (b, h, 64 keys).  For the queries t >= u (32 staged at a time) it recomputes
 //     a_tu and ds_tu and accumulates this head's part of dc_u = sum_t a_tu do_lat_t + scale ds_tu q_abs_t.
@@ -42,8 +42,9 @@ template <typename In>
 struct BwdParams {
     const In *q, *c, *w_uk, *w_uv, *gate, *dout;
     float *dq, *dc, *dw_uk, *dw_uv, *dgate;
-    float *ws_qa, *ws_dol, *ws_st;   // [B,H,T,r], [B,H,T,r], [B,H,T,4] = (m, l, delta, 0)
+    float *ws_qa, *ws_dol, *ws_st;   // [B,H,T,r], [B,H,T,r], [B,H,T,4] = (m, 1 / l, delta, 0)
     float scale;
+    float scale_log2;                // scale log2(e): the scores in base 2, m in the same units
     int B, T, H, d_q, d_v, r;
 };
 
@@ -109,7 +110,11 @@ struct QLayout {
         wuk = o, o += dq * (RP + 1);        // [d_q][RP + 1]  W_UK[h], zero-padded
         wuv = o, o += dv * (RP + 1);        // [d_v][RP + 1]  W_UV[h], zero-padded
         q = o, o += kTile * (dq + 1);       // [kTile][d_q + 1]  the tile's q rows
-        dO = o, o += kTile * (dv + 1);      // [kTile][d_v + 1]  do
+        if (kTile * (dv + 1) <= kChunk * kTile) {
+            dO = pT;                        // [kTile][d_v + 1]  do: only between the passes, when pT is idle
+        } else {
+            dO = o, o += kTile * (dv + 1);
+        }
         st = o, o += 3 * kTile;             // m, l, delta of each row
         total = o;
     }
@@ -127,7 +132,7 @@ struct KLayout {
         dsT = o, o += kChunk * kTile;       // [kChunk][kTile]  scale ds, swizzled
         qaT = o, o += 2 * RP * kCP;         // 2 x [RP][kCP]  staged q_abs, transposed
         dolT = o, o += 2 * RP * kCP;        // 2 x [RP][kCP]  staged do_lat, transposed
-        st = o, o += 2 * 3 * kChunk;        // 2 x m, l, delta of the staged queries
+        st = o, o += 2 * 3 * kChunk;        // 2 x m, 1 / l, delta of the staged queries
         total = o;
     }
 };
@@ -245,7 +250,7 @@ __device__ __forceinline__ void acc2_4xn(const float *pT, const float *rows, con
 }
 
 template <typename In, int RP>
-__global__ void __launch_bounds__(kThreads, 3) bwd_query_kernel(const BwdParams<In> p) {
+__global__ void __launch_bounds__(kThreads, RP <= 32 ? 4 : 3) bwd_query_kernel(const BwdParams<In> p) {
     constexpr int NC = RP / 8;
     extern __shared__ float4 smem4[];
     float *sm = reinterpret_cast<float *>(smem4);
@@ -315,14 +320,14 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_query_kernel(const BwdParams<
             float mx = -INFINITY;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                s[i][k] = k0 + 4 * tx + k <= t ? s[i][k] * p.scale : -INFINITY;
+                s[i][k] = k0 + 4 * tx + k <= t ? s[i][k] * p.scale_log2 : -INFINITY;
                 mx = fmaxf(mx, s[i][k]);
             }
             const float m_new = fmaxf(m[i], oct_max(mx));   // finite: key 0 is in chunk 0
-            corr[i] = expf(m[i] - m_new);   // 0 on the first chunk
+            corr[i] = exp2f(m[i] - m_new);   // 0 on the first chunk
             float sum = 0.f;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) sum += (s[i][k] = expf(s[i][k] - m_new));   // s now holds p
+            for (int k = 0; k < 4; ++k) sum += (s[i][k] = exp2f(s[i][k] - m_new));   // s now holds p
             l[i] = fmaf(l[i], corr[i], oct_sum(sum));
             m[i] = m_new;
         }
@@ -390,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_query_kernel(const BwdParams<
         if (lane == 0) s_dl[row] = acc;
     }
     __syncthreads();
-    // q_abs, do_lat and (m, l, delta) of the tile's rows, for the key kernel
+    // q_abs, do_lat and (m, 1 / l, delta) of the tile's rows, for the key kernel (m in base-2 units)
     const size_t ws_row0 = (static_cast<size_t>(b) * H + h) * T + t0;
     for (int i = tid; i < kTile * r; i += kThreads) {
         const int row = i / r, j = i - row * r;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_query_kernel(const BwdParams<
     }
     if (tid < kTile && t0 + tid < T) {
         float *st = p.ws_st + (ws_row0 + tid) * 4;
-        st[0] = s_m[tid], st[1] = s_l[tid], st[2] = s_dl[tid], st[3] = 0.f;
+        st[0] = s_m[tid], st[1] = 1.f / s_l[tid], st[2] = s_dl[tid], st[3] = 0.f;
     }
 
     // pass 2: dq_abs = scale sum_u ds_tu c_u with ds_tu = a_tu (do_lat_t . c_u - delta_t)
@@ -427,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_query_kernel(const BwdParams<
             const int t = min(t0 + 4 * ty + i, T - 1);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {   // s becomes scale ds
-                const float a = expf(s[i][k] * p.scale - mr[i]) * linv[i];
+                const float a = exp2f(s[i][k] * p.scale_log2 - mr[i]) * linv[i];
                 s[i][k] = k0 + 4 * tx + k <= t ? p.scale * a * (da[i][k] - dr[i]) : 0.f;
             }
         }
@@ -467,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_key_kernel(const BwdParams<In
     float *sm = reinterpret_cast<float *>(smem4);
     const KLayout L(RP);
     float *s_ckT = sm + L.ckT, *s_qa = sm + L.qa, *s_dol = sm + L.dol, *s_aT = sm + L.aT, *s_dsT = sm + L.dsT;
-    float *s_qaT = sm + L.qaT, *s_dolT = sm + L.dolT, *s_st = sm + L.st;   // s_st: 2 x (m, l, delta) x kChunk
+    float *s_qaT = sm + L.qaT, *s_dolT = sm + L.dolT, *s_st = sm + L.st;   // s_st: 2 x (m, 1 / l, delta) x kChunk
     const int T = p.T, H = p.H, r = p.r;
     const int u0 = static_cast<int>(blockIdx.y) * kTile;   // keys [u0, u0 + 64); the first tiles are the heaviest
     const int b = static_cast<int>(blockIdx.x) / p.H, h = static_cast<int>(blockIdx.x) % p.H;
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_key_kernel(const BwdParams<In
         sq.load(qa_g, tq0, T, r);
         sd.load(dol_g, tq0, T, r);
         if (tid < kChunk) {
-            st3[0] = 0.f, st3[1] = 1.f, st3[2] = 0.f;
+            st3[0] = 0.f, st3[1] = 1.f, st3[2] = 0.f;   // (m, 1 / l, delta) past T: never used
             if (tq0 + tid < T) {
                 const float *st = p.ws_st + (ws0 + tq0 + tid) * 4;
                 st3[0] = st[0], st3[1] = st[1], st3[2] = st[2];
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_key_kernel(const BwdParams<In
         float s[4][4] = {}, da[4][4] = {};   // [key][query]
         dot_4x4x2<RP>(s_ckT, s_qaT + buf * Stage::kRowsT, s_dolT + buf * Stage::kRowsT, ty, tx, s, da);
         const float4 mq4 = ld4(sm_ + 4 * tx), lq4 = ld4(sm_ + kChunk + 4 * tx), dq4 = ld4(sm_ + 2 * kChunk + 4 * tx);
-        const float mq[4] = {mq4.x, mq4.y, mq4.z, mq4.w}, lq[4] = {lq4.x, lq4.y, lq4.z, lq4.w};
+        const float mq[4] = {mq4.x, mq4.y, mq4.z, mq4.w}, linv[4] = {lq4.x, lq4.y, lq4.z, lq4.w};
         const float dq_[4] = {dq4.x, dq4.y, dq4.z, dq4.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -526,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 3) bwd_key_kernel(const BwdParams<In
 #pragma unroll
             for (int i = 0; i < 4; ++i) {   // s becomes a, da becomes scale ds
                 const bool vis = t < T && u0 + 4 * ty + i <= t;   // query t sees key u
-                const float a = vis ? expf(s[i][k] * p.scale - mq[k]) / lq[k] : 0.f;
+                const float a = vis ? exp2f(s[i][k] * p.scale_log2 - mq[k]) * linv[k] : 0.f;
                 da[i][k] = p.scale * a * (da[i][k] - dq_[k]);
                 s[i][k] = a;
             }
@@ -595,6 +600,7 @@ cudaError_t launch_typed(const BackwardArgs &a, cudaStream_t s) {
     p.ws_dol = p.ws_qa + rows * a.r;
     p.ws_st = p.ws_dol + rows * a.r;
     p.scale = a.scale;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
     p.B = a.B;
     p.T = a.T;
     p.H = a.H;
