@@ -79,7 +79,7 @@ typedef enum {
  *   scale               softmax scale applied to the score (1.0 = the page's listing)
  *   out   [B,T,H*d_v]   result, flat index h*d_v + v; must not alias an input
  * Masking: token t attends to tokens 0..t of its own sequence.
- * Supported: F32 with r, d_q, d_v <= 64; BF16 with (r, d_q, d_v) = (512, 128, 128),
+ * Supported: F32 with r, d_q, d_v <= 64 and T <= 1,048,560; BF16 with (r, d_q, d_v) = (512, 128, 128),
  * or r in {32, 64} with d_q, d_v in {16, 32, 48, 64}.  B*T == 0 is a no-op
  * returning MLA_OK.
  * Alignment: every pointer 16-byte aligned.
@@ -106,8 +106,8 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
  * `dtype` (MLA_DTYPE_F32 or MLA_DTYPE_BF16; bf16 values are widened to fp32).
  * workspace: >= mla_absorbed_attn_bwd_workspace_size(...) bytes, 16-byte
  * aligned (per-row q_abs, do_lat and softmax statistics between the kernels).
- * Supported: r, d_q, d_v <= 64 (the toy sizes), fp32 arithmetic throughout;
- * larger widths return MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
+ * Supported: r, d_q, d_v <= 64 (the toy sizes) and T <= 4,194,240, fp32
+ * arithmetic throughout; other shapes return MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
  * blocks formed with atomics, so their last bits may differ between calls.
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
  */
@@ -213,7 +213,7 @@ MLA_API size_t mla_gated_layer_workspace_size(int B, int T, int D, int H, int d_
  *   w_gate   [H*d_v, D]   w_o [D, H*d_v]
  * x [B,T,D] and y [B,T,D], row-major.  All tensors share `dtype`.
  *
- * Supported: MLA_DTYPE_F32 with r, d_q, d_v <= 64 (SIMT fp32, no TF32);
+ * Supported: MLA_DTYPE_F32 with r, d_q, d_v <= 64 and T <= 1,048,560 (SIMT fp32, no TF32);
  * MLA_DTYPE_BF16 with r = 512, d_q = d_v = 128, H even, D and r_q multiples of
  * 256 (tensor-core GEMMs, fp32 accumulation, bf16 intermediate results).
  *

@@ -127,7 +127,7 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
     const bool f32 = dtype == MLA_DTYPE_F32;
     const bool ok_shape = f32 ? prefill_f32_simt_supports(r, d_q, d_v)
                               : (prefill_bf16_r512_supports(r, d_q, d_v) || prefill_bf16_small_supports(r, d_q, d_v));
-    if (!ok_shape) return MLA_ERR_UNSUPPORTED;
+    if (!ok_shape || (f32 && T > kPrefillF32MaxT)) return MLA_ERR_UNSUPPORTED;
     if (rows == 0) return MLA_OK;
 
     DeviceInfo *dev = nullptr;
@@ -167,7 +167,7 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
         !aligned16(dq) || !aligned16(dc) || !aligned16(dw_uk) || !aligned16(dw_uv) || (gate && !aligned16(gate)) ||
         (dgate && !aligned16(dgate)))
         return MLA_ERR_ALIGN;
-    if (!backward_f32_supports(r, d_q, d_v)) return MLA_ERR_UNSUPPORTED;
+    if (!backward_f32_supports(r, d_q, d_v) || T > kBackwardMaxT) return MLA_ERR_UNSUPPORTED;
     if (rows == 0) return MLA_OK;
     if (!workspace) return MLA_ERR_WORKSPACE;
     if (!aligned16(workspace)) return MLA_ERR_ALIGN;
@@ -260,7 +260,7 @@ MLA_API int mla_gated_layer_fwd(const void *x, const void *w_q_down, const void 
         !aligned16(w_kv_up) || !aligned16(w_gate) || !aligned16(w_o) || !aligned16(y))
         return MLA_ERR_ALIGN;
     const bool f32 = dtype == MLA_DTYPE_F32;
-    if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32)) return MLA_ERR_UNSUPPORTED;
+    if (!gated_layer_supports(D, H, d_q, d_v, r, r_q, f32) || (f32 && T > kPrefillF32MaxT)) return MLA_ERR_UNSUPPORTED;
     if (M == 0) return MLA_OK;
     const size_t need = gated_layer_workspace_bytes(M, D, H, d_q, d_v, r, r_q, f32);
     if (!workspace || workspace_bytes < need) return MLA_ERR_WORKSPACE;

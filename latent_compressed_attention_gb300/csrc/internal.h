@@ -45,6 +45,10 @@ struct BackwardArgs {
 // precondition) and never synchronises.
 cudaError_t launch_prefill_f32_simt(const PrefillArgs &a, cudaStream_t s);
 bool prefill_f32_simt_supports(int r, int d_q, int d_v);
+// Longest sequences of the fp32 prefill and of the backward: their grids put the tile rank (16 or 64
+// tokens) on the y index, at most 65535.
+constexpr long long kPrefillF32MaxT = 65535LL * 16;
+constexpr long long kBackwardMaxT = 65535LL * 64;
 
 cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s);
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v);

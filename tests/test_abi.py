@@ -74,7 +74,7 @@ def test_prefill_bad_dtype(lib):
 
 @pytest.mark.parametrize("kw", [dict(r=65), dict(dq=100), dict(dtype=BF16, r=48, dq=16, dv=16),
                                 dict(dtype=BF16, r=512, dq=64, dv=128), dict(dtype=BF16, r=32, dq=8, dv=16),
-                                dict(dtype=BF16, r=64, dq=16, dv=80)])
+                                dict(dtype=BF16, r=64, dq=16, dv=80), dict(B=1, T=1_048_561)])
 def test_prefill_unsupported_shape(lib, kw):
     assert prefill(lib, **kw) == ERR_UNSUPPORTED
 
@@ -150,7 +150,7 @@ def test_layer_bad_shape(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [dict(H=3), dict(D=320), dict(rq=320), dict(r=256), dict(dq=64),
-                                dict(dtype=F32, r=128, dq=16, dv=16)])
+                                dict(dtype=F32, r=128, dq=16, dv=16), dict(dtype=F32, r=32, dq=16, dv=16, B=1, T=1_048_561)])
 def test_layer_unsupported(lib, kw):
     assert layer(lib, **kw) == ERR_UNSUPPORTED
 
@@ -234,7 +234,8 @@ def test_backward_misaligned(lib, field):
     assert bwd_call(lib, **{field: FAKE + 4}) == ERR_ALIGN
 
 
-@pytest.mark.parametrize("kw", [dict(r=65), dict(dq_dim=128), dict(dv=65), dict(r=512, dq_dim=128, dv=128)])
+@pytest.mark.parametrize("kw", [dict(r=65), dict(dq_dim=128), dict(dv=65), dict(r=512, dq_dim=128, dv=128),
+                                dict(B=1, T=4_194_241)])
 def test_backward_unsupported(lib, kw):
     assert bwd_call(lib, **kw) == ERR_UNSUPPORTED
 
