@@ -85,6 +85,17 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     return v;
 }
 
+// Barrier of the two softmax warps (one per group) that share TMEM lanes 32 pair .. 32 pair + 31; the ids
+// are literals so the kernel reserves barriers 0-5 only.
+__device__ __forceinline__ void pair_bar_sync(int pair) {
+    switch (pair) {
+        case 0: named_bar_sync(2, 64); break;
+        case 1: named_bar_sync(3, 64); break;
+        case 2: named_bar_sync(4, 64); break;
+        default: named_bar_sync(5, 64); break;
+    }
+}
+
 struct Params {
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
@@ -120,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         mbar_init(B_(bars->s_full), 1);
         mbar_init(B_(bars->s_free), kMath);
-        mbar_init(B_(bars->p_full), 1);
+        mbar_init(B_(bars->p_full), kMath);   // every softmax thread arrives after storing its part of P
         mbar_init(B_(bars->pv_done), 1);
         mbar_init(B_(bars->olat_ready), 1);
         mbar_init(B_(bars->ep_done), 1);
@@ -234,11 +245,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         named_bar_sync(1, kMath);
         if (leader && ok) mbar_arrive(B_(bars->qabs_ready));
+        if (!ok) *abort_flag = 1;   // every later wait then returns at once
 
         float m_run = -INFINITY, l_run = 0.f;   // l_run: this group's part of the row sum
-        for (int j = 0; ok && j < nkv; ++j) {
-            fail = !mbar_wait(B_(bars->s_full), j & 1, p.err, abort_flag);
-            if (named_bar_or(1, kMath, fail)) { ok = false; break; }
+        // Per block the only barrier is between the two warps (one per group) that share these rows.  A wait
+        // that fails sets the abort flag, after which every wait returns at once: all threads still run the
+        // same barrier sequence, and one vote after the loop settles the outcome.
+        const int pair = warp & 3;
+        for (int j = 0; j < nkv; ++j) {
+            if (!mbar_wait(B_(bars->s_full), j & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
             tc_fence_after();
             float s[2][32];
 #pragma unroll
@@ -255,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                         if (c2 * 32 + i > lim) s[c2][i] = -INFINITY;
             }
             st_shared_f32(base + PMAX + ((j & 1) * 2 + g) * kBM * 4 + row * 4, tree_max64(s));
-            named_bar_sync(1, kMath);   // publishes both groups' partial maxima
+            pair_bar_sync(pair);   // publishes both groups' partial maxima of these rows
             const float mx = fmaxf(ld_shared_f32(base + PMAX + ((j & 1) * 2 + 0) * kBM * 4 + row * 4),
                                    ld_shared_f32(base + PMAX + ((j & 1) * 2 + 1) * kBM * 4 + row * 4));
             float factor = 1.f;
@@ -269,32 +284,26 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int i = 0; i < 32; ++i) s[c2][i] = fast_exp2(s[c2][i] - m_run);
             l_run = l_run * factor + tree_sum64(s);
             if (j > 0) {   // P and o_lat are free once the previous block's product completed
-                fail = !mbar_wait(B_(bars->pv_done), (j - 1) & 1, p.err, abort_flag);
-                if (named_bar_or(1, kMath, fail)) { ok = false; break; }
-                if (named_bar_or(1, kMath, factor != 1.f)) {
+                if (!mbar_wait(B_(bars->pv_done), (j - 1) & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
+                if (__any_sync(0xffffffffu, factor != 1.f)) {   // this warp's rows of o_lat (warp-collective)
                     tc_fence_after();
-                    if (__any_sync(0xffffffffu, factor != 1.f)) {
-                        float v[32];
-                        tmem_ld32(trow + O_COL + g * 32, v);
-                        tmem_wait_ld();
+                    float v[32];
+                    tmem_ld32(trow + O_COL + g * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] *= factor;
-                        tmem_st32(trow + O_COL + g * 32, v);
-                        tmem_wait_st();
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] *= factor;
+                    tmem_st32(trow + O_COL + g * 32, v);
+                    tmem_wait_st();
                     tc_fence_before();
                 }
             }
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) store_row32_bf16(base + PT, kTile, row, 2 * g + c2, s[c2], 1.f);
             fence_proxy_async_smem();
-            named_bar_sync(1, kMath);
-            if (leader) mbar_arrive(B_(bars->p_full));
+            mbar_arrive(B_(bars->p_full));
         }
-        if (ok) {
-            fail = !mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag);
-            ok = !named_bar_or(1, kMath, fail);
-        }
+        if (!mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
+        ok = !named_bar_or(1, kMath, !ok);
         // the row sum: both groups' parts
         st_shared_f32(base + LSUM + g * kBM * 4 + row * 4, l_run);
         named_bar_sync(1, kMath);
