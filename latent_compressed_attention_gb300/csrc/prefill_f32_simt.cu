@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *_
     __shared__ float s_c[kKeys * kPad];                         // staged latent rows, padded
     __shared__ float s_qa[kWarps][kRowsPerWarp][kMaxDim];       // q_abs of each warp's rows
     __shared__ float s_p[kWarps][kKeys];                        // one chunk's softmax weights
+    __shared__ float s_wk[kMaxDim * kMaxDim];                   // W_UK[h] as [d_q][r]
+    __shared__ float s_wv[kMaxDim * kPad];                      // W_UV[h] as [d_v][r], rows padded
 
     const int n_tiles = (T + kRows - 1) / kRows;
     const int tile = n_tiles - 1 - static_cast<int>(blockIdx.y);   // heaviest first, over all heads
@@ -57,6 +59,13 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *_
     const int t0 = tile * kRows;
     const float *wuk = w_uk + static_cast<size_t>(h) * d_q * r;
     const float *wuv = w_uv + static_cast<size_t>(h) * d_v * r;
+    // this head's weights, read once per CTA with coalesced loads
+    for (int i = threadIdx.x; i < d_q * r; i += kWarps * 32) s_wk[i] = __ldg(wuk + i);
+    for (int i = threadIdx.x; i < d_v * r; i += kWarps * 32) {
+        const int v = i / r, j = i - v * r;
+        s_wv[v * kPad + j] = __ldg(wuv + i);
+    }
+    __syncthreads();
 
     // step 2, absorb: q_abs[t, j] = sum_d q[b, t, h, d] W_UK[h, d, j]; lane j holds columns j and j + 32
     float o[kRowsPerWarp][2], m[kRowsPerWarp], l[kRowsPerWarp];
@@ -71,8 +80,8 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *_
         float a0 = 0.f, a1 = 0.f;
         for (int d = 0; d < d_q; ++d) {
             const float qd = __ldg(qrow + d);
-            if (lane < r) a0 = fmaf(qd, __ldg(wuk + d * r + lane), a0);
-            if (lane + 32 < r) a1 = fmaf(qd, __ldg(wuk + d * r + lane + 32), a1);
+            if (lane < r) a0 = fmaf(qd, s_wk[d * r + lane], a0);
+            if (lane + 32 < r) a1 = fmaf(qd, s_wk[d * r + lane + 32], a1);
         }
         s_qa[warp][i][lane] = a0;
         s_qa[warp][i][lane + 32] = a1;
@@ -145,9 +154,9 @@ __global__ void __launch_bounds__(kWarps * 32) prefill_f32_kernel(const float *_
         for (int half = 0; half < 2; ++half) {
             const int v = lane + 32 * half;
             if (v >= d_v) continue;
-            const float *wv = wuv + static_cast<size_t>(v) * r;
+            const float *wv = s_wv + v * kPad;   // lanes read rows kPad apart: distinct banks
             float acc = 0.f;
-            for (int j = 0; j < r; ++j) acc = fmaf(ol[j], __ldg(wv + j), acc);
+            for (int j = 0; j < r; ++j) acc = fmaf(ol[j], wv[j], acc);
             if (grow) acc = acc / (1.f + expf(-grow[v]));
             orow[v] = acc;
         }
