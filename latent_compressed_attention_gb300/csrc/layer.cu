@@ -73,24 +73,43 @@ Layout layout(long long M, int D, int H, int d_q, int d_v, int r, int r_q, size_
 }
 
 // ---------------------------------------------------------------- fp32 SIMT kernels
-constexpr int kT = 16;
+constexpr int kT = 16;    // output tile edge
+constexpr int kKT = 64;   // K step: few dependent global round trips for the toy layer's short K
 
-// C[M,N] = A[M,K] . B[N,K]^T in fp32, 16 x 16 output tiles staged through shared memory.
+// C[M,N] = A[M,K] . B[N,K]^T in fp32, 16 x 16 output tiles.  Each K step stages 16 x 64 of A and of B
+// in shared memory (coalesced along K); the next step's values are loaded into registers while the
+// current one is used, so a call of K = 256 makes four global round trips, not sixteen.
 __global__ void __launch_bounds__(kT *kT) gemm_f32_kernel(const float *A, const float *B, float *C, int M, int N,
                                                           int K) {
-    __shared__ float sa[kT][kT + 1], sb[kT][kT + 1];
+    constexpr int kPer = kT * kKT / (kT * kT);   // staged values of each operand per thread: 4
+    __shared__ float sa[kT][kKT + 1], sb[kT][kKT + 1];
     const int tx = threadIdx.x % kT, ty = threadIdx.x / kT;
-    const int m = blockIdx.y * kT + ty, n = blockIdx.x * kT + tx;
-    const int bn = blockIdx.x * kT + ty;   // B row this thread loads
-    float acc = 0.f;
-    for (int k0 = 0; k0 < K; k0 += kT) {
-        sa[ty][tx] = (m < M && k0 + tx < K) ? A[static_cast<size_t>(m) * K + k0 + tx] : 0.f;
-        sb[ty][tx] = (bn < N && k0 + tx < K) ? B[static_cast<size_t>(bn) * K + k0 + tx] : 0.f;
-        __syncthreads();
+    const int m0 = blockIdx.y * kT, n0 = blockIdx.x * kT;
+    float va[kPer], vb[kPer];
+    auto load = [&](int k0) {
 #pragma unroll
-        for (int k = 0; k < kT; ++k) acc = fmaf(sa[ty][k], sb[tx][k], acc);
+        for (int e = 0; e < kPer; ++e) {
+            const int i = static_cast<int>(threadIdx.x) + e * kT * kT, row = i / kKT, k = k0 + i % kKT;
+            va[e] = (m0 + row < M && k < K) ? A[static_cast<size_t>(m0 + row) * K + k] : 0.f;
+            vb[e] = (n0 + row < N && k < K) ? B[static_cast<size_t>(n0 + row) * K + k] : 0.f;
+        }
+    };
+    float acc = 0.f;
+    load(0);
+    for (int k0 = 0; k0 < K; k0 += kKT) {
+        __syncthreads();   // the previous step's tiles are consumed
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int i = static_cast<int>(threadIdx.x) + e * kT * kT;
+            sa[i / kKT][i % kKT] = va[e];
+            sb[i / kKT][i % kKT] = vb[e];
+        }
         __syncthreads();
+        if (k0 + kKT < K) load(k0 + kKT);
+#pragma unroll 16
+        for (int k = 0; k < kKT; ++k) acc = fmaf(sa[ty][k], sb[tx][k], acc);
     }
+    const int m = m0 + ty, n = n0 + tx;
     if (m < M && n < N) C[static_cast<size_t>(m) * N + n] = acc;
 }
 
