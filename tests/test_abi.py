@@ -127,6 +127,19 @@ def test_binding_refuses_cpu_tensors():
         lca.mla_absorbed_attn_fwd(x, torch.zeros(1, 4, 32), torch.zeros(2, 16, 32), torch.zeros(2, 16, 32))
 
 
+def test_binding_refuses_cpu_tensors_everywhere():
+    """Every entry point checks its tensors before any call into the library: there is no CPU path."""
+    torch = pytest.importorskip("torch")
+    z = torch.zeros
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lca.mla_absorbed_attn_bwd(z(1, 4, 2, 16), z(1, 4, 32), z(2, 16, 32), z(2, 16, 32), None, 1.0, z(1, 4, 32))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lca.mla_latent_decode(z(2, 8, 512), z(2, 64, 512), torch.ones(2, dtype=torch.int32), z(8, 128, 512))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lca.mla_gated_layer_fwd(z(1, 4, 256), z(64, 256), z(32, 64), z(32, 256), z(64, 32), z(32, 256), z(256, 32),
+                                2, 16, 16)
+
+
 # ----------------------------------------------------------------------------- whole layer
 def layer(lib, x=FAKE, wqd=FAKE, wqu=FAKE, wkvd=FAKE, wkvu=FAKE, wg=FAKE, wo=FAKE, y=FAKE, B=1, T=16, D=256, H=2,
           dq=128, dv=128, r=512, rq=256, dtype=BF16, ws=FAKE, ws_bytes=1 << 40):
