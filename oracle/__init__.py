@@ -128,19 +128,20 @@ def layer_forward(x, p, H: int, d_q: int, d_v: int, scale: float = 1.0, rows=Non
     kv_down, kv_up, gate, o_proj.  Only the requested rows' q, g and o are formed; c is
     formed for every row (each row's attention reads all earlier latents).
     Returns [B,T,D], or [len(rows), D].
-    Parity: a composition of pinned parts (tests/test_oracle.py checks it against the
-    all-rows composition of ``layer.step1``, ``prefill`` and ``layer.output_projection``).
+    Parity: a composition of pinned parts (``layer``'s functions are pinned in
+    tests/test_oracle_layer.py; tests/test_oracle.py checks the composition against
+    explicit decompression).
     """
     from . import layer
     x = _f64(x)
     B, T, D = x.shape
     flat = x.reshape(B * T, D)
     sel = np.arange(B * T) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
-    c = layer.rmsnorm(flat @ _f64(p["kv_down"]).T).reshape(B, T, -1)
+    c = layer.latent(flat, p["kv_down"]).reshape(B, T, -1)
     q = np.zeros((B * T, H * d_q))
-    q[sel] = layer.rmsnorm(flat[sel] @ _f64(p["q_down"]).T) @ _f64(p["q_up"]).T
+    q[sel] = layer.query(flat[sel], p["q_down"], p["q_up"])
     g = np.zeros((B * T, H * d_v))
-    g[sel] = flat[sel] @ _f64(p["gate"]).T
+    g[sel] = layer.gate_logits(flat[sel], p["gate"])
     w_uk, w_uv = layer.split_kv_up(_f64(p["kv_up"]), H, d_q, d_v)
     o = prefill(q.reshape(B, T, H, d_q), c, w_uk, w_uv, g.reshape(B, T, H * d_v), scale, rows=sel)
     y = layer.output_projection(o, p["o_proj"])

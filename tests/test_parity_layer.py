@@ -66,9 +66,9 @@ def check(env, w, p, rows, tol):
     assert rel_err(y[rows], ref) <= tol
     # step-1 intermediates on the same rows, and the latent for every row
     flat = p["x"].reshape(w.B * w.T, w.D)
-    q_ref = layer.rmsnorm(flat[rows] @ p["q_down"].T) @ p["q_up"].T
-    g_ref = flat[rows] @ p["gate"].T
-    c_ref = layer.rmsnorm(flat @ p["kv_down"].T)
+    q_ref = layer.query(flat[rows], p["q_down"], p["q_up"])
+    g_ref = layer.gate_logits(flat[rows], p["gate"])
+    c_ref = layer.latent(flat, p["kv_down"])
     assert rel_err(q.reshape(w.B * w.T, -1)[rows], q_ref) <= tol
     assert rel_err(g.reshape(w.B * w.T, -1)[rows], g_ref) <= tol
     assert rel_err(c.reshape(w.B * w.T, -1), c_ref) <= tol

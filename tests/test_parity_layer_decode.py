@@ -100,9 +100,9 @@ def decode_against_oracle(env, w, B, max_len, seed):
     assert lca.mla_get_device_error() == 0
 
     # oracle: step 1 for the new tokens, absorb W_UK, append, decode over lens+1 rows, W_o
-    c_t = layer.rmsnorm(x_t @ p["kv_down"].T)
-    q = (layer.rmsnorm(x_t @ p["q_down"].T) @ p["q_up"].T).reshape(B, w.H, w.d_q)
-    g = x_t @ p["gate"].T
+    c_t = layer.latent(x_t, p["kv_down"])
+    q = layer.query(x_t, p["q_down"], p["q_up"]).reshape(B, w.H, w.d_q)
+    g = layer.gate_logits(x_t, p["gate"])
     w_uk, w_uv = layer.split_kv_up(p["kv_up"], w.H, w.d_q, w.d_v)
     q_abs = np.einsum("bhd,hdj->bhj", q, w_uk)
     for b in range(B):
