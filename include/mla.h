@@ -177,7 +177,10 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
  * - The call allocates and frees nothing, on the host or the device.
  * - The first call on a device looks up the scratch array's device address
  *   on that device (cudaGetSymbolAddress); make that first call before any
- *   stream capture.
+ *   stream capture.  If that lookup fails (for example inside a capture, or
+ *   when the library's device code cannot be loaded on the device) the call
+ *   returns MLA_ERR_CUDA, clears the runtime's pending error and launches
+ *   nothing; a later call retries the lookup.
  * - Every call uses the same scratch array: calls whose kernels can overlap
  *   on the GPU (different streams, no ordering between them) race on it and
  *   give wrong results.  Calls on one stream, or otherwise ordered, are safe.

@@ -1096,7 +1096,12 @@ cudaError_t decode_noalloc_scratch(void **ptr) {
     if (!g_noalloc_ptr[dev]) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
+        if (e != cudaSuccess) {
+            // a failed lookup (the module cannot be loaded on this device, or the first call came
+            // inside a stream capture) must not leave an error pending for the caller's next CUDA call
+            (void)cudaGetLastError();
+            return e;
+        }
         g_noalloc_ptr[dev] = p;
     }
     *ptr = g_noalloc_ptr[dev];

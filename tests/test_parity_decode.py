@@ -156,3 +156,25 @@ def test_decode_full_workload_sampled(env):
         rows = W.decode_cache_rows(w, b, int(lens[b]), seed=0)[None]
         ref = oracle.decode(d["q_abs"][b:b + 1], rows, lens[b:b + 1], d["w_uv"], None, w.scale)
         assert rel_err(got[b:b + 1], ref) <= TOL_BF16, f"sequence {b} (len {lens[b]})"
+
+
+@pytest.mark.parametrize("lens", [[32768, 0, 5, 1000], [0, 3000, 1, 0, 20000, 129]])
+def test_decode_stale_workspace_is_never_read(env, lens):
+    """The merge reads only the partial-result slots that the split kernel of the same call wrote:
+    a caller workspace filled with NaN beforehand (ragged lengths, zeros, and one sequence long enough
+    to be split across far more than 32 clusters) still gives the oracle's result, finite everywhere."""
+    torch, lca, oracle = env
+    H, max_len = 96, max(lens)
+    d, cache, lens, _ = make_case(H, lens, max_len, seed=21)
+    B = lens.size
+    need = lca.mla_latent_decode_workspace_size(B, H, 512, max_len)
+    ws = torch.full((need // 4 + 1,), float("nan"), dtype=torch.float32, device="cuda")
+    out = lca.mla_latent_decode(bf(torch, d["q_abs"]), bf(torch, cache), torch.tensor(lens, device="cuda"),
+                                bf(torch, d["w_uv"]), None, 1.0, workspace=ws.view(torch.uint8))
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    got = out.float().double().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    assert rel_err(got, oracle_ref(oracle, d, cache, lens)) <= TOL_BF16
+    for b in np.flatnonzero(lens == 0):
+        assert np.all(got[b] == 0.0)
