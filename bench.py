@@ -6,7 +6,8 @@ causal softmax, the latent weighting, the W_UV up-projection and the gate, all
 in the library's fused kernel.  The cached-latent decode (B=64, cache lengths
 uniform in [1024, 32768], H=96, r=512) is timed in the same run and reported
 under "decode", and the whole layer at the prefill's size (step-1 projections
-with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".  The two
+with RMSNorm, the attention, W_o: x [B,T,D] -> y) under "layer".  The
+mid-size prefill (B=4, T=4096, H=16) runs under "mid_prefill".  The two
 small configurations run under "small_prefill" (r=32 at T=2048, bf16, bound by
 the exponential unit), "toy_layer" (the fp32 toy layer, bound by launch
 latency), "toy_backward" (the gradients of the toy layer's attention, fp32) and
@@ -14,7 +15,8 @@ latency), "toy_backward" (the gradients of the toy layer's attention, fp32) and
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One JSON line on stdout (rank 0).  ``value`` is TFLOP/s on the algorithmic
+One JSON line on stdout (rank 0), ending with ``summary``: every section's
+headline figure and roofline fraction.  ``value`` is TFLOP/s on the algorithmic
 causal FLOP count B*H*[2 r T(T+1) + 2 T r (d_q+d_v)], device time of the
 kernel launches, L2 flushed between steps; ``e2e`` is the same metric through
 the public API with pinned host buffers, copies included.  Under torchrun each
@@ -155,8 +157,8 @@ def max_over_ranks(x, world):
 
 
 # ----------------------------------------------------------------------------- our arm
-def prefill_inputs(torch, dev):
-    d = W.draw_prefill_direct(PREFILL, seed=0)
+def prefill_inputs(torch, dev, w=None):
+    d = W.draw_prefill_direct(PREFILL if w is None else w, seed=0)
     to = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)  # noqa: E731
     host = {k: to(v).pin_memory() for k, v in d.items() if v is not None}
     devt = {k: v.to(dev) for k, v in host.items()}
@@ -214,8 +216,9 @@ def run_ours(args):
     host, d = prefill_inputs(torch, dev)
     out = torch.empty((PREFILL.B, PREFILL.T, PREFILL.H * PREFILL.d_v), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ws = prefill_workspace(torch, lca, PREFILL, dev)
     step = lambda: lca.mla_absorbed_attn_fwd(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"],  # noqa: E731
-                                             PREFILL.scale, out=out)
+                                             PREFILL.scale, out=out, workspace=ws)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -242,9 +245,12 @@ def run_ours(args):
     d2h = out.numel() * out.element_size()
     e2e_value = e2e_ms = None
     if not args.no_e2e:
-        e2e_ms = max_over_ranks(e2e_pipelined(torch, lca, dev, stream, host, out, max(4, args.steps // 2)), world)
+        e2e_ms = max_over_ranks(e2e_pipelined(torch, lca, dev, stream, host, out, ws, max(4, args.steps // 2)),
+                                world)
         e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
+    mid = run_mid_prefill(torch, lca, dev, stream, flush, args, pk) \
+        if not args.no_mid and PREFILL.name != W.MID_PREFILL_BF16.name else None
     decode = run_decode(torch, lca, dev, stream, flush, args, pk) if not args.no_decode else None
     layer_line = run_layer(torch, lca, dev, stream, flush, args, pk) if not args.no_layer else None
     layer_dec = run_layer_decode(torch, lca, dev, stream, flush, args, pk) \
@@ -279,29 +285,47 @@ def run_ours(args):
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
-        if decode is not None:
-            line["decode"] = decode
-        if layer_line is not None:
-            line["layer"] = layer_line
-        if layer_dec is not None:
-            line["layer_decode"] = layer_dec
-        if small is not None:
-            line["small_prefill"] = small
-        if toy is not None:
-            line["toy_layer"] = toy
-        if toy_bwd is not None:
-            line["toy_backward"] = toy_bwd
-        if small_bwd is not None:
-            line["small_backward"] = small_bwd
+        sections = [("mid_prefill", mid), ("decode", decode), ("layer", layer_line), ("layer_decode", layer_dec),
+                    ("small_prefill", small), ("toy_layer", toy), ("toy_backward", toy_bwd),
+                    ("small_backward", small_bwd)]
+        for name, sec in sections:
+            if sec is not None:
+                line[name] = sec
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        line["summary"] = summary(line, sections)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
 
 
-def e2e_pipelined(torch, lca, dev, stream, host, out, steps):
+def summary(line, sections):
+    """Every section's headline figure and roofline fraction in a few hundred bytes, last on the line."""
+    def brief(sec):
+        if "unavailable" in sec:
+            return {"unavailable": sec["unavailable"]}
+        rf = sec.get("roofline", {})
+        return {"value": sec["value"], "unit": sec["unit"], "frac": rf.get("frac"), "bound": rf.get("bound")}
+    out = {line["config"]["workload"]: {"value": line["value"], "unit": line["unit"],
+                                        "frac": line["roofline"]["frac"], "bound": "tensor"}}
+    if line.get("e2e"):
+        out["e2e_ms_per_step"] = line["e2e"]["ms_per_step"]
+    for name, sec in sections:
+        if sec is not None:
+            out[name] = brief(sec)
+    if "cpu_baseline" in line:
+        out["cpu_oracle_tflops"] = line["cpu_baseline"]["value"]
+    return out
+
+
+def prefill_workspace(torch, lca, w, dev):
+    """The prefill's device workspace for workload w, allocated once outside every timed region (None if none)."""
+    need = lca.mla_absorbed_attn_fwd_workspace_size(w.B, w.T, w.H, w.d_q, w.d_v, w.r, torch.bfloat16)
+    return torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+
+
+def e2e_pipelined(torch, lca, dev, stream, host, out, ws, steps):
     """Per-step milliseconds of `steps` end-to-end prefill steps: step i copies its inputs host -> device on a
     copy stream, runs the prefill on `stream`, copies its output device -> host on a third stream; two device
     buffer sets let step i+1's input copy and step i-1's output copy overlap step i's kernel.  Timed with CUDA
@@ -309,6 +333,7 @@ def e2e_pipelined(torch, lca, dev, stream, host, out, steps):
     h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     bufs = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     outs = [out, torch.empty_like(out)]
+    wss = [ws, None if ws is None else torch.empty_like(ws)]
     outs_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
     in_ready, comp_done, out_read = [ev(), ev()], [ev(), ev()], [ev(), ev()]
@@ -327,7 +352,7 @@ def e2e_pipelined(torch, lca, dev, stream, host, out, steps):
             stream.wait_event(out_read[j])       # the previous output of set j has been copied out
         b = bufs[j]
         lca.mla_absorbed_attn_fwd(b["q"], b["c"], b["w_uk"], b["w_uv"], b["gate"], PREFILL.scale, out=outs[j],
-                                  stream=stream)
+                                  workspace=wss[j], stream=stream)
         comp_done[j].record(stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(comp_done[j])
@@ -345,6 +370,31 @@ def e2e_pipelined(torch, lca, dev, stream, host, out, steps):
     t1.record(d2h_s)
     torch.cuda.synchronize()
     return t0.elapsed_time(t1) / steps
+
+
+def run_mid_prefill(torch, lca, dev, stream, flush, args, pk):
+    """The mid-size prefill (B=4, T=4096, H=16, d_q=d_v=128, r=512, bf16, scale 1/sqrt(128)): the same fused
+    kernel as the step, with 16 heads instead of 96 sharing each latent tile and 4x shorter key rows."""
+    w = W.MID_PREFILL_BF16
+    _, d = prefill_inputs(torch, dev, w)
+    out = torch.empty((w.B, w.T, w.H * w.d_v), dtype=torch.bfloat16, device=dev)
+    ws = prefill_workspace(torch, lca, w, dev)
+    step = lambda: lca.mla_absorbed_attn_fwd(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], w.scale,  # noqa: E731
+                                             out=out, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    ms = statistics.mean(times)
+    tf = w.prefill_flops() / (ms * 1e-3) / 1e12
+    return {"workload": w.name, "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "flops_per_step": w.prefill_flops(),
+            "config": {"B": w.B, "T": w.T, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "scale": w.scale,
+                       "l2": "flushed between steps"},
+            "roofline": {"kernel": "prefill_r512_kernel", "bound": "tensor", "achieved": round(tf, 2),
+                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": round(tf / pk["bf16_tflops"], 4),
+                         "peak_source": pk["source"] + " (burst bf16)", "traffic": None},
+            "gpu_launches": launches}
 
 
 def run_decode(torch, lca, dev, stream, flush, args, pk):
@@ -458,8 +508,11 @@ def run_layer_decode(torch, lca, dev, stream, flush, args, pk):
             "gpu_launches": launches}
 
 
-# Exponentials per clock per SM on the multi-function unit (ex2, fp32), and fp32 FMA lanes per SM.
-MUFU_EX2_PER_CLK_SM = 16
+# Exponentials per clock per SM on the multi-function unit: measured on GB300 by a throughput probe (152 SMs x
+# 2048 threads, eight independent ex2.approx.ftz.f32 chains per thread, CUDA events): 9.47e12 ex2/s, 30.1 per
+# clock per SM at 2070 MHz (the f16x2 and bf16x2 forms give the same 32 exponentials per clock).  fp32 FMA
+# lanes per SM (the same probe measured 121.7 FMA per clock per SM).
+MUFU_EX2_PER_CLK_SM = 30.1
 FP32_LANES_SM = 128
 SM_MAX_MHZ = 2070.0
 
@@ -471,8 +524,9 @@ def run_small_prefill(torch, lca, dev, stream, flush, args):
     d = W.draw_prefill_direct(w, seed=0)
     t = {k: torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16).to(dev) for k, v in d.items() if v is not None}
     out = torch.empty((w.B, w.T, w.H * w.d_v), dtype=torch.bfloat16, device=dev)
+    ws = prefill_workspace(torch, lca, w, dev)
     step = lambda: lca.mla_absorbed_attn_fwd(t["q"], t["c"], t["w_uk"], t["w_uv"], t["gate"], w.scale,  # noqa: E731
-                                             out=out)
+                                             out=out, workspace=ws)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -488,7 +542,8 @@ def run_small_prefill(torch, lca, dev, stream, flush, args):
                        "l2": "flushed between steps"},
             "roofline": {"kernel": "prefill_small_kernel", "bound": "alu", "achieved": round(achieved, 1),
                          "peak": round(peak, 1), "unit": "G ex2/s", "frac": round(achieved / peak, 4),
-                         "peak_source": f"derived: {MUFU_EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {SM_MAX_MHZ:.0f} MHz",
+                         "peak_source": f"measured ex2 throughput: {MUFU_EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x "
+                                        f"{SM_MAX_MHZ:.0f} MHz",
                          "traffic": None},
             "gpu_launches": launches}
 
@@ -652,6 +707,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-mid", action="store_true", help="skip the mid-size prefill section")
     ap.add_argument("--no-small", action="store_true", help="skip the small-rank prefill and the fp32 toy layer")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")

@@ -60,6 +60,8 @@ typedef enum {
 
 /*
  * mla_absorbed_attn_fwd - causal prefill of the absorbed Gated MLA.
+ * mla_absorbed_attn_fwd_workspace_size - bytes of workspace it needs for these
+ * sizes (0 when none; also 0 for invalid or unsupported sizes).
  *
  * Page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）":
  *   step 2  q_abs[b,t,h,:] = q[b,t,h,:] . W_UK[h]                  [B,T,H,r]
@@ -78,17 +80,27 @@ typedef enum {
  *   gate  [B,T,H*d_v]   pre-sigmoid gate logits W_g x, or NULL for no gate
  *   scale               softmax scale applied to the score (1.0 = the page's listing)
  *   out   [B,T,H*d_v]   result, flat index h*d_v + v; must not alias an input
+ *   workspace           device buffer of >= mla_absorbed_attn_fwd_workspace_size(...)
+ *                       bytes, 16-byte aligned, not used by any other call in flight;
+ *                       may be NULL when that size is 0.  The r = 512 kernel keeps an
+ *                       f16 copy of c there (see precision below).
  * Masking: token t attends to tokens 0..t of its own sequence.
+ * Precision (BF16): the score operand q_abs * scale is not rounded to bf16.  At
+ * r = 512 the score product runs on f16 copies of q_abs and c, each scaled by a
+ * power of two (per query row, per sequence) into the f16 range and scaled back
+ * exactly in the softmax; at r <= 64 q_abs is split into two bf16 parts.  The
+ * softmax weights, o_lat / l and the output are rounded to bf16.
  * Supported: F32 with r, d_q, d_v <= 64 and T <= 1,048,560; BF16 with (r, d_q, d_v) = (512, 128, 128),
  * or r in {32, 64} with d_q, d_v in {16, 32, 48, 64}.  B*T == 0 is a no-op
  * returning MLA_OK.
  * Alignment: every pointer 16-byte aligned.
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
  */
+MLA_API size_t mla_absorbed_attn_fwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype);
 MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
                                   const void *gate, float scale, void *out,
                                   int B, int T, int H, int d_q, int d_v, int r,
-                                  int dtype, void *stream);
+                                  int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * mla_absorbed_attn_bwd - gradients of the attention (steps 2-4 of section

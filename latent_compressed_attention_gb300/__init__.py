@@ -7,7 +7,8 @@ computation runs in the library's CUDA kernels.  There is no CPU fallback: if
 the library is missing or a call fails, an exception is raised.
 
 Entry points (same names as the C functions):
-    mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale=1.0, out=None)
+    mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale=1.0, out=None, workspace=None)
+    mla_absorbed_attn_fwd_workspace_size(B, T, H, d_q, d_v, r, dtype)
     mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale=1.0, out=None, workspace=None)
     mla_latent_decode_workspace_size(B, H, r, max_len)
     mla_get_device_error(stream=None)
@@ -20,7 +21,8 @@ import threading
 
 from ._build import LIB_PATH, build
 
-__all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd", "mla_latent_decode",
+__all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd",
+           "mla_absorbed_attn_fwd_workspace_size", "mla_latent_decode",
            "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
            "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout",
            "mla_absorbed_attn_bwd", "mla_gated_layer_fwd", "mla_gated_layer_workspace_size",
@@ -53,8 +55,10 @@ def library():
                                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
             lib = ctypes.CDLL(LIB_PATH)
             vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
-            lib.mla_absorbed_attn_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, i, i, i, i, i, i, i, vp]
+            lib.mla_absorbed_attn_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, i, i, i, i, i, i, i, vp, sz, vp]
             lib.mla_absorbed_attn_fwd.restype = i
+            lib.mla_absorbed_attn_fwd_workspace_size.argtypes = [i] * 7
+            lib.mla_absorbed_attn_fwd_workspace_size.restype = sz
             lib.mla_latent_decode_workspace_size.argtypes = [i, i, i, i]
             lib.mla_latent_decode_workspace_size.restype = sz
             lib.mla_latent_decode.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp, sz, vp]
@@ -139,11 +143,20 @@ def _stream_ptr(stream, device):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=None, stream=None):
+def mla_absorbed_attn_fwd_workspace_size(B: int, T: int, H: int, d_q: int, d_v: int, r: int, dtype) -> int:
+    """Bytes of workspace mla_absorbed_attn_fwd needs (0 when none)."""
+    torch = _torch()
+    code = dtype if isinstance(dtype, int) else (DTYPE_BF16 if dtype == torch.bfloat16 else
+                                                 DTYPE_F32 if dtype == torch.float32 else -1)
+    return int(library().mla_absorbed_attn_fwd_workspace_size(B, T, H, d_q, d_v, r, code))
+
+
+def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=None, workspace=None, stream=None):
     """Causal absorbed Gated-MLA prefill; returns out [B,T,H*d_v] (allocated if not given).
 
     q [B,T,H,d_q], c [B,T,r], w_uk [H,d_q,r], w_uv [H,d_v,r], gate [B,T,H*d_v]
     (pre-sigmoid logits) or None; all CUDA, contiguous, one dtype (bf16/fp32).
+    A workspace (uint8 CUDA tensor) is allocated when the call needs one and none is given.
     """
     torch = _torch()
     B, T, H, d_q = q.shape
@@ -159,9 +172,15 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
     if out is None:
         out = torch.empty((B, T, H * d_v), dtype=dt, device=dev)
     _check(out, "out", dt, dev, (B, T, H * d_v))
-    rc = library().mla_absorbed_attn_fwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(),
-                                         None if gate is None else gate.data_ptr(), float(scale), out.data_ptr(),
-                                         B, T, H, d_q, d_v, r, _dtype_code(q), _stream_ptr(stream, dev))
+    lib = library()
+    need = int(lib.mla_absorbed_attn_fwd_workspace_size(B, T, H, d_q, d_v, r, _dtype_code(q)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_absorbed_attn_fwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(),
+                                   None if gate is None else gate.data_ptr(), float(scale), out.data_ptr(),
+                                   B, T, H, d_q, d_v, r, _dtype_code(q), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_absorbed_attn_fwd")
     return out

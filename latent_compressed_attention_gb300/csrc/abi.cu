@@ -111,9 +111,16 @@ MLA_API int mla_version(void) { return 100; }
 
 MLA_API unsigned long long mla_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+MLA_API size_t mla_absorbed_attn_fwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype) {
+    if ((dtype != MLA_DTYPE_F32 && dtype != MLA_DTYPE_BF16) || B < 0 || T < 0 || H <= 0) return 0;
+    if (static_cast<long long>(B) * T > INT_MAX || !mul_fits(static_cast<long long>(B) * T, r, LLONG_MAX / 8)) return 0;
+    return prefill_workspace_bytes(B, T, r, d_q, d_v, dtype == MLA_DTYPE_F32);
+}
+
 MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
                                   const void *gate, float scale, void *out, int B, int T, int H, int d_q,
-                                  int d_v, int r, int dtype, void *stream) {
+                                  int d_v, int r, int dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
     if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
     if (B < 0 || T < 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0) return MLA_ERR_SHAPE;
     const long long rows = static_cast<long long>(B) * T;
@@ -129,10 +136,14 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
                               : (prefill_bf16_r512_supports(r, d_q, d_v) || prefill_bf16_small_supports(r, d_q, d_v));
     if (!ok_shape || (f32 && T > kPrefillF32MaxT)) return MLA_ERR_UNSUPPORTED;
     if (rows == 0) return MLA_OK;
+    const size_t need = prefill_workspace_bytes(B, T, r, d_q, d_v, f32);
+    if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return MLA_ERR_ALIGN;
 
     DeviceInfo *dev = nullptr;
     if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
-    PrefillArgs a{q, c, w_uk, w_uv, gate, out, scale, B, T, H, d_q, d_v, r, dev->err_word, dev->num_sms};
+    PrefillArgs a{q, c, w_uk, w_uv, gate, out, scale, B, T, H, d_q, d_v, r, dev->err_word, dev->num_sms,
+                  workspace, workspace_bytes};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (f32)

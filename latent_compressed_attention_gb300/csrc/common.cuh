@@ -282,6 +282,11 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Arrive on a named barrier without waiting (the producer side of a producer/consumer pair of warpgroups).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Barrier over `nthreads` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool pred) {
     uint32_t out;
@@ -320,6 +325,13 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, i
            | (static_cast<uint32_t>(b_mn) << 16)      // B major
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor for kind::f16 with f16 A/B and fp32 accumulation.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4)                                  // D format: f32 (A and B format fields 0: f16)
+           | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16)
+           | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -443,6 +455,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Pack two fp32 into an f16x2 word (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 2^k for an integer k in [-126, 127], exactly.
+__host__ __device__ __forceinline__ float exp2_int(int k) {
+    union { uint32_t u; float f; } v;
+    v.u = static_cast<uint32_t>(k + 127) << 23;
+    return v.f;
+}
+
+// The power-of-two exponent e that brings a positive magnitude `a` into [2^13, 2^14) (a * 2^e), clamped to
+// [-60, 60]; 0 for a zero or non-finite magnitude.  Values scaled by it keep the full f16 precision with a
+// factor 4 of headroom below the f16 maximum.
+__device__ __forceinline__ int f16_range_exponent(float a) {
+    const uint32_t bits = __float_as_uint(a) & 0x7FFFFFFFu;
+    if (bits == 0u || bits >= 0x7F800000u) return 0;
+    const int E = static_cast<int>(bits >> 23) - 127;   // floor(log2 a) for normal a (-127 for subnormal a)
+    const int e = 13 - E;
+    return e < -60 ? -60 : (e > 60 ? 60 : e);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

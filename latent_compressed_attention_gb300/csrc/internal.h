@@ -15,6 +15,8 @@ struct PrefillArgs {
     int B, T, H, d_q, d_v, r;
     int *dev_err;  // device error word of the current device
     int num_sms;
+    void *workspace = nullptr;   // prefill_workspace_bytes() bytes (none for the fp32 and small-rank kernels)
+    size_t workspace_bytes = 0;
 };
 
 struct DecodeArgs {
@@ -52,6 +54,11 @@ constexpr long long kBackwardMaxT = 65535LL * 64;
 
 cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s);
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v);
+size_t prefill_bf16_r512_workspace_bytes(long long B, long long T);
+// Device workspace a prefill call of these sizes needs (0 for the kernels that need none).
+inline size_t prefill_workspace_bytes(long long B, long long T, int r, int d_q, int d_v, bool f32) {
+    return (!f32 && prefill_bf16_r512_supports(r, d_q, d_v)) ? prefill_bf16_r512_workspace_bytes(B, T) : 0;
+}
 
 cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s);
 

@@ -34,7 +34,7 @@ constexpr float kRmsEps = 1e-6f;
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t q, c, g, o, yq, ss, acc, end;
+    size_t q, c, g, o, yq, pre, ss, acc, end;
 };
 
 }  // namespace
@@ -65,7 +65,9 @@ Layout layout(long long M, int D, int H, int d_q, int d_v, int r, int r_q, size_
     L.g = L.c + align256(static_cast<size_t>(M) * r * es);
     L.o = L.g + align256(static_cast<size_t>(M) * H * d_v * es);
     L.yq = L.o + align256(static_cast<size_t>(M) * H * d_v * es);
-    L.ss = L.yq + align256(static_cast<size_t>(M) * r_q * es);
+    // the prefill's own workspace, sized for B = M sequences of one token: a bound for every B * T = M
+    L.pre = L.yq + align256(static_cast<size_t>(M) * r_q * es);
+    L.ss = L.pre + align256(prefill_workspace_bytes(M, 1, r, d_q, d_v, es == 4));
     L.acc = L.ss + align256(static_cast<size_t>(M) * sizeof(float));   // split-K scratch, right after ss
     size_t off[kLayerGemms + 1];
     L.end = L.acc + (es == 2 ? layer_split_plan(M, D, H, d_q, d_v, r, r_q, off) : 0);
@@ -211,7 +213,8 @@ cudaError_t launch_gated_layer(const LayerArgs &a, cudaStream_t s) {
             return e;
         if ((e = run(kGate, a.x, a.D, a.w_gate, g, Hv, a.D, kGemmPlain, 0.f)) != cudaSuccess) return e;
     }
-    PrefillArgs pa{q, c, a.w_kv_up, w_uv, g, o, a.scale, a.B, a.T, a.H, a.d_q, a.d_v, a.r, a.dev_err, a.num_sms};
+    PrefillArgs pa{q, c, a.w_kv_up, w_uv, g, o, a.scale, a.B, a.T, a.H, a.d_q, a.d_v, a.r, a.dev_err, a.num_sms,
+                   ws + L.pre, L.ss - L.pre};
     e = a.f32 ? launch_prefill_f32_simt(pa, s) : launch_prefill_bf16_r512(pa, s);
     if (e != cudaSuccess) return e;
     if (a.f32) return gemm_f32(o, a.w_o, a.y, M, a.D, Hv, s);

@@ -13,8 +13,9 @@
 // latent accumulator o_lat is 128 x 512 = all 512 TMEM columns of an SM, so
 // the tile runs on a cluster of two CTAs:
 //   rank 0, the score CTA: absorbs W_UK into q (tcgen05, fp32 in TMEM), packs
-//     q_abs * scale * log2(e) as bf16 into TMEM columns 0-255, where it is the
-//     A operand of S = q_abs c^T; S is double-buffered in columns 256-511.
+//     q_abs * scale * log2(e) as f16 into TMEM columns 0-255, where it is the
+//     A operand of S = q_abs c^T against an f16 copy of c (times a power of two
+//     per sequence); S sits in columns 256-511.
 //     Two warpgroups run the online softmax (64 columns of each row each; the
 //     row maximum is exchanged through smem).  P (bf16) and per-row (rescale
 //     factor, partial sums) are staged in double-buffered smem and shipped to
@@ -24,6 +25,17 @@
 //     more than 2^16), then divides by the row sum, projects with W_UV^T on
 //     the tensor cores and applies the sigmoid gate.
 // Each CTA loads its own c tiles (no multicast); both read them from L2.
+//
+// Precision of the score: a bf16 operand (8 significant bits) would put a
+// relative error of 2^-9 on every score, a few percent of the softmax weights
+// once scores spread over ~25 natural-log units.  The score product therefore
+// runs in f16 (11 significant bits) on both sides: latent_amax_kernel and
+// latent_f16_kernel convert c once per call into the workspace, each sequence
+// scaled by the power of two that brings its largest |c| into [2^13, 2^14);
+// f16 keeps 11 significant bits between 2^-14 and 2^15, so the score CTA
+// packs the query operand unscaled and only a row whose largest element is
+// outside [2^-10, 2^15) (recomputed on a rare slow path) gets a power of two.  The powers of two are folded back
+// into the softmax's one FMA per score (exp2(s * F - m)): exact and free.  The value product keeps the bf16 latent and bf16 weights P.
 // Every wait is bounded; a CTA that gives up records an error, stops issuing
 // work and still meets its partner at the final cluster barrier.
 #include <cuda.h>
@@ -53,6 +65,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Keep a stale row maximum until the new one exceeds it by this (log2 units):
 // p <= 2^16, far inside the fp32 range of the row sums and the accumulator.
 constexpr float kRescaleLog2 = 16.0f;
+// Range of a row's largest |x| in which the score operand is packed as f16 directly: below 2^15 nothing
+// overflows, and from 2^-10 up the large elements keep f16's 11 significant bits (the elements that fall into
+// f16's subnormals are 2^-4 or less of the largest and err by 2^-25 at most).  A row outside it (other than an
+// all-zero row) is recomputed times a power of two.
+constexpr float kF16Limit = 32768.0f, kF16Floor = 0.0009765625f;
 
 constexpr uint32_t kSlab = 16384;  // [128 rows x 64 bf16] with 128-byte swizzle
 // score CTA
@@ -71,17 +88,18 @@ constexpr uint32_t O_P = kOStages * kOStage;         // 2 P tiles (also the epil
 constexpr uint32_t O_ROWINFO = O_P + 2 * kPBytes;    // 2 row-info blocks
 constexpr uint32_t BARS = S_PST + 2 * kPUnit;
 constexpr uint32_t PMAX = BARS + 512;                // [2 parities][2 warpgroups][128 rows] partial maxima
-constexpr uint32_t kSmemUsed = PMAX + 2 * 2 * kBM * 4;
+constexpr uint32_t QMAX = PMAX + 2 * 2 * kBM * 4;    // [2 warpgroups][128 rows] half-row maxima of |x|
+constexpr uint32_t kSmemUsed = QMAX + 2 * kBM * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 // TMEM columns of the score CTA
-constexpr uint32_t S_QCOL = 0;     // packed bf16 q_abs: K step ks (16 latent columns) at columns 8 ks .. 8 ks + 7
+constexpr uint32_t S_QCOL = 0;     // packed f16 q_abs: K step ks (16 latent columns) at columns 8 ks .. 8 ks + 7
 constexpr uint32_t S_SCOL = 256;   // S for one 256-key block
 static_assert(O_ROWINFO + 2 * kRowInfoBytes <= BARS, "value-CTA layout overlaps the barriers");
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit");
 static_assert(S_PST % 1024 == 0 && (S_PST + kPUnit) % 1024 == 0 && O_P % 1024 == 0, "alignment");
 
 constexpr uint32_t kIdescAbsorb = make_idesc_bf16(128, 256, 0, 1);  // q (K-major) x W_UK (MN-major)
-constexpr uint32_t kIdescQK = make_idesc_bf16(128, 256, 0, 0);      // q_abs (TMEM) x c (K-major), 256 keys
+constexpr uint32_t kIdescQK = make_idesc_f16(128, 256, 0, 0);       // f16 q_abs (TMEM) x f16 c (K-major), 256 keys
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);      // P (K-major) x c (MN-major)
 constexpr uint32_t kIdescEp = make_idesc_bf16(128, 128, 0, 0);      // o_lat (K-major) x W_UV (K-major)
 
@@ -124,6 +142,8 @@ __device__ long long g_ptl[kTLEvents][kTLMax];
 struct Params {
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
+    const float *sscale;   // [B]: 2^-e_b, the scale of sequence b's f16 latent copy
+    const __nv_bfloat16 *w_uk;   // [H, d_q, r], read only by the rare recompute of a row beyond f16's range
     int *err;
     int T, H, n_qtiles, bh_count;
     int n_tiles;   // n_qtiles * bh_count work tiles, numbered heaviest first
@@ -156,6 +176,11 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+__device__ __forceinline__ float ld_shared_bf16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+    return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
 __device__ __forceinline__ float2 ld_shared_v2f(uint32_t addr) {
     float2 v;
@@ -518,11 +543,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const int t = ti.t0 + row;
                     fail = fail || !mbar_wait(B_(bars->absorb_done), k & 1, p.err, abort_flag);
                     if (named_bar_or(1, 256, fail)) { ok = false; break; }
+                    // the score operand x = q_abs * scale * log2(e) is packed as f16 pairs by warpgroup 0: chunk kc
+                    // (fp32 columns 64kc .. 64kc+63) lands in columns 32kc .. 32kc+31, which this thread has already
+                    // read, so the compaction is in place, chunk by chunk in increasing order.  The thread tracks
+                    // its row's largest |x|; a row whose largest |x| is outside [2^-10, 2^15) is recomputed below.
+                    tc_fence_after();
+                    float amax = 0.f;
                     if (wg == 0) {
-                        // q_abs (fp32, TMEM columns 0-511) -> q_abs * scale * log2(e) packed as bf16 pairs into
-                        // columns 0-255; chunk k (64 latent columns) lands in 32k..32k+31, which this thread has
-                        // already read, so the compaction is in place, chunk by chunk in increasing order
-                        tc_fence_after();
     #pragma unroll 1
                         for (int kc = 0; kc < kR / 64; ++kc) {
                             float v[2][32], w[32];
@@ -530,15 +557,65 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tmem_ld32(trow + kc * 64 + 32, v[1]);
                             tmem_wait_ld();
     #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                w[i] = __uint_as_float(pack_bf16x2(v[i >> 4][2 * (i & 15)] * p.qk_scale_log2,
-                                                                   v[i >> 4][2 * (i & 15) + 1] * p.qk_scale_log2));
+                            for (int q = 0; q < 32; ++q) {
+                                const float x0 = v[q >> 4][2 * (q & 15)] * p.qk_scale_log2;
+                                const float x1 = v[q >> 4][2 * (q & 15) + 1] * p.qk_scale_log2;
+                                amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
+                                w[q] = __uint_as_float(pack_f16x2(x0, x1));
+                            }
                             tmem_st32(trow + S_QCOL + kc * 32, w);
                             tmem_wait_st();
                         }
-                        tc_fence_before();
                     }
-                    named_bar_sync(1, 256);
+                    st_shared_f32(base + QMAX + wg * kBM * 4 + row * 4, amax);
+                    tc_fence_before();
+                    int e_row = 0;
+                    if (named_bar_or(1, 256, amax >= kF16Limit || (amax > 0.f && amax < kF16Floor))) {
+                        // rare: some row's largest |x| is outside [2^-10, 2^15).  Every warp recomputes its rows' x
+                        // from the q tile and
+                        // W_UK (fp32 SIMT), times 2^e_row (0 for rows inside the range), and stores this warpgroup's
+                        // half of the packed row (tcgen05.st is warp-collective)
+                        const float xmax =
+                            fmaxf(ld_shared_f32(base + QMAX + row * 4), ld_shared_f32(base + QMAX + kBM * 4 + row * 4));
+                        e_row = (xmax >= kF16Limit || xmax < kF16Floor) ? f16_range_exponent(xmax) : 0;
+                        const float up = exp2_int(e_row);
+                        const __nv_bfloat16 *wk = p.w_uk + static_cast<size_t>(ti.h) * kD * kR + wg * 256;
+    #pragma unroll 1
+                        for (int jb = 0; jb < 8; ++jb) {
+                            float acc[32];
+    #pragma unroll
+                            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+    #pragma unroll 1
+                            for (int d = 0; d < kD; ++d) {
+                                const uint32_t qa = base + S_PST + (d >> 6) * kSlab + sw128_offset(row, (d & 63) >> 3) +
+                                                    (d & 7) * 2;
+                                const float qd = ld_shared_bf16(qa);
+                                const uint4 *w4 = reinterpret_cast<const uint4 *>(wk + static_cast<size_t>(d) * kR + jb * 32);
+    #pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const uint4 wv = __ldg(w4 + u);
+                                    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    #pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        acc[u * 8 + 2 * e] = fmaf(qd, __uint_as_float(ww[e] << 16), acc[u * 8 + 2 * e]);
+                                        acc[u * 8 + 2 * e + 1] = fmaf(qd, __uint_as_float(ww[e] & 0xFFFF0000u), acc[u * 8 + 2 * e + 1]);
+                                    }
+                                }
+                            }
+                            float pk[16];
+    #pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                pk[q] = __uint_as_float(pack_f16x2((acc[2 * q] * p.qk_scale_log2) * up,
+                                                                   (acc[2 * q + 1] * p.qk_scale_log2) * up));
+                            tc_fence_after();
+                            tmem_st16(trow + S_QCOL + wg * 128 + jb * 16, pk);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                        named_bar_sync(1, 256);
+                    }
+                    // the score in log2 units is the product times F = 2^-e_row * 2^-e_b (the latent copy's scale)
+                    const float F = exp2_int(-e_row) * __ldg(p.sscale + ti.b);
                     if (threadIdx.x == 128) mbar_arrive(B_(bars->qabs_ready));
                     TR(if (threadIdx.x == 128) { TR_ADD(TR_S_PROLOGUE, clock64() - t_start); TR_ADD(TR_TILES, 1);
                                                  TR_ADD(TR_BLOCKS, ti.nkv); })
@@ -565,7 +642,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     for (int i = 0; i < 32; ++i)
                                         if (c4 * 32 + i > lim) s[c4][i] = -INFINITY;
                             }
-                            st_shared_f32(base + PMAX + ((gb & 1) * 2 + wg) * kBM * 4 + row * 4, tree_max128(s));
+                            st_shared_f32(base + PMAX + ((gb & 1) * 2 + wg) * kBM * 4 + row * 4, tree_max128(s) * F);
                         }
                         TR(long long _x = clock64();)
                         if (named_bar_or(1, 256, fail)) { ok = false; break; }   // also publishes the partial maxima
@@ -580,7 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4)
     #pragma unroll
-                            for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(s[c4][i] - m_run);
+                            for (int i = 0; i < 32; ++i) s[c4][i] = fast_exp2(fmaf(s[c4][i], F, -m_run));
                         l_part = l_part * factor + tree_sum128(s);
 
                         TR(long long _s = clock64();)
@@ -754,12 +831,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cluster_sync_all();   // the partner no longer touches this CTA's shared memory
 }
 
+// The f16 copy of the latent for the score product, in two passes over c [B, T, 512] bf16 (one CTA per
+// 128-key group g of sequence b in each): latent_amax_kernel writes the group's largest |c| to gmax[b][g];
+// latent_f16_kernel takes the sequence's maximum over its groups, the power of two 2^e_b that brings it into
+// [2^13, 2^14), and writes c16 = c * 2^e_b (f16, round to nearest even) and sscale[b] = 2^-e_b.
+constexpr int kCvtThreads = 512;
+constexpr int kCvtChunks = kBM * kR / 8 / kCvtThreads;   // 16-byte chunks per thread
+
+__device__ __forceinline__ float block_max(float v, float *wmax) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = v;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kCvtThreads / 32; ++i) v = fmaxf(v, wmax[i]);
+    return v;
+}
+
+__global__ void __launch_bounds__(kCvtThreads) latent_amax_kernel(const uint4 *__restrict__ c, float *__restrict__ gmax,
+                                                                  int T, int n_groups) {
+    __shared__ float wmax[kCvtThreads / 32];
+    const int b = static_cast<int>(blockIdx.x) / n_groups, g = static_cast<int>(blockIdx.x) % n_groups;
+    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kBM) * (kR / 8);
+    const int n = min(kBM, T - g * kBM) * (kR / 8);
+    float amax = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < kCvtChunks; ++k) {
+        const int u = static_cast<int>(threadIdx.x) + k * kCvtThreads;
+        if (u < n) {
+            const uint4 v = __ldg(c + first + u);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+    }
+    amax = block_max(amax, wmax);
+    if (threadIdx.x == 0) gmax[blockIdx.x] = amax;
+}
+
+__global__ void __launch_bounds__(kCvtThreads) latent_f16_kernel(const uint4 *__restrict__ c, const float *__restrict__ gmax,
+                                                                 uint4 *__restrict__ c16, float *__restrict__ sscale,
+                                                                 int T, int n_groups) {
+    __shared__ float wmax[kCvtThreads / 32];
+    const int b = static_cast<int>(blockIdx.x) / n_groups, g = static_cast<int>(blockIdx.x) % n_groups;
+    float amax = 0.f;
+    for (int i = static_cast<int>(threadIdx.x); i < n_groups; i += kCvtThreads)
+        amax = fmaxf(amax, gmax[static_cast<size_t>(b) * n_groups + i]);
+    amax = block_max(amax, wmax);
+    const int e = f16_range_exponent(amax);
+    const float up = exp2_int(e);
+    if (g == 0 && threadIdx.x == 0) sscale[b] = exp2_int(-e);
+    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kBM) * (kR / 8);
+    const int n = min(kBM, T - g * kBM) * (kR / 8);
+#pragma unroll 8
+    for (int k = 0; k < kCvtChunks; ++k) {
+        const int u = static_cast<int>(threadIdx.x) + k * kCvtThreads;
+        if (u < n) {
+            const uint4 v = __ldg(c + first + u);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                o[i] = pack_f16x2(__uint_as_float(w[i] << 16) * up, __uint_as_float(w[i] & 0xFFFF0000u) * up);
+            c16[first + u] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
 CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                    const cuuint32_t *box) {
+                    const cuuint32_t *box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
     if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, es,
+    return fn(m, type, rank, const_cast<void *>(ptr), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -767,6 +912,13 @@ CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t 
 }  // namespace
 
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v) { return r == kR && d_q == kD && d_v == kD; }
+
+// Workspace of the r = 512 prefill: the f16 latent copy [B, T, 512], the group maxima [B][ceil(T / 128)] and
+// the sequence scales [B].
+size_t prefill_bf16_r512_workspace_bytes(long long B, long long T) {
+    const size_t c16 = (static_cast<size_t>(B) * T * kR * 2 + 255) & ~static_cast<size_t>(255);
+    return c16 + static_cast<size_t>(B) * ((T + kBM - 1) / kBM + 1) * sizeof(float);
+}
 
 #ifdef MLA_TRACE
 // Diagnostic build only: copy (and optionally clear) the wait-accounting slots.
@@ -789,7 +941,13 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_prefill_timeline
 
 cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_bf16_r512_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
+    if (!a.workspace || a.workspace_bytes < prefill_bf16_r512_workspace_bytes(a.B, a.T)) return cudaErrorInvalidValue;
     const cuuint64_t B = a.B, T = a.T, H = a.H;
+    const int n_groups = (a.T + kBM - 1) / kBM;
+    void *c16 = a.workspace;
+    float *gmax = reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
+                                            ((static_cast<size_t>(a.B) * a.T * kR * 2 + 255) & ~static_cast<size_t>(255)));
+    float *sscale = gmax + static_cast<size_t>(a.B) * n_groups;
     CUtensorMap tm_q, tm_c, tm_c256, tm_wuk, tm_wuv;
     {
         const cuuint64_t dims[4] = {kD, H, T, B};
@@ -803,7 +961,8 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
         const cuuint32_t box[3] = {64, kBN, 1};
         if (encode_map(&tm_c, a.c, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
         const cuuint32_t box256[3] = {64, kBS, 1};
-        if (encode_map(&tm_c256, a.c, 3, dims, strides, box256) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        if (encode_map(&tm_c256, c16, 3, dims, strides, box256, CU_TENSOR_MAP_DATA_TYPE_FLOAT16) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[2] = {kR, H * kD};
@@ -815,6 +974,8 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     Params p;
     p.gate = static_cast<const __nv_bfloat16 *>(a.gate);
     p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.sscale = sscale;
+    p.w_uk = static_cast<const __nv_bfloat16 *>(a.w_uk);
     p.err = a.dev_err;
     p.T = a.T;
     p.H = a.H;
@@ -836,6 +997,14 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
+    note_launch();
+    latent_amax_kernel<<<static_cast<unsigned>(a.B * n_groups), kCvtThreads, 0, s>>>(
+        static_cast<const uint4 *>(a.c), gmax, a.T, n_groups);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    note_launch();
+    latent_f16_kernel<<<static_cast<unsigned>(a.B * n_groups), kCvtThreads, 0, s>>>(
+        static_cast<const uint4 *>(a.c), gmax, static_cast<uint4 *>(c16), sscale, a.T, n_groups);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     note_launch();
     prefill_r512_kernel<<<static_cast<unsigned>(2 * p.G), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk,
                                                                                     tm_wuv, p);

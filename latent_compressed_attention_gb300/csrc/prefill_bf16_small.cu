@@ -12,6 +12,13 @@
 // owns 64 keys of a block; the row maximum and the row sums are exchanged
 // through shared memory), with tree reductions to keep dependency chains short.
 //
+// The score operand q_abs * scale * log2(e) is rounded to a pair of bf16 values
+// (hi + lo, about 16 significant bits): one bf16 rounding alone puts a relative
+// error of 2^-9 on every score, which at a score spread of ~25 natural-log
+// units moves the softmax weights by a few percent.  hi sits in the q tile, lo
+// in spare TMEM columns, and S = hi . c^T + lo . c^T; at r = 32 the four K
+// steps of one 64-column product are exactly the two of hi and the two of lo.
+//
 // Narrow rows (r = 32: 64 bytes; d = 16: 32 bytes) are widened to the 128-byte
 // swizzled layout by TMA's zero fill past the tensor's inner extent: every
 // operand is a [rows x 64] bf16 tile, the padding columns are zero, and they
@@ -45,7 +52,9 @@ constexpr uint32_t LSUM = PMAX + 2 * 2 * kBM * 4;   // [2 groups][128 rows] part
 constexpr uint32_t kSmemBytes = LSUM + 2 * kBM * 4 + 1024;   // + alignment slack
 static_assert(RING % 1024 == 0 && PT % 1024 == 0, "alignment");
 
-constexpr uint32_t S_COL = 0, O_COL = 128;
+// TMEM columns: S (128 keys), o_lat (the absorb's output first), and the low bf16 part of the score operand
+// (packed pairs, r / 2 columns)
+constexpr uint32_t S_COL = 0, O_COL = 128, LO_COL = 192;
 
 struct Bars {
     uint64_t pro_full, absorb_done, qabs_ready;
@@ -100,7 +109,7 @@ struct Params {
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
     int *err;
-    int T, H, d_q, d_v, n_qtiles, bh_count;
+    int T, H, d_q, d_v, r, n_qtiles, bh_count;
     float qk_scale_log2;
 };
 
@@ -186,14 +195,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = mbar_wait(B_(bars->qabs_ready), 0, p.err, abort_flag);
         }
         // S(j + 1) is issued as soon as the softmax has read S(j) out of TMEM, so the next block's scores are
-        // ready when the softmax finishes block j; then P(j) . c(j)
+        // ready when the softmax finishes block j; then P(j) . c(j).  The score operand is the pair hi + lo
+        // (hi from the q tile, lo from TMEM): S = hi . c^T + lo . c^T, over the r latent columns only.
+        const int ksteps = p.r / 16;
         auto issue_scores = [&](int j) {
             const int st = j % kStages;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < ksteps; ++kk)
                 umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
                           make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, kk > 0);
+            for (int kk = 0; kk < ksteps; ++kk)
+                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + kk * 8,
+                                 make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, 1);
             umma_commit(B_(bars->s_full));
         };
         if (ok && (ok = mbar_wait(B_(bars->c_full[0]), 0, p.err, abort_flag))) issue_scores(0);
@@ -234,12 +247,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         const bool leader = threadIdx.x == 64;   // arrives on the barriers the MMA warp waits for
         bool fail = !mbar_wait(B_(bars->absorb_done), 0, p.err, abort_flag);
         bool ok = !named_bar_or(1, kMath, fail);
-        if (ok) {   // q_abs (fp32 TMEM) -> q_abs * scale * log2(e), bf16, into the q tile
+        if (ok) {   // q_abs (fp32 TMEM) -> x = q_abs * scale * log2(e) as hi = bf16(x) into the q tile and
+                    // lo = bf16(x - hi) packed into TMEM: the score operand keeps about 16 significant bits
             tc_fence_after();
-            float v[32];
+            float v[32], lo[16];
             tmem_ld32(trow + O_COL + g * 32, v);
             tmem_wait_ld();
-            store_row32_bf16(base + QT, kTile, row, g, v, p.qk_scale_log2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float x0 = v[2 * i] * p.qk_scale_log2, x1 = v[2 * i + 1] * p.qk_scale_log2;
+                const uint32_t hw = pack_bf16x2(x0, x1);
+                lo[i] = __uint_as_float(pack_bf16x2(x0 - __uint_as_float(hw << 16), x1 - __uint_as_float(hw & 0xFFFF0000u)));
+                v[2 * i] = x0;
+                v[2 * i + 1] = x1;
+            }
+            store_row32_bf16(base + QT, kTile, row, g, v, 1.f);
+            tmem_st16(trow + LO_COL + g * 16, lo);
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
         }
@@ -413,6 +437,7 @@ cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s) {
     p.H = a.H;
     p.d_q = a.d_q;
     p.d_v = a.d_v;
+    p.r = a.r;
     p.n_qtiles = (a.T + kBM - 1) / kBM;
     p.bh_count = a.B * a.H;
     p.qk_scale_log2 = a.scale * kLog2e;

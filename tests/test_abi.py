@@ -48,8 +48,28 @@ def test_status_strings(lib):
 
 
 def prefill(lib, q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=None, out=FAKE, B=1, T=16, H=2, dq=16, dv=16, r=32,
-            dtype=F32):
-    return lib.mla_absorbed_attn_fwd(q, c, wuk, wuv, gate, 1.0, out, B, T, H, dq, dv, r, dtype, None)
+            dtype=F32, ws=None, ws_bytes=0):
+    return lib.mla_absorbed_attn_fwd(q, c, wuk, wuv, gate, 1.0, out, B, T, H, dq, dv, r, dtype, ws, ws_bytes, None)
+
+
+def test_prefill_workspace_sizes(lib):
+    """Only the r = 512 kernel needs a workspace: an f16 copy of c (2 bytes per latent value), one maximum
+    per 128 keys of each sequence and one scale per sequence."""
+    assert lib.mla_absorbed_attn_fwd_workspace_size(2, 100, 4, 16, 16, 32, F32) == 0
+    assert lib.mla_absorbed_attn_fwd_workspace_size(2, 100, 4, 16, 16, 32, BF16) == 0
+    B, T = 3, 300
+    need = lib.mla_absorbed_attn_fwd_workspace_size(B, T, 16, 128, 128, 512, BF16)
+    c16 = (B * T * 512 * 2 + 255) // 256 * 256
+    assert need == c16 + B * (3 + 1) * 4
+    assert lib.mla_absorbed_attn_fwd_workspace_size(B, T, 16, 128, 128, 512, 9) == 0
+
+
+def test_prefill_r512_needs_its_workspace(lib):
+    kw = dict(dtype=BF16, r=512, dq=128, dv=128, T=256)
+    need = lib.mla_absorbed_attn_fwd_workspace_size(1, 256, 2, 128, 128, 512, BF16)
+    assert prefill(lib, **kw) == ERR_WORKSPACE
+    assert prefill(lib, ws=FAKE, ws_bytes=need - 1, **kw) == ERR_WORKSPACE
+    assert prefill(lib, ws=FAKE + 8, ws_bytes=need, **kw) == ERR_ALIGN
 
 
 @pytest.mark.parametrize("field", ["q", "c", "wuk", "wuv", "out"])

@@ -79,13 +79,58 @@ def test_r512_no_gate(env):
 def test_r512_peaky_attention(env, wuk_std):
     """Larger q and W_UK spread the scores (std about 5 and 10 in natural-log
     units): attention is peaky, exercising the mask, the lazy rescale of the
-    latent accumulator and the online maximum.  The bf16 rounding of q_abs
-    bounds the accuracy: its score error grows with the spread (about
-    2^-9/sqrt(3) * |q_abs| * rms(c)), so the spread stays where the bf16 bar holds."""
+    latent accumulator and the online maximum."""
     _, _, oracle = env
     d = r512(1, 700, 2, seed=11, wuk_std=wuk_std, q_std=1.0)
     got = run_prefill(env, d, 1.0).reshape(1, 700, -1)
     ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def score_std(d, scale, n=64, seed=0):
+    """Standard deviation of the causal scores scale * q_abs . c over a sample of rows (natural-log units)."""
+    rng = np.random.default_rng(seed)
+    B, T, H, _ = d["q"].shape
+    vals = []
+    for _ in range(n):
+        b, t, h = rng.integers(B), rng.integers(1, T), rng.integers(H)
+        qa = d["q"][b, t, h] @ d["w_uk"][h]
+        vals.append(scale * (d["c"][b, : t + 1] @ qa))
+    return float(np.std(np.concatenate(vals)))
+
+
+def test_r512_stress_wide_scores(env):
+    """Scores spread over about 30 natural-log units (q ~ N(0,1), W_UK ~ N(0, 0.12^2), scale 1): nearly one-hot
+    attention.  With a bf16 score operand the error here was about 3e-2 of max|o|; the f16 operand with its
+    row and sequence powers of two keeps it well inside the bar."""
+    _, _, oracle = env
+    d = r512(1, 1024, 2, seed=13, wuk_std=0.12, q_std=1.0)
+    assert score_std(d, 1.0) >= 25.0
+    got = run_prefill(env, d, 1.0).reshape(1, 1024, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("c_mul,q_mul", [(2.0**17, 1.0), (2.0**-16, 1.0), (1.0, 2.0**12), (1.0, 2.0**-14),
+                                         (2.0**-14, 2.0**14)])
+def test_r512_latent_and_query_far_from_unit_scale(env, c_mul, q_mul):
+    """The f16 score operand covers bf16's range.  A latent beyond f16's largest value (2^17) or deep in its
+    subnormals (2^-16) is rescaled by an exact power of two per sequence; the scale argument that keeps the
+    scores moderate then puts the query operand near 1e-5 or past 2^15, and queries scaled by 2^14 with scale 1
+    put it past 2^15 too: those rows are recomputed times a power of two.  Queries scaled by 2^12 or 2^-14 stay
+    inside f16's range once the scale applies."""
+    _, _, oracle = env
+    d = r512(1, 300, 2, seed=17, wuk_std=0.04, q_std=1.0)
+    d = dict(d)
+    d["c"] = d["c"] * c_mul
+    d["q"] = d["q"] * q_mul
+    scale = 1.0 / (c_mul * q_mul) if c_mul * q_mul != 1.0 else 1.0
+    if c_mul != 1.0 and q_mul != 1.0:
+        x = np.abs(np.einsum("bthd,hdj->bthj", d["q"], d["w_uk"])) * scale * np.log2(np.e)
+        assert x.max() >= 2.0**15   # the query operand does leave f16's range
+    got = run_prefill(env, d, scale).reshape(1, 300, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale)
+    assert np.all(np.isfinite(got))
     assert rel_err(got, ref) <= TOL_BF16
 
 
@@ -164,6 +209,19 @@ def test_small_rank_peaky(env):
     _, _, oracle = env
     d = small_case(2, 600, 2, seed=21, wuk_std=0.3)
     got = run_prefill(env, d, 1.0).reshape(2, 600, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
+def test_small_rank_stress_unit_weights(env):
+    """The stress case with unit weights: the toy long-context shape (B=4, T=2048, H=8, d=16, r=32) with
+    W_UK ~ N(0,1) and scale 1, q ~ N(0,1): scores spread over about 23 natural-log units, nearly one-hot
+    attention.  The score operand's hi + lo bf16 split keeps the error far inside the bar."""
+    _, _, oracle = env
+    w = W.TOY_LONG_BF16
+    d = W.draw_prefill_direct(w, seed=0, wuk_std=1.0)
+    assert score_std(d, 1.0) >= 20.0
+    got = run_prefill(env, d, 1.0).reshape(w.B, w.T, -1)
     ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0)
     assert rel_err(got, ref) <= TOL_BF16
 
