@@ -259,6 +259,7 @@ def run_ours(args):
     toy = run_toy_layer(torch, lca, dev, stream, flush, args) if not args.no_small else None
     toy_bwd = run_toy_backward(torch, lca, dev, stream, flush, args) if not args.no_small else None
     small_bwd = run_toy_backward(torch, lca, dev, stream, flush, args, W.TOY_LONG_BF16) if not args.no_small else None
+    mid_bwd = run_backward_r512(torch, lca, dev, stream, flush, args, pk) if not args.no_bwd else None
     if lca.mla_get_device_error() != 0:
         raise RuntimeError("device error word set after the timed region")
 
@@ -287,7 +288,7 @@ def run_ours(args):
         }
         sections = [("mid_prefill", mid), ("decode", decode), ("layer", layer_line), ("layer_decode", layer_dec),
                     ("small_prefill", small), ("toy_layer", toy), ("toy_backward", toy_bwd),
-                    ("small_backward", small_bwd)]
+                    ("small_backward", small_bwd), ("mid_backward", mid_bwd)]
         for name, sec in sections:
             if sec is not None:
                 line[name] = sec
@@ -314,6 +315,9 @@ def summary(line, sections):
     for name, sec in sections:
         if sec is not None:
             out[name] = brief(sec)
+            if name == "decode" and sec.get("fp8"):
+                out["decode_fp8"] = brief(sec["fp8"])
+                out["decode_rows_per_s"] = {"bf16": sec.get("rows_per_s"), "fp8": sec["fp8"].get("rows_per_s")}
     if "cpu_baseline" in line:
         out["cpu_oracle_tflops"] = line["cpu_baseline"]["value"]
     return out
@@ -416,12 +420,44 @@ def run_decode(torch, lca, dev, stream, flush, args, pk):
     ms = statistics.mean(times)
     cache_bytes = int(d["lens_np"].astype(np.int64).sum()) * DECODE.r * 2
     gbs = cache_bytes / (ms * 1e-3) / 1e9
+    fp8 = run_decode_fp8(torch, lca, dev, stream, flush, args, pk, d) if not args.no_fp8 else None
     return {"workload": DECODE.name, "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
-            "cache_bytes_per_step": cache_bytes, "sum_lens": int(d["lens_np"].sum()),
+            "rows_per_s": round(int(d["lens_np"].sum()) / (ms * 1e-3), 1),
+            "cache_bytes_per_step": cache_bytes, "sum_lens": int(d["lens_np"].sum()), "fp8": fp8,
             "roofline": {"kernel": "decode (pair + merge)", "bound": "hbm", "achieved": round(gbs, 1),
                          "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "peak_source": pk["source"],
                          "traffic": committed_traffic("decode", DECODE_SRC)},
+            "gpu_launches": launches}
+
+
+FP8_CACHE_SCALE = 0.0625   # RMSNorm rows (|c| <= sqrt(512)) map inside e4m3's +-448
+
+
+def run_decode_fp8(torch, lca, dev, stream, flush, args, pk, d):
+    """The decode workload over the same cache stored as e4m3 (quantised once, outside the timed region):
+    half the bytes per cached token."""
+    c8 = lca.mla_quantize_latent_fp8(d["cache"], FP8_CACHE_SCALE)
+    ws = torch.empty(lca.library().mla_latent_decode_fp8_workspace_size(DECODE.B, DECODE.H, DECODE.r,
+                                                                        DECODE.max_len), dtype=torch.uint8, device=dev)
+    out = torch.empty((DECODE.B, DECODE.H * DECODE.d_v), dtype=torch.bfloat16, device=dev)
+    step = lambda: lca.mla_latent_decode_fp8(d["q_abs"], c8, d["lens"], d["w_uv"], FP8_CACHE_SCALE, None,  # noqa: E731
+                                             DECODE.scale, out=out, workspace=ws)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    del c8
+    ms = statistics.mean(times)
+    sum_lens = int(d["lens_np"].astype(np.int64).sum())
+    cache_bytes = sum_lens * DECODE.r
+    gbs = cache_bytes / (ms * 1e-3) / 1e9
+    return {"workload": DECODE.name.replace("bf16", "fp8"), "value": round(gbs, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "rows_per_s": round(sum_lens / (ms * 1e-3), 1),
+            "cache_bytes_per_step": cache_bytes, "cache_scale": FP8_CACHE_SCALE,
+            "roofline": {"kernel": "decode over the e4m3 cache (query split, pair + merge)", "bound": "hbm",
+                         "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / pk["hbm_gbs"], 4), "peak_source": pk["source"], "traffic": None},
             "gpu_launches": launches}
 
 
@@ -628,6 +664,38 @@ def run_toy_backward(torch, lca, dev, stream, flush, args, w=None):
             "gpu_launches": launches}
 
 
+def run_backward_r512(torch, lca, dev, stream, flush, args, pk):
+    """Gradients of the attention at the mid-size prefill's shape (B=4, T=4096, H=16, r=512, d=128, bf16 inputs,
+    fp32 gradients) on the tensor cores: the forward recomputed with its row statistics, then the chain rule's
+    products as batched GEMMs over per-head attention matrices."""
+    w = W.MID_PREFILL_BF16
+    d = W.draw_prefill_direct(w, seed=0)
+    dout = W.round_bf16(np.random.default_rng(1).standard_normal((w.B, w.T, w.H * w.d_v)))
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
+    q, c, g, w_uk, w_uv, dout = (t(a) for a in (d["q"], d["c"], d["gate"], d["w_uk"], d["w_uv"], dout))
+    ws = torch.empty(lca.library().mla_absorbed_attn_bwd_workspace_size(w.B, w.T, w.H, w.d_q, w.d_v, w.r,
+                                                                        lca.DTYPE_BF16), dtype=torch.uint8, device=dev)
+    step = lambda: lca.mla_absorbed_attn_bwd(q, c, w_uk, w_uv, g, w.scale, dout, workspace=ws)  # noqa: E731
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    times, launches = timed_steps(torch, step, args.steps, flush, stream)
+    del ws
+    ms = statistics.mean(times)
+    fl = backward_flops(w)
+    tf = fl / (ms * 1e-3) / 1e12
+    return {"workload": "mid_backward_bf16", "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+            "flops_per_step": fl, "kernels_per_call": launches // max(args.steps, 1),
+            "config": {"B": w.B, "T": w.T, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "scale": w.scale,
+                       "inputs": "direct draws of the mid-size workload, dout ~ N(0,1), bf16",
+                       "dtype": "bf16 operands, fp32 accumulation and gradients", "l2": "flushed between steps"},
+            "roofline": {"kernel": "backward (forward recompute, gate, 10 batched tcgen05 GEMMs)", "bound": "tensor",
+                         "achieved": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": round(tf / pk["bf16_tflops"], 4), "peak_source": pk["source"] + " (burst bf16)",
+                         "traffic": None},
+            "gpu_launches": launches}
+
+
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
 def oracle_inputs():
     return W.draw_prefill_direct(PREFILL, seed=0)
@@ -708,6 +776,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-mid", action="store_true", help="skip the mid-size prefill section")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-cache decode")
+    ap.add_argument("--no-bwd", action="store_true", help="skip the r = 512 backward")
     ap.add_argument("--no-small", action="store_true", help="skip the small-rank prefill and the fp32 toy layer")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")

@@ -118,9 +118,19 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
  * `dtype` (MLA_DTYPE_F32 or MLA_DTYPE_BF16; bf16 values are widened to fp32).
  * workspace: >= mla_absorbed_attn_bwd_workspace_size(...) bytes, 16-byte
  * aligned (per-row q_abs, do_lat and softmax statistics between the kernels).
- * Supported: r, d_q, d_v <= 64 (the toy sizes) and T <= 4,194,240, fp32
- * arithmetic throughout; other shapes return MLA_ERR_UNSUPPORTED.  dc, dw_uk and dw_uv are sums over thread
- * blocks formed with atomics, so their last bits may differ between calls.
+ * Supported:
+ *  - r, d_q, d_v <= 64 (the toy sizes), F32 or BF16, T <= 4,194,240: fp32
+ *    arithmetic throughout (SIMT).  dc, dw_uk and dw_uv are sums over thread
+ *    blocks formed with atomics, so their last bits may differ between calls.
+ *  - BF16 with (r, d_q, d_v) = (512, 128, 128): tensor cores.  The call runs the
+ *    forward once more (its output before the gate and each row's softmax
+ *    statistics), then every product of the chain rule as a batched bf16 GEMM
+ *    with fp32 accumulation over per-head matrices kept in the workspace: the
+ *    attention matrix and its gradient ([T, T] per head, bf16, causal tiles
+ *    only), q_abs, do_lat, o_lat and dq_abs ([T, r] per head, bf16).  The
+ *    workspace is therefore O(B H T^2): about 2 B H T^2 + 9 B H T r bytes.
+ *    Deterministic (no atomics).
+ * Other shapes return MLA_ERR_UNSUPPORTED.
  * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
  */
 MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype);
@@ -169,6 +179,53 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
                               int max_len, const void *w_uv, const void *gate, float scale, void *out,
                               int B, int H, int d_v, int r, int dtype,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mla_latent_decode_fp8 - mla_latent_decode over a latent cache stored in
+ * 8-bit floating point (e4m3: 1 sign, 4 exponent, 3 mantissa bits; largest
+ * finite value 448), half the bytes per cached token of the bf16 cache.
+ *
+ * This carries the cache-size argument of the page "Gated MLA（矩阵吸收版）"
+ * (sections "标准 MHA 的 KV cache 问题" and "形状与参数对比": only r values per
+ * token are cached) one step further; the page itself caches bf16/fp32 c.
+ * The cache holds c / cache_scale: cache row u of sequence b dequantises to
+ * cache_scale * e4m3(c8_cache[b, u, :]), and the call computes exactly
+ * mla_latent_decode over those dequantised rows.
+ *
+ * Arguments as for mla_latent_decode, except:
+ *   c8_cache     e4m3 bytes; element (b,u,j) at byte b*max_len*ld_cache + u*ld_cache + j
+ *   ld_cache     row stride in bytes (>= r, multiple of 16)
+ *   cache_scale  positive, finite
+ *   q_abs, w_uv, gate, out  bf16 as in mla_latent_decode (there is no dtype argument)
+ *   workspace    >= mla_latent_decode_fp8_workspace_size(...) bytes, 16-byte
+ *                aligned, not used by any other call in flight
+ * Precision: both products run on the 8-bit tensor cores.  The query q_abs is
+ * split into two e4m3 parts (after a power-of-two scale per head) and so are
+ * the softmax weights, which keeps about 8 significant bits of each, as a
+ * bf16 operand would; the cache values themselves are exact.
+ * Supported: r = 512, d_v = 128, 1 <= H <= 96.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API size_t mla_latent_decode_fp8_workspace_size(int B, int H, int r, int max_len);
+MLA_API int mla_latent_decode_fp8(const void *q_abs, const void *c8_cache, long long ld_cache, const int *lens,
+                                  int max_len, float cache_scale, const void *w_uv, const void *gate, float scale,
+                                  void *out, int B, int H, int d_v, int r, void *workspace, size_t workspace_bytes,
+                                  void *stream);
+
+/*
+ * mla_quantize_latent_fp8 - fill an e4m3 latent cache from bf16 latent rows:
+ * c8[i, j] = e4m3(c[i, j] * (1 / cache_scale)), the product formed in fp32
+ * (1 / cache_scale rounded to fp32 first), rounded to the nearest e4m3 value
+ * (ties to even) and clamped to +-448.  Same section as mla_latent_decode_fp8.
+ *   c      bf16 [rows, r] with row stride ld_c elements (multiple of 8)
+ *   c8     bytes [rows, r] with row stride ld_c8 bytes (multiple of 16)
+ * r a multiple of 8; both pointers 16-byte aligned; rows == 0 is a no-op.
+ * Latent rows from RMSNorm with unit gain have |c| <= sqrt(r) (22.6 at
+ * r = 512), so cache_scale = 1/16 maps them inside e4m3's range.
+ * Returns MLA_OK or a negative mla_status_t; nothing is launched on error.
+ */
+MLA_API int mla_quantize_latent_fp8(const void *c, long long ld_c, void *c8, long long ld_c8, long long rows, int r,
+                                    float cache_scale, void *stream);
 
 /*
  * mla_latent_decode_noalloc - mla_latent_decode for callers that cannot

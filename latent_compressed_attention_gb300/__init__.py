@@ -11,6 +11,8 @@ Entry points (same names as the C functions):
     mla_absorbed_attn_fwd_workspace_size(B, T, H, d_q, d_v, r, dtype)
     mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale=1.0, out=None, workspace=None)
     mla_latent_decode_workspace_size(B, H, r, max_len)
+    mla_latent_decode_fp8(q_abs, c8_cache, lens, w_uv, cache_scale, gate=None, scale=1.0, out=None, workspace=None)
+    mla_quantize_latent_fp8(c, cache_scale, out=None)
     mla_get_device_error(stream=None)
 """
 from __future__ import annotations
@@ -23,7 +25,8 @@ from ._build import LIB_PATH, build
 
 __all__ = ["MLAError", "build", "library", "library_path", "mla_absorbed_attn_fwd",
            "mla_absorbed_attn_fwd_workspace_size", "mla_latent_decode",
-           "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_get_device_error",
+           "mla_latent_decode_workspace_size", "mla_latent_decode_noalloc", "mla_latent_decode_fp8",
+           "mla_quantize_latent_fp8", "mla_get_device_error",
            "mla_status_string", "mla_version", "mla_kernel_launches", "mla_debug_wait_timeout",
            "mla_absorbed_attn_bwd", "mla_gated_layer_fwd", "mla_gated_layer_workspace_size",
            "mla_gated_layer_decode", "layer_workspace_views", "DTYPE_BF16", "DTYPE_F32"]
@@ -63,6 +66,12 @@ def library():
             lib.mla_latent_decode_workspace_size.restype = sz
             lib.mla_latent_decode.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp, sz, vp]
             lib.mla_latent_decode.restype = i
+            lib.mla_latent_decode_fp8_workspace_size.argtypes = [i, i, i, i]
+            lib.mla_latent_decode_fp8_workspace_size.restype = sz
+            lib.mla_latent_decode_fp8.argtypes = [vp, vp, ll, vp, i, f, vp, vp, f, vp, i, i, i, i, vp, sz, vp]
+            lib.mla_latent_decode_fp8.restype = i
+            lib.mla_quantize_latent_fp8.argtypes = [vp, ll, vp, ll, ll, i, f, vp]
+            lib.mla_quantize_latent_fp8.restype = i
             lib.mla_latent_decode_noalloc.argtypes = [vp, vp, ll, vp, i, vp, vp, f, vp, i, i, i, i, i, vp]
             lib.mla_latent_decode_noalloc.restype = i
             lib.mla_gated_layer_workspace_size.argtypes = [i, i, i, i, i, i, i, i, i]
@@ -188,7 +197,8 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
 
 def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=None, stream=None) -> dict:
     """Gradients of sum(dout * mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate, scale)): a dict with dq, dc, dw_uk,
-    dw_uv and dgate (None without a gate), allocated here as fp32.  Inputs fp32 or bf16; r, d_q, d_v <= 64."""
+    dw_uv and dgate (None without a gate), allocated here as fp32.  Inputs fp32 or bf16 with r, d_q, d_v <= 64,
+    or bf16 with r = 512, d_q = d_v = 128 (tensor cores; the workspace is O(B H T^2))."""
     torch = _torch()
     B, T, H, d_q = q.shape
     r = c.shape[-1]
@@ -364,6 +374,69 @@ def mla_latent_decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0,
                                _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_latent_decode")
+    return out
+
+
+def _cache_layout(c_cache, B, r):
+    if c_cache.dim() != 3 or c_cache.shape[0] != B or c_cache.shape[2] != r or c_cache.stride(2) != 1 \
+            or c_cache.stride(0) != c_cache.shape[1] * c_cache.stride(1):
+        raise ValueError("cache must be [B,max_len,r] with unit inner stride and batch stride max_len*row_stride")
+    return c_cache.shape[1], c_cache.stride(1)
+
+
+def mla_latent_decode_fp8(q_abs, c8_cache, lens, w_uv, cache_scale: float, gate=None, scale: float = 1.0, out=None,
+                          workspace=None, stream=None):
+    """Decode over an e4m3 latent cache; returns out [B,H*d_v] (bf16).
+
+    c8_cache: uint8 [B,max_len,r] (or a row-strided view, row stride a multiple of 16 bytes) holding
+    e4m3(c / cache_scale), e.g. from mla_quantize_latent_fp8; q_abs [B,H,r], w_uv [H,d_v,r] and gate
+    [B,H*d_v] (or None) bf16; lens int32 [B].  A workspace is allocated when not given.
+    """
+    torch = _torch()
+    B, H, r = q_abs.shape
+    d_v = w_uv.shape[1]
+    dev = q_abs.device
+    _check(q_abs, "q_abs", torch.bfloat16, dev)
+    if c8_cache.dtype != torch.uint8 or c8_cache.device != dev:
+        raise TypeError("c8_cache must be a uint8 CUDA tensor on the query's device")
+    max_len, ld = _cache_layout(c8_cache, B, r)
+    _check(lens, "lens", torch.int32, dev, (B,))
+    _check(w_uv, "w_uv", torch.bfloat16, dev, (H, d_v, r))
+    if gate is not None:
+        _check(gate, "gate", torch.bfloat16, dev, (B, H * d_v))
+    if out is None:
+        out = torch.empty((B, H * d_v), dtype=torch.bfloat16, device=dev)
+    _check(out, "out", torch.bfloat16, dev, (B, H * d_v))
+    lib = library()
+    need = int(lib.mla_latent_decode_fp8_workspace_size(B, H, r, max_len))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = None if workspace is None else workspace.data_ptr()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.mla_latent_decode_fp8(q_abs.data_ptr(), c8_cache.data_ptr(), ld, lens.data_ptr(), max_len,
+                                   float(cache_scale), w_uv.data_ptr(), None if gate is None else gate.data_ptr(),
+                                   float(scale), out.data_ptr(), B, H, d_v, r, ws_ptr, ws_bytes,
+                                   _stream_ptr(stream, dev))
+    if rc != 0:
+        raise MLAError(rc, "mla_latent_decode_fp8")
+    return out
+
+
+def mla_quantize_latent_fp8(c, cache_scale: float, out=None, stream=None):
+    """e4m3 bytes of c / cache_scale: c bf16 [..., r] (rows contiguous) -> uint8 [..., r]."""
+    torch = _torch()
+    if c.dtype != torch.bfloat16 or not c.is_cuda or not c.is_contiguous():
+        raise ValueError("c must be a contiguous bf16 CUDA tensor")
+    r = c.shape[-1]
+    rows = c.numel() // max(r, 1)
+    if out is None:
+        out = torch.empty(c.shape, dtype=torch.uint8, device=c.device)
+    if out.dtype != torch.uint8 or tuple(out.shape) != tuple(c.shape) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor of c's shape")
+    rc = library().mla_quantize_latent_fp8(c.data_ptr(), r, out.data_ptr(), r, rows, r, float(cache_scale),
+                                           _stream_ptr(stream, c.device))
+    if rc != 0:
+        raise MLAError(rc, "mla_quantize_latent_fp8")
     return out
 
 

@@ -157,6 +157,11 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
 
 MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype) {
     if ((dtype != MLA_DTYPE_F32 && dtype != MLA_DTYPE_BF16) || B <= 0 || T <= 0 || H <= 0) return 0;
+    if (dtype == MLA_DTYPE_BF16 && backward_bf16_r512_supports(r, d_q, d_v)) {
+        if (static_cast<long long>(B) * T > INT_MAX || !mul_fits(static_cast<long long>(B) * H * T, T + 128LL, LLONG_MAX / 8))
+            return 0;
+        return backward_bf16_r512_workspace_bytes(B, T, H);
+    }
     if (!backward_f32_supports(r, d_q, d_v)) return 0;
     if (!mul_fits(static_cast<long long>(B) * T, static_cast<long long>(H) * (2 * r + 4), LLONG_MAX / 8)) return 0;
     return backward_f32_workspace_bytes(B, T, H, r);
@@ -178,6 +183,21 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
         !aligned16(dq) || !aligned16(dc) || !aligned16(dw_uk) || !aligned16(dw_uv) || (gate && !aligned16(gate)) ||
         (dgate && !aligned16(dgate)))
         return MLA_ERR_ALIGN;
+    const bool r512 = dtype == MLA_DTYPE_BF16 && backward_bf16_r512_supports(r, d_q, d_v);
+    if (r512) {
+        if (!mul_fits(rows * H, T + 128LL, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+        if (rows == 0) return MLA_OK;
+        if (!workspace) return MLA_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+        if (workspace_bytes < backward_bf16_r512_workspace_bytes(B, T, H)) return MLA_ERR_WORKSPACE;
+        DeviceInfo *dev = nullptr;
+        if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+        BackwardR512Args a{q, c, w_uk, w_uv, gate, dout, static_cast<float *>(dq), static_cast<float *>(dc),
+                           static_cast<float *>(dw_uk), static_cast<float *>(dw_uv), static_cast<float *>(dgate),
+                           scale, B, T, H, d_q, d_v, r, workspace, workspace_bytes, dev->err_word, dev->num_sms};
+        const cudaError_t e = launch_backward_bf16_r512(a, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    }
     if (!backward_f32_supports(r, d_q, d_v) || T > kBackwardMaxT) return MLA_ERR_UNSUPPORTED;
     if (rows == 0) return MLA_OK;
     if (!workspace) return MLA_ERR_WORKSPACE;
@@ -218,6 +238,54 @@ MLA_API int mla_latent_decode(const void *q_abs, const void *c_cache, long long 
     DecodeArgs a{q_abs, c_cache, w_uv, gate, lens, out, ld_cache, max_len, scale, B, H, d_v, r,
                  workspace, workspace_bytes, dev->err_word, dev->num_sms};
     const cudaError_t e = launch_decode_bf16(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API size_t mla_latent_decode_fp8_workspace_size(int B, int H, int r, int max_len) {
+    if (B <= 0 || H <= 0 || r <= 0 || max_len < 0) return 0;
+    if (!decode_bf16_supports(H, 128, r)) return 0;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return 0;
+    return decode_fp8_workspace_bytes(B, H, r, max_len, dev->num_sms);
+}
+
+MLA_API int mla_latent_decode_fp8(const void *q_abs, const void *c8_cache, long long ld_cache, const int *lens,
+                                  int max_len, float cache_scale, const void *w_uv, const void *gate, float scale,
+                                  void *out, int B, int H, int d_v, int r, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    if (B < 0 || H <= 0 || d_v <= 0 || r <= 0 || max_len < 0 || ld_cache < r) return MLA_ERR_SHAPE;
+    if (!(cache_scale > 0.f) || cache_scale > 3.0e38f) return MLA_ERR_SHAPE;   // positive and finite
+    if (!mul_fits(static_cast<long long>(B) * max_len, ld_cache, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (!q_abs || !c8_cache || !lens || !w_uv || !out) return MLA_ERR_NULL;
+    if (!aligned16(q_abs) || !aligned16(c8_cache) || !aligned16(w_uv) || !aligned16(out) || !aligned16(lens) ||
+        (gate && !aligned16(gate)) || (ld_cache % 16) != 0)
+        return MLA_ERR_ALIGN;
+    if (!decode_bf16_supports(H, d_v, r)) return MLA_ERR_UNSUPPORTED;
+    if (B == 0) return MLA_OK;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const size_t need = decode_fp8_workspace_bytes(B, H, r, max_len, dev->num_sms);
+    if (!workspace || workspace_bytes < need) return MLA_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+    DecodeArgs a{q_abs, c8_cache, w_uv, gate, lens, out, ld_cache, max_len, scale, B, H, d_v, r,
+                 workspace, workspace_bytes, dev->err_word, dev->num_sms, cache_scale};
+    const cudaError_t e = launch_decode_fp8(a, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+MLA_API int mla_quantize_latent_fp8(const void *c, long long ld_c, void *c8, long long ld_c8, long long rows, int r,
+                                    float cache_scale, void *stream) {
+    if (rows < 0 || r <= 0 || (r % 8) != 0 || ld_c < r || ld_c8 < r) return MLA_ERR_SHAPE;
+    if (!(cache_scale > 0.f) || cache_scale > 3.0e38f) return MLA_ERR_SHAPE;
+    if (!mul_fits(rows, ld_c, LLONG_MAX / 8) || !mul_fits(rows, ld_c8, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
+    if (rows == 0) return MLA_OK;
+    if (!c || !c8) return MLA_ERR_NULL;
+    if (!aligned16(c) || !aligned16(c8) || (ld_c % 8) != 0 || (ld_c8 % 16) != 0) return MLA_ERR_ALIGN;
+    DeviceInfo *dev = nullptr;
+    if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const float inv_scale = 1.0f / cache_scale;
+    const cudaError_t e = launch_quantize_latent_e4m3(c, ld_c, c8, ld_c8, rows, r, inv_scale,
+                                                      static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

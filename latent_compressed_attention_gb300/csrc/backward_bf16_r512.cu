@@ -1,0 +1,480 @@
+// Gradients of the absorbed Gated-MLA attention at r = 512, d_q = d_v = 128 on the sm_103a tensor cores.
+//
+// The page "Gated MLA（矩阵吸收版）" gives the forward only (section "完整计算流（四步）", steps 2-4); this is
+// the chain rule back through it, for L = sum(dout * out):
+//   sigma = sigmoid(g), do = dout * sigma, dgate = dout * o * sigma * (1 - sigma)   (step 4, o before the gate)
+//   do_lat = do . W_UV[h], dW_UV[h] = sum do^T o_lat                                 (step 3, W_UV)
+//   dA[t,u] = do_lat_t . c_u, delta_t = sum_u A dA = do_t . o_t                        (step 3, A . c)
+//   dS = A * (dA - delta) * scale                                                     (softmax, step 2)
+//   dq_abs = dS . c, dc += dS^T . q_abs + A^T . do_lat (summed over heads)            (step 2, both uses of c)
+//   dq = dq_abs . W_UK[h]^T, dW_UK[h] = sum q^T dq_abs                                (step 2, the absorb)
+//
+// Design: the forward kernel recomputes the output o (no gate) and each row's softmax statistics (m, l);
+// every product above is then one launch of a batched tcgen05 GEMM over materialised per-head matrices:
+// the attention matrix P and the score gradient dS ([T, T] per head, bf16, only the causal tiles written
+// or read), q_abs, do_lat, o_lat and dq_abs ([T, r] per head, bf16).  The GEMM takes each operand K-major
+// or MN-major through its own TMA tensor map, skips tiles above the diagonal, limits K to the causal range
+// of each tile, runs K over a second index (heads for dc, sequences for the weight gradients), and fuses
+// the softmax (P = exp2(S - m) / l) and the dS epilogues.  fp32 accumulation in TMEM; the gradients are
+// written in fp32, the intermediate matrices in bf16.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <initializer_list>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kR = 512, kD = 128;
+constexpr int kBM = 128, kBN = 128, kBK = 64;
+constexpr int kStages = 3;
+constexpr uint32_t kOpBytes = 128 * 128;            // an operand's stage: [128 x 64] K-major or 2 x [64 x 64] MN-major
+constexpr uint32_t kStageBytes = 2 * kOpBytes;
+constexpr uint32_t kBarOff = kStages * kStageBytes;
+constexpr uint32_t kSmem = kBarOff + 256 + 1024;    // two CTAs per SM
+constexpr int kThreads = 192;                       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue (thread = row)
+constexpr float kLog2e = 1.4426950408889634f;
+
+// The products of the backward.  Operand layouts: "K" = K-major (K contiguous), "MN" = M or N contiguous.
+enum Problem : int {
+    kQAbs = 0,   // q_abs[z]   = q[b,:,h,:] . W_UK[h]          M=T  N=r   K=d        A K   B MN   bf16 [z,T,r]
+    kDoLat,      // do_lat[z]  = do[z] . W_UV[h]                M=T  N=r   K=d_v      A K   B MN   bf16
+    kP,          // P[z]       = exp2(S - m) / l, S = q_abs.c^T  M=T  N=T   K=r        A K   B K    bf16 [z,T,Tp]
+    kDS,         // dS[z]      = scale P (do_lat . c^T - delta)  M=T  N=T   K=r        A K   B K    bf16
+    kOLat,       // o_lat[z]   = P . c                          M=T  N=r   K=u<=t     A K   B MN   bf16
+    kDqAbs,      // dq_abs[z]  = dS . c                         M=T  N=r   K=u<=t     A K   B MN   bf16
+    kDc,         // dc[b]      = sum_h P^T do_lat + dS^T q_abs   M=T  N=r   K=(h,t>=u) A MN  B MN   f32 [B,T,r]
+    kDq,         // dq[b,:,h,:] = dq_abs . W_UK[h]^T             M=T  N=d   K=r        A K   B K    f32 [B,T,H,d]
+    kDWuk,       // dW_UK[h]   = sum_b q^T . dq_abs             M=d  N=r   K=(b,t)    A MN  B MN   f32 [H,d,r]
+    kDWuv,       // dW_UV[h]   = sum_b do^T . o_lat             M=d_v N=r  K=(b,t)    A MN  B MN   f32 [H,d_v,r]
+};
+
+struct GemmP {
+    int problem;
+    int B, T, H, Tp;      // Tp: row stride of P and dS (T rounded up to 128)
+    int M, N;             // output extent of one batch item
+    float scale_log2;     // kP: softmax scale * log2(e)
+    float scale;          // kDS: softmax scale
+    const float *st_m, *st_l, *delta;   // [z, T]
+    const __nv_bfloat16 *p_in;          // kDS: P
+    void *out;
+    int *err;
+};
+
+__device__ __forceinline__ bool a_mn(int pr) { return pr == kDc || pr == kDWuk || pr == kDWuv; }
+__device__ __forceinline__ bool b_mn(int pr) { return pr == kQAbs || pr == kDoLat || pr == kOLat || pr == kDqAbs ||
+                                                      pr == kDc || pr == kDWuk || pr == kDWuv; }
+__device__ __forceinline__ bool causal_tiles(int pr) { return pr == kP || pr == kDS; }
+
+// The K walk of output tile (m0, z): `outer` runs over a second index (heads for dc, sequences for the weight
+// gradients), the inner K over [lo, hi) in steps of 64; dc takes two operand pairs per step.
+struct KWalk {
+    int outer, lo, hi, pairs;
+};
+__device__ __forceinline__ KWalk k_walk(const GemmP &p, int m0) {
+    switch (p.problem) {
+        case kQAbs: case kDoLat: return {1, 0, kD, 1};
+        case kP: case kDS: case kDq: return {1, 0, kR, 1};
+        case kOLat: case kDqAbs: return {1, 0, min(p.T, m0 + kBM), 1};           // u <= t
+        case kDc: return {p.H, m0, p.T, 2};                                        // t >= u, every head
+        default: return {p.B, 0, p.T, 1};                                          // kDWuk, kDWuv: every sequence
+    }
+}
+
+// TMA loads of one K step into stage memory: A at sa, B at sb (each 16 KB).  z: batch item of the output tile,
+// o: the outer K index, k: the inner K offset, pair: which operand pair (dc).
+__device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta, const CUtensorMap *tb,
+                                          const CUtensorMap *ta2, const CUtensorMap *tb2, uint32_t sa, uint32_t sb,
+                                          uint32_t bar, int z, int o, int k, int pair, int m0, int n0) {
+    const int b = p.problem == kDWuk || p.problem == kDWuv ? o : (p.problem == kDc ? z : z / p.H);
+    const int h = p.problem == kDc ? o : (p.problem == kDWuk || p.problem == kDWuv ? z : z % p.H);
+    const int zz = b * p.H + h;   // head-major batch item of the per-head matrices
+    switch (p.problem) {
+        case kQAbs:   // A = q [B,T,H,d] (K-major), B = W_UK [H,d,r] (MN-major)
+            tma_load_4d(sa, ta, bar, k, h, m0, b);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            break;
+        case kDoLat:  // A = do [z,T,d_v], B = W_UV [H,d_v,r]
+            tma_load_3d(sa, ta, bar, k, m0, zz);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            break;
+        case kP: case kDS:   // A = q_abs or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
+            tma_load_3d(sa, ta, bar, k, m0, zz);
+            tma_load_3d(sb, tb, bar, k, n0, b);
+            break;
+        case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
+            tma_load_3d(sa, ta, bar, k, m0, zz);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, b);
+            break;
+        case kDc: {   // A = P^T or dS^T (MN-major: rows t, u contiguous), B = do_lat or q_abs (MN-major: rows t)
+            const CUtensorMap *a = pair ? ta2 : ta, *bm = pair ? tb2 : tb;
+            for (int s = 0; s < 2; ++s) tma_load_3d(sa + s * 8192, a, bar, m0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, bm, bar, n0 + 64 * s, k, zz);
+            break;
+        }
+        case kDq:   // A = dq_abs [z,T,r] (K-major), B = W_UK [H,d,r] (K-major: rows d)
+            tma_load_3d(sa, ta, bar, k, m0, zz);
+            tma_load_3d(sb, tb, bar, k, n0, h);
+            break;
+        case kDWuk:   // A = q^T (MN-major: rows t, d contiguous), B = dq_abs (MN-major: rows t)
+            for (int s = 0; s < 2; ++s) tma_load_4d(sa + s * 8192, ta, bar, m0 + 64 * s, h, k, b);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            break;
+        default:   // kDWuv: A = do^T (MN-major: rows t), B = o_lat (MN-major: rows t)
+            for (int s = 0; s < 2; ++s) tma_load_3d(sa + s * 8192, ta, bar, m0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            break;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+    bwd_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
+                    const GemmP p) {
+    const int mt = static_cast<int>(blockIdx.x), nt = static_cast<int>(blockIdx.y), z = static_cast<int>(blockIdx.z);
+    if (causal_tiles(p.problem) && nt > mt) return;   // entirely above the diagonal: never written, never read
+    const int m0 = mt * kBM, n0 = nt * kBN;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gbase + kBarOff);
+    uint64_t *empty = full + kStages;
+    uint64_t *done = empty + kStages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const KWalk kw = k_walk(p, m0);
+    const int inner = kw.hi > kw.lo ? (kw.hi - kw.lo + kBK - 1) / kBK : 0;
+    const int steps = kw.outer * inner * kw.pairs;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 1);
+        }
+        mbar_init(smem_u32(done), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        bool ok = true;
+        int it = 0;
+        for (int o = 0; ok && o < kw.outer; ++o)
+            for (int ks = 0; ok && ks < inner; ++ks)
+                for (int pr = 0; pr < kw.pairs; ++pr, ++it) {
+                    const int st = it % kStages;
+                    if (it >= kStages && !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages) - 1) & 1, p.err, abort_flag)))
+                        break;
+                    const uint32_t bar = smem_u32(full + st);
+                    mbar_arrive_expect_tx(bar, kStageBytes);
+                    load_step(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
+                              bar, z, o, kw.lo + ks * kBK, pr, m0, n0);
+                }
+        if (!ok) *abort_flag = 1;
+        for (int q = (it > kStages ? it - kStages : 0); q < it; ++q)   // no load may still be landing at exit
+            mbar_wait(smem_u32(full + q % kStages), (q / kStages) & 1, p.err);
+    } else if (warp == 1 && lane == 0) {
+        const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
+        const uint32_t idesc = make_idesc_bf16(128, 128, amn ? 1 : 0, bmn ? 1 : 0);
+        bool ok = true;
+        for (int it = 0; it < steps; ++it) {
+            const int st = it % kStages;
+            if (!(ok = mbar_wait(smem_u32(full + st), (it / kStages) & 1, p.err, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t sa = base + st * kStageBytes, sb = sa + kOpBytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint64_t a = amn ? make_smem_desc(sa + kk * 2048, 8192, 1024) : make_smem_desc(sa + kk * 32, 16, 1024);
+                const uint64_t b = bmn ? make_smem_desc(sb + kk * 2048, 8192, 1024) : make_smem_desc(sb + kk * 32, 16, 1024);
+                umma_bf16(tmem, a, b, idesc, (it | kk) != 0);
+            }
+            umma_commit(smem_u32(empty + st));
+        }
+        if (ok) umma_commit(smem_u32(done));
+        else *abort_flag = 1;
+    } else if (warp >= 2) {
+        // epilogue: thread `row` owns TMEM lane row (warp w reads lanes 32 (w % 4) .. + 31)
+        const int row = (warp & 3) * 32 + lane;
+        const int m = m0 + row;
+        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        bool ok = true;
+        if (steps > 0) ok = mbar_wait(smem_u32(done), 0, p.err, abort_flag);
+        tc_fence_after();
+        if (__all_sync(0xffffffffu, ok)) {
+            const int pr = p.problem;
+            float mrow = 0.f, inv_l = 0.f, drow = 0.f;
+            if (m < p.M && (pr == kP || pr == kDS)) {
+                const size_t ri = static_cast<size_t>(z) * p.T + m;
+                if (pr == kP) {
+                    mrow = __ldg(p.st_m + ri);
+                    inv_l = 1.f / __ldg(p.st_l + ri);
+                } else {
+                    drow = __ldg(p.delta + ri);
+                }
+            }
+#pragma unroll 1
+            for (int c4 = 0; c4 < kBN / 32; ++c4) {
+                float v[32];
+                if (steps > 0) {
+                    tmem_ld32(trow + c4 * 32, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                const int nb = n0 + c4 * 32;
+                if (m >= p.M || nb >= p.N) continue;
+                if (pr == kP || pr == kDS) {
+                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb;
+                    float pv[32];
+                    if (pr == kDS) {
+                        const uint4 *pin = reinterpret_cast<const uint4 *>(p.p_in + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w = __ldg(pin + q);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                pv[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
+                                pv[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const bool vis = nb + i <= m;   // causal: key u <= query t
+                        if (pr == kP)
+                            v[i] = vis ? fast_exp2(fmaf(v[i], p.scale_log2, -mrow)) * inv_l : 0.f;
+                        else
+                            v[i] = vis ? p.scale * pv[i] * (v[i] - drow) : 0.f;
+                    }
+                    uint4 *o4 = reinterpret_cast<uint4 *>(o);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                } else if (pr <= kDqAbs) {   // bf16 [z, T, r]
+                    uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                                          (static_cast<size_t>(z) * p.T + m) * kR + nb);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                } else {   // fp32 gradients
+                    size_t off;
+                    if (pr == kDc) off = (static_cast<size_t>(z) * p.T + m) * kR + nb;
+                    else if (pr == kDq) off = ((static_cast<size_t>(z / p.H) * p.T + m) * p.H + z % p.H) * kD + nb;
+                    else off = (static_cast<size_t>(z) * p.M + m) * kR + nb;   // dW_UK, dW_UV [H, 128, r]
+                    float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, 128);
+}
+
+// do = dout * sigmoid(g) (head-major [z, T, d_v] bf16), dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
+// [B, T, H d_v]) and delta = do . o (fp32 [z, T]): one warp per (b, t, h), lane j holds columns 4j .. 4j + 3.
+__global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ g,
+                                                       const __nv_bfloat16 *__restrict__ o, __nv_bfloat16 *__restrict__ do_hm,
+                                                       float *__restrict__ dgate, float *__restrict__ delta, int B, int T, int H) {
+    const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (w >= static_cast<long long>(B) * T * H) return;
+    const int h = static_cast<int>(w % H);
+    const long long bt = w / H;
+    const int b = static_cast<int>(bt / T), t = static_cast<int>(bt % T);
+    const size_t off = static_cast<size_t>(w) * kD + lane * 4;
+    const uint2 dv = __ldg(reinterpret_cast<const uint2 *>(dout + off));
+    const uint2 ov = __ldg(reinterpret_cast<const uint2 *>(o + off));
+    const uint2 gv = g ? __ldg(reinterpret_cast<const uint2 *>(g + off)) : make_uint2(0u, 0u);
+    const uint32_t dw[2] = {dv.x, dv.y}, ow[2] = {ov.x, ov.y}, gw[2] = {gv.x, gv.y};
+    float dov[4], dg[4], dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t sh = (i & 1) ? 0u : 16u;
+        const float d = __uint_as_float((dw[i >> 1] << sh) & 0xFFFF0000u);
+        const float ov_ = __uint_as_float((ow[i >> 1] << sh) & 0xFFFF0000u);
+        const float sg = g ? 1.f / (1.f + expf(-__uint_as_float((gw[i >> 1] << sh) & 0xFFFF0000u))) : 1.f;
+        dov[i] = d * sg;
+        dg[i] = d * ov_ * sg * (1.f - sg);
+        dot += dov[i] * ov_;
+    }
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
+    const size_t hm = ((static_cast<size_t>(b) * H + h) * T + t) * kD + lane * 4;
+    *reinterpret_cast<uint2 *>(do_hm + hm) = make_uint2(pack_bf16x2(dov[0], dov[1]), pack_bf16x2(dov[2], dov[3]));
+    if (dgate) *reinterpret_cast<float4 *>(dgate + off) = make_float4(dg[0], dg[1], dg[2], dg[3]);
+    if (lane == 0) delta[(static_cast<size_t>(b) * H + h) * T + t] = dot;
+}
+
+CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
+             const cuuint32_t *box) {
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides_bytes, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct BwdLayout {
+    size_t o, pre, st_m, st_l, delta, do_hm, qa, dl, ol, dqa, P, dS, end;
+};
+BwdLayout bwd_layout(long long B, long long T, long long H) {
+    const long long Tp = (T + 127) / 128 * 128;
+    const size_t rows = static_cast<size_t>(B) * H * T;
+    BwdLayout L;
+    L.o = 0;
+    L.pre = L.o + al(static_cast<size_t>(B) * T * H * kD * 2);
+    L.st_m = L.pre + al(prefill_bf16_r512_workspace_bytes(B, T));
+    L.st_l = L.st_m + al(rows * 4);
+    L.delta = L.st_l + al(rows * 4);
+    L.do_hm = L.delta + al(rows * 4);
+    L.qa = L.do_hm + al(rows * kD * 2);
+    L.dl = L.qa + al(rows * kR * 2);
+    L.ol = L.dl + al(rows * kR * 2);
+    L.dqa = L.ol + al(rows * kR * 2);
+    L.P = L.dqa + al(rows * kR * 2);
+    L.dS = L.P + al(rows * Tp * 2);
+    L.end = L.dS + al(rows * Tp * 2);
+    return L;
+}
+
+}  // namespace
+
+bool backward_bf16_r512_supports(int r, int d_q, int d_v) { return r == kR && d_q == kD && d_v == kD; }
+
+size_t backward_bf16_r512_workspace_bytes(long long B, long long T, long long H) { return bwd_layout(B, T, H).end; }
+
+cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s) {
+    if (!backward_bf16_r512_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
+    const int B = a.B, T = a.T, H = a.H;
+    const int Tp = (T + 127) / 128 * 128;
+    const BwdLayout L = bwd_layout(B, T, H);
+    if (a.workspace_bytes < L.end) return cudaErrorInvalidValue;
+    char *ws = static_cast<char *>(a.workspace);
+    auto bf = [&](size_t off) { return reinterpret_cast<__nv_bfloat16 *>(ws + off); };
+    auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
+    const size_t rowsz = static_cast<size_t>(B) * H;   // head-major batch items
+
+    // 1. the forward without the gate: o, and each row's softmax statistics
+    PrefillArgs pa{a.q, a.c, a.w_uk, a.w_uv, nullptr, bf(L.o), a.scale, B, T, H, kD, kD, kR, a.dev_err, a.num_sms,
+                   ws + L.pre, L.st_m - L.pre};
+    pa.stats_m = f32(L.st_m);
+    pa.stats_l = f32(L.st_l);
+    cudaError_t e = launch_prefill_bf16_r512(pa, s);
+    if (e != cudaSuccess) return e;
+    // 2. the gate's backward, do and delta
+    {
+        const long long warps = static_cast<long long>(B) * T * H;
+        note_launch();
+        bwd_gate_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
+            static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.gate), bf(L.o),
+            bf(L.do_hm), static_cast<float *>(a.dgate), f32(L.delta), B, T, H);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // tensor maps (dims innermost first, strides in bytes)
+    const cuuint64_t uT = T, uH = H, uB = B, uZ = rowsz, uTp = Tp;
+    CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqa_mn, mdl_k, mdl_mn, mol_mn, mdqa_k,
+        mdqa_mn, mc_k, mc_mn, mP_k, mP_mn, mdS_k, mdS_mn;
+    bool okm = true;
+    auto E = [&](CUtensorMap *m, const void *ptr, int rank, std::initializer_list<cuuint64_t> d,
+                 std::initializer_list<cuuint64_t> st, std::initializer_list<cuuint32_t> bx) {
+        cuuint64_t dd[5], ss[4];
+        cuuint32_t bb[5];
+        int i = 0;
+        for (auto v : d) dd[i++] = v;
+        i = 0;
+        for (auto v : st) ss[i++] = v;
+        i = 0;
+        for (auto v : bx) bb[i++] = v;
+        okm = okm && enc(m, ptr, rank, dd, ss, bb) == CUDA_SUCCESS;
+    };
+    const cuuint64_t hd2 = static_cast<cuuint64_t>(H) * kD * 2;
+    E(&mq_k, a.q, 4, {kD, uH, uT, uB}, {kD * 2, hd2, hd2 * T}, {64, 1, 128, 1});
+    E(&mq_mn, a.q, 4, {kD, uH, uT, uB}, {kD * 2, hd2, hd2 * T}, {64, 1, 64, 1});
+    E(&mwuk_mn, a.w_uk, 3, {kR, kD, uH}, {kR * 2, kR * kD * 2}, {64, 64, 1});
+    E(&mwuk_k, a.w_uk, 3, {kR, kD, uH}, {kR * 2, kR * kD * 2}, {64, 128, 1});
+    E(&mwuv_mn, a.w_uv, 3, {kR, kD, uH}, {kR * 2, kR * kD * 2}, {64, 64, 1});
+    E(&mdo_k, bf(L.do_hm), 3, {kD, uT, uZ}, {kD * 2, kD * 2 * uT}, {64, 128, 1});
+    E(&mdo_mn, bf(L.do_hm), 3, {kD, uT, uZ}, {kD * 2, kD * 2 * uT}, {64, 64, 1});
+    auto EKM = [&](CUtensorMap *mk, CUtensorMap *mm, size_t off) {   // a [z, T, r] matrix, K-major and MN-major boxes
+        E(mk, bf(off), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 128, 1});
+        E(mm, bf(off), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
+    };
+    EKM(&mqa_k, &mqa_mn, L.qa);
+    EKM(&mdl_k, &mdl_mn, L.dl);
+    EKM(&mdqa_k, &mdqa_mn, L.dqa);
+    E(&mol_mn, bf(L.ol), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
+    E(&mc_k, a.c, 3, {kR, uT, uB}, {kR * 2, kR * 2 * uT}, {64, 128, 1});
+    E(&mc_mn, a.c, 3, {kR, uT, uB}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
+    auto ETT = [&](CUtensorMap *mk, CUtensorMap *mm, size_t off) {   // a [z, T, Tp] matrix
+        E(mk, bf(off), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 128, 1});
+        E(mm, bf(off), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 64, 1});
+    };
+    ETT(&mP_k, &mP_mn, L.P);
+    ETT(&mdS_k, &mdS_mn, L.dS);
+    if (!okm) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
+    if (e != cudaSuccess) return e;
+    auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
+                    const CUtensorMap &tb2, int M, int N, int Z, void *out) {
+        GemmP gp{};
+        gp.problem = pr;
+        gp.B = B;
+        gp.T = T;
+        gp.H = H;
+        gp.Tp = Tp;
+        gp.M = M;
+        gp.N = N;
+        gp.scale_log2 = a.scale * kLog2e;
+        gp.scale = a.scale;
+        gp.st_m = f32(L.st_m);
+        gp.st_l = f32(L.st_l);
+        gp.delta = f32(L.delta);
+        gp.p_in = bf(L.P);
+        gp.out = out;
+        gp.err = a.dev_err;
+        const dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN, Z);
+        note_launch();
+        bwd_gemm_kernel<<<grid, kThreads, kSmem, s>>>(ta, tb, ta2, tb2, gp);
+        return cudaGetLastError();
+    };
+    const int Z = static_cast<int>(rowsz);
+    // 3. q_abs and do_lat; 4. P, then dS (reads P); 5. o_lat and dq_abs; 6. dc and dq; 7. the weight gradients
+    if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa))) != cudaSuccess) return e;
+    if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl))) != cudaSuccess) return e;
+    if ((e = gemm(kP, mqa_k, mc_k, mqa_k, mc_k, T, T, Z, bf(L.P))) != cudaSuccess) return e;
+    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS))) != cudaSuccess) return e;
+    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol))) != cudaSuccess) return e;
+    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa))) != cudaSuccess) return e;
+    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc)) != cudaSuccess) return e;
+    if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq)) != cudaSuccess) return e;
+    if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk)) != cudaSuccess) return e;
+    return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv);
+}
+
+}  // namespace mla

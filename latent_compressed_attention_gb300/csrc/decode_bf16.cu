@@ -100,6 +100,15 @@ constexpr uint32_t S_SCOL = 256;   // S for one 256-row block
 
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, 256, 0, 0);   // q_abs (TMEM) x c (K-major), 256 rows
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);   // P (K-major) x c (MN-major)
+// The e4m3 cache (kF8): the same products as kind::f8f6f4 (K = 32 per instruction, twice the bf16 rate), each
+// 16-bit operand split into e4m3 hi + lo parts that both multiply the cache tile.  TMEM: q_abs hi in columns
+// 0-127 and lo in 128-255 (four e4m3 per column, 8 columns per K step of 32).
+constexpr uint32_t S_QLO = 128;
+constexpr uint32_t kIdescQK8 = make_idesc_e4m3(128, 256, 0, 0);
+constexpr uint32_t kIdescPV8 = make_idesc_e4m3(128, 256, 0, 1);
+// kF8 softmax weights: p' = exp2(s - m + 4), rescaled once the maximum grows by more than 4, so p' <= 2^8
+// (inside e4m3's 448) and weights down to 2^-13 of the maximum keep their lo part.
+constexpr float kRescaleLog2F8 = 4.0f, kPBiasF8 = 4.0f;
 
 struct PairBars {
     uint64_t qabs_ready;                              // score CTA
@@ -143,7 +152,9 @@ __device__ long long g_mtrace[8][1024];   // per merge CTA: phase end times (cyc
 
 struct PairParams {
     const int *lens;
-    const __nv_bfloat16 *q_abs;
+    const __nv_bfloat16 *q_abs;   // kF8: [B][H] rows of 1024 bytes, e4m3 hi (512) then lo (512)
+    const float *qmul;            // kF8: [B][H], the power of two that undoes q_abs's split scale
+    float cache_scale;            // kF8: the cache holds c / cache_scale
     __nv_bfloat16 *ws_o;   // [slots][H][r], unnormalised o_lat rounded to bf16
     float *ws_m;   // [slots][H]
     float *ws_l;   // [slots][H]
@@ -279,9 +290,18 @@ __device__ __forceinline__ void q_store(uint32_t trow, int wg, int half, const u
     }
 }
 
+template <bool kF8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const __grid_constant__ CUtensorMap tm_c256, const __grid_constant__ CUtensorMap tm_c,
                        const PairParams p) {
+    // a score stage holds 256 rows x 128 bytes: 64 bf16 or 128 e4m3 latent columns
+    constexpr int kStagesPerBlock = kF8 ? 4 : 8;
+    constexpr int kStageCols = kF8 ? 128 : 64;
+    // a value stage holds 64 rows x 256 latent columns: 4 slabs of 64 bf16 or 2 of 128 e4m3 columns
+    constexpr int kVSlabs = kF8 ? 2 : 4;
+    constexpr uint32_t kOStageBytes = kVSlabs * kVSlab;
+    constexpr float kRescale = kF8 ? kRescaleLog2F8 : kRescaleLog2;
+    constexpr float kPBias = kF8 ? kPBiasF8 : 0.f;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -352,7 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         const int key = k0 + j * kBS;
                         if (has_next && j + 2 >= nblk)   // the softmax loads it one to two blocks from now
                             bulk_prefetch_l2(p.q_abs + static_cast<size_t>(n_seq) * H * kR, static_cast<uint32_t>(H) * kR * 2);
-                        for (int kc = 0; kc < 8; ++kc, ++it) {
+                        for (int kc = 0; kc < kStagesPerBlock; ++kc, ++it) {
                             const int st = it % kSStages;
                             TR(const long long _a = clock64();)
                             if (it >= kSStages &&
@@ -360,8 +380,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 break;
                             TR(TR_ADD(DT_S_PROD_EMPTY, clock64() - _a);)
                             mbar_arrive_expect_tx(B_(bars->sc_full[st]), kSStage);
-                            tma_load_3d_hint(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]), kc * 64, key,
-                                             seq, keep);
+                            tma_load_3d_hint(base + S_RING + st * kSStage, &tm_c256, B_(bars->sc_full[st]),
+                                             kc * kStageCols, key, seq, keep);
                         }
                     }
                 }
@@ -385,7 +405,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (jb >= 1 && !(ok = mbar_wait(B_(bars->s_free), (jb - 1) & 1, p.err, abort_flag))) break;
                         TR(w_free += clock64() - _a; TL(0, jb, clock64() - t_start); long long w_blk = 0;)
                         tc_fence_after();
-                        for (int kc = 0; kc < 8; ++kc, ++it) {
+                        for (int kc = 0; kc < kStagesPerBlock; ++kc, ++it) {
                             const int st = it % kSStages;
                             TR(long long _b = clock64();)
                             if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
@@ -394,8 +414,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {
                                 const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
-                                umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
-                                                 (kc | kk) != 0);
+                                if constexpr (kF8) {   // S = hi . c^T + lo . c^T
+                                    umma_f8_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK8,
+                                                   (kc | kk) != 0);
+                                    umma_f8_tmem_a(tmem + S_SCOL, tmem + S_QLO + (kc * 4 + kk) * 8, bd, kIdescQK8, 1);
+                                } else {
+                                    umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
+                                                     (kc | kk) != 0);
+                                }
                             }
                             umma_commit(B_(bars->sc_empty[st]));
                         }
@@ -429,10 +455,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 break;
                             TR(TR_ADD(DT_O_PROD_EMPTY, clock64() - _a);)
                             const uint32_t full = B_(bars->oc_full[st]);
-                            mbar_arrive_expect_tx(full, kOStage);
-                            for (int q4 = 0; q4 < 4; ++q4)
+                            mbar_arrive_expect_tx(full, kOStageBytes);
+                            for (int q4 = 0; q4 < kVSlabs; ++q4)
                                 tma_load_3d_hint(base + O_RING + st * kOStage + q4 * kVSlab, &tm_c, full,
-                                                 ((nq >> 1) * 4 + q4) * 64, key + (nq & 1) * kVRows, seq, done_with);
+                                                 ((nq >> 1) * kVSlabs + q4) * (kF8 ? 128 : 64), key + (nq & 1) * kVRows,
+                                                 seq, done_with);
                         }
                     }
                 }
@@ -484,7 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
                                 TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
                                 if (nvalid < kVRows) {
-                                    for (int sl = 0; sl < 4; ++sl) {
+                                    for (int sl = 0; sl < kVSlabs; ++sl) {
                                         const uint32_t tile = base + O_RING + st * kOStage + sl * kVSlab;
                                         for (int r = max(nvalid, 0) + lane; r < kVRows; r += 32)
 #pragma unroll
@@ -496,14 +523,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 }
                                 tc_fence_after();
                                 if (leader) {
+                                    if constexpr (kF8) {
+                                        // P hi and lo slabs [heads x 128 rows], 128 bytes a head; K steps of 32 rows
 #pragma unroll
-                                    for (int j = 0; j < kVRows / 16; ++j) {
-                                        const int kk = hr * 4 + j;   // K step within the unit's 128 rows
-                                        const uint64_t a = make_smem_desc(
-                                            base + O_P + pb * kPBytes + hr * kPSlab + j * 32, 16, 1024);
-                                        const uint64_t bd =
-                                            make_smem_desc(base + O_RING + st * kOStage + j * 2048, kVSlab, 1024);
-                                        umma_bf16(tmem + (nq >> 1) * 256, a, bd, kIdescPV, (u > 0 || kk > 0));
+                                        for (int j = 0; j < kVRows / 32; ++j) {
+                                            const int kk = hr * 2 + j;   // K step within the unit's 128 rows
+                                            const uint32_t pa = base + O_P + pb * kPBytes + kk * 32;
+                                            const uint64_t bd =
+                                                make_smem_desc(base + O_RING + st * kOStage + j * 4096, kVSlab, 1024);
+                                            umma_f8(tmem + (nq >> 1) * 256, make_smem_desc(pa, 16, 1024), bd, kIdescPV8,
+                                                    (u > 0 || kk > 0));
+                                            umma_f8(tmem + (nq >> 1) * 256, make_smem_desc(pa + kPSlab, 16, 1024), bd,
+                                                    kIdescPV8, 1);
+                                        }
+                                    } else {
+#pragma unroll
+                                        for (int j = 0; j < kVRows / 16; ++j) {
+                                            const int kk = hr * 4 + j;   // K step within the unit's 128 rows
+                                            const uint64_t a = make_smem_desc(
+                                                base + O_P + pb * kPBytes + hr * kPSlab + j * 32, 16, 1024);
+                                            const uint64_t bd =
+                                                make_smem_desc(base + O_RING + st * kOStage + j * 2048, kVSlab, 1024);
+                                            umma_bf16(tmem + (nq >> 1) * 256, a, bd, kIdescPV, (u > 0 || kk > 0));
+                                        }
                                     }
                                     umma_commit(B_(bars->oc_empty[st]));
                                 }
@@ -554,7 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const bool head = row < H;
             const uint32_t ptile = base + S_PST + wg * kPUnit;
             const uint32_t ri = ptile + kPBytes;
-            const float c_log2 = p.qk_scale_log2;
+            float c_log2 = p.qk_scale_log2;
             uint32_t jb = 0;
             bool ok = true, fail = false;
             TR(long long tl0 = clock64(), w_sfull = 0, w_xbar = 0, w_pfree = 0, w_q = 0;)
@@ -578,6 +620,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     first = false;
                     TR(w_q += clock64() - _q;)
                 }
+                if constexpr (kF8)   // the score product's units: (q_abs * 2^e) . (c / cache_scale)
+                    c_log2 = p.qk_scale_log2 * p.cache_scale * __ldg(p.qmul + static_cast<size_t>(seq) * H + (head ? row : 0));
                 float m_run = -INFINITY, l_part = 0.f;
                 for (int j = 0; j < nblk; ++j, ++jb) {
                     // in the segment's last block the next segment's query goes into TMEM as soon as this
@@ -639,11 +683,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float mx = fmaxf(ld_shared_f32(base + PMAX + ((jb & 1) * 2 + 0) * 512 + row * 4),
                                            ld_shared_f32(base + PMAX + ((jb & 1) * 2 + 1) * 512 + row * 4));
                     float factor = 1.f;
-                    if (mx > m_run + kRescaleLog2) {
+                    if (mx > m_run + kRescale) {
                         factor = fast_exp2(m_run - mx);
                         m_run = mx;
                     }
-                    const float neg_m = -m_run;
+                    const float neg_m = kPBias - m_run;
                     if (lim < 128) {
 #pragma unroll
                         for (int c4 = 0; c4 < 4; ++c4)
@@ -661,16 +705,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // the staging unit is free once this warpgroup's previous copy has read it
                     if ((threadIdx.x & 127) == 0) bulk_wait_read_all();
                     named_bar_sync(2 + wg, 128);
-                    if (head)
+                    if (head) {
+                        if constexpr (kF8) {   // hi slab, then lo slab: 16 rows (bytes) per 16-byte chunk
 #pragma unroll
-                        for (int c4 = 0; c4 < 4; ++c4)
+                            for (int ch = 0; ch < 8; ++ch) {
+                                const float *v = &s[ch >> 1][(ch & 1) * 16];
+                                uint32_t hw[4], lw[4];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const float *v = &s[c4][8 * k];
-                                st_shared_v4(ptile + (c4 >> 1) * kPSlab + sw128_offset(row, (c4 & 1) * 4 + k),
-                                             pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                                for (int k = 0; k < 4; ++k) {
+                                    const uint32_t a = split_e4m3x2(v[4 * k], v[4 * k + 1]);
+                                    const uint32_t b = split_e4m3x2(v[4 * k + 2], v[4 * k + 3]);
+                                    hw[k] = (a & 0xFFFFu) | (b << 16);
+                                    lw[k] = (a >> 16) | (b & 0xFFFF0000u);
+                                }
+                                st_shared_v4(ptile + sw128_offset(row, ch), hw[0], hw[1], hw[2], hw[3]);
+                                st_shared_v4(ptile + kPSlab + sw128_offset(row, ch), lw[0], lw[1], lw[2], lw[3]);
                             }
+                        } else {
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4)
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const float *v = &s[c4][8 * k];
+                                    st_shared_v4(ptile + (c4 >> 1) * kPSlab + sw128_offset(row, (c4 & 1) * 4 + k),
+                                                 pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                 pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+                                }
+                        }
+                    }
                     // unit 2j carries the block's rescale factor; unit 2j+1 shares its maximum (factor 1)
                     st_shared_v2f(ri + row * 8, wg == 0 ? factor : 1.f, l_part);
                     fence_proxy_async_smem();
@@ -697,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                if (wg == 0 && head) p.ws_m[static_cast<size_t>(cl + seq) * H + row] = m_run;
+                if (wg == 0 && head) p.ws_m[static_cast<size_t>(cl + seq) * H + row] = m_run - kPBias;
             }
             TR(if (threadIdx.x == 128) {
                 TR_ADD(DT_S_SM_LOOP, clock64() - tl0); TR_ADD(DT_S_SM_SFULL, w_sfull); TR_ADD(DT_S_SM_XBAR, w_xbar);
@@ -766,6 +828,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     float v[32];
                     tmem_ld32(trow + wg * 256 + cc * 32, v);
                     tmem_wait_ld();
+                    if constexpr (kF8)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= p.cache_scale;
                     if (head)
 #pragma unroll
                         for (int q = 0; q < 4; ++q)
@@ -1129,7 +1194,7 @@ int pair_clusters(int num_sms) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemPair;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_pair_kernel<false>, &cfg) != cudaSuccess || n < 1) {
         (void)cudaGetLastError();
         n = cap;
     }
@@ -1172,9 +1237,85 @@ extern "C" __attribute__((visibility("default"))) int mla_debug_decode_clusters(
 }
 #endif
 
-cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
-    if (!decode_bf16_supports(a.H, a.d_v, a.r)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+namespace {
+// q_abs [B][H][512] bf16 -> per row (b, h): 2^e scaling its largest |q_abs| into [128, 256), then e4m3 hi and lo
+// parts (hi = e4m3(x), lo = e4m3(x - hi)) as a 1024-byte row [hi | lo], and qmul[b][h] = 2^-e.  A warp per row,
+// lane j holds latent columns 16j .. 16j + 15.
+__global__ void __launch_bounds__(256) qabs_split_e4m3_kernel(const __nv_bfloat16 *__restrict__ q_abs, uint8_t *__restrict__ q8,
+                                                              float *__restrict__ qmul, int rows) {
+    const int r = static_cast<int>(blockIdx.x) * 8 + static_cast<int>(threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const uint4 *src = reinterpret_cast<const uint4 *>(q_abs + static_cast<size_t>(r) * kR) + lane * 2;
+    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float x[16], amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        amax = fmaxf(amax, fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1])));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    // f16_range_exponent brings the maximum into [2^13, 2^14); 6 fewer gives [2^7, 2^8), inside e4m3's 448
+    const int e = amax > 0.f && amax < 3.0e38f ? f16_range_exponent(amax) - 6 : 0;
+    const float up = exp2_int(e);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t a = split_e4m3x2(x[4 * k] * up, x[4 * k + 1] * up);
+        const uint32_t b = split_e4m3x2(x[4 * k + 2] * up, x[4 * k + 3] * up);
+        hw[k] = (a & 0xFFFFu) | (b << 16);
+        lw[k] = (a >> 16) | (b & 0xFFFF0000u);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(q8 + static_cast<size_t>(r) * 1024);
+    dst[lane] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    dst[32 + lane] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    if (lane == 0) qmul[r] = exp2_int(-e);
+}
+
+// c [rows][r] bf16 (row stride ld_c) -> c8 = e4m3(c * inv_scale) [rows][r] (row stride ld_c8 bytes): 8 values
+// (16 bytes in, 8 out) per thread.
+__global__ void __launch_bounds__(256) quantize_latent_e4m3_kernel(const __nv_bfloat16 *__restrict__ c, long long ld_c,
+                                                                   uint8_t *__restrict__ c8, long long ld_c8,
+                                                                   long long rows, int r, float inv_scale) {
+    const long long per_row = r / 8;
+    const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * per_row) return;
+    const long long row = i / per_row, g = i % per_row;
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(c + row * ld_c) + g);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t a = cvt_e4m3x2(__uint_as_float(w[2 * k] << 16) * inv_scale,
+                                      __uint_as_float(w[2 * k] & 0xFFFF0000u) * inv_scale);
+        const uint32_t b = cvt_e4m3x2(__uint_as_float(w[2 * k + 1] << 16) * inv_scale,
+                                      __uint_as_float(w[2 * k + 1] & 0xFFFF0000u) * inv_scale);
+        o[k] = a | (b << 16);
+    }
+    *reinterpret_cast<uint2 *>(c8 + row * ld_c8 + g * 8) = make_uint2(o[0], o[1]);
+}
+
+CUresult encode_map_u8(CUtensorMap *m, const void *ptr, const cuuint64_t *dims, const cuuint64_t *strides,
+                       const cuuint32_t *box) {
+    auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
+    if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+size_t partials_bytes(int B, int H, int G) {
+    return slot_count(B, G) * static_cast<size_t>(H) * (kR * sizeof(__nv_bfloat16) + 2 * sizeof(float));
+}
+
+// The pair kernel (bf16 or e4m3 cache) and the merge, on workspace partials laid out as [o | m | l].
+template <bool kF8>
+cudaError_t launch_pair_and_merge(const DecodeArgs &a, const void *q_rows, const float *qmul, int G, cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemPair));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(decode_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1182,27 +1323,31 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     {   // the kernel's register split assumes this launch budget
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, decode_pair_kernel);
+        e = cudaFuncGetAttributes(&fa, decode_pair_kernel<kF8>);
         if (e != cudaSuccess) return e;
         if (fa.numRegs != static_cast<int>(kRegsLaunch)) return cudaErrorInvalidConfiguration;
     }
-    const int G = pair_clusters(a.num_sms);
-    if (G > kMaxClusters) return cudaErrorInvalidConfiguration;
     const size_t slots = slot_count(a.B, G);
-    if (slots * static_cast<size_t>(a.H) * (kR * sizeof(__nv_bfloat16) + 2 * sizeof(float)) > a.workspace_bytes)
-        return cudaErrorInvalidValue;
     __nv_bfloat16 *ws_o = static_cast<__nv_bfloat16 *>(a.workspace);
     float *ws_m = reinterpret_cast<float *>(ws_o + slots * a.H * kR);
     float *ws_l = ws_m + slots * a.H;
     CUtensorMap tm_c256, tm_c, tm_wuv;
     {
         const cuuint64_t rows = static_cast<cuuint64_t>(a.max_len > 0 ? a.max_len : 1);
+        const cuuint64_t es = kF8 ? 1 : 2;   // bytes per cache element
         const cuuint64_t dims[3] = {kR, rows, static_cast<cuuint64_t>(a.B)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_cache) * 2, rows * a.ld_cache * 2};
-        const cuuint32_t box256[3] = {64, kBS, 1};
-        if (encode_map(&tm_c256, a.c_cache, 3, dims, strides, box256) != CUDA_SUCCESS) return cudaErrorInvalidValue;
-        const cuuint32_t box64[3] = {64, kVRows, 1};
-        if (encode_map(&tm_c, a.c_cache, 3, dims, strides, box64) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.ld_cache) * es, rows * a.ld_cache * es};
+        const cuuint32_t box256[3] = {kF8 ? 128u : 64u, kBS, 1};
+        const cuuint32_t box64[3] = {kF8 ? 128u : 64u, kVRows, 1};
+        if (kF8) {
+            if (encode_map_u8(&tm_c256, a.c_cache, dims, strides, box256) != CUDA_SUCCESS ||
+                encode_map_u8(&tm_c, a.c_cache, dims, strides, box64) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        } else {
+            if (encode_map(&tm_c256, a.c_cache, 3, dims, strides, box256) != CUDA_SUCCESS ||
+                encode_map(&tm_c, a.c_cache, 3, dims, strides, box64) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
     }
     {
         const cuuint64_t dims[2] = {kR, static_cast<cuuint64_t>(a.H) * kDV};
@@ -1212,7 +1357,9 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     }
     PairParams pp;
     pp.lens = a.lens;
-    pp.q_abs = static_cast<const __nv_bfloat16 *>(a.q_abs);
+    pp.q_abs = static_cast<const __nv_bfloat16 *>(q_rows);
+    pp.qmul = qmul;
+    pp.cache_scale = a.cache_scale;
     pp.ws_o = ws_o;
     pp.ws_m = ws_m;
     pp.ws_l = ws_l;
@@ -1221,7 +1368,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     pp.H = a.H;
     pp.max_len = a.max_len;
     pp.qk_scale_log2 = a.scale * kLog2e;
-    decode_pair_kernel<<<2 * G, kThreads, kSmemPair, s>>>(tm_c256, tm_c, pp);
+    decode_pair_kernel<kF8><<<2 * G, kThreads, kSmemPair, s>>>(tm_c256, tm_c, pp);
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1249,6 +1396,54 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
     cfg.numAttrs = 1;
     note_launch();
     return cudaLaunchKernelEx(&cfg, decode_merge_kernel, tm_wuv, mp);
+}
+}  // namespace
+
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
+    if (!decode_bf16_supports(a.H, a.d_v, a.r)) return cudaErrorInvalidValue;
+    const int G = pair_clusters(a.num_sms);
+    if (G > kMaxClusters) return cudaErrorInvalidConfiguration;
+    if (partials_bytes(a.B, a.H, G) > a.workspace_bytes) return cudaErrorInvalidValue;
+    return launch_pair_and_merge<false>(a, a.q_abs, nullptr, G, s);
+}
+
+// Workspace of the e4m3-cache decode: the partials (as for bf16), then the split query rows [B][H][1024 bytes]
+// and their multipliers [B][H].
+size_t decode_fp8_workspace_bytes(int B, int H, int r, int max_len, int num_sms) {
+    const size_t part = decode_bf16_workspace_bytes(B, H, r, max_len, num_sms);
+    if (part == 0) return 0;
+    const size_t aligned = (part + 255) & ~static_cast<size_t>(255);
+    return aligned + static_cast<size_t>(B) * H * (1024 + sizeof(float));
+}
+
+cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s) {
+    if (!decode_bf16_supports(a.H, a.d_v, a.r)) return cudaErrorInvalidValue;
+    const int G = pair_clusters(a.num_sms);
+    if (G > kMaxClusters) return cudaErrorInvalidConfiguration;
+    if (decode_fp8_workspace_bytes(a.B, a.H, a.r, a.max_len, a.num_sms) > a.workspace_bytes)
+        return cudaErrorInvalidValue;
+    // the split rows start after the largest partials any cluster count needs (G <= num_sms / 2)
+    const size_t part = (decode_bf16_workspace_bytes(a.B, a.H, a.r, a.max_len, a.num_sms) + 255) & ~static_cast<size_t>(255);
+    uint8_t *q8 = static_cast<uint8_t *>(a.workspace) + part;
+    float *qmul = reinterpret_cast<float *>(q8 + static_cast<size_t>(a.B) * a.H * 1024);
+    const int rows = a.B * a.H;
+    note_launch();
+    qabs_split_e4m3_kernel<<<(rows + 7) / 8, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(a.q_abs), q8, qmul, rows);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_pair_and_merge<true>(a, q8, qmul, G, s);
+}
+
+cudaError_t launch_quantize_latent_e4m3(const void *c, long long ld_c, void *c8, long long ld_c8, long long rows, int r,
+                                        float inv_scale, cudaStream_t s) {
+    const long long n = rows * (r / 8);
+    if (n <= 0) return cudaSuccess;
+    const long long blocks = (n + 255) / 256;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    note_launch();
+    quantize_latent_e4m3_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(c), ld_c, static_cast<uint8_t *>(c8), ld_c8, rows, r, inv_scale);
+    return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -17,6 +17,10 @@ struct PrefillArgs {
     int num_sms;
     void *workspace = nullptr;   // prefill_workspace_bytes() bytes (none for the fp32 and small-rank kernels)
     size_t workspace_bytes = 0;
+    // optional (r = 512 kernel): each row's softmax statistics, [B, H, T] fp32: the log2-domain maximum the
+    // kernel used (m) and the sum of exp2(s - m) over the row (l), so attn = exp2(s - m) / l with s the scaled
+    // score in log2 units
+    float *stats_m = nullptr, *stats_l = nullptr;
 };
 
 struct DecodeArgs {
@@ -31,6 +35,7 @@ struct DecodeArgs {
     size_t workspace_bytes;
     int *dev_err;
     int num_sms;
+    float cache_scale = 1.f;   // e4m3 cache: it holds c / cache_scale
 };
 
 struct BackwardArgs {
@@ -62,6 +67,21 @@ inline size_t prefill_workspace_bytes(long long B, long long T, int r, int d_q, 
 
 cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s);
 
+// Gradients of the attention at r = 512, d_q = d_v = 128, bf16 inputs, fp32 gradients (tensor cores).
+struct BackwardR512Args {
+    const void *q, *c, *w_uk, *w_uv, *gate, *dout;
+    float *dq, *dc, *dw_uk, *dw_uv, *dgate;
+    float scale;
+    int B, T, H, d_q, d_v, r;
+    void *workspace;
+    size_t workspace_bytes;
+    int *dev_err;
+    int num_sms;
+};
+bool backward_bf16_r512_supports(int r, int d_q, int d_v);
+size_t backward_bf16_r512_workspace_bytes(long long B, long long T, long long H);
+cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s);
+
 // fp32 gradients of the attention (steps 2-4); r, d_q, d_v <= 64.
 bool backward_f32_supports(int r, int d_q, int d_v);
 size_t backward_f32_workspace_bytes(long long B, long long T, long long H, int r);
@@ -70,6 +90,12 @@ bool prefill_bf16_small_supports(int r, int d_q, int d_v);
 
 size_t decode_bf16_workspace_bytes(int B, int H, int r, int max_len, int num_sms);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+// The same decode over an e4m3 latent cache (c_cache holds bytes, ld_cache in bytes).
+size_t decode_fp8_workspace_bytes(int B, int H, int r, int max_len, int num_sms);
+cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s);
+// c [rows][r] bf16 -> e4m3(c * inv_scale) [rows][r] bytes.
+cudaError_t launch_quantize_latent_e4m3(const void *c, long long ld_c, void *c8, long long ld_c8, long long rows, int r,
+                                        float inv_scale, cudaStream_t s);
 bool decode_bf16_supports(int H, int d_v, int r);
 
 // Scratch of the no-alloc decode entry point: capacity in bytes, and its

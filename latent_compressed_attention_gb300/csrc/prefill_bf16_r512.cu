@@ -144,6 +144,7 @@ struct Params {
     __nv_bfloat16 *out;
     const float *sscale;   // [B]: 2^-e_b, the scale of sequence b's f16 latent copy
     const __nv_bfloat16 *w_uk;   // [H, d_q, r], read only by the rare recompute of a row beyond f16's range
+    float *st_m, *st_l;          // optional [B, H, T] row statistics (the backward's input)
     int *err;
     int T, H, n_qtiles, bh_count;
     int n_tiles;   // n_qtiles * bh_count work tiles, numbered heaviest first
@@ -696,6 +697,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ++nu;
                     }
                     if (!ok) break;
+                    if (p.st_m && wg == 0 && t < p.T)
+                        p.st_m[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = m_run;
                     // the first staging buffer takes the next tile's q tile once this tile's last copy has read it
                     if (issuer) bulk_wait_read_all();
                     if (issuer && wg == 0) mbar_arrive(B_(bars->q_free));
@@ -763,6 +766,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                     TR(const long long t_ep = clock64();)
                     const float inv_l = 1.f / (l_even + l_odd);
+                    if (p.st_l && wg == 0 && t < p.T)
+                        p.st_l[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = l_even + l_odd;
                     for (int kh = 0; ok && kh < 2; ++kh) {
                         if (kh == 1) {   // the staging tile is free once the first half's product completed
                             fail = !mbar_wait(B_(bars->ep_done[0]), k & 1, p.err, abort_flag);
@@ -976,6 +981,8 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.sscale = sscale;
     p.w_uk = static_cast<const __nv_bfloat16 *>(a.w_uk);
+    p.st_m = a.stats_m;
+    p.st_l = a.stats_l;
     p.err = a.dev_err;
     p.T = a.T;
     p.H = a.H;

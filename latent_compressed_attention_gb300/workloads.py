@@ -104,6 +104,42 @@ def round_bf16(a) -> np.ndarray:
     return bits.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+# e4m3 (the OCP FP8 format: 1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities, the all-ones
+# pattern is NaN; largest finite 448, smallest normal 2^-6, subnormals k * 2^-9).
+E4M3_MAX = 448.0
+
+
+def encode_e4m3(a) -> np.ndarray:
+    """Bytes of the nearest e4m3 value of each (finite) element, ties to even, saturating at +-448."""
+    x = np.asarray(a, dtype=np.float64)
+    mag = np.minimum(np.abs(x), E4M3_MAX)
+    e = np.floor(np.log2(np.maximum(mag, 2.0**-40)))
+    quantum = 2.0 ** (np.maximum(e, -6.0) - 3.0)          # spacing of the binade (2^-9 for subnormals)
+    q = np.minimum(np.round(mag / quantum) * quantum, E4M3_MAX)   # np.round: ties to even
+    code = np.zeros(x.shape, dtype=np.uint8)
+    sub = q < 2.0**-6
+    code[sub] = np.round(q[sub] / 2.0**-9).astype(np.uint8)
+    qn = q[~sub]
+    en = np.floor(np.log2(qn))
+    mant = np.round((qn / 2.0**en - 1.0) * 8.0)
+    code[~sub] = ((en + 7).astype(np.uint8) << 3) | mant.astype(np.uint8)
+    return code | (np.signbit(x) & (q != 0)).astype(np.uint8) << 7
+
+
+def decode_e4m3(codes) -> np.ndarray:
+    """fp64 values of e4m3 bytes (the all-ones exponent and mantissa pattern, NaN, is not produced here)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e, m = (c >> 3) & 15, c & 7
+    v = np.where(e == 0, m * 2.0**-9, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.where(c >> 7, -v, v)
+
+
+def quantize_e4m3(a, inv_scale: float) -> np.ndarray:
+    """The fp8 latent cache's bytes: e4m3(fp32(a) * fp32(inv_scale)), the product rounded to fp32 first."""
+    prod = np.asarray(a, np.float32) * np.float32(inv_scale)
+    return encode_e4m3(prod.astype(np.float64))
+
+
 def round_f32(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64).astype(np.float32).astype(np.float64)
 

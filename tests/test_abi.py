@@ -130,6 +130,50 @@ def test_decode_unsupported(lib, kw):
     assert decode(lib, **kw) == ERR_UNSUPPORTED
 
 
+def decode_fp8(lib, q=FAKE, cache=FAKE, ld=512, lens=FAKE, max_len=64, cache_scale=0.0625, wuv=FAKE, gate=None,
+               out=FAKE, B=2, H=8, dv=128, r=512, ws=None, ws_bytes=0):
+    return lib.mla_latent_decode_fp8(q, cache, ld, lens, max_len, cache_scale, wuv, gate, 1.0, out, B, H, dv, r, ws,
+                                     ws_bytes, None)
+
+
+@pytest.mark.parametrize("field", ["q", "cache", "lens", "wuv", "out"])
+def test_decode_fp8_null_pointer(lib, field):
+    assert decode_fp8(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(B=-1), dict(H=0), dict(r=0), dict(max_len=-1), dict(ld=100),
+                                dict(cache_scale=0.0), dict(cache_scale=-1.0), dict(cache_scale=float("inf")),
+                                dict(cache_scale=float("nan"))])
+def test_decode_fp8_bad_shape(lib, kw):
+    assert decode_fp8(lib, **kw) == ERR_SHAPE
+
+
+@pytest.mark.parametrize("kw", [dict(ld=520), dict(cache=FAKE + 8), dict(lens=FAKE + 4)])
+def test_decode_fp8_misaligned(lib, kw):
+    assert decode_fp8(lib, **kw) == ERR_ALIGN
+
+
+@pytest.mark.parametrize("kw", [dict(H=97), dict(r=256, ld=256), dict(dv=64)])
+def test_decode_fp8_unsupported(lib, kw):
+    assert decode_fp8(lib, **kw) == ERR_UNSUPPORTED
+
+
+def test_decode_fp8_empty_batch_is_noop(lib):
+    assert decode_fp8(lib, B=0) == OK
+
+
+def quantize(lib, c=FAKE, ld_c=512, c8=FAKE, ld_c8=512, rows=4, r=512, cache_scale=0.0625):
+    return lib.mla_quantize_latent_fp8(c, ld_c, c8, ld_c8, rows, r, cache_scale, None)
+
+
+@pytest.mark.parametrize("kw,want", [(dict(r=12, ld_c=12, ld_c8=16), ERR_SHAPE), (dict(rows=-1), ERR_SHAPE),
+                                     (dict(cache_scale=0.0), ERR_SHAPE), (dict(ld_c8=100), ERR_SHAPE),
+                                     (dict(ld_c8=520), ERR_ALIGN), (dict(ld_c=516), ERR_ALIGN),
+                                     (dict(c=FAKE + 2), ERR_ALIGN), (dict(c=None), ERR_NULL), (dict(rows=0), OK)])
+def test_quantize_fp8_validation(lib, kw, want):
+    assert quantize(lib, **kw) == want
+
+
 def test_decode_bad_dtype(lib):
     assert decode(lib, dtype=3) == ERR_DTYPE
 

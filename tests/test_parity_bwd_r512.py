@@ -1,0 +1,92 @@
+"""GPU parity of the attention's backward at the real sizes (r = 512, d_q = d_v = 128, bf16 inputs, fp32
+gradients, tensor cores) against the fp64 oracle's gradients (oracle.prefill_backward, pinned by finite
+differences in tests/test_oracle_backward.py), through the C ABI.
+
+Bar: the bf16 one, max|gpu - oracle| <= 2e-2 * max|oracle| for every gradient, on the same bf16 inputs.
+Every product of the chain rule runs on bf16 operands (the attention matrix, its gradient and the per-head
+intermediates are kept in bf16), so the gradients carry bf16-level error, not fp32's.  Shapes span several
+128-token tiles and ragged tails, T = 1, with and without the gate, two softmax scales.
+"""
+import numpy as np
+import pytest
+
+from latent_compressed_attention_gb300 import workloads as W
+from tests.conftest import gpu_available
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+KEYS = ("dq", "dc", "dw_uk", "dw_uv", "dgate")
+
+
+@pytest.fixture(scope="module")
+def env():
+    if not gpu_available():
+        pytest.skip("no CUDA device")
+    import torch
+
+    import latent_compressed_attention_gb300 as lca
+    import oracle
+    from latent_compressed_attention_gb300 import _build
+    _build.build()
+    oracle.build()
+    return torch, lca, oracle
+
+
+def case(B, T, H, seed, gate=True, wuk_std=W.WEIGHT_STD):
+    w = W.MID_PREFILL_BF16
+    d = W.draw_prefill_direct(w, seed=seed, T=T, B=B, H=H, wuk_std=wuk_std)
+    if not gate:
+        d["gate"] = None
+    d["dout"] = W.round_bf16(np.random.default_rng(seed + 1000).standard_normal((B, T, H * w.d_v)))
+    return d
+
+
+def run(env, d, scale):
+    torch, lca, oracle = env
+    t = lambda a: None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)  # noqa: E731
+    got = lca.mla_absorbed_attn_bwd(t(d["q"]), t(d["c"]), t(d["w_uk"]), t(d["w_uv"]), t(d["gate"]), scale,
+                                    t(d["dout"]))
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    ref = oracle.prefill_backward(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale, d["dout"])
+    return {k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref
+
+
+def check(got, ref):
+    for k in KEYS:
+        if ref[k] is None:
+            assert got[k] is None
+            continue
+        assert np.all(np.isfinite(got[k])), k
+        err = float(np.max(np.abs(got[k] - ref[k]))) / max(float(np.max(np.abs(ref[k]))), 1e-30)
+        assert err <= TOL_BF16, f"{k}: {err:.3e}"
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 512, 2), (2, 300, 2), (1, 129, 3), (1, 1, 2), (2, 640, 1)])
+@pytest.mark.parametrize("scale", [1.0 / np.sqrt(128.0), 1.0])
+def test_bwd_r512_shapes(env, B, T, H, scale):
+    got, ref = run(env, case(B, T, H, seed=T + 7 * H), scale)
+    check(got, ref)
+
+
+def test_bwd_r512_no_gate(env):
+    got, ref = run(env, case(1, 384, 2, seed=5, gate=False), 1.0)
+    check(got, ref)
+
+
+def test_bwd_r512_peaky(env):
+    """W_UK ~ N(0, 0.04^2) with q ~ N(0, 1.5^2): a score spread of several natural-log units."""
+    d = case(1, 400, 2, seed=9, wuk_std=0.04)
+    d["q"] = W.round_bf16(d["q"] / W.MID_PREFILL_BF16.q_std * 1.5)
+    got, ref = run(env, d, 1.0)
+    check(got, ref)
+
+
+def test_bwd_r512_repeatable(env):
+    """No atomics: two calls give the same bits."""
+    d = case(1, 256, 2, seed=11)
+    a, _ = run(env, d, 1.0)
+    b, _ = run(env, d, 1.0)
+    for k in KEYS:
+        assert np.array_equal(a[k], b[k]), k
