@@ -669,6 +669,8 @@ def run_backward_r512(torch, lca, dev, stream, flush, args, pk):
     fp32 gradients) on the tensor cores: the forward recomputed with its row statistics, then the chain rule's
     products as batched GEMMs over per-head attention matrices."""
     w = W.MID_PREFILL_BF16
+    if args.bwd_T != w.T:   # a shorter sequence, for profiling only
+        w = dataclasses.replace(w, T=args.bwd_T, name=f"{w.name}_t{args.bwd_T}")
     d = W.draw_prefill_direct(w, seed=0)
     dout = W.round_bf16(np.random.default_rng(1).standard_normal((w.B, w.T, w.H * w.d_v)))
     t = lambda a: torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
@@ -684,7 +686,7 @@ def run_backward_r512(torch, lca, dev, stream, flush, args, pk):
     ms = statistics.mean(times)
     fl = backward_flops(w)
     tf = fl / (ms * 1e-3) / 1e12
-    return {"workload": "mid_backward_bf16", "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
+    return {"workload": w.name.replace("prefill", "backward"), "value": round(tf, 2), "unit": "TFLOP/s", "ms_per_step": round(ms, 4),
             "flops_per_step": fl, "kernels_per_call": launches // max(args.steps, 1),
             "config": {"B": w.B, "T": w.T, "H": w.H, "d_q": w.d_q, "d_v": w.d_v, "r": w.r, "scale": w.scale,
                        "inputs": "direct draws of the mid-size workload, dout ~ N(0,1), bf16",
@@ -778,6 +780,8 @@ def main():
     ap.add_argument("--no-mid", action="store_true", help="skip the mid-size prefill section")
     ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-cache decode")
     ap.add_argument("--no-bwd", action="store_true", help="skip the r = 512 backward")
+    ap.add_argument("--bwd-T", type=int, default=W.MID_PREFILL_BF16.T,
+                    help="sequence length of the r = 512 backward (4096 is the benchmark; shorter is for profiling)")
     ap.add_argument("--no-small", action="store_true", help="skip the small-rank prefill and the fp32 toy layer")
     ap.add_argument("--workload", choices=["k3_prefill_bf16", "mid_prefill_bf16"], default="k3_prefill_bf16",
                     help="prefill workload of a step (the K3 size is the benchmark; the mid size is for profiling)")

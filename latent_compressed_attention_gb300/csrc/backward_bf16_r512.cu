@@ -4,7 +4,7 @@
 // the chain rule back through it, for L = sum(dout * out):
 //   sigma = sigmoid(g), do = dout * sigma, dgate = dout * o * sigma * (1 - sigma)   (step 4, o before the gate)
 //   do_lat = do . W_UV[h], dW_UV[h] = sum do^T o_lat                                 (step 3, W_UV)
-//   dA[t,u] = do_lat_t . c_u, delta_t = sum_u A dA = do_t . o_t                        (step 3, A . c)
+//   dA[t,u] = do_lat_t . c_u, delta_t = sum_u A dA                                     (step 3, A . c)
 //   dS = A * (dA - delta) * scale                                                     (softmax, step 2)
 //   dq_abs = dS . c, dc += dS^T . q_abs + A^T . do_lat (summed over heads)            (step 2, both uses of c)
 //   dq = dq_abs . W_UK[h]^T, dW_UK[h] = sum q^T dq_abs                                (step 2, the absorb)
@@ -17,6 +17,14 @@
 // of each tile, runs K over a second index (heads for dc, sequences for the weight gradients), and fuses
 // the softmax (P = exp2(S - m) / l) and the dS epilogues.  fp32 accumulation in TMEM; the gradients are
 // written in fp32, the intermediate matrices in bf16.
+//
+// delta is the mean of dA under the rounded attention matrix the products use, delta_t = sum_u P dA / sum_u P
+// (the numerator is do_lat_t . o_lat_t with o_lat = P . c; both sums come from the P and o_lat epilogues),
+// so sum_u P (dA - delta) = 0 holds for the rows as computed.  Taking delta from the rounded output instead
+// (do . o) makes dA - delta cancel catastrophically where one key dominates a row.  The partial sums of each
+// tile go to slots of their own and are added in a fixed order, so the gradients are the same bits on every
+// call.  The scores that rebuild P use q_abs as a bf16 pair hi + lo (about 16 significant bits), as the
+// forward's statistics came from a score operand more precise than bf16.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,11 +48,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // The products of the backward.  Operand layouts: "K" = K-major (K contiguous), "MN" = M or N contiguous.
 enum Problem : int {
-    kQAbs = 0,   // q_abs[z]   = q[b,:,h,:] . W_UK[h]          M=T  N=r   K=d        A K   B MN   bf16 [z,T,r]
+    kQAbs = 0,   // q_abs[z]   = q[b,:,h,:] . W_UK[h]          M=T  N=r   K=d        A K   B MN   bf16 hi, lo [z,T,r]
     kDoLat,      // do_lat[z]  = do[z] . W_UV[h]                M=T  N=r   K=d_v      A K   B MN   bf16
-    kP,          // P[z]       = exp2(S - m) / l, S = q_abs.c^T  M=T  N=T   K=r        A K   B K    bf16 [z,T,Tp]
+    kP,          // P[z]       = exp2(S - m) / l, S = q_abs.c^T  M=T  N=T   K=(hi,lo)r A K   B K    bf16 [z,T,Tp]
+                 //              (+ this tile's row sums of the rounded P)
     kDS,         // dS[z]      = scale P (do_lat . c^T - delta)  M=T  N=T   K=r        A K   B K    bf16
     kOLat,       // o_lat[z]   = P . c                          M=T  N=r   K=u<=t     A K   B MN   bf16
+                 //              (+ this tile's do_lat . o_lat; N tile 0 also adds up P's row sums)
     kDqAbs,      // dq_abs[z]  = dS . c                         M=T  N=r   K=u<=t     A K   B MN   bf16
     kDc,         // dc[b]      = sum_h P^T do_lat + dS^T q_abs   M=T  N=r   K=(h,t>=u) A MN  B MN   f32 [B,T,r]
     kDq,         // dq[b,:,h,:] = dq_abs . W_UK[h]^T             M=T  N=d   K=r        A K   B K    f32 [B,T,H,d]
@@ -58,8 +68,14 @@ struct GemmP {
     int M, N;             // output extent of one batch item
     float scale_log2;     // kP: softmax scale * log2(e)
     float scale;          // kDS: softmax scale
-    const float *st_m, *st_l, *delta;   // [z, T]
+    const float *st_m, *st_l;           // [z, T]: the forward's row statistics
+    float *psum;                        // [z, T]: row sums of P (o_lat's N tile 0 adds up psum_part)
+    float *psum_part;                   // [Tp / 128][z, T]: P's row sums, one slot per key tile
+    float *dnum_part;                   // [4][z, T]: do_lat . o_lat, one slot per o_lat N tile
+    long long rows;                     // B * H * T
+    void *out2;                         // kQAbs: the lo part
     const __nv_bfloat16 *p_in;          // kDS: P
+    const __nv_bfloat16 *dl_in;         // kOLat: do_lat
     void *out;
     int *err;
 };
@@ -77,7 +93,8 @@ struct KWalk {
 __device__ __forceinline__ KWalk k_walk(const GemmP &p, int m0) {
     switch (p.problem) {
         case kQAbs: case kDoLat: return {1, 0, kD, 1};
-        case kP: case kDS: case kDq: return {1, 0, kR, 1};
+        case kP: return {1, 0, kR, 2};                                             // hi and lo
+        case kDS: case kDq: return {1, 0, kR, 1};
         case kOLat: case kDqAbs: return {1, 0, min(p.T, m0 + kBM), 1};           // u <= t
         case kDc: return {p.H, m0, p.T, 2};                                        // t >= u, every head
         default: return {p.B, 0, p.T, 1};                                          // kDWuk, kDWuv: every sequence
@@ -101,8 +118,8 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
             tma_load_3d(sa, ta, bar, k, m0, zz);
             for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
             break;
-        case kP: case kDS:   // A = q_abs or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
-            tma_load_3d(sa, ta, bar, k, m0, zz);
+        case kP: case kDS:   // A = q_abs (hi, then lo) or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
+            tma_load_3d(sa, pair ? ta2 : ta, bar, k, m0, zz);
             tma_load_3d(sb, tb, bar, k, n0, b);
             break;
         case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
@@ -217,14 +234,17 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         if (__all_sync(0xffffffffu, ok)) {
             const int pr = p.problem;
-            float mrow = 0.f, inv_l = 0.f, drow = 0.f;
+            float mrow = 0.f, inv_l = 0.f, drow = 0.f, rsum = 0.f;
+            const size_t ri = static_cast<size_t>(z) * p.T + m;
             if (m < p.M && (pr == kP || pr == kDS)) {
-                const size_t ri = static_cast<size_t>(z) * p.T + m;
                 if (pr == kP) {
                     mrow = __ldg(p.st_m + ri);
                     inv_l = 1.f / __ldg(p.st_l + ri);
-                } else {
-                    drow = __ldg(p.delta + ri);
+                } else {   // written by earlier launches, added in a fixed order
+                    float num = 0.f;
+#pragma unroll
+                    for (int q = 0; q < kR / kBN; ++q) num += p.dnum_part[q * p.rows + ri];
+                    drow = num / p.psum[ri];
                 }
             }
 #pragma unroll 1
@@ -238,7 +258,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
                 const int nb = n0 + c4 * 32;
-                if (m >= p.M || nb >= p.N) continue;
+                // P and dS rows are written out to their padded width Tp (zeros past the diagonal): the products
+                // that read them take K in steps of 64 up to the end of the diagonal tile
+                if (m >= p.M || nb >= ((pr == kP || pr == kDS) ? p.Tp : p.N)) continue;
                 if (pr == kP || pr == kDS) {
                     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb;
                     float pv[32];
@@ -265,10 +287,44 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                     uint4 *o4 = reinterpret_cast<uint4 *>(o);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t wq[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            wq[e] = pack_bf16x2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                            if (pr == kP)   // the row sum of P as rounded
+                                rsum += __uint_as_float(wq[e] << 16) + __uint_as_float(wq[e] & 0xFFFF0000u);
+                        }
+                        o4[q] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    }
                 } else if (pr <= kDqAbs) {   // bf16 [z, T, r]
+                    if (pr == kQAbs) {   // the lo part: bf16(x - bf16(x))
+                        uint4 *l4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out2) +
+                                                              (static_cast<size_t>(z) * p.T + m) * kR + nb);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint32_t lw[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = v[8 * q + 2 * e], x1 = v[8 * q + 2 * e + 1];
+                                const uint32_t hw = pack_bf16x2(x0, x1);
+                                lw[e] = pack_bf16x2(x0 - __uint_as_float(hw << 16), x1 - __uint_as_float(hw & 0xFFFF0000u));
+                            }
+                            l4[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        }
+                    }
+                    if (pr == kOLat) {   // do_lat . o_lat over these 32 columns
+                        const uint4 *dl = reinterpret_cast<const uint4 *>(p.dl_in + (static_cast<size_t>(z) * p.T + m) * kR + nb);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 w = __ldg(dl + q);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                rsum += v[8 * q + 2 * e] * __uint_as_float(ww[e] << 16) +
+                                        v[8 * q + 2 * e + 1] * __uint_as_float(ww[e] & 0xFFFF0000u);
+                        }
+                    }
                     uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                                           (static_cast<size_t>(z) * p.T + m) * kR + nb);
 #pragma unroll
@@ -285,6 +341,15 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
+            if (m < p.M && pr == kP) p.psum_part[static_cast<size_t>(nt) * p.rows + ri] = rsum;
+            if (m < p.M && pr == kOLat) {
+                p.dnum_part[static_cast<size_t>(nt) * p.rows + ri] = rsum;
+                if (nt == 0) {   // the P launch has finished: its row sums, key tiles 0 .. mt, in order
+                    float ps = 0.f;
+                    for (int j = 0; j <= mt; ++j) ps += p.psum_part[static_cast<size_t>(j) * p.rows + ri];
+                    p.psum[ri] = ps;
+                }
+            }
         }
     }
     __syncwarp();
@@ -293,11 +358,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == 1) tmem_dealloc(tmem, 128);
 }
 
-// do = dout * sigmoid(g) (head-major [z, T, d_v] bf16), dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
-// [B, T, H d_v]) and delta = do . o (fp32 [z, T]): one warp per (b, t, h), lane j holds columns 4j .. 4j + 3.
+// do = dout * sigmoid(g) (head-major [z, T, d_v] bf16) and dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
+// [B, T, H d_v]).  One warp per (b, t, h), lane j holds columns 4j .. 4j + 3.
 __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ g,
                                                        const __nv_bfloat16 *__restrict__ o, __nv_bfloat16 *__restrict__ do_hm,
-                                                       float *__restrict__ dgate, float *__restrict__ delta, int B, int T, int H) {
+                                                       float *__restrict__ dgate, int B, int T, int H) {
     const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= static_cast<long long>(B) * T * H) return;
@@ -309,7 +374,7 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__re
     const uint2 ov = __ldg(reinterpret_cast<const uint2 *>(o + off));
     const uint2 gv = g ? __ldg(reinterpret_cast<const uint2 *>(g + off)) : make_uint2(0u, 0u);
     const uint32_t dw[2] = {dv.x, dv.y}, ow[2] = {ov.x, ov.y}, gw[2] = {gv.x, gv.y};
-    float dov[4], dg[4], dot = 0.f;
+    float dov[4], dg[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const uint32_t sh = (i & 1) ? 0u : 16u;
@@ -318,14 +383,11 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__re
         const float sg = g ? 1.f / (1.f + expf(-__uint_as_float((gw[i >> 1] << sh) & 0xFFFF0000u))) : 1.f;
         dov[i] = d * sg;
         dg[i] = d * ov_ * sg * (1.f - sg);
-        dot += dov[i] * ov_;
     }
-#pragma unroll
-    for (int s = 16; s >= 1; s >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, s);
     const size_t hm = ((static_cast<size_t>(b) * H + h) * T + t) * kD + lane * 4;
     *reinterpret_cast<uint2 *>(do_hm + hm) = make_uint2(pack_bf16x2(dov[0], dov[1]), pack_bf16x2(dov[2], dov[3]));
     if (dgate) *reinterpret_cast<float4 *>(dgate + off) = make_float4(dg[0], dg[1], dg[2], dg[3]);
-    if (lane == 0) delta[(static_cast<size_t>(b) * H + h) * T + t] = dot;
+
 }
 
 CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
@@ -341,7 +403,7 @@ CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, 
 size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
-    size_t o, pre, st_m, st_l, delta, do_hm, qa, dl, ol, dqa, P, dS, end;
+    size_t o, pre, st_m, st_l, psum, psum_part, dnum_part, do_hm, qa, qlo, dl, ol, dqa, P, dS, end;
 };
 BwdLayout bwd_layout(long long B, long long T, long long H) {
     const long long Tp = (T + 127) / 128 * 128;
@@ -351,10 +413,13 @@ BwdLayout bwd_layout(long long B, long long T, long long H) {
     L.pre = L.o + al(static_cast<size_t>(B) * T * H * kD * 2);
     L.st_m = L.pre + al(prefill_bf16_r512_workspace_bytes(B, T));
     L.st_l = L.st_m + al(rows * 4);
-    L.delta = L.st_l + al(rows * 4);
-    L.do_hm = L.delta + al(rows * 4);
+    L.psum = L.st_l + al(rows * 4);
+    L.psum_part = L.psum + al(rows * 4);
+    L.dnum_part = L.psum_part + al(rows * 4 * static_cast<size_t>(Tp / 128));
+    L.do_hm = L.dnum_part + al(rows * 4 * (kR / kBN));
     L.qa = L.do_hm + al(rows * kD * 2);
-    L.dl = L.qa + al(rows * kR * 2);
+    L.qlo = L.qa + al(rows * kR * 2);
+    L.dl = L.qlo + al(rows * kR * 2);
     L.ol = L.dl + al(rows * kR * 2);
     L.dqa = L.ol + al(rows * kR * 2);
     L.P = L.dqa + al(rows * kR * 2);
@@ -393,12 +458,12 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         note_launch();
         bwd_gate_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
             static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.gate), bf(L.o),
-            bf(L.do_hm), static_cast<float *>(a.dgate), f32(L.delta), B, T, H);
+            bf(L.do_hm), static_cast<float *>(a.dgate), B, T, H);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // tensor maps (dims innermost first, strides in bytes)
     const cuuint64_t uT = T, uH = H, uB = B, uZ = rowsz, uTp = Tp;
-    CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqa_mn, mdl_k, mdl_mn, mol_mn, mdqa_k,
+    CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqa_mn, mqlo_k, mqlo_mn, mdl_k, mdl_mn, mol_mn, mdqa_k,
         mdqa_mn, mc_k, mc_mn, mP_k, mP_mn, mdS_k, mdS_mn;
     bool okm = true;
     auto E = [&](CUtensorMap *m, const void *ptr, int rank, std::initializer_list<cuuint64_t> d,
@@ -426,6 +491,7 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         E(mm, bf(off), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
     };
     EKM(&mqa_k, &mqa_mn, L.qa);
+    EKM(&mqlo_k, &mqlo_mn, L.qlo);
     EKM(&mdl_k, &mdl_mn, L.dl);
     EKM(&mdqa_k, &mdqa_mn, L.dqa);
     E(&mol_mn, bf(L.ol), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
@@ -454,8 +520,13 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.scale = a.scale;
         gp.st_m = f32(L.st_m);
         gp.st_l = f32(L.st_l);
-        gp.delta = f32(L.delta);
+        gp.psum = f32(L.psum);
+        gp.psum_part = f32(L.psum_part);
+        gp.dnum_part = f32(L.dnum_part);
+        gp.rows = static_cast<long long>(rowsz) * T;
+        gp.out2 = bf(L.qlo);
         gp.p_in = bf(L.P);
+        gp.dl_in = bf(L.dl);
         gp.out = out;
         gp.err = a.dev_err;
         const dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN, Z);
@@ -464,12 +535,13 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         return cudaGetLastError();
     };
     const int Z = static_cast<int>(rowsz);
-    // 3. q_abs and do_lat; 4. P, then dS (reads P); 5. o_lat and dq_abs; 6. dc and dq; 7. the weight gradients
+    // 3. q_abs and do_lat; 4. P (and its row sums), o_lat (and do_lat . o_lat), then dS (reads P and both sums);
+    // 5. dq_abs; 6. dc and dq; 7. the weight gradients
     if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa))) != cudaSuccess) return e;
     if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl))) != cudaSuccess) return e;
-    if ((e = gemm(kP, mqa_k, mc_k, mqa_k, mc_k, T, T, Z, bf(L.P))) != cudaSuccess) return e;
-    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS))) != cudaSuccess) return e;
+    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P))) != cudaSuccess) return e;
     if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol))) != cudaSuccess) return e;
+    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS))) != cudaSuccess) return e;
     if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa))) != cudaSuccess) return e;
     if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc)) != cudaSuccess) return e;
     if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq)) != cudaSuccess) return e;

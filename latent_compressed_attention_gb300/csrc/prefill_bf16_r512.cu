@@ -279,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tma_prefetch_desc(&tm_c256);
                 tma_prefetch_desc(&tm_wuk);
                 int it = 0, k = 0;
-                bool ok = true;
+                bool ok = true, converted = false;
                 for (; ok; ++k) {
                     const int tile = tile_of(k);
                     if (tile >= p.n_tiles) break;
@@ -299,6 +299,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 tma_load_2d(base + S_RING + st * kSStage + s * kSlab, &tm_wuk, full, (2 * i + s) * 64,
                                             ti.h * kD);
                         } else {
+                            if (!converted) {   // launched as a dependent of the latent's conversion: its copy
+                                grid_dependency_wait();   // is complete and visible only after this
+                                converted = true;
+                            }
                             const int q = i - 4;
                             tma_load_3d(base + S_RING + st * kSStage, &tm_c256, full, (q & 7) * 64, (q >> 3) * kBS, ti.b);
                         }
@@ -549,7 +553,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // read, so the compaction is in place, chunk by chunk in increasing order.  The thread tracks
                     // its row's largest |x|; a row whose largest |x| is outside [2^-10, 2^15) is recomputed below.
                     tc_fence_after();
-                    float amax = 0.f;
+                    uint32_t hmax = 0;   // the two halves' largest |f16| bit patterns
                     if (wg == 0) {
     #pragma unroll 1
                         for (int kc = 0; kc < kR / 64; ++kc) {
@@ -559,63 +563,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             tmem_wait_ld();
     #pragma unroll
                             for (int q = 0; q < 32; ++q) {
-                                const float x0 = v[q >> 4][2 * (q & 15)] * p.qk_scale_log2;
-                                const float x1 = v[q >> 4][2 * (q & 15) + 1] * p.qk_scale_log2;
-                                amax = fmaxf(amax, fmaxf(fabsf(x0), fabsf(x1)));
-                                w[q] = __uint_as_float(pack_f16x2(x0, x1));
+                                const uint32_t h2 = pack_f16x2(v[q >> 4][2 * (q & 15)] * p.qk_scale_log2,
+                                                               v[q >> 4][2 * (q & 15) + 1] * p.qk_scale_log2);
+                                hmax = __vmaxu2(hmax, h2 & 0x7FFF7FFFu);   // |f16| bit patterns order as magnitudes
+                                w[q] = __uint_as_float(h2);
                             }
                             tmem_st32(trow + S_QCOL + kc * 32, w);
                             tmem_wait_st();
                         }
                     }
-                    st_shared_f32(base + QMAX + wg * kBM * 4 + row * 4, amax);
+                    // largest |x| as f16: 0x7800 = 2^15 (0x7C00 and up: the packing overflowed), 0x1400 = 2^-10
+                    const uint32_t hm = max(hmax & 0xFFFFu, hmax >> 16);
+                    const float amax = hm >= 0x7800u ? kF16Limit : (hm == 0u ? 0.f : (hm < 0x1400u ? kF16Floor * 0.5f : 1.f));
                     tc_fence_before();
                     int e_row = 0;
                     if (named_bar_or(1, 256, amax >= kF16Limit || (amax > 0.f && amax < kF16Floor))) {
                         // rare: some row's largest |x| is outside [2^-10, 2^15).  Every warp recomputes its rows' x
-                        // from the q tile and
-                        // W_UK (fp32 SIMT), times 2^e_row (0 for rows inside the range), and stores this warpgroup's
-                        // half of the packed row (tcgen05.st is warp-collective)
-                        const float xmax =
-                            fmaxf(ld_shared_f32(base + QMAX + row * 4), ld_shared_f32(base + QMAX + kBM * 4 + row * 4));
-                        e_row = (xmax >= kF16Limit || xmax < kF16Floor) ? f16_range_exponent(xmax) : 0;
-                        const float up = exp2_int(e_row);
+                        // from the q tile and W_UK (fp32 SIMT) in two passes over this warpgroup's half of the row:
+                        // the largest |x| (both halves through shared memory), then x * 2^e_row (e_row = 0 for rows
+                        // inside the range) packed into this half's columns (tcgen05.st is warp-collective)
                         const __nv_bfloat16 *wk = p.w_uk + static_cast<size_t>(ti.h) * kD * kR + wg * 256;
+                        float xm = 0.f;
     #pragma unroll 1
-                        for (int jb = 0; jb < 8; ++jb) {
-                            float acc[32];
-    #pragma unroll
-                            for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+                        for (int pass = 0; pass < 2; ++pass) {
+                            const float up = exp2_int(e_row);
     #pragma unroll 1
-                            for (int d = 0; d < kD; ++d) {
-                                const uint32_t qa = base + S_PST + (d >> 6) * kSlab + sw128_offset(row, (d & 63) >> 3) +
-                                                    (d & 7) * 2;
-                                const float qd = ld_shared_bf16(qa);
-                                const uint4 *w4 = reinterpret_cast<const uint4 *>(wk + static_cast<size_t>(d) * kR + jb * 32);
+                            for (int jb = 0; jb < 8; ++jb) {
+                                float acc[32];
     #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const uint4 wv = __ldg(w4 + u);
-                                    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+                                for (int q = 0; q < 32; ++q) acc[q] = 0.f;
+    #pragma unroll 1
+                                for (int d = 0; d < kD; ++d) {
+                                    const uint32_t qa = base + S_PST + (d >> 6) * kSlab + sw128_offset(row, (d & 63) >> 3) +
+                                                        (d & 7) * 2;
+                                    const float qd = ld_shared_bf16(qa);
+                                    const uint4 *w4 = reinterpret_cast<const uint4 *>(wk + static_cast<size_t>(d) * kR + jb * 32);
     #pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        acc[u * 8 + 2 * e] = fmaf(qd, __uint_as_float(ww[e] << 16), acc[u * 8 + 2 * e]);
-                                        acc[u * 8 + 2 * e + 1] = fmaf(qd, __uint_as_float(ww[e] & 0xFFFF0000u), acc[u * 8 + 2 * e + 1]);
+                                    for (int u = 0; u < 4; ++u) {
+                                        const uint4 wv = __ldg(w4 + u);
+                                        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+    #pragma unroll
+                                        for (int e = 0; e < 4; ++e) {
+                                            acc[u * 8 + 2 * e] = fmaf(qd, __uint_as_float(ww[e] << 16), acc[u * 8 + 2 * e]);
+                                            acc[u * 8 + 2 * e + 1] =
+                                                fmaf(qd, __uint_as_float(ww[e] & 0xFFFF0000u), acc[u * 8 + 2 * e + 1]);
+                                        }
                                     }
                                 }
-                            }
-                            float pk[16];
+                                if (pass == 0) {
     #pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                pk[q] = __uint_as_float(pack_f16x2((acc[2 * q] * p.qk_scale_log2) * up,
-                                                                   (acc[2 * q + 1] * p.qk_scale_log2) * up));
-                            tc_fence_after();
-                            tmem_st16(trow + S_QCOL + wg * 128 + jb * 16, pk);
+                                    for (int q = 0; q < 32; ++q) xm = fmaxf(xm, fabsf(acc[q] * p.qk_scale_log2));
+                                    continue;
+                                }
+                                float pk[16];
+    #pragma unroll
+                                for (int q = 0; q < 16; ++q)
+                                    pk[q] = __uint_as_float(pack_f16x2((acc[2 * q] * p.qk_scale_log2) * up,
+                                                                       (acc[2 * q + 1] * p.qk_scale_log2) * up));
+                                tc_fence_after();
+                                tmem_st16(trow + S_QCOL + wg * 128 + jb * 16, pk);
+                            }
+                            if (pass == 0) {
+                                st_shared_f32(base + QMAX + wg * kBM * 4 + row * 4, xm);
+                                named_bar_sync(1, 256);
+                                const float xmax = fmaxf(ld_shared_f32(base + QMAX + row * 4),
+                                                         ld_shared_f32(base + QMAX + kBM * 4 + row * 4));
+                                e_row = (xmax >= kF16Limit || xmax < kF16Floor) ? f16_range_exponent(xmax) : 0;
+                            }
                         }
                         tmem_wait_st();
                         tc_fence_before();
                         named_bar_sync(1, 256);
                     }
                     // the score in log2 units is the product times F = 2^-e_row * 2^-e_b (the latent copy's scale)
+                    if (k == 0) grid_dependency_wait();   // the conversion's sequence scale
                     const float F = exp2_int(-e_row) * __ldg(p.sscale + ti.b);
                     if (threadIdx.x == 128) mbar_arrive(B_(bars->qabs_ready));
                     TR(if (threadIdx.x == 128) { TR_ADD(TR_S_PROLOGUE, clock64() - t_start); TR_ADD(TR_TILES, 1);
@@ -857,6 +878,7 @@ __global__ void __launch_bounds__(kCvtThreads) latent_amax_kernel(const uint4 *_
                                                                   int T, int n_groups) {
     __shared__ float wmax[kCvtThreads / 32];
     const int b = static_cast<int>(blockIdx.x) / n_groups, g = static_cast<int>(blockIdx.x) % n_groups;
+    grid_launch_dependents();
     const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kBM) * (kR / 8);
     const int n = min(kBM, T - g * kBM) * (kR / 8);
     float amax = 0.f;
@@ -880,6 +902,8 @@ __global__ void __launch_bounds__(kCvtThreads) latent_f16_kernel(const uint4 *__
                                                                  int T, int n_groups) {
     __shared__ float wmax[kCvtThreads / 32];
     const int b = static_cast<int>(blockIdx.x) / n_groups, g = static_cast<int>(blockIdx.x) % n_groups;
+    grid_launch_dependents();   // the prefill may take SMs as they free up; it waits for this grid before use
+    grid_dependency_wait();     // launched as a dependent of latent_amax_kernel: gmax is complete after this
     float amax = 0.f;
     for (int i = static_cast<int>(threadIdx.x); i < n_groups; i += kCvtThreads)
         amax = fmaxf(amax, gmax[static_cast<size_t>(b) * n_groups + i]);
@@ -1008,14 +1032,26 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     latent_amax_kernel<<<static_cast<unsigned>(a.B * n_groups), kCvtThreads, 0, s>>>(
         static_cast<const uint4 *>(a.c), gmax, a.T, n_groups);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the conversion and the prefill are programmatic dependents of the kernel before them: their prologues
+    // overlap it, and each waits (griddepcontrol.wait) before reading what it wrote
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B * n_groups));
+    cfg.blockDim = dim3(kCvtThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     note_launch();
-    latent_f16_kernel<<<static_cast<unsigned>(a.B * n_groups), kCvtThreads, 0, s>>>(
-        static_cast<const uint4 *>(a.c), gmax, static_cast<uint4 *>(c16), sscale, a.T, n_groups);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, latent_f16_kernel, static_cast<const uint4 *>(a.c), static_cast<const float *>(gmax),
+                           static_cast<uint4 *>(c16), sscale, static_cast<int>(a.T), n_groups);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * p.G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
     note_launch();
-    prefill_r512_kernel<<<static_cast<unsigned>(2 * p.G), kThreads, kSmemBytes, s>>>(tm_q, tm_c, tm_c256, tm_wuk,
-                                                                                    tm_wuv, p);
-    return cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, prefill_r512_kernel, tm_q, tm_c, tm_c256, tm_wuk, tm_wuv, p);
 }
 
 }  // namespace mla

@@ -54,12 +54,16 @@ def run(env, d, scale):
 
 
 def check(got, ref):
+    """Each gradient against the bar relative to its own largest value.  Where the oracle's gradient is zero by
+    a closed form (T = 1: a single visible key makes dS, dq and dW_UK vanish), the relative error is undefined;
+    there the largest of all the gradients, times 1e-3, is the floor of the denominator."""
+    top_all = max(float(np.max(np.abs(ref[k]))) for k in KEYS if ref[k] is not None)
     for k in KEYS:
         if ref[k] is None:
             assert got[k] is None
             continue
         assert np.all(np.isfinite(got[k])), k
-        err = float(np.max(np.abs(got[k] - ref[k]))) / max(float(np.max(np.abs(ref[k]))), 1e-30)
+        err = float(np.max(np.abs(got[k] - ref[k]))) / max(float(np.max(np.abs(ref[k]))), 1e-3 * top_all)
         assert err <= TOL_BF16, f"{k}: {err:.3e}"
 
 
@@ -90,3 +94,19 @@ def test_bwd_r512_repeatable(env):
     b, _ = run(env, d, 1.0)
     for k in KEYS:
         assert np.array_equal(a[k], b[k]), k
+
+
+def test_bwd_r512_stale_workspace(env):
+    """Every workspace value a product reads was written by the same call: a workspace filled with NaN
+    beforehand (a ragged T, so the last tiles have padding columns) still gives finite gradients that match."""
+    torch, lca, _ = env
+    d = case(1, 300, 2, seed=13)
+    need = lca.library().mla_absorbed_attn_bwd_workspace_size(1, 300, 2, 128, 128, 512, lca.DTYPE_BF16)
+    ws = torch.full((need // 4 + 1,), float("nan"), dtype=torch.float32, device="cuda").view(torch.uint8)
+    t = lambda a: None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)  # noqa: E731
+    got = lca.mla_absorbed_attn_bwd(t(d["q"]), t(d["c"]), t(d["w_uk"]), t(d["w_uv"]), t(d["gate"]), 1.0, t(d["dout"]),
+                                    workspace=ws)
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    _, ref = run(env, d, 1.0)
+    check({k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref)
