@@ -858,11 +858,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // The f16 copy of the latent for the score product, in two passes over c [B, T, 512] bf16 (one CTA per
-// 128-key group g of sequence b in each): latent_amax_kernel writes the group's largest |c| to gmax[b][g];
+// 32-key group g of sequence b in each): latent_amax_kernel writes the group's largest |c| to gmax[b][g];
 // latent_f16_kernel takes the sequence's maximum over its groups, the power of two 2^e_b that brings it into
 // [2^13, 2^14), and writes c16 = c * 2^e_b (f16, round to nearest even) and sscale[b] = 2^-e_b.
-constexpr int kCvtThreads = 512;
-constexpr int kCvtChunks = kBM * kR / 8 / kCvtThreads;   // 16-byte chunks per thread
+constexpr int kCvtThreads = 256;
+constexpr int kCvtRows = 32;                                   // keys per conversion CTA
+constexpr int kCvtChunks = kCvtRows * kR / 8 / kCvtThreads;    // 16-byte chunks per thread
 
 __device__ __forceinline__ float block_max(float v, float *wmax) {
 #pragma unroll
@@ -879,10 +880,10 @@ __global__ void __launch_bounds__(kCvtThreads) latent_amax_kernel(const uint4 *_
     __shared__ float wmax[kCvtThreads / 32];
     const int b = static_cast<int>(blockIdx.x) / n_groups, g = static_cast<int>(blockIdx.x) % n_groups;
     grid_launch_dependents();
-    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kBM) * (kR / 8);
-    const int n = min(kBM, T - g * kBM) * (kR / 8);
+    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kCvtRows) * (kR / 8);
+    const int n = min(kCvtRows, T - g * kCvtRows) * (kR / 8);
     float amax = 0.f;
-#pragma unroll 8
+#pragma unroll
     for (int k = 0; k < kCvtChunks; ++k) {
         const int u = static_cast<int>(threadIdx.x) + k * kCvtThreads;
         if (u < n) {
@@ -911,8 +912,8 @@ __global__ void __launch_bounds__(kCvtThreads) latent_f16_kernel(const uint4 *__
     const int e = f16_range_exponent(amax);
     const float up = exp2_int(e);
     if (g == 0 && threadIdx.x == 0) sscale[b] = exp2_int(-e);
-    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kBM) * (kR / 8);
-    const int n = min(kBM, T - g * kBM) * (kR / 8);
+    const size_t first = (static_cast<size_t>(b) * T + static_cast<size_t>(g) * kCvtRows) * (kR / 8);
+    const int n = min(kCvtRows, T - g * kCvtRows) * (kR / 8);
 #pragma unroll 8
     for (int k = 0; k < kCvtChunks; ++k) {
         const int u = static_cast<int>(threadIdx.x) + k * kCvtThreads;
@@ -942,11 +943,11 @@ CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t 
 
 bool prefill_bf16_r512_supports(int r, int d_q, int d_v) { return r == kR && d_q == kD && d_v == kD; }
 
-// Workspace of the r = 512 prefill: the f16 latent copy [B, T, 512], the group maxima [B][ceil(T / 128)] and
+// Workspace of the r = 512 prefill: the f16 latent copy [B, T, 512], the group maxima [B][ceil(T / 32)] and
 // the sequence scales [B].
 size_t prefill_bf16_r512_workspace_bytes(long long B, long long T) {
     const size_t c16 = (static_cast<size_t>(B) * T * kR * 2 + 255) & ~static_cast<size_t>(255);
-    return c16 + static_cast<size_t>(B) * ((T + kBM - 1) / kBM + 1) * sizeof(float);
+    return c16 + static_cast<size_t>(B) * ((T + kCvtRows - 1) / kCvtRows + 1) * sizeof(float);
 }
 
 #ifdef MLA_TRACE
@@ -972,7 +973,7 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     if (!prefill_bf16_r512_supports(a.r, a.d_q, a.d_v)) return cudaErrorInvalidValue;
     if (!a.workspace || a.workspace_bytes < prefill_bf16_r512_workspace_bytes(a.B, a.T)) return cudaErrorInvalidValue;
     const cuuint64_t B = a.B, T = a.T, H = a.H;
-    const int n_groups = (a.T + kBM - 1) / kBM;
+    const int n_groups = (a.T + kCvtRows - 1) / kCvtRows;   // conversion groups of 32 keys
     void *c16 = a.workspace;
     float *gmax = reinterpret_cast<float *>(static_cast<char *>(a.workspace) +
                                             ((static_cast<size_t>(a.B) * a.T * kR * 2 + 255) & ~static_cast<size_t>(255)));

@@ -54,13 +54,13 @@ def prefill(lib, q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=None, out=FAKE, B=1, T
 
 def test_prefill_workspace_sizes(lib):
     """Only the r = 512 kernel needs a workspace: an f16 copy of c (2 bytes per latent value), one maximum
-    per 128 keys of each sequence and one scale per sequence."""
+    per 32 keys of each sequence and one scale per sequence."""
     assert lib.mla_absorbed_attn_fwd_workspace_size(2, 100, 4, 16, 16, 32, F32) == 0
     assert lib.mla_absorbed_attn_fwd_workspace_size(2, 100, 4, 16, 16, 32, BF16) == 0
     B, T = 3, 300
     need = lib.mla_absorbed_attn_fwd_workspace_size(B, T, 16, 128, 128, 512, BF16)
     c16 = (B * T * 512 * 2 + 255) // 256 * 256
-    assert need == c16 + B * (3 + 1) * 4
+    assert need == c16 + B * (10 + 1) * 4   # ceil(300 / 32) = 10 groups of 32 keys, and one scale
     assert lib.mla_absorbed_attn_fwd_workspace_size(B, T, 16, 128, 128, 512, 9) == 0
 
 
