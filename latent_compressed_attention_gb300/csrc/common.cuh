@@ -315,6 +315,11 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
     return d;
 }
 
+// The same descriptor for a 64-byte-swizzled operand (layout type 4): 64-byte rows in 512-byte atoms of 8 rows.
+__device__ __forceinline__ uint64_t make_smem_desc_sw64(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    return (make_smem_desc(saddr, lbo_bytes, sbo_bytes) & ~(7ull << 61)) | (4ull << 61);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 accumulation.
 // a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {

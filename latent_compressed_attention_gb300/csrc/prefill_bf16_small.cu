@@ -43,9 +43,12 @@ constexpr uint32_t kTile = 16384;   // [128 rows x 64 bf16], 128B swizzle
 constexpr uint32_t QT = 0;          // q tile, then q_abs, then the epilogue's o_lat
 constexpr uint32_t WK = QT + kTile;             // W_UK[h] [d_q rows x 64]
 constexpr uint32_t WV = WK + 8192;              // W_UV[h] [d_v rows x 64]
-constexpr uint32_t RING = WV + 8192;            // c tiles
-constexpr int kStages = 2;
-constexpr uint32_t PT = RING + kStages * kTile; // P [128 rows x 128 keys] = 2 tiles
+// c tiles [128 keys x r]: at r = 64 two stages of 128-byte-swizzled rows; at r = 32 the rows are 64 bytes and
+// four stages of 64-byte-swizzled tiles fit the same bytes, so the loads run further ahead of the products
+constexpr uint32_t RING = WV + 8192;
+constexpr int kMaxStages = 4;
+constexpr uint32_t kRingBytes = 2 * kTile;
+constexpr uint32_t PT = RING + kRingBytes;      // P [128 rows x 128 keys] = 2 tiles
 constexpr uint32_t BARS = PT + 2 * kTile;
 constexpr uint32_t PMAX = BARS + 256;            // [2 parities][2 groups][128 rows] partial row maxima
 constexpr uint32_t LSUM = PMAX + 2 * 2 * kBM * 4;   // [2 groups][128 rows] partial row sums
@@ -58,7 +61,7 @@ constexpr uint32_t S_COL = 0, O_COL = 128, LO_COL = 192;
 
 struct Bars {
     uint64_t pro_full, absorb_done, qabs_ready;
-    uint64_t c_full[kStages], c_empty[kStages];
+    uint64_t c_full[kMaxStages], c_empty[kMaxStages];
     uint64_t s_full, s_free, p_full, pv_done, olat_ready, ep_done;
     uint32_t tmem_base;
     int abort;
@@ -105,6 +108,17 @@ __device__ __forceinline__ void pair_bar_sync(int pair) {
     }
 }
 
+// Opt-in timeline (build with MLA_NVCC_FLAGS=-DMLA_TRACE): per key block of CTA 0 (a heaviest tile), the
+// cycle at which each role passed its waits, and every CTA's start and end on the global timer.
+#ifdef MLA_TRACE
+constexpr int kSTEv = 9, kSTBlk = 64;
+__device__ long long g_stl[kSTEv][kSTBlk];
+__device__ unsigned long long g_scta[3][4096];   // start ns, end ns, SM id
+#define STL(ev, j) do { if (blockIdx.x == 0 && (j) < kSTBlk) g_stl[ev][j] = clock64() - st_t0; } while (0)
+#else
+#define STL(ev, j) (void)0
+#endif
+
 struct Params {
     const __nv_bfloat16 *gate;
     __nv_bfloat16 *out;
@@ -129,12 +143,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int b = bh / p.H, h = bh % p.H;
     const int t0 = qt * kBM;
     const int nkv = qt + 1;
+    const bool narrow = p.r == 32;   // 64-byte latent rows
+    const int n_stages = narrow ? 4 : 2;
+    const uint32_t st_bytes = kRingBytes / static_cast<uint32_t>(n_stages);
+#ifdef MLA_TRACE
+    const long long st_t0 = clock64();
+    if (threadIdx.x == 0 && blockIdx.x < 4096) {
+        g_scta[0][blockIdx.x] = globaltimer_ns();
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        g_scta[2][blockIdx.x] = smid;
+    }
+#endif
 
     if (threadIdx.x == 0) {
         mbar_init(B_(bars->pro_full), 1);
         mbar_init(B_(bars->absorb_done), 1);
         mbar_init(B_(bars->qabs_ready), 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(B_(bars->c_full[i]), 1);
             mbar_init(B_(bars->c_empty[i]), 1);
         }
@@ -168,22 +194,23 @@ __global__ void __launch_bounds__(kThreads, 2)
         bool ok = true;
         int j = 0;
         for (; ok && j < nkv; ++j) {
-            const int st = j % kStages;
-            if (j >= kStages &&
-                !(ok = mbar_wait(B_(bars->c_empty[st]), ((j / kStages) - 1) & 1, p.err, abort_flag)))
+            const int st = j % n_stages;
+            if (j >= n_stages &&
+                !(ok = mbar_wait(B_(bars->c_empty[st]), ((j / n_stages) - 1) & 1, p.err, abort_flag)))
                 break;
-            mbar_arrive_expect_tx(B_(bars->c_full[st]), kTile);
-            tma_load_3d(base + RING + st * kTile, &tm_c, B_(bars->c_full[st]), 0, j * kBN, b);
+            mbar_arrive_expect_tx(B_(bars->c_full[st]), st_bytes);
+            tma_load_3d(base + RING + st * st_bytes, &tm_c, B_(bars->c_full[st]), 0, j * kBN, b);
+            STL(7, j);
         }
         if (!ok) *abort_flag = 1;
         mbar_wait(pro, 0, p.err);
-        for (int k = (j > kStages ? j - kStages : 0); k < j; ++k)
-            mbar_wait(B_(bars->c_full[k % kStages]), (k / kStages) & 1, p.err);
+        for (int k = (j > n_stages ? j - n_stages : 0); k < j; ++k)
+            mbar_wait(B_(bars->c_full[k % n_stages]), (k / n_stages) & 1, p.err);
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer
         const uint32_t id_absorb = make_idesc_bf16(128, 64, 0, 1);
         const uint32_t id_qk = make_idesc_bf16(128, kBN, 0, 0);
-        const uint32_t id_pv = make_idesc_bf16(128, 64, 0, 1);
+        const uint32_t id_pv = make_idesc_bf16(128, p.r, 0, 1);
         const uint32_t id_ep = make_idesc_bf16(128, p.d_v, 0, 0);
         bool ok = mbar_wait(B_(bars->pro_full), 0, p.err, abort_flag);
         if (ok) {
@@ -198,40 +225,47 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ready when the softmax finishes block j; then P(j) . c(j).  The score operand is the pair hi + lo
         // (hi from the q tile, lo from TMEM): S = hi . c^T + lo . c^T, over the r latent columns only.
         const int ksteps = p.r / 16;
+        // the latent tile as the score product's K-major operand (latent columns = K)
+        auto c_kmajor = [&](int st, int kk) {
+            const uint32_t a = base + RING + st * st_bytes + kk * 32;
+            return narrow ? make_smem_desc_sw64(a, 16, 512) : make_smem_desc(a, 16, 1024);
+        };
         auto issue_scores = [&](int j) {
-            const int st = j % kStages;
+            const int st = j % n_stages;
             tc_fence_after();
             for (int kk = 0; kk < ksteps; ++kk)
-                umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
-                          make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, kk > 0);
+                umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024), c_kmajor(st, kk), id_qk, kk > 0);
             for (int kk = 0; kk < ksteps; ++kk)
-                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + kk * 8,
-                                 make_smem_desc(base + RING + st * kTile + kk * 32, 16, 1024), id_qk, 1);
+                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + kk * 8, c_kmajor(st, kk), id_qk, 1);
             umma_commit(B_(bars->s_full));
+            STL(0, j);
         };
         if (ok && (ok = mbar_wait(B_(bars->c_full[0]), 0, p.err, abort_flag))) issue_scores(0);
         for (int j = 0; ok && j < nkv; ++j) {
             if (j + 1 < nkv) {
-                const int sn = (j + 1) % kStages;
-                if (!(ok = mbar_wait(B_(bars->c_full[sn]), ((j + 1) / kStages) & 1, p.err, abort_flag))) break;
+                const int sn = (j + 1) % n_stages;
+                if (!(ok = mbar_wait(B_(bars->c_full[sn]), ((j + 1) / n_stages) & 1, p.err, abort_flag))) break;
                 if (!(ok = mbar_wait(B_(bars->s_free), j & 1, p.err, abort_flag))) break;
                 issue_scores(j + 1);
             }
             if (!(ok = mbar_wait(B_(bars->p_full), j & 1, p.err, abort_flag))) break;
+            STL(1, j);
             tc_fence_after();
-            const int st = j % kStages;
+            const int st = j % n_stages;
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
                 umma_bf16(tmem + O_COL, make_smem_desc(base + PT + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024),
-                          make_smem_desc(base + RING + st * kTile + kk * 2048, 8192, 1024), id_pv,
-                          (j > 0 || kk > 0));
+                          narrow ? make_smem_desc_sw64(base + RING + st * st_bytes + kk * 1024, 8192, 512)
+                                 : make_smem_desc(base + RING + st * st_bytes + kk * 2048, 8192, 1024),
+                          id_pv, (j > 0 || kk > 0));
             umma_commit(B_(bars->c_empty[st]));
             umma_commit(B_(bars->pv_done));
+            STL(2, j);
         }
         if (ok && (ok = mbar_wait(B_(bars->olat_ready), 0, p.err, abort_flag))) {
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < p.r / 16; ++kk)   // o_lat's columns past r are not products
                 umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024),
                           make_smem_desc(base + WV + kk * 32, 16, 1024), id_ep, kk > 0);
             umma_commit(B_(bars->ep_done));
@@ -278,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int pair = warp & 3;
         for (int j = 0; j < nkv; ++j) {
             if (!mbar_wait(B_(bars->s_full), j & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
+            if (leader) STL(3, j);
             tc_fence_after();
             float s[2][32];
 #pragma unroll
@@ -307,8 +342,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) s[c2][i] = fast_exp2(s[c2][i] - m_run);
             l_run = l_run * factor + tree_sum64(s);
+            if (leader) STL(4, j);
             if (j > 0) {   // P and o_lat are free once the previous block's product completed
                 if (!mbar_wait(B_(bars->pv_done), (j - 1) & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
+                if (leader) STL(5, j);
                 if (__any_sync(0xffffffffu, factor != 1.f)) {   // this warp's rows of o_lat (warp-collective)
                     tc_fence_after();
                     float v[32];
@@ -325,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int c2 = 0; c2 < 2; ++c2) store_row32_bf16(base + PT, kTile, row, 2 * g + c2, s[c2], 1.f);
             fence_proxy_async_smem();
             mbar_arrive(B_(bars->p_full));
+            if (leader) STL(6, j);
         }
         if (!mbar_wait(B_(bars->pv_done), (nkv - 1) & 1, p.err, abort_flag)) ok = false, *abort_flag = 1;
         ok = !named_bar_or(1, kMath, !ok);
@@ -382,22 +420,34 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+#ifdef MLA_TRACE
+    if (threadIdx.x == 0 && blockIdx.x < 4096) g_scta[1][blockIdx.x] = globaltimer_ns();
+#endif
     if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 CUresult encode_map(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
-                    const cuuint32_t *box) {
+                    const cuuint32_t *box, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
     if (!fn) return CUDA_ERROR_NOT_SUPPORTED;
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
 bool dim_ok(int d) { return d == 16 || d == 32 || d == 48 || d == 64; }
 
 }  // namespace
+
+#ifdef MLA_TRACE
+// Diagnostic build only: the timeline of CTA 0 ([9][64] cycles) and every CTA's [start, end, SM] ([3][4096]).
+extern "C" __attribute__((visibility("default"))) int mla_debug_small_trace(long long *tl, unsigned long long *ctas) {
+    if (cudaMemcpyFromSymbol(tl, g_stl, sizeof(g_stl)) != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(ctas, g_scta, sizeof(g_scta)) != cudaSuccess) return -1;
+    return 0;
+}
+#endif
 
 bool prefill_bf16_small_supports(int r, int d_q, int d_v) { return (r == 32 || r == 64) && dim_ok(d_q) && dim_ok(d_v); }
 
@@ -414,8 +464,11 @@ cudaError_t launch_prefill_bf16_small(const PrefillArgs &a, cudaStream_t s) {
     {
         const cuuint64_t dims[3] = {r, T, B};
         const cuuint64_t strides[2] = {r * 2, T * r * 2};
-        const cuuint32_t box[3] = {64, kBN, 1};
-        if (encode_map(&tm_c, a.c, 3, dims, strides, box) != CUDA_SUCCESS) return cudaErrorInvalidValue;
+        // r = 32: rows of 64 bytes, staged with 64-byte swizzle; r = 64: 128-byte rows and swizzle
+        const cuuint32_t box[3] = {static_cast<cuuint32_t>(r), kBN, 1};
+        if (encode_map(&tm_c, a.c, 3, dims, strides, box,
+                       r == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[2] = {r, H * dq};
