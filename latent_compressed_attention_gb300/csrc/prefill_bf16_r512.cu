@@ -22,8 +22,9 @@
 //     the value CTA by asynchronous DSMEM bulk copies.
 //   rank 1, the value CTA: accumulates o_lat += P . c in TMEM (512 columns),
 //     rescales o_lat when a row maximum grew (lazily: only when it grew by
-//     more than 2^16), then divides by the row sum, projects with W_UV^T on
-//     the tensor cores and applies the sigmoid gate.
+//     more than 2^16), then divides by the row sum, packing o_lat/l as bf16 in
+//     place in TMEM, where it is the A operand of the W_UV^T product, and
+//     applies the sigmoid gate.
 // Each CTA loads its own c tiles (no multicast); both read them from L2.
 //
 // Precision of the score: a bf16 operand (8 significant bits) would put a
@@ -84,7 +85,7 @@ constexpr uint32_t S_PST = S_RING + kSStages * kSStage;
 constexpr uint32_t O_RING = 0;
 constexpr int kOStages = 2;
 constexpr uint32_t kOStage = 4 * kSlab;              // 256 latent columns x 128 keys
-constexpr uint32_t O_P = kOStages * kOStage;         // 2 P tiles (also the epilogue's o_lat staging)
+constexpr uint32_t O_P = kOStages * kOStage;         // 2 P tiles
 constexpr uint32_t O_ROWINFO = O_P + 2 * kPBytes;    // 2 row-info blocks
 constexpr uint32_t BARS = S_PST + 2 * kPUnit;
 constexpr uint32_t PMAX = BARS + 512;                // [2 parities][2 warpgroups][128 rows] partial maxima
@@ -101,7 +102,12 @@ static_assert(S_PST % 1024 == 0 && (S_PST + kPUnit) % 1024 == 0 && O_P % 1024 ==
 constexpr uint32_t kIdescAbsorb = make_idesc_bf16(128, 256, 0, 1);  // q (K-major) x W_UK (MN-major)
 constexpr uint32_t kIdescQK = make_idesc_f16(128, 256, 0, 0);       // f16 q_abs (TMEM) x f16 c (K-major), 256 keys
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 256, 0, 1);      // P (K-major) x c (MN-major)
-constexpr uint32_t kIdescEp = make_idesc_bf16(128, 128, 0, 0);      // o_lat (K-major) x W_UV (K-major)
+constexpr uint32_t kIdescEp = make_idesc_bf16(128, 128, 0, 0);      // o_lat/l (TMEM) x W_UV (K-major)
+// TMEM columns of the value CTA in the epilogue: o_lat/l packed as bf16 pairs in place, latent columns
+// 0-255 into columns 0-127 and 256-511 into columns 384-511 (K step ks of 16 latent columns at
+// ep_acol(ks)); the product o = (o_lat/l) . W_UV^T lands in columns 128-255.
+__device__ __forceinline__ uint32_t ep_acol(int ks) { return ks < 16 ? 8 * ks : 384 + 8 * (ks - 16); }
+constexpr uint32_t O_EPCOL = 128;
 
 struct Bars {
     uint64_t pro_full, absorb_done, qabs_ready, q_free;   // score CTA
@@ -111,7 +117,7 @@ struct Bars {
     uint64_t oc_full[kOStages], oc_empty[kOStages];  // value CTA
     uint64_t p_full[2];                           // bulk-copy transactions from the score CTA
     uint64_t pv_done[2], ri_read[2], corr_done;
-    uint64_t olat_ready[2], ep_done[2], ep_read;
+    uint64_t olat_ready, ep_done, ep_read;
     uint32_t tmem_base;
     int abort;
 };
@@ -123,7 +129,7 @@ enum TraceSlot {
     TR_S_MMA_LOOP, TR_S_MMA_SFREE, TR_S_MMA_SCFULL, TR_S_SM_LOOP, TR_S_SM_SFULL, TR_S_SM_XBAR, TR_S_SM_PFREE,
     TR_S_SM_STORE, TR_O_MMA_LOOP, TR_O_MMA_PFULL, TR_O_MMA_OCFULL, TR_O_MMA_CORR, TR_O_COR_LOOP, TR_S_PROD_EMPTY,
     TR_O_PROD_EMPTY, TR_TILES, TR_BLOCKS, TR_CORRECTIONS, TR_S_PROLOGUE, TR_O_EPILOGUE, TR_S_TOTAL, TR_O_TOTAL,
-    TR_S_SM_RELEASE, TR_COUNT
+    TR_S_SM_RELEASE, TR_O_EP_PACK, TR_O_EP_WAIT, TR_O_EP_OUT, TR_COUNT
 };
 #ifdef MLA_TRACE
 __device__ unsigned long long g_trace[TR_COUNT];
@@ -247,14 +253,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_init(B_(bars->p_full[i]), 1);   // the value CTA's expect-tx arrival
             mbar_init(B_(bars->pv_done[i]), 1);
             mbar_init(B_(bars->ri_read[i]), 256);
-            mbar_init(B_(bars->olat_ready[i]), 1);
-            mbar_init(B_(bars->ep_done[i]), 1);
         }
         for (int i = 0; i < kOStages; ++i) {
             mbar_init(B_(bars->oc_full[i]), 1);
             mbar_init(B_(bars->oc_empty[i]), 1);
         }
         mbar_init(B_(bars->corr_done), 256);
+        mbar_init(B_(bars->olat_ready), 1);
+        mbar_init(B_(bars->ep_done), 1);
         mbar_init(B_(bars->ep_read), 256);
         bars->abort = 0;
         fence_mbar_init();
@@ -478,21 +484,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (leader) umma_commit(B_(bars->pv_done[pb]));
                         TR(if (leader && tl_on) { TL(9, j, clock64() - t_start); TL(10, j, w_u); })
                     }
+                    // the epilogue: o = (o_lat/l) . W_UV^T with A from TMEM (packed in place by the correction
+                    // warpgroups) and W_UV[h] in the ring's next two stages
+                    if (ok) ok = wait_all(bars->olat_ready, k & 1, false);
                     for (int kh = 0; ok && kh < 2; ++kh, ++it) {
-                        if (!(ok = wait_all(bars->olat_ready[kh], k & 1, false))) break;
                         const int st = it % kOStages;
                         if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
                         tc_fence_after();
                         if (leader) {
     #pragma unroll
                             for (int kk = 0; kk < 16; ++kk) {
-                                const uint64_t a = make_smem_desc(base + O_P + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
                                 const uint64_t bd = make_smem_desc(
                                     base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                                umma_bf16(tmem, a, bd, kIdescEp, (kh > 0 || kk > 0));
+                                umma_bf16_tmem_a(tmem + O_EPCOL, tmem + ep_acol(kh * 16 + kk), bd, kIdescEp,
+                                                 (kh > 0 || kk > 0));
                             }
                             umma_commit(B_(bars->oc_empty[st]));
-                            umma_commit(B_(bars->ep_done[kh]));
+                            if (kh == 1) umma_commit(B_(bars->ep_done));
                         }
                         __syncwarp();
                     }
@@ -503,8 +511,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 })
                 if (!ok && leader) *abort_flag = 1;
             } else if (warp == 2 && lane == 0) {
-                // ---- relay: P buffer pb is free again once its product completed and its row info was read; the
-                // buffers of a tile's last two units are also the epilogue's staging, free after its second product
+                // ---- relay: P buffer pb is free again once its product completed and its row info was read
                 int gu = 0;
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
@@ -514,8 +521,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < ti.nkv; ++j, ++gu) {
                         const int pb = gu & 1;
                         if (!mbar_wait(B_(bars->pv_done[pb]), (gu >> 1) & 1, p.err, abort_flag) ||
-                            !mbar_wait(B_(bars->ri_read[pb]), (gu >> 1) & 1, p.err, abort_flag) ||
-                            (j >= ti.nkv - 2 && !mbar_wait(B_(bars->ep_done[1]), k & 1, p.err, abort_flag))) {
+                            !mbar_wait(B_(bars->ri_read[pb]), (gu >> 1) & 1, p.err, abort_flag)) {
                             *abort_flag = 1;
                             ok = false;
                             break;
@@ -786,50 +792,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (named_bar_or(4, 256, fail)) { ok = false; break; }
                     }
                     TR(const long long t_ep = clock64();)
+                    // this row's gate values (read once, from DRAM) are requested now: their latency runs under
+                    // the packing and the W_UV product
+                    const size_t off = ((static_cast<size_t>(ti.b) * p.T + t) * p.H + ti.h) * kD + wg * 64;
+                    uint4 gv[8];
+    #pragma unroll
+                    for (int v8 = 0; v8 < 8; ++v8)
+                        gv[v8] = (p.gate && t < p.T) ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off) + v8)
+                                                     : make_uint4(0, 0, 0, 0);
                     const float inv_l = 1.f / (l_even + l_odd);
                     if (p.st_l && wg == 0 && t < p.T)
                         p.st_l[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = l_even + l_odd;
-                    for (int kh = 0; ok && kh < 2; ++kh) {
-                        if (kh == 1) {   // the staging tile is free once the first half's product completed
-                            fail = !mbar_wait(B_(bars->ep_done[0]), k & 1, p.err, abort_flag);
-                            if (named_bar_or(4, 256, fail)) { ok = false; break; }
-                        }
-                        tc_fence_after();
+                    // o_lat/l packed as bf16 pairs in place, the A operand of the W_UV product: warpgroup 0 takes
+                    // latent columns 0-255 into TMEM columns 0-127 (chunks in increasing order), warpgroup 1
+                    // latent columns 256-511 into columns 384-511 (decreasing order), so no column is written
+                    // before it has been read
+                    tc_fence_after();
     #pragma unroll 1
-                        for (int i = 0; i < 4; ++i) {
-                            const int cc = wg * 4 + i;   // 32-column chunk within this 256-column half
-                            float v[32];
-                            tmem_ld32(trow + kh * 256 + cc * 32, v);
-                            tmem_wait_ld();
-                            store_row32_bf16(base + O_P, kSlab, row, cc, v, inv_l);
-                        }
-                        fence_proxy_async_smem();
-                        tc_fence_before();
-                        named_bar_sync(4, 256);
-                        if (threadIdx.x == 128) mbar_arrive(B_(bars->olat_ready[kh]));
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = wg == 0 ? i : 7 - i;
+                        float v[32], w[16];
+                        tmem_ld32(trow + wg * 256 + c * 32, v);
+                        tmem_wait_ld();
+    #pragma unroll
+                        for (int q = 0; q < 16; ++q) w[q] = __uint_as_float(pack_bf16x2(v[2 * q] * inv_l, v[2 * q + 1] * inv_l));
+                        tmem_st16(trow + (wg == 0 ? 16 * c : 384 + 16 * c), w);
                     }
-                    if (!ok) break;
-                    fail = !mbar_wait(B_(bars->ep_done[1]), k & 1, p.err, abort_flag);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    named_bar_sync(4, 256);
+                    if (threadIdx.x == 128) mbar_arrive(B_(bars->olat_ready));
+                    TR(const long long t_pk = clock64(); if (threadIdx.x == 128) TR_ADD(TR_O_EP_PACK, t_pk - t_ep);)
+                    fail = !mbar_wait(B_(bars->ep_done), k & 1, p.err, abort_flag);
                     if (named_bar_or(4, 256, fail)) { ok = false; break; }
+                    TR(const long long t_md = clock64(); if (threadIdx.x == 128) TR_ADD(TR_O_EP_WAIT, t_md - t_pk);)
                     tc_fence_after();
                     float o[2][32];
     #pragma unroll
-                    for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + wg * 64 + c2 * 32, o[c2]);
+                    for (int c2 = 0; c2 < 2; ++c2) tmem_ld32(trow + O_EPCOL + wg * 64 + c2 * 32, o[c2]);
                     tmem_wait_ld();
                     tc_fence_before();
                     mbar_arrive(B_(bars->ep_read));   // the next tile may overwrite these TMEM columns
                     if (t < p.T) {
-                        const size_t off = ((static_cast<size_t>(ti.b) * p.T + t) * p.H + ti.h) * kD + wg * 64;
-                        const uint4 *g4 = p.gate ? reinterpret_cast<const uint4 *>(p.gate + off) : nullptr;
                         uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
     #pragma unroll
                         for (int v8 = 0; v8 < 8; ++v8) {
                             float y[8];
     #pragma unroll
                             for (int i = 0; i < 8; ++i) y[i] = o[(v8 * 8 + i) >> 5][(v8 * 8 + i) & 31];
-                            if (g4) {
-                                const uint4 gv = __ldg(g4 + v8);
-                                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                            if (p.gate) {
+                                const uint32_t gw[4] = {gv[v8].x, gv[v8].y, gv[v8].z, gv[v8].w};
     #pragma unroll
                                 for (int i = 0; i < 4; ++i) {
                                     const float g_lo = __uint_as_float(gw[i] << 16);
@@ -842,7 +854,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                         }
                     }
-                    TR(if (threadIdx.x == 128) TR_ADD(TR_O_EPILOGUE, clock64() - t_ep);)
+                    TR(if (threadIdx.x == 128) { TR_ADD(TR_O_EPILOGUE, clock64() - t_ep); TR_ADD(TR_O_EP_OUT, clock64() - t_md); })
                 }
                 TR(if (threadIdx.x == 128) TR_ADD(TR_O_COR_LOOP, clock64() - tl0);)
                 if (!ok) *abort_flag = 1;
