@@ -315,6 +315,11 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
     return d;
 }
 
+// A descriptor moved by `bytes` (a multiple of 16): the start address is the low field, in 16-byte units, and
+// no operand here reaches 256 KB, so the field never carries.  One add per MMA instead of rebuilding the
+// descriptor: the issuing thread stays ahead of the tensor pipe.
+__device__ __forceinline__ uint64_t desc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // The same descriptor for a 64-byte-swizzled operand (layout type 4): 64-byte rows in 512-byte atoms of 8 rows.
 __device__ __forceinline__ uint64_t make_smem_desc_sw64(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
     return (make_smem_desc(saddr, lbo_bytes, sbo_bytes) & ~(7ull << 61)) | (4ull << 61);

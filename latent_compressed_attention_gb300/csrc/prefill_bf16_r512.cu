@@ -352,13 +352,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (ok && gb >= 1) ok = mbar_wait(B_(bars->s_free[0]), (gb - 1) & 1, p.err, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
-    #pragma unroll 1
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint64_t a = make_smem_desc(base + S_PST + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
+                    {
+                        const uint64_t aq = make_smem_desc(base + S_PST, 16, 1024);
+                        const uint64_t bw = make_smem_desc(base + S_RING, kSlab, 1024);
     #pragma unroll
-                        for (int nh = 0; nh < 2; ++nh) {
-                            const uint64_t bd = make_smem_desc(base + S_RING + nh * 2 * kSStage + kk * 2048, kSlab, 1024);
-                            umma_bf16(tmem + nh * 256, a, bd, kIdescAbsorb, kk > 0);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint64_t a = desc_add(aq, (kk >> 2) * kSlab + (kk & 3) * 32);
+    #pragma unroll
+                            for (int nh = 0; nh < 2; ++nh)
+                                umma_bf16(tmem + nh * 256, a, desc_add(bw, nh * 2 * kSStage + kk * 2048), kIdescAbsorb,
+                                          kk > 0);
                         }
                     }
                     umma_commit(B_(bars->absorb_done));
@@ -375,12 +378,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             if (!(ok = mbar_wait(B_(bars->sc_full[st]), (it / kSStages) & 1, p.err, abort_flag))) break;
                             TR(w_full += clock64() - _b; w_blk += clock64() - _b;)
                             tc_fence_after();
+                            const uint64_t b0 = make_smem_desc(base + S_RING + st * kSStage, 16, 1024);
+                            const uint32_t a0 = tmem + S_QCOL + kc * 32;
     #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t bd = make_smem_desc(base + S_RING + st * kSStage + kk * 32, 16, 1024);
-                                umma_bf16_tmem_a(tmem + S_SCOL, tmem + S_QCOL + (kc * 4 + kk) * 8, bd, kIdescQK,
-                                                 (kc | kk) != 0);
-                            }
+                            for (int kk = 0; kk < 4; ++kk)
+                                umma_bf16_tmem_a(tmem + S_SCOL, a0 + kk * 8, desc_add(b0, kk * 32), kIdescQK, (kc | kk) != 0);
                             umma_commit(B_(bars->sc_empty[st]));
                         }
                         if (!ok) break;
@@ -468,14 +470,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             TR(w_oc += clock64() - _o; w_u += clock64() - _o;)
                             tc_fence_after();
                             if (leader) {
+                                const uint64_t a0 = make_smem_desc(base + O_P + pb * kPBytes, 16, 1024);
+                                const uint64_t b0 = make_smem_desc(base + O_RING + st * kOStage, kSlab, 1024);
     #pragma unroll
-                                for (int kk = 0; kk < kBN / 16; ++kk) {
-                                    const uint64_t a = make_smem_desc(
-                                        base + O_P + pb * kPBytes + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                                    const uint64_t bd =
-                                        make_smem_desc(base + O_RING + st * kOStage + kk * 2048, kSlab, 1024);
-                                    umma_bf16(tmem + nh * 256, a, bd, kIdescPV, (j > 0 || kk > 0));
-                                }
+                                for (int kk = 0; kk < kBN / 16; ++kk)
+                                    umma_bf16(tmem + nh * 256, desc_add(a0, (kk >> 2) * kSlab + (kk & 3) * 32),
+                                              desc_add(b0, kk * 2048), kIdescPV, (j > 0 || kk > 0));
                                 umma_commit(B_(bars->oc_empty[st]));
                             }
                             __syncwarp();
@@ -492,13 +492,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (!(ok = wait_all(bars->oc_full[st], (it / kOStages) & 1, false))) break;
                         tc_fence_after();
                         if (leader) {
+                            const uint64_t b0 = make_smem_desc(base + O_RING + st * kOStage, 16, 1024);
     #pragma unroll
-                            for (int kk = 0; kk < 16; ++kk) {
-                                const uint64_t bd = make_smem_desc(
-                                    base + O_RING + st * kOStage + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024);
-                                umma_bf16_tmem_a(tmem + O_EPCOL, tmem + ep_acol(kh * 16 + kk), bd, kIdescEp,
-                                                 (kh > 0 || kk > 0));
-                            }
+                            for (int kk = 0; kk < 16; ++kk)
+                                umma_bf16_tmem_a(tmem + O_EPCOL, tmem + ep_acol(kh * 16 + kk),
+                                                 desc_add(b0, (kk >> 2) * kSlab + (kk & 3) * 32), kIdescEp, (kh > 0 || kk > 0));
                             umma_commit(B_(bars->oc_empty[st]));
                             if (kh == 1) umma_commit(B_(bars->ep_done));
                         }
