@@ -224,19 +224,32 @@ __global__ void __launch_bounds__(kThreads, 2)
         // S(j + 1) is issued as soon as the softmax has read S(j) out of TMEM, so the next block's scores are
         // ready when the softmax finishes block j; then P(j) . c(j).  The score operand is the pair hi + lo
         // (hi from the q tile, lo from TMEM): S = hi . c^T + lo . c^T, over the r latent columns only.
-        const int ksteps = p.r / 16;
-        // the latent tile as the score product's K-major operand (latent columns = K)
-        auto c_kmajor = [&](int st, int kk) {
-            const uint32_t a = base + RING + st * st_bytes + kk * 32;
+        // Descriptors: built once per block from the stage's base and advanced by adding offsets, with no
+        // branch between two MMAs, so the issuing thread keeps up with these short products.  The latent tile
+        // is the score product's K-major operand (latent columns = K) and P . c's MN-major one.
+        const uint64_t q_desc = make_smem_desc(base + QT, 16, 1024);
+        auto c_desc = [&](int st) {   // K step kk at + 32 kk bytes (K-major); 16 keys at + kv_step (MN-major)
+            const uint32_t a = base + RING + st * st_bytes;
             return narrow ? make_smem_desc_sw64(a, 16, 512) : make_smem_desc(a, 16, 1024);
         };
+        const uint32_t kv_step = narrow ? 1024u : 2048u;
+        const uint64_t pv_b_lbo = static_cast<uint64_t>((8192u - 16u) >> 4) << 16;   // leading offset 16 -> 8192
         auto issue_scores = [&](int j) {
-            const int st = j % n_stages;
+            const uint64_t cb = c_desc(j % n_stages);
             tc_fence_after();
-            for (int kk = 0; kk < ksteps; ++kk)
-                umma_bf16(tmem + S_COL, make_smem_desc(base + QT + kk * 32, 16, 1024), c_kmajor(st, kk), id_qk, kk > 0);
-            for (int kk = 0; kk < ksteps; ++kk)
-                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + kk * 8, c_kmajor(st, kk), id_qk, 1);
+            if (narrow) {   // r = 32: two K steps of hi, two of lo
+                umma_bf16(tmem + S_COL, q_desc, cb, id_qk, 0);
+                umma_bf16(tmem + S_COL, desc_add(q_desc, 32), desc_add(cb, 32), id_qk, 1);
+                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL, cb, id_qk, 1);
+                umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + 8, desc_add(cb, 32), id_qk, 1);
+            } else {        // r = 64: four of each
+    #pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(tmem + S_COL, desc_add(q_desc, kk * 32), desc_add(cb, kk * 32), id_qk, kk > 0);
+    #pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16_tmem_a(tmem + S_COL, tmem + LO_COL + kk * 8, desc_add(cb, kk * 32), id_qk, 1);
+            }
             umma_commit(B_(bars->s_full));
             STL(0, j);
         };
@@ -252,12 +265,13 @@ __global__ void __launch_bounds__(kThreads, 2)
             STL(1, j);
             tc_fence_after();
             const int st = j % n_stages;
+            // the MN-major view of the tile: leading byte offset 8192 (the next 64 latent columns, read at r = 64)
+            const uint64_t cv = c_desc(st) + pv_b_lbo;
+            const uint64_t pa = make_smem_desc(base + PT, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-                umma_bf16(tmem + O_COL, make_smem_desc(base + PT + (kk >> 2) * kTile + (kk & 3) * 32, 16, 1024),
-                          narrow ? make_smem_desc_sw64(base + RING + st * st_bytes + kk * 1024, 8192, 512)
-                                 : make_smem_desc(base + RING + st * st_bytes + kk * 2048, 8192, 1024),
-                          id_pv, (j > 0 || kk > 0));
+                umma_bf16(tmem + O_COL, desc_add(pa, (kk >> 2) * kTile + (kk & 3) * 32), desc_add(cv, kk * kv_step), id_pv,
+                          (j > 0 || kk > 0));
             umma_commit(B_(bars->c_empty[st]));
             umma_commit(B_(bars->pv_done));
             STL(2, j);
