@@ -208,18 +208,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else if (warp == 1 && lane == 0) {
         const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
         const uint32_t idesc = make_idesc_bf16(128, 128, amn ? 1 : 0, bmn ? 1 : 0);
+        // descriptors of stage 0; a stage and a K step of 16 move them by constant offsets (MN-major operands:
+        // two 64-wide slabs 8 KB apart, 2 KB per K step; K-major: 32 bytes per K step), so the issue loop is
+        // one add per operand per MMA
+        const uint64_t a0 = make_smem_desc(base, amn ? 8192 : 16, 1024);
+        const uint64_t b0 = make_smem_desc(base + kOpBytes, bmn ? 8192 : 16, 1024);
+        const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         for (int it = 0; it < steps; ++it) {
             const int st = it % kStages;
             if (!(ok = mbar_wait(smem_u32(full + st), (it / kStages) & 1, p.err, abort_flag))) break;
             tc_fence_after();
-            const uint32_t sa = base + st * kStageBytes, sb = sa + kOpBytes;
+            const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t a = amn ? make_smem_desc(sa + kk * 2048, 8192, 1024) : make_smem_desc(sa + kk * 32, 16, 1024);
-                const uint64_t b = bmn ? make_smem_desc(sb + kk * 2048, 8192, 1024) : make_smem_desc(sb + kk * 32, 16, 1024);
-                umma_bf16(tmem, a, b, idesc, (it | kk) != 0);
-            }
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                umma_bf16(tmem, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (it | kk) != 0);
             umma_commit(smem_u32(empty + st));
         }
         if (ok) umma_commit(smem_u32(done));
