@@ -134,6 +134,22 @@ def test_r512_latent_and_query_far_from_unit_scale(env, c_mul, q_mul):
     assert rel_err(got, ref) <= TOL_BF16
 
 
+def test_r512_latent_groups_far_apart_in_scale(env):
+    """Latent rows 2^24 apart in magnitude within one sequence (32-key groups alternating between 2^12 and
+    2^-12, a ragged last group): the f16 copy's power of two fits the large rows, the small ones keep f16's
+    subnormal precision, and their scores and values are negligible next to the large rows' in the output."""
+    _, _, oracle = env
+    B, T, H = 2, 300, 2
+    d = r512(B, T, H, seed=21)
+    rows = np.arange(T)
+    mul = np.where((rows // 32) % 2 == 0, 2.0**12, 2.0**-12).astype(np.float32)
+    d["c"] = d["c"] * mul[None, :, None]
+    scale = 2.0**-12 / np.sqrt(128)
+    got = run_prefill(env, d, scale).reshape(B, T, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale)
+    assert rel_err(got, ref) <= TOL_BF16
+
+
 def test_r512_causality_bitwise(env):
     torch, lca, _ = env
     d = r512(1, 400, 2, seed=5)
