@@ -77,6 +77,11 @@ struct GemmP {
     const __nv_bfloat16 *p_in;          // kDS: P
     const __nv_bfloat16 *dl_in;         // kOLat: do_lat
     void *out;
+    float *part;                        // split K: part k of a tile's sum at part + k * part_n, out's layout
+    long long part_n;                   // elements of one part
+    int nmt, nnt, nz;                   // row tiles, column tiles, batch items
+    int ksplit;                         // dc and the weight gradients: parts each tile's K steps are cut into
+    int items;                          // work items of the launch
     int *err;
 };
 
@@ -99,6 +104,68 @@ __device__ __forceinline__ KWalk k_walk(const GemmP &p, int m0) {
         case kDc: return {p.H, m0, p.T, 2};                                        // t >= u, every head
         default: return {p.B, 0, p.T, 1};                                          // kDWuk, kDWuv: every sequence
     }
+}
+
+// A work item: output tile (mt, nt) of batch item z, and for a split K the part ks of the tile's K steps.
+// The order puts the longest items first where K depends on the row tile, and keeps the items that share
+// an operand next to each other (the column tiles of one row tile run side by side).
+struct Item {
+    int mt, nt, z, ks;
+};
+__device__ __forceinline__ Item item_of(const GemmP &p, int idx) {
+    Item t{0, 0, 0, 0};
+    if (causal_tiles(p.problem)) {   // the lower triangle (nt <= mt) of one batch item after another
+        const int ntri = p.nmt * (p.nmt + 1) / 2;
+        t.z = idx / ntri;
+        const int r = idx - t.z * ntri;
+        int mt = static_cast<int>((sqrtf(8.f * static_cast<float>(r) + 1.f) - 1.f) * 0.5f);
+        while ((mt + 1) * (mt + 2) / 2 <= r) ++mt;
+        while (mt > 0 && mt * (mt + 1) / 2 > r) --mt;
+        t.mt = mt;
+        t.nt = r - mt * (mt + 1) / 2;
+        return t;
+    }
+    t.nt = idx % p.nnt;
+    const int r = idx / p.nnt;
+    switch (p.problem) {
+        case kOLat: case kDqAbs:   // K = the causal prefix of the row tile: the last row tiles first
+            t.z = r % p.nz;
+            t.mt = p.nmt - 1 - r / p.nz;
+            break;
+        case kDc: {                // K = keys t >= u: the first row tiles first
+            const int zk = r % (p.nz * p.ksplit);
+            t.mt = r / (p.nz * p.ksplit);
+            t.z = zk % p.nz;
+            t.ks = zk / p.nz;
+            break;
+        }
+        case kDWuk: case kDWuv:    // a single row tile
+            t.z = r % p.nz;
+            t.ks = r / p.nz;
+            break;
+        default:
+            t.mt = r % p.nmt;
+            t.z = r / p.nmt;
+            break;
+    }
+    return t;
+}
+
+// The K steps of an item: steps s_lo .. s_hi - 1 of the tile's walk, step s = (outer o, inner k, pair pr)
+// with pr = s % pairs, k = lo + 64 ((s / pairs) % inner), o = s / (pairs inner).
+struct Walk {
+    int lo, inner, pairs, s_lo, s_hi;
+};
+__device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
+    const KWalk kw = k_walk(p, t.mt * kBM);
+    Walk w;
+    w.lo = kw.lo;
+    w.pairs = kw.pairs;
+    w.inner = kw.hi > kw.lo ? (kw.hi - kw.lo + kBK - 1) / kBK : 0;
+    const long long total = static_cast<long long>(kw.outer) * w.inner * kw.pairs;
+    w.s_lo = static_cast<int>(total * t.ks / p.ksplit);
+    w.s_hi = static_cast<int>(total * (t.ks + 1) / p.ksplit);
+    return w;
 }
 
 // TMA loads of one K step into stage memory: A at sa, B at sb (each 16 KB).  z: batch item of the output tile,
@@ -147,38 +214,40 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
     }
 }
 
+// Persistent: CTA i takes items i, i + G, i + 2G, ... (G = the grid).  The TMA ring runs on across items, and
+// the accumulator alternates between two 128-column halves of the CTA's TMEM, so one item's epilogue overlaps
+// the next item's products.
 __global__ void __launch_bounds__(kThreads, 2)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
                     const GemmP p) {
-    const int mt = static_cast<int>(blockIdx.x), nt = static_cast<int>(blockIdx.y), z = static_cast<int>(blockIdx.z);
-    if (causal_tiles(p.problem) && nt > mt) return;   // entirely above the diagonal: never written, never read
-    const int m0 = mt * kBM, n0 = nt * kBN;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + kBarOff);
     uint64_t *empty = full + kStages;
-    uint64_t *done = empty + kStages;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    uint64_t *acc_full = empty + kStages;     // [2] the accumulator holds an item's finished sums
+    uint64_t *acc_empty = acc_full + 2;       // [2] the epilogue has read them out
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const KWalk kw = k_walk(p, m0);
-    const int inner = kw.hi > kw.lo ? (kw.hi - kw.lo + kBK - 1) / kBK : 0;
-    const int steps = kw.outer * inner * kw.pairs;
+    const int G = static_cast<int>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(full + i), 1);
             mbar_init(smem_u32(empty + i), 1);
         }
-        mbar_init(smem_u32(done), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(acc_full + i), 1);
+            mbar_init(smem_u32(acc_empty + i), 128);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 128);
+        tmem_alloc(smem_u32(tmem_slot), 256);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -191,17 +260,20 @@ __global__ void __launch_bounds__(kThreads, 2)
         tma_prefetch_desc(&tm_b);
         bool ok = true;
         int it = 0;
-        for (int o = 0; ok && o < kw.outer; ++o)
-            for (int ks = 0; ok && ks < inner; ++ks)
-                for (int pr = 0; pr < kw.pairs; ++pr, ++it) {
-                    const int st = it % kStages;
-                    if (it >= kStages && !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages) - 1) & 1, p.err, abort_flag)))
-                        break;
-                    const uint32_t bar = smem_u32(full + st);
-                    mbar_arrive_expect_tx(bar, kStageBytes);
-                    load_step(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
-                              bar, z, o, kw.lo + ks * kBK, pr, m0, n0);
-                }
+        for (int idx = static_cast<int>(blockIdx.x); ok && idx < p.items; idx += G) {
+            const Item t = item_of(p, idx);
+            const Walk w = walk_of(p, t);
+            for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
+                const int st = it % kStages;
+                if (it >= kStages && !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages) - 1) & 1, p.err, abort_flag)))
+                    break;
+                const int pr = s % w.pairs, s2 = s / w.pairs;
+                const uint32_t bar = smem_u32(full + st);
+                mbar_arrive_expect_tx(bar, kStageBytes);
+                load_step(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
+                          bar, t.z, s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * kBM, t.nt * kBN);
+            }
+        }
         if (!ok) *abort_flag = 1;
         for (int q = (it > kStages ? it - kStages : 0); q < it; ++q)   // no load may still be landing at exit
             mbar_wait(smem_u32(full + q % kStages), (q / kStages) & 1, p.err);
@@ -215,28 +287,46 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint64_t b0 = make_smem_desc(base + kOpBytes, bmn ? 8192 : 16, 1024);
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
-        for (int it = 0; it < steps; ++it) {
-            const int st = it % kStages;
-            if (!(ok = mbar_wait(smem_u32(full + st), (it / kStages) & 1, p.err, abort_flag))) break;
+        int it = 0, lt = 0;
+        for (int idx = static_cast<int>(blockIdx.x); ok && idx < p.items; idx += G, ++lt) {
+            const Walk w = walk_of(p, item_of(p, idx));
+            const int acc = lt & 1;
+            if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
             tc_fence_after();
-            const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
+            const uint32_t d = tmem + acc * 128;
+            const int n = w.s_hi - w.s_lo;
+            for (int j = 0; j < n; ++j, ++it) {
+                const int st = it % kStages;
+                if (!(ok = mbar_wait(smem_u32(full + st), (it / kStages) & 1, p.err, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                umma_bf16(tmem, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (it | kk) != 0);
-            umma_commit(smem_u32(empty + st));
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma_bf16(d, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (j | kk) != 0);
+                umma_commit(smem_u32(empty + st));
+            }
+            if (!ok) break;
+            if (n > 0) umma_commit(smem_u32(acc_full + acc));
+            else mbar_arrive(smem_u32(acc_full + acc));   // nothing to add up: the epilogue writes zeros
         }
-        if (ok) umma_commit(smem_u32(done));
-        else *abort_flag = 1;
+        if (!ok) *abort_flag = 1;
     } else if (warp >= 2) {
         // epilogue: thread `row` owns TMEM lane row (warp w reads lanes 32 (w % 4) .. + 31)
         const int row = (warp & 3) * 32 + lane;
-        const int m = m0 + row;
-        const uint32_t trow = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-        bool ok = true;
-        if (steps > 0) ok = mbar_wait(smem_u32(done), 0, p.err, abort_flag);
-        tc_fence_after();
-        if (__all_sync(0xffffffffu, ok)) {
-            const int pr = p.problem;
+        const int pr = p.problem;
+        int lt = 0;
+        for (int idx = static_cast<int>(blockIdx.x); idx < p.items; idx += G, ++lt) {
+            const Item t = item_of(p, idx);
+            const Walk w = walk_of(p, t);
+            const bool any = w.s_hi > w.s_lo;
+            const int acc = lt & 1;
+            const int mt = t.mt, nt = t.nt, z = t.z;
+            const int m = mt * kBM + row, n0 = nt * kBN;
+            const uint32_t trow = tmem + acc * 128 + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
+            if (!ok) *abort_flag = 1;   // every later wait of every role then returns at once
+            tc_fence_after();
+            if (!__all_sync(0xffffffffu, ok)) break;
             float mrow = 0.f, inv_l = 0.f, drow = 0.f, rsum = 0.f;
             const size_t ri = static_cast<size_t>(z) * p.T + m;
             if (m < p.M && (pr == kP || pr == kDS)) {
@@ -250,12 +340,20 @@ __global__ void __launch_bounds__(kThreads, 2)
                     drow = num / p.psum[ri];
                 }
             }
+            if (!any) {   // the accumulator was not touched: release it now
+                tc_fence_before();
+                mbar_arrive(smem_u32(acc_empty + acc));
+            }
 #pragma unroll 1
             for (int c4 = 0; c4 < kBN / 32; ++c4) {
                 float v[32];
-                if (steps > 0) {
+                if (any) {
                     tmem_ld32(trow + c4 * 32, v);
                     tmem_wait_ld();
+                    if (c4 == kBN / 32 - 1) {   // every column is in registers: the next item may accumulate here
+                        tc_fence_before();
+                        mbar_arrive(smem_u32(acc_empty + acc));
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -339,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                     if (pr == kDc) off = (static_cast<size_t>(z) * p.T + m) * kR + nb;
                     else if (pr == kDq) off = ((static_cast<size_t>(z / p.H) * p.T + m) * p.H + z % p.H) * kD + nb;
                     else off = (static_cast<size_t>(z) * p.M + m) * kR + nb;   // dW_UK, dW_UV [H, 128, r]
-                    float4 *o4 = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off);
+                    float *dst = p.ksplit > 1 ? p.part + static_cast<size_t>(t.ks) * p.part_n : static_cast<float *>(p.out);
+                    float4 *o4 = reinterpret_cast<float4 *>(dst + off);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
@@ -358,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 128);
+    if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
 // do = dout * sigmoid(g) (head-major [z, T, d_v] bf16) and dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
@@ -393,6 +492,22 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__re
 
 }
 
+// out = part[0] + part[1] + ... + part[parts - 1], in that order (the gradients are the same bits on every call).
+__global__ void __launch_bounds__(256) split_sum_kernel(const float4 *__restrict__ part, int parts, long long n4,
+                                                        float4 *__restrict__ out) {
+    const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+    if (i >= n4) return;
+    float4 acc = __ldg(part + i);
+    for (int k = 1; k < parts; ++k) {
+        const float4 v = __ldg(part + static_cast<long long>(k) * n4 + i);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
+    out[i] = acc;
+}
+
 CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides_bytes,
              const cuuint32_t *box) {
     auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_fn());
@@ -406,8 +521,11 @@ CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, 
 size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
-    size_t o, pre, st_m, st_l, psum, psum_part, dnum_part, do_hm, qa, qlo, dl, ol, dqa, P, dS, end;
+    size_t o, pre, st_m, st_l, psum, psum_part, dnum_part, do_hm, qa, qlo, dl, ol, dqa, P, dS, part, end;
 };
+// dc and the weight gradients cut each tile's K steps into up to this many parts (fp32 partial sums in the
+// workspace, added in a fixed order afterwards), so that their few long tiles spread over the SMs
+constexpr int kMaxSplit = 8;
 BwdLayout bwd_layout(long long B, long long T, long long H) {
     const long long Tp = (T + 127) / 128 * 128;
     const size_t rows = static_cast<size_t>(B) * H * T;
@@ -427,7 +545,8 @@ BwdLayout bwd_layout(long long B, long long T, long long H) {
     L.dqa = L.ol + al(rows * kR * 2);
     L.P = L.dqa + al(rows * kR * 2);
     L.dS = L.P + al(rows * Tp * 2);
-    L.end = L.dS + al(rows * Tp * 2);
+    L.part = L.dS + al(rows * Tp * 2);
+    L.end = L.part + al(static_cast<size_t>(kMaxSplit) * static_cast<size_t>(B * T > H * kD ? B * T : H * kD) * kR * 4);
     return L;
 }
 
@@ -509,6 +628,11 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     if (!okm) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
     if (e != cudaSuccess) return e;
+    const int G = 2 * (a.num_sms > 0 ? a.num_sms : 1);   // two CTAs per SM
+    auto split_for = [&](long long base_items) {   // parts per tile: about four items per CTA
+        const long long k = (4LL * G + base_items - 1) / base_items;
+        return static_cast<int>(k < 1 ? 1 : (k > kMaxSplit ? kMaxSplit : k));
+    };
     auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                     const CUtensorMap &tb2, int M, int N, int Z, void *out) {
         GemmP gp{};
@@ -532,9 +656,30 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.dl_in = bf(L.dl);
         gp.out = out;
         gp.err = a.dev_err;
-        const dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN, Z);
+        gp.nmt = (M + kBM - 1) / kBM;
+        gp.nnt = (N + kBN - 1) / kBN;
+        gp.nz = Z;
+        gp.ksplit = 1;
+        gp.part = f32(L.part);
+        gp.part_n = static_cast<long long>(Z) * M * N;
+        long long items;
+        if (pr == kP || pr == kDS) {
+            items = static_cast<long long>(Z) * gp.nmt * (gp.nmt + 1) / 2;
+        } else {
+            if (pr == kDc || pr == kDWuk || pr == kDWuv) gp.ksplit = split_for(static_cast<long long>(gp.nmt) * gp.nnt * Z);
+            items = static_cast<long long>(gp.nmt) * gp.nnt * Z * gp.ksplit;
+        }
+        if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
+        gp.items = static_cast<int>(items);
+        const unsigned grid = static_cast<unsigned>(items < G ? items : G);
         note_launch();
         bwd_gemm_kernel<<<grid, kThreads, kSmem, s>>>(ta, tb, ta2, tb2, gp);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess || gp.ksplit == 1) return err;
+        const long long n4 = gp.part_n / 4;   // N = r: a multiple of 4
+        note_launch();
+        split_sum_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, s>>>(
+            reinterpret_cast<const float4 *>(gp.part), gp.ksplit, n4, static_cast<float4 *>(out));
         return cudaGetLastError();
     };
     const int Z = static_cast<int>(rowsz);

@@ -110,3 +110,20 @@ def test_bwd_r512_stale_workspace(env):
     assert lca.mla_get_device_error() == 0
     _, ref = run(env, d, 1.0)
     check({k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref)
+
+
+def test_bwd_r512_many_items_per_cta(env):
+    """More work items than resident CTAs in the large products (624 attention-matrix tiles, 384 o_lat and dq_abs
+    tiles, dc and the weight gradients split over K), a ragged T: each CTA's TMA ring runs on across items and
+    its accumulator alternates between two TMEM halves.  Two calls give the same bits."""
+    torch, lca, _ = env
+    d = case(2, 1500, 4, seed=31)
+    got, ref = run(env, d, 1.0 / np.sqrt(128.0))
+    check(got, ref)
+    t = lambda a: None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)  # noqa: E731
+    again = lca.mla_absorbed_attn_bwd(t(d["q"]), t(d["c"]), t(d["w_uk"]), t(d["w_uv"]), t(d["gate"]),
+                                      1.0 / np.sqrt(128.0), t(d["dout"]))
+    torch.cuda.synchronize()
+    for k in KEYS:
+        if got[k] is not None:
+            assert np.array_equal(got[k], again[k].double().cpu().numpy()), k
