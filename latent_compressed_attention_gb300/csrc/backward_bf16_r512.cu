@@ -79,6 +79,7 @@ struct GemmP {
     void *out;
     float *part;                        // split K: part k of a tile's sum at part + k * part_n, out's layout
     long long part_n;                   // elements of one part
+    int tile_m;                         // rows (and columns) of an output tile: 128, or 256 for a CTA pair
     int nmt, nnt, nz;                   // row tiles, column tiles, batch items
     int ksplit;                         // dc and the weight gradients: parts each tile's K steps are cut into
     int items;                          // work items of the launch
@@ -100,7 +101,7 @@ __device__ __forceinline__ KWalk k_walk(const GemmP &p, int m0) {
         case kQAbs: case kDoLat: return {1, 0, kD, 1};
         case kP: return {1, 0, kR, 2};                                             // hi and lo
         case kDS: case kDq: return {1, 0, kR, 1};
-        case kOLat: case kDqAbs: return {1, 0, min(p.T, m0 + kBM), 1};           // u <= t
+        case kOLat: case kDqAbs: return {1, 0, min(p.T, m0 + p.tile_m), 1};      // u <= t
         case kDc: return {p.H, m0, p.T, 2};                                        // t >= u, every head
         default: return {p.B, 0, p.T, 1};                                          // kDWuk, kDWuv: every sequence
     }
@@ -114,8 +115,18 @@ struct Item {
 };
 __device__ __forceinline__ Item item_of(const GemmP &p, int idx) {
     Item t{0, 0, 0, 0};
-    if (causal_tiles(p.problem)) {   // the lower triangle (nt <= mt) of one batch item after another
+    if (causal_tiles(p.problem)) {
+        // The lower triangle (nt <= mt) of one batch item after another.  With 128-row tiles, the items after
+        // those are the tiles just above the diagonal at even mt (no K steps: zeros), which the 256-row dc
+        // products read.
         const int ntri = p.nmt * (p.nmt + 1) / 2;
+        if (p.tile_m == 128 && idx >= p.nz * ntri) {
+            const int j = idx - p.nz * ntri, nzt = p.nmt / 2;
+            t.z = j / nzt;
+            t.mt = 2 * (j % nzt);
+            t.nt = t.mt + 1;
+            return t;
+        }
         t.z = idx / ntri;
         const int r = idx - t.z * ntri;
         int mt = static_cast<int>((sqrtf(8.f * static_cast<float>(r) + 1.f) - 1.f) * 0.5f);
@@ -157,12 +168,13 @@ struct Walk {
     int lo, inner, pairs, s_lo, s_hi;
 };
 __device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
-    const KWalk kw = k_walk(p, t.mt * kBM);
+    const KWalk kw = k_walk(p, t.mt * p.tile_m);
     Walk w;
     w.lo = kw.lo;
     w.pairs = kw.pairs;
     w.inner = kw.hi > kw.lo ? (kw.hi - kw.lo + kBK - 1) / kBK : 0;
-    const long long total = static_cast<long long>(kw.outer) * w.inner * kw.pairs;
+    long long total = static_cast<long long>(kw.outer) * w.inner * kw.pairs;
+    if (causal_tiles(p.problem) && t.nt > t.mt) total = 0;   // a tile of zeros
     w.s_lo = static_cast<int>(total * t.ks / p.ksplit);
     w.s_hi = static_cast<int>(total * (t.ks + 1) / p.ksplit);
     return w;
@@ -170,6 +182,19 @@ __device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
 
 // TMA loads of one K step into stage memory: A at sa, B at sb (each 16 KB).  z: batch item of the output tile,
 // o: the outer K index, k: the inner K offset, pair: which operand pair (dc).
+template <bool kPair>
+__device__ __forceinline__ void tl3(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z) {
+    if constexpr (kPair) tma2_load_3d(dst, m, bar, x, y, z);
+    else tma_load_3d(dst, m, bar, x, y, z);
+}
+template <bool kPair>
+__device__ __forceinline__ void tl4(uint32_t dst, const CUtensorMap *m, uint32_t bar, int x, int y, int z, int w) {
+    if constexpr (kPair) tma2_load_4d(dst, m, bar, x, y, z, w);
+    else tma_load_4d(dst, m, bar, x, y, z, w);
+}
+
+// (kPair: the loads of one CTA of a pair, completing on the pair's even CTA's barrier `bar`.)
+template <bool kPair>
 __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta, const CUtensorMap *tb,
                                           const CUtensorMap *ta2, const CUtensorMap *tb2, uint32_t sa, uint32_t sb,
                                           uint32_t bar, int z, int o, int k, int pair, int m0, int n0) {
@@ -178,39 +203,177 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
     const int zz = b * p.H + h;   // head-major batch item of the per-head matrices
     switch (p.problem) {
         case kQAbs:   // A = q [B,T,H,d] (K-major), B = W_UK [H,d,r] (MN-major)
-            tma_load_4d(sa, ta, bar, k, h, m0, b);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            tl4<kPair>(sa, ta, bar, k, h, m0, b);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
             break;
         case kDoLat:  // A = do [z,T,d_v], B = W_UV [H,d_v,r]
-            tma_load_3d(sa, ta, bar, k, m0, zz);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            tl3<kPair>(sa, ta, bar, k, m0, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
             break;
         case kP: case kDS:   // A = q_abs (hi, then lo) or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
-            tma_load_3d(sa, pair ? ta2 : ta, bar, k, m0, zz);
-            tma_load_3d(sb, tb, bar, k, n0, b);
+            tl3<kPair>(sa, pair ? ta2 : ta, bar, k, m0, zz);
+            tl3<kPair>(sb, tb, bar, k, n0, b);
             break;
         case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
-            tma_load_3d(sa, ta, bar, k, m0, zz);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, b);
+            tl3<kPair>(sa, ta, bar, k, m0, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, b);
             break;
         case kDc: {   // A = P^T or dS^T (MN-major: rows t, u contiguous), B = do_lat or q_abs (MN-major: rows t)
             const CUtensorMap *a = pair ? ta2 : ta, *bm = pair ? tb2 : tb;
-            for (int s = 0; s < 2; ++s) tma_load_3d(sa + s * 8192, a, bar, m0 + 64 * s, k, zz);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, bm, bar, n0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sa + s * 8192, a, bar, m0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, bm, bar, n0 + 64 * s, k, zz);
             break;
         }
         case kDq:   // A = dq_abs [z,T,r] (K-major), B = W_UK [H,d,r] (K-major: rows d)
-            tma_load_3d(sa, ta, bar, k, m0, zz);
-            tma_load_3d(sb, tb, bar, k, n0, h);
+            tl3<kPair>(sa, ta, bar, k, m0, zz);
+            tl3<kPair>(sb, tb, bar, k, n0, h);
             break;
         case kDWuk:   // A = q^T (MN-major: rows t, d contiguous), B = dq_abs (MN-major: rows t)
-            for (int s = 0; s < 2; ++s) tma_load_4d(sa + s * 8192, ta, bar, m0 + 64 * s, h, k, b);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tl4<kPair>(sa + s * 8192, ta, bar, m0 + 64 * s, h, k, b);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
             break;
         default:   // kDWuv: A = do^T (MN-major: rows t), B = o_lat (MN-major: rows t)
-            for (int s = 0; s < 2; ++s) tma_load_3d(sa + s * 8192, ta, bar, m0 + 64 * s, k, zz);
-            for (int s = 0; s < 2; ++s) tma_load_3d(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sa + s * 8192, ta, bar, m0 + 64 * s, k, zz);
+            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
             break;
+    }
+}
+
+// The epilogue's per-row inputs of an item, read before its sums are ready: the softmax statistics (P) or
+// delta (dS).
+struct RowIn {
+    float mrow, inv_l, drow;
+};
+__device__ __forceinline__ void read_row_stats(const GemmP &p, int z, int m, RowIn &r) {
+    const int pr = p.problem;
+    r.mrow = r.inv_l = r.drow = 0.f;
+    if (m >= p.M) return;
+    const size_t ri = static_cast<size_t>(z) * p.T + m;
+    if (pr == kP) {
+        r.mrow = __ldg(p.st_m + ri);
+        r.inv_l = 1.f / __ldg(p.st_l + ri);
+    } else if (pr == kDS) {   // written by earlier launches, added in a fixed order
+        float num = 0.f;
+#pragma unroll
+        for (int q = 0; q < kR / kBN; ++q) num += p.dnum_part[q * p.rows + ri];
+        r.drow = num / p.psum[ri];
+    }
+}
+// 32 bf16 of row m's P (dS) or do_lat (o_lat) from column nb, for the chunk of the epilogue that needs them.
+__device__ __forceinline__ void read_chunk_input(const GemmP &p, int z, int m, int nb, uint4 (&in)[4]) {
+    const int pr = p.problem;
+    if (m >= p.M || (pr != kDS && pr != kOLat)) return;
+    const size_t ri = static_cast<size_t>(z) * p.T + m;
+    const uint4 *src = reinterpret_cast<const uint4 *>(pr == kDS ? p.p_in + ri * p.Tp + nb : p.dl_in + ri * kR + nb);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) in[q] = __ldg(src + q);
+}
+
+// One 32-column chunk of an item's epilogue: row m of batch item z, columns nb .. nb + 31, the fp32 sums v.
+// (mrow, inv_l: the row's softmax statistics for P; drow: its delta for dS; rsum: the row's running sum of
+// P as rounded, or of do_lat . o_lat; ks: the K part of a split item; in: the chunk's 32 bf16 of P (dS) or of
+// do_lat (o_lat).)
+__device__ __forceinline__ void epilogue_chunk(const GemmP &p, int z, int m, int nb, int ks, float (&v)[32], float mrow,
+                                               float inv_l, float drow, float &rsum, const uint4 (&in)[4]) {
+    const int pr = p.problem;
+    // P and dS rows are written out to their padded width Tp (zeros past the diagonal): the products
+    // that read them take K in steps of 64 up to the end of the diagonal tile
+    if (m >= p.M || nb >= ((pr == kP || pr == kDS) ? p.Tp : p.N)) return;
+    if (pr == kP || pr == kDS) {
+        __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb;
+        float pv[32];
+        if (pr == kDS) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = in[q];
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    pv[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
+                    pv[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const bool vis = nb + i <= m;   // causal: key u <= query t
+            if (pr == kP)
+                v[i] = vis ? fast_exp2(fmaf(v[i], p.scale_log2, -mrow)) * inv_l : 0.f;
+            else
+                v[i] = vis ? p.scale * pv[i] * (v[i] - drow) : 0.f;
+        }
+        uint4 *o4 = reinterpret_cast<uint4 *>(o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t wq[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                wq[e] = pack_bf16x2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
+                if (pr == kP)   // the row sum of P as rounded
+                    rsum += __uint_as_float(wq[e] << 16) + __uint_as_float(wq[e] & 0xFFFF0000u);
+            }
+            o4[q] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+    } else if (pr <= kDqAbs) {   // bf16 [z, T, r]
+        if (pr == kQAbs) {   // the lo part: bf16(x - bf16(x))
+            uint4 *l4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out2) +
+                                                  (static_cast<size_t>(z) * p.T + m) * kR + nb);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x0 = v[8 * q + 2 * e], x1 = v[8 * q + 2 * e + 1];
+                    const uint32_t hw = pack_bf16x2(x0, x1);
+                    lw[e] = pack_bf16x2(x0 - __uint_as_float(hw << 16), x1 - __uint_as_float(hw & 0xFFFF0000u));
+                }
+                l4[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+        if (pr == kOLat) {   // do_lat . o_lat over these 32 columns
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = in[q];
+                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    rsum += v[8 * q + 2 * e] * __uint_as_float(ww[e] << 16) +
+                            v[8 * q + 2 * e + 1] * __uint_as_float(ww[e] & 0xFFFF0000u);
+            }
+        }
+        uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
+                                              (static_cast<size_t>(z) * p.T + m) * kR + nb);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                               pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+    } else {   // fp32 gradients
+        size_t off;
+        if (pr == kDc) off = (static_cast<size_t>(z) * p.T + m) * kR + nb;
+        else if (pr == kDq) off = ((static_cast<size_t>(z / p.H) * p.T + m) * p.H + z % p.H) * kD + nb;
+        else off = (static_cast<size_t>(z) * p.M + m) * kR + nb;   // dW_UK, dW_UV [H, 128, r]
+        float *dst = p.ksplit > 1 ? p.part + static_cast<size_t>(ks) * p.part_n : static_cast<float *>(p.out);
+        float4 *o4 = reinterpret_cast<float4 *>(dst + off);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+}
+
+// After the chunks of a row: the row sum of the rounded P over one 128-column key tile (slot = the key tile),
+// or do_lat . o_lat over one 128-column tile of o_lat (slot = that tile); the o_lat tile of columns 0-127 also
+// adds up P's slots of key tiles 0 .. m / 128, in order.
+__device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int slot, float rsum) {
+    const int pr = p.problem;
+    if (m >= p.M) return;
+    const size_t ri = static_cast<size_t>(z) * p.T + m;
+    if (pr == kP && slot < p.Tp / kBM) p.psum_part[static_cast<size_t>(slot) * p.rows + ri] = rsum;
+    if (pr == kOLat) {
+        p.dnum_part[static_cast<size_t>(slot) * p.rows + ri] = rsum;
+        if (slot == 0) {   // the P launch has finished
+            float ps = 0.f;
+            for (int j = 0; j <= m / kBM; ++j) ps += p.psum_part[static_cast<size_t>(j) * p.rows + ri];
+            p.psum[ri] = ps;
+        }
     }
 }
 
@@ -270,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const int pr = s % w.pairs, s2 = s / w.pairs;
                 const uint32_t bar = smem_u32(full + st);
                 mbar_arrive_expect_tx(bar, kStageBytes);
-                load_step(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
+                load_step<false>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
                           bar, t.z, s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * kBM, t.nt * kBN);
             }
         }
@@ -313,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else if (warp >= 2) {
         // epilogue: thread `row` owns TMEM lane row (warp w reads lanes 32 (w % 4) .. + 31)
         const int row = (warp & 3) * 32 + lane;
-        const int pr = p.problem;
         int lt = 0;
         for (int idx = static_cast<int>(blockIdx.x); idx < p.items; idx += G, ++lt) {
             const Item t = item_of(p, idx);
@@ -323,29 +485,21 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int mt = t.mt, nt = t.nt, z = t.z;
             const int m = mt * kBM + row, n0 = nt * kBN;
             const uint32_t trow = tmem + acc * 128 + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            RowIn rin;
+            uint4 cur[4];
+            read_row_stats(p, z, m, rin);   // in flight while the products finish
             const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
             if (!ok) *abort_flag = 1;   // every later wait of every role then returns at once
             tc_fence_after();
             if (!__all_sync(0xffffffffu, ok)) break;
-            float mrow = 0.f, inv_l = 0.f, drow = 0.f, rsum = 0.f;
-            const size_t ri = static_cast<size_t>(z) * p.T + m;
-            if (m < p.M && (pr == kP || pr == kDS)) {
-                if (pr == kP) {
-                    mrow = __ldg(p.st_m + ri);
-                    inv_l = 1.f / __ldg(p.st_l + ri);
-                } else {   // written by earlier launches, added in a fixed order
-                    float num = 0.f;
-#pragma unroll
-                    for (int q = 0; q < kR / kBN; ++q) num += p.dnum_part[q * p.rows + ri];
-                    drow = num / p.psum[ri];
-                }
-            }
+            float rsum = 0.f;
             if (!any) {   // the accumulator was not touched: release it now
                 tc_fence_before();
                 mbar_arrive(smem_u32(acc_empty + acc));
             }
 #pragma unroll 1
             for (int c4 = 0; c4 < kBN / 32; ++c4) {
+                read_chunk_input(p, z, m, n0 + c4 * 32, cur);
                 float v[32];
                 if (any) {
                     tmem_ld32(trow + c4 * 32, v);
@@ -358,106 +512,179 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
-                const int nb = n0 + c4 * 32;
-                // P and dS rows are written out to their padded width Tp (zeros past the diagonal): the products
-                // that read them take K in steps of 64 up to the end of the diagonal tile
-                if (m >= p.M || nb >= ((pr == kP || pr == kDS) ? p.Tp : p.N)) continue;
-                if (pr == kP || pr == kDS) {
-                    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.out) + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb;
-                    float pv[32];
-                    if (pr == kDS) {
-                        const uint4 *pin = reinterpret_cast<const uint4 *>(p.p_in + (static_cast<size_t>(z) * p.T + m) * p.Tp + nb);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 w = __ldg(pin + q);
-                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                pv[8 * q + 2 * e] = __uint_as_float(ww[e] << 16);
-                                pv[8 * q + 2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const bool vis = nb + i <= m;   // causal: key u <= query t
-                        if (pr == kP)
-                            v[i] = vis ? fast_exp2(fmaf(v[i], p.scale_log2, -mrow)) * inv_l : 0.f;
-                        else
-                            v[i] = vis ? p.scale * pv[i] * (v[i] - drow) : 0.f;
-                    }
-                    uint4 *o4 = reinterpret_cast<uint4 *>(o);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t wq[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            wq[e] = pack_bf16x2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1]);
-                            if (pr == kP)   // the row sum of P as rounded
-                                rsum += __uint_as_float(wq[e] << 16) + __uint_as_float(wq[e] & 0xFFFF0000u);
-                        }
-                        o4[q] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                    }
-                } else if (pr <= kDqAbs) {   // bf16 [z, T, r]
-                    if (pr == kQAbs) {   // the lo part: bf16(x - bf16(x))
-                        uint4 *l4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out2) +
-                                                              (static_cast<size_t>(z) * p.T + m) * kR + nb);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t lw[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float x0 = v[8 * q + 2 * e], x1 = v[8 * q + 2 * e + 1];
-                                const uint32_t hw = pack_bf16x2(x0, x1);
-                                lw[e] = pack_bf16x2(x0 - __uint_as_float(hw << 16), x1 - __uint_as_float(hw & 0xFFFF0000u));
-                            }
-                            l4[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                        }
-                    }
-                    if (pr == kOLat) {   // do_lat . o_lat over these 32 columns
-                        const uint4 *dl = reinterpret_cast<const uint4 *>(p.dl_in + (static_cast<size_t>(z) * p.T + m) * kR + nb);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 w = __ldg(dl + q);
-                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                rsum += v[8 * q + 2 * e] * __uint_as_float(ww[e] << 16) +
-                                        v[8 * q + 2 * e + 1] * __uint_as_float(ww[e] & 0xFFFF0000u);
-                        }
-                    }
-                    uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
-                                                          (static_cast<size_t>(z) * p.T + m) * kR + nb);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-                } else {   // fp32 gradients
-                    size_t off;
-                    if (pr == kDc) off = (static_cast<size_t>(z) * p.T + m) * kR + nb;
-                    else if (pr == kDq) off = ((static_cast<size_t>(z / p.H) * p.T + m) * p.H + z % p.H) * kD + nb;
-                    else off = (static_cast<size_t>(z) * p.M + m) * kR + nb;   // dW_UK, dW_UV [H, 128, r]
-                    float *dst = p.ksplit > 1 ? p.part + static_cast<size_t>(t.ks) * p.part_n : static_cast<float *>(p.out);
-                    float4 *o4 = reinterpret_cast<float4 *>(dst + off);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-                }
+                epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
             }
-            if (m < p.M && pr == kP) p.psum_part[static_cast<size_t>(nt) * p.rows + ri] = rsum;
-            if (m < p.M && pr == kOLat) {
-                p.dnum_part[static_cast<size_t>(nt) * p.rows + ri] = rsum;
-                if (nt == 0) {   // the P launch has finished: its row sums, key tiles 0 .. mt, in order
-                    float ps = 0.f;
-                    for (int j = 0; j <= mt; ++j) ps += p.psum_part[static_cast<size_t>(j) * p.rows + ri];
-                    p.psum[ri] = ps;
-                }
-            }
+            epilogue_row(p, z, m, nt, rsum);
         }
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// The pair form, for dc (few tiles, each with a long K): a cluster of two CTAs, one
+// per SM, computes 256 x 256 tiles with cta_group::2 MMAs.  CTA r of the pair stages rows 128 r .. 128 r + 127
+// of the tile's A and columns 128 r .. 128 r + 127 of its B, so each SM loads 32 KB per K step of 64 for
+// twice the products of a 128 x 128 tile, and holds rows 128 r .. 128 r + 127 of the 256 x 256 sums in TMEM
+// (two 256-column accumulators).  The even CTA issues the MMAs; both CTAs' loads complete on its barriers, its
+// commits arrive on both CTAs' barriers, and both CTAs' epilogue warps report to it when an accumulator is read.
+constexpr int kStages2 = 6;
+constexpr uint32_t kSmem2 = kStages2 * kStageBytes + 256 + 1024;   // one CTA per SM
+constexpr int kThreads2 = 320;   // warp 0 TMA, warp 1 MMA (even CTA), warps 2-9 epilogue (two column halves)
+static_assert(kSmem2 <= 232448, "exceeds the 227 KB shared-memory limit");
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
+    bwd_gemm2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                     const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
+                     const GemmP p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gbase + kStages2 * kStageBytes);   // even CTA: both CTAs' loads
+    uint64_t *empty = full + kStages2;         // each CTA's own: the stage's products completed
+    uint64_t *acc_full = empty + kStages2;     // [2] each CTA's own: the accumulator holds an item's sums
+    uint64_t *acc_empty = acc_full + 2;        // [2] even CTA: every epilogue warp of both CTAs has read it out
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();   // 0: the pair's MMA issuer
+    const int pair_id = static_cast<int>(blockIdx.x) >> 1, n_pairs = static_cast<int>(gridDim.x) >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages2; ++i) {
+            mbar_init(smem_u32(full + i), 1);
+            mbar_init(smem_u32(empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(acc_full + i), 1);
+            mbar_init(smem_u32(acc_empty + i), 16);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {   // one warp of each CTA of the pair, together
+        tmem_alloc2(smem_u32(tmem_slot), 512);
+        tmem_relinquish2();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // both CTAs' barriers exist before any remote arrival or load
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+        bool ok = true;
+        int it = 0;
+        for (int idx = pair_id; ok && idx < p.items; idx += n_pairs) {
+            const Item t = item_of(p, idx);
+            const Walk w = walk_of(p, t);
+            for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
+                const int st = it % kStages2;
+                if (it >= kStages2 &&
+                    !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages2) - 1) & 1, p.err, abort_flag)))
+                    break;
+                const int pr = s % w.pairs, s2 = s / w.pairs;
+                if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + st), 2 * kStageBytes);
+                load_step<true>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes,
+                                base + st * kStageBytes + kOpBytes, mapa_shared(smem_u32(full + st), 0), t.z,
+                                s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * 256 + 128 * rank,
+                                t.nt * 256 + 128 * rank);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+        if (rank == 0)   // no load of either CTA may still be landing at exit
+            for (int q = (it > kStages2 ? it - kStages2 : 0); q < it; ++q)
+                mbar_wait(smem_u32(full + q % kStages2), (q / kStages2) & 1, p.err);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
+        const uint32_t idesc = make_idesc_bf16(256, 256, amn ? 1 : 0, bmn ? 1 : 0);
+        const uint64_t a0 = make_smem_desc(base, amn ? 8192 : 16, 1024);
+        const uint64_t b0 = make_smem_desc(base + kOpBytes, bmn ? 8192 : 16, 1024);
+        const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
+        bool ok = true;
+        int it = 0, lt = 0;
+        for (int idx = pair_id; ok && idx < p.items; idx += n_pairs, ++lt) {
+            const Walk w = walk_of(p, item_of(p, idx));
+            const int acc = lt & 1;
+            if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
+            tc_fence_after();
+            const uint32_t d = tmem + acc * 256;
+            const int n = w.s_hi - w.s_lo;
+            for (int j = 0; j < n; ++j, ++it) {
+                const int st = it % kStages2;
+                if (!(ok = mbar_wait(smem_u32(full + st), (it / kStages2) & 1, p.err, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    umma2(d, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (j | kk) != 0);
+                umma2_commit(smem_u32(empty + st), 0x3);
+            }
+            if (!ok) break;
+            if (n > 0) {
+                umma2_commit(smem_u32(acc_full + acc), 0x3);
+            } else {   // nothing to add up: both CTAs' epilogues write zeros
+                mbar_arrive(smem_u32(acc_full + acc));
+                mbar_arrive_remote(smem_u32(acc_full + acc), 1);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 2) {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (this CTA's rows of the tile) and columns
+        // 128 g .. 128 g + 127 of the accumulator, g = (w - 2) / 4
+        const int g = (warp - 2) >> 2;
+        const int row = (warp & 3) * 32 + lane;
+        int lt = 0;
+        for (int idx = pair_id; idx < p.items; idx += n_pairs, ++lt) {
+            const Item t = item_of(p, idx);
+            const Walk w = walk_of(p, t);
+            const bool any = w.s_hi > w.s_lo;
+            const int acc = lt & 1;
+            const int z = t.z;
+            const int m = t.mt * 256 + 128 * static_cast<int>(rank) + row, n0 = t.nt * 256 + 128 * g;
+            const uint32_t trow = tmem + acc * 256 + 128 * g + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            RowIn rin;
+            uint4 cur[4];
+            read_row_stats(p, z, m, rin);   // in flight while the products finish
+            const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
+            if (!ok) *abort_flag = 1;
+            tc_fence_after();
+            if (!__all_sync(0xffffffffu, ok)) break;
+            float rsum = 0.f;
+            auto release = [&]() {   // this warp has read its part of the accumulator
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank == 0) mbar_arrive(smem_u32(acc_empty + acc));
+                    else mbar_arrive_remote(smem_u32(acc_empty + acc), 0);
+                }
+            };
+            if (!any) release();
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                read_chunk_input(p, z, m, n0 + c4 * 32, cur);
+                float v[32];
+                if (any) {
+                    tmem_ld32(trow + c4 * 32, v);
+                    tmem_wait_ld();
+                    if (c4 == 3) release();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                }
+                epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
+            }
+            epilogue_row(p, z, m, 2 * t.nt + g, rsum);
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    cluster_sync_all();   // no pair product is in flight and neither CTA reads the other's barriers any more
+    if (warp == 1) tmem_dealloc2(tmem, 512);
+    cluster_sync_all();
 }
 
 // do = dout * sigmoid(g) (head-major [z, T, d_v] bf16) and dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
@@ -628,13 +855,19 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     if (!okm) return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
     if (e != cudaSuccess) return e;
-    const int G = 2 * (a.num_sms > 0 ? a.num_sms : 1);   // two CTAs per SM
-    auto split_for = [&](long long base_items) {   // parts per tile: about four items per CTA
-        const long long k = (4LL * G + base_items - 1) / base_items;
+    if ((e = cudaFuncSetAttribute(bwd_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kSmem2))) != cudaSuccess)
+        return e;
+    const int sms = a.num_sms > 1 ? a.num_sms : 2;
+    auto split_for = [&](long long base_items, int slots) {   // parts per tile: about four items per slot
+        const long long k = (4LL * slots + base_items - 1) / base_items;
         return static_cast<int>(k < 1 ? 1 : (k > kMaxSplit ? kMaxSplit : k));
     };
+    // pair: 256 x 256 tiles on CTA pairs (one CTA per SM); otherwise 128 x 128 tiles, two CTAs per SM
     auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
-                    const CUtensorMap &tb2, int M, int N, int Z, void *out) {
+                    const CUtensorMap &tb2, int M, int N, int Z, void *out, bool pair) {
+        const int tile = pair ? 256 : 128;
+        const int slots = pair ? sms / 2 : 2 * sms;   // pairs, or CTAs, resident at once
         GemmP gp{};
         gp.problem = pr;
         gp.B = B;
@@ -656,24 +889,27 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.dl_in = bf(L.dl);
         gp.out = out;
         gp.err = a.dev_err;
-        gp.nmt = (M + kBM - 1) / kBM;
-        gp.nnt = (N + kBN - 1) / kBN;
+        gp.tile_m = tile;
+        gp.nmt = (M + tile - 1) / tile;
+        gp.nnt = (N + tile - 1) / tile;
         gp.nz = Z;
         gp.ksplit = 1;
         gp.part = f32(L.part);
         gp.part_n = static_cast<long long>(Z) * M * N;
         long long items;
         if (pr == kP || pr == kDS) {
-            items = static_cast<long long>(Z) * gp.nmt * (gp.nmt + 1) / 2;
+            items = static_cast<long long>(Z) * (static_cast<long long>(gp.nmt) * (gp.nmt + 1) / 2 + (pair ? 0 : gp.nmt / 2));
         } else {
-            if (pr == kDc || pr == kDWuk || pr == kDWuv) gp.ksplit = split_for(static_cast<long long>(gp.nmt) * gp.nnt * Z);
+            if (pr == kDc || pr == kDWuk || pr == kDWuv)
+                gp.ksplit = split_for(static_cast<long long>(gp.nmt) * gp.nnt * Z, slots);
             items = static_cast<long long>(gp.nmt) * gp.nnt * Z * gp.ksplit;
         }
         if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
         gp.items = static_cast<int>(items);
-        const unsigned grid = static_cast<unsigned>(items < G ? items : G);
+        const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
         note_launch();
-        bwd_gemm_kernel<<<grid, kThreads, kSmem, s>>>(ta, tb, ta2, tb2, gp);
+        if (pair) bwd_gemm2_kernel<<<2 * grid, kThreads2, kSmem2, s>>>(ta, tb, ta2, tb2, gp);
+        else bwd_gemm_kernel<<<grid, kThreads, kSmem, s>>>(ta, tb, ta2, tb2, gp);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess || gp.ksplit == 1) return err;
         const long long n4 = gp.part_n / 4;   // N = r: a multiple of 4
@@ -685,16 +921,16 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     const int Z = static_cast<int>(rowsz);
     // 3. q_abs and do_lat; 4. P (and its row sums), o_lat (and do_lat . o_lat), then dS (reads P and both sums);
     // 5. dq_abs; 6. dc and dq; 7. the weight gradients
-    if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa))) != cudaSuccess) return e;
-    if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl))) != cudaSuccess) return e;
-    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P))) != cudaSuccess) return e;
-    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol))) != cudaSuccess) return e;
-    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS))) != cudaSuccess) return e;
-    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa))) != cudaSuccess) return e;
-    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc)) != cudaSuccess) return e;
-    if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq)) != cudaSuccess) return e;
-    if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk)) != cudaSuccess) return e;
-    return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv);
+    if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa), false)) != cudaSuccess) return e;
+    if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl), false)) != cudaSuccess) return e;
+    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), false)) != cudaSuccess) return e;
+    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), false)) != cudaSuccess) return e;
+    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS), false)) != cudaSuccess) return e;
+    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), false)) != cudaSuccess) return e;
+    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc, true)) != cudaSuccess) return e;
+    if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq, false)) != cudaSuccess) return e;
+    if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk, false)) != cudaSuccess) return e;
+    return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv, false);
 }
 
 }  // namespace mla
