@@ -38,12 +38,9 @@ namespace {
 
 constexpr int kR = 512, kD = 128;
 constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStages = 3;
 constexpr uint32_t kOpBytes = 128 * 128;            // an operand's stage: [128 x 64] K-major or 2 x [64 x 64] MN-major
-constexpr uint32_t kStageBytes = 2 * kOpBytes;
-constexpr uint32_t kBarOff = kStages * kStageBytes;
-constexpr uint32_t kSmem = kBarOff + 256 + 1024;    // two CTAs per SM
-constexpr int kThreads = 192;                       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue (thread = row)
+constexpr uint32_t kStageBytes = 2 * kOpBytes;      // A and B of a 128 x 128 tile
+// warp 0 TMA, warp 1 MMA, then the epilogue warps (thread = row)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // The products of the backward.  Operand layouts: "K" = K-major (K contiguous), "MN" = M or N contiguous.
@@ -79,7 +76,8 @@ struct GemmP {
     void *out;
     float *part;                        // split K: part k of a tile's sum at part + k * part_n, out's layout
     long long part_n;                   // elements of one part
-    int tile_m;                         // rows (and columns) of an output tile: 128, or 256 for a CTA pair
+    int tile_m;                         // rows of an output tile: 128, or 256 for a CTA pair
+    int tile_n;                         // columns of an output tile: 128 or 256
     int nmt, nnt, nz;                   // row tiles, column tiles, batch items
     int ksplit;                         // dc and the weight gradients: parts each tile's K steps are cut into
     int items;                          // work items of the launch
@@ -116,6 +114,25 @@ struct Item {
 __device__ __forceinline__ Item item_of(const GemmP &p, int idx) {
     Item t{0, 0, 0, 0};
     if (causal_tiles(p.problem)) {
+        if (p.tile_n == 256) {
+            // 128-row tiles by 256-column blocks, the lower triangle (block nt starts at or left of the diagonal:
+            // nt <= mt / 2) of one batch item after another; row tile mt starts at item C(mt) of its batch item,
+            // C(2a) = a (a + 1), C(2a + 1) = (a + 1)^2.  At even mt the diagonal block's right half is zeros.
+            const int ntri = p.nmt % 2 == 0 ? (p.nmt / 2) * (p.nmt / 2 + 1) : (p.nmt / 2 + 1) * (p.nmt / 2 + 1);
+            t.z = idx / ntri;
+            const int r = idx - t.z * ntri;
+            int a = static_cast<int>((sqrtf(4.f * static_cast<float>(r) + 1.f) - 1.f) * 0.5f);
+            while ((a + 1) * (a + 2) <= r) ++a;
+            while (a > 0 && a * (a + 1) > r) --a;
+            if (r < a * (a + 1) + a + 1) {
+                t.mt = 2 * a;
+                t.nt = r - a * (a + 1);
+            } else {
+                t.mt = 2 * a + 1;
+                t.nt = r - (a + 1) * (a + 1);
+            }
+            return t;
+        }
         // The lower triangle (nt <= mt) of one batch item after another.  With 128-row tiles, the items after
         // those are the tiles just above the diagonal at even mt (no K steps: zeros), which the 256-row dc
         // products read.
@@ -174,7 +191,7 @@ __device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
     w.pairs = kw.pairs;
     w.inner = kw.hi > kw.lo ? (kw.hi - kw.lo + kBK - 1) / kBK : 0;
     long long total = static_cast<long long>(kw.outer) * w.inner * kw.pairs;
-    if (causal_tiles(p.problem) && t.nt > t.mt) total = 0;   // a tile of zeros
+    if (causal_tiles(p.problem) && t.nt * p.tile_n >= (t.mt + 1) * p.tile_m) total = 0;   // a tile of zeros
     w.s_lo = static_cast<int>(total * t.ks / p.ksplit);
     w.s_hi = static_cast<int>(total * (t.ks + 1) / p.ksplit);
     return w;
@@ -193,48 +210,55 @@ __device__ __forceinline__ void tl4(uint32_t dst, const CUtensorMap *m, uint32_t
     else tma_load_4d(dst, m, bar, x, y, z, w);
 }
 
-// (kPair: the loads of one CTA of a pair, completing on the pair's even CTA's barrier `bar`.)
+// (kPair: the loads of one CTA of a pair, completing on the pair's even CTA's barrier `bar`.  nbp: B's columns
+// in parts of 128, part j at sb + 16 KB j: MN-major 64-column slabs stay 8 KB apart, K-major rows 128 B apart.)
 template <bool kPair>
 __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta, const CUtensorMap *tb,
                                           const CUtensorMap *ta2, const CUtensorMap *tb2, uint32_t sa, uint32_t sb,
-                                          uint32_t bar, int z, int o, int k, int pair, int m0, int n0) {
+                                          uint32_t bar, int z, int o, int k, int pair, int m0, int n0, int nbp = 1) {
     const int b = p.problem == kDWuk || p.problem == kDWuv ? o : (p.problem == kDc ? z : z / p.H);
     const int h = p.problem == kDc ? o : (p.problem == kDWuk || p.problem == kDWuv ? z : z % p.H);
     const int zz = b * p.H + h;   // head-major batch item of the per-head matrices
     switch (p.problem) {
         case kQAbs:   // A = q [B,T,H,d] (K-major), B = W_UK [H,d,r] (MN-major)
             tl4<kPair>(sa, ta, bar, k, h, m0, b);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, h);
             break;
         case kDoLat:  // A = do [z,T,d_v], B = W_UV [H,d_v,r]
             tl3<kPair>(sa, ta, bar, k, m0, zz);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, h);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, h);
             break;
         case kP: case kDS:   // A = q_abs (hi, then lo) or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
             tl3<kPair>(sa, pair ? ta2 : ta, bar, k, m0, zz);
-            tl3<kPair>(sb, tb, bar, k, n0, b);
+            for (int j = 0; j < nbp; ++j) tl3<kPair>(sb + j * 16384, tb, bar, k, n0 + 128 * j, b);
             break;
         case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
             tl3<kPair>(sa, ta, bar, k, m0, zz);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, b);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, b);
             break;
         case kDc: {   // A = P^T or dS^T (MN-major: rows t, u contiguous), B = do_lat or q_abs (MN-major: rows t)
             const CUtensorMap *a = pair ? ta2 : ta, *bm = pair ? tb2 : tb;
             for (int s = 0; s < 2; ++s) tl3<kPair>(sa + s * 8192, a, bar, m0 + 64 * s, k, zz);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, bm, bar, n0 + 64 * s, k, zz);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, bm, bar, n0 + 128 * j + 64 * s, k, zz);
             break;
         }
         case kDq:   // A = dq_abs [z,T,r] (K-major), B = W_UK [H,d,r] (K-major: rows d)
             tl3<kPair>(sa, ta, bar, k, m0, zz);
-            tl3<kPair>(sb, tb, bar, k, n0, h);
+            for (int j = 0; j < nbp; ++j) tl3<kPair>(sb + j * 16384, tb, bar, k, n0 + 128 * j, h);
             break;
         case kDWuk:   // A = q^T (MN-major: rows t, d contiguous), B = dq_abs (MN-major: rows t)
             for (int s = 0; s < 2; ++s) tl4<kPair>(sa + s * 8192, ta, bar, m0 + 64 * s, h, k, b);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, zz);
             break;
         default:   // kDWuv: A = do^T (MN-major: rows t), B = o_lat (MN-major: rows t)
             for (int s = 0; s < 2; ++s) tl3<kPair>(sa + s * 8192, ta, bar, m0 + 64 * s, k, zz);
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sb + s * 8192, tb, bar, n0 + 64 * s, k, zz);
+            for (int j = 0; j < nbp; ++j)
+                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, zz);
             break;
     }
 }
@@ -378,9 +402,23 @@ __device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int s
 }
 
 // Persistent: CTA i takes items i, i + G, i + 2G, ... (G = the grid).  The TMA ring runs on across items, and
-// the accumulator alternates between two 128-column halves of the CTA's TMEM, so one item's epilogue overlaps
-// the next item's products.
-__global__ void __launch_bounds__(kThreads, 2)
+// the accumulator alternates between two kW-column halves of the CTA's TMEM, so one item's epilogue overlaps
+// the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256 tiles (B staged as
+// two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue column groups.
+template <int kW>
+struct Shape {
+    static constexpr int kStagesW = kW == 256 ? 4 : 3;
+    static constexpr uint32_t kStageW = kOpBytes + kW * 128;   // A [128 x 64] + B [kW x 64]
+    static constexpr uint32_t kBarOffW = kStagesW * kStageW;
+    static constexpr uint32_t kSmemW = kBarOffW + 256 + 1024;
+    static constexpr int kGroups = kW / 128;                   // epilogue column groups of four warps
+    static constexpr int kThreadsW = 96 + 128 * kGroups;       // warps 0 and 2 TMA, warp 1 MMA, then the epilogue
+    static constexpr int kMinBlocks = kW == 256 ? 1 : 2;
+};
+static_assert(Shape<256>::kSmemW <= 232448 && 2 * Shape<128>::kSmemW <= 233472, "shared memory");
+
+template <int kW>
+__global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
                     const GemmP p) {
@@ -388,7 +426,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    uint64_t *full = reinterpret_cast<uint64_t *>(gbase + kBarOff);
+    using S = Shape<kW>;
+    constexpr int kStages = S::kStagesW;
+    constexpr uint32_t kStageBytes = S::kStageW;
+    uint64_t *full = reinterpret_cast<uint64_t *>(gbase + S::kBarOffW);
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;     // [2] the accumulator holds an item's finished sums
     uint64_t *acc_empty = acc_full + 2;       // [2] the epilogue has read them out
@@ -404,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(acc_full + i), 1);
-            mbar_init(smem_u32(acc_empty + i), 128);
+            mbar_init(smem_u32(acc_empty + i), 128 * S::kGroups);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), 256);
+        tmem_alloc(smem_u32(tmem_slot), 2 * kW);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -418,15 +459,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_b);
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        // two producers, on alternate ring positions: one thread's TMA issues are too slow to keep the ring full
+        const int pi = warp >> 1;
+        if (pi == 0) {
+            tma_prefetch_desc(&tm_a);
+            tma_prefetch_desc(&tm_b);
+        }
         bool ok = true;
         int it = 0;
         for (int idx = static_cast<int>(blockIdx.x); ok && idx < p.items; idx += G) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
+                if ((it & 1) != pi) continue;
                 const int st = it % kStages;
                 if (it >= kStages && !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages) - 1) & 1, p.err, abort_flag)))
                     break;
@@ -434,15 +480,16 @@ __global__ void __launch_bounds__(kThreads, 2)
                 const uint32_t bar = smem_u32(full + st);
                 mbar_arrive_expect_tx(bar, kStageBytes);
                 load_step<false>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
-                          bar, t.z, s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * kBM, t.nt * kBN);
+                                 bar, t.z, s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * kBM, t.nt * kW,
+                                 S::kGroups);
             }
         }
         if (!ok) *abort_flag = 1;
         for (int q = (it > kStages ? it - kStages : 0); q < it; ++q)   // no load may still be landing at exit
-            mbar_wait(smem_u32(full + q % kStages), (q / kStages) & 1, p.err);
+            if ((q & 1) == pi) mbar_wait(smem_u32(full + q % kStages), (q / kStages) & 1, p.err);
     } else if (warp == 1 && lane == 0) {
         const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
-        const uint32_t idesc = make_idesc_bf16(128, 128, amn ? 1 : 0, bmn ? 1 : 0);
+        const uint32_t idesc = make_idesc_bf16(128, kW, amn ? 1 : 0, bmn ? 1 : 0);
         // descriptors of stage 0; a stage and a K step of 16 move them by constant offsets (MN-major operands:
         // two 64-wide slabs 8 KB apart, 2 KB per K step; K-major: 32 bytes per K step), so the issue loop is
         // one add per operand per MMA
@@ -456,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int acc = lt & 1;
             if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
             tc_fence_after();
-            const uint32_t d = tmem + acc * 128;
+            const uint32_t d = tmem + acc * kW;
             const int n = w.s_hi - w.s_lo;
             for (int j = 0; j < n; ++j, ++it) {
                 const int st = it % kStages;
@@ -473,8 +520,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             else mbar_arrive(smem_u32(acc_full + acc));   // nothing to add up: the epilogue writes zeros
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp >= 2) {
-        // epilogue: thread `row` owns TMEM lane row (warp w reads lanes 32 (w % 4) .. + 31)
+    } else if (warp >= 3) {
+        // epilogue: thread `row` owns TMEM lane row (warp w reads lanes 32 (w % 4) .. + 31) and columns
+        // 128 g .. 128 g + 127 of the accumulator, g = (w - 3) / 4
+        const int g = (warp - 3) >> 2;
         const int row = (warp & 3) * 32 + lane;
         int lt = 0;
         for (int idx = static_cast<int>(blockIdx.x); idx < p.items; idx += G, ++lt) {
@@ -482,9 +531,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             const Walk w = walk_of(p, t);
             const bool any = w.s_hi > w.s_lo;
             const int acc = lt & 1;
-            const int mt = t.mt, nt = t.nt, z = t.z;
-            const int m = mt * kBM + row, n0 = nt * kBN;
-            const uint32_t trow = tmem + acc * 128 + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+            const int z = t.z;
+            const int m = t.mt * kBM + row, n0 = t.nt * kW + 128 * g;
+            const uint32_t trow = tmem + acc * kW + 128 * g + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             RowIn rin;
             uint4 cur[4];
             read_row_stats(p, z, m, rin);   // in flight while the products finish
@@ -498,13 +547,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mbar_arrive(smem_u32(acc_empty + acc));
             }
 #pragma unroll 1
-            for (int c4 = 0; c4 < kBN / 32; ++c4) {
+            for (int c4 = 0; c4 < 4; ++c4) {
                 read_chunk_input(p, z, m, n0 + c4 * 32, cur);
                 float v[32];
                 if (any) {
                     tmem_ld32(trow + c4 * 32, v);
                     tmem_wait_ld();
-                    if (c4 == kBN / 32 - 1) {   // every column is in registers: the next item may accumulate here
+                    if (c4 == 3) {   // every column is in registers: the next item may accumulate here
                         tc_fence_before();
                         mbar_arrive(smem_u32(acc_empty + acc));
                     }
@@ -514,13 +563,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
                 epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
             }
-            epilogue_row(p, z, m, nt, rsum);
+            epilogue_row(p, z, m, t.nt * S::kGroups + g, rsum);
         }
     }
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 2 * kW);
 }
 
 // The pair form, for dc (few tiles, each with a long K): a cluster of two CTAs, one
@@ -531,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // commits arrive on both CTAs' barriers, and both CTAs' epilogue warps report to it when an accumulator is read.
 constexpr int kStages2 = 6;
 constexpr uint32_t kSmem2 = kStages2 * kStageBytes + 256 + 1024;   // one CTA per SM
-constexpr int kThreads2 = 320;   // warp 0 TMA, warp 1 MMA (even CTA), warps 2-9 epilogue (two column halves)
+constexpr int kThreads2 = 352;   // warps 0 and 2 TMA, warp 1 MMA (even CTA), warps 3-10 epilogue (two column halves)
 static_assert(kSmem2 <= 232448, "exceeds the 227 KB shared-memory limit");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
@@ -573,15 +622,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_b);
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        const int pi = warp >> 1;   // two producers, on alternate ring positions
+        if (pi == 0) {
+            tma_prefetch_desc(&tm_a);
+            tma_prefetch_desc(&tm_b);
+        }
         bool ok = true;
         int it = 0;
         for (int idx = pair_id; ok && idx < p.items; idx += n_pairs) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
+                if ((it & 1) != pi) continue;
                 const int st = it % kStages2;
                 if (it >= kStages2 &&
                     !(ok = mbar_wait(smem_u32(empty + st), ((it / kStages2) - 1) & 1, p.err, abort_flag)))
@@ -597,7 +650,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         if (!ok) *abort_flag = 1;
         if (rank == 0)   // no load of either CTA may still be landing at exit
             for (int q = (it > kStages2 ? it - kStages2 : 0); q < it; ++q)
-                mbar_wait(smem_u32(full + q % kStages2), (q / kStages2) & 1, p.err);
+                if ((q & 1) == pi) mbar_wait(smem_u32(full + q % kStages2), (q / kStages2) & 1, p.err);
     } else if (warp == 1 && lane == 0 && rank == 0) {
         const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
         const uint32_t idesc = make_idesc_bf16(256, 256, amn ? 1 : 0, bmn ? 1 : 0);
@@ -632,10 +685,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
             }
         }
         if (!ok) *abort_flag = 1;
-    } else if (warp >= 2) {
+    } else if (warp >= 3) {
         // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (this CTA's rows of the tile) and columns
-        // 128 g .. 128 g + 127 of the accumulator, g = (w - 2) / 4
-        const int g = (warp - 2) >> 2;
+        // 128 g .. 128 g + 127 of the accumulator, g = (w - 3) / 4
+        const int g = (warp - 3) >> 2;
         const int row = (warp & 3) * 32 + lane;
         int lt = 0;
         for (int idx = pair_id; idx < p.items; idx += n_pairs, ++lt) {
@@ -853,9 +906,11 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     ETT(&mP_k, &mP_mn, L.P);
     ETT(&mdS_k, &mdS_mn, L.dS);
     if (!okm) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(bwd_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmem));
-    if (e != cudaSuccess) return e;
-    if ((e = cudaFuncSetAttribute(bwd_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape<128>::kSmemW))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape<256>::kSmemW))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kSmem2))) != cudaSuccess)
         return e;
     const int sms = a.num_sms > 1 ? a.num_sms : 2;
@@ -863,11 +918,12 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         const long long k = (4LL * slots + base_items - 1) / base_items;
         return static_cast<int>(k < 1 ? 1 : (k > kMaxSplit ? kMaxSplit : k));
     };
-    // pair: 256 x 256 tiles on CTA pairs (one CTA per SM); otherwise 128 x 128 tiles, two CTAs per SM
+    // kind 0: 128 x 128 tiles, two CTAs per SM; 1: 128 x 256 tiles, one CTA per SM; 2: 256 x 256 tiles on CTA
+    // pairs (one CTA per SM)
     auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
-                    const CUtensorMap &tb2, int M, int N, int Z, void *out, bool pair) {
-        const int tile = pair ? 256 : 128;
-        const int slots = pair ? sms / 2 : 2 * sms;   // pairs, or CTAs, resident at once
+                    const CUtensorMap &tb2, int M, int N, int Z, void *out, int kind) {
+        const int tm = kind == 2 ? 256 : 128, tn = kind == 0 ? 128 : 256;
+        const int slots = kind == 0 ? 2 * sms : (kind == 1 ? sms : sms / 2);   // CTAs, or pairs, resident at once
         GemmP gp{};
         gp.problem = pr;
         gp.B = B;
@@ -889,16 +945,20 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.dl_in = bf(L.dl);
         gp.out = out;
         gp.err = a.dev_err;
-        gp.tile_m = tile;
-        gp.nmt = (M + tile - 1) / tile;
-        gp.nnt = (N + tile - 1) / tile;
+        gp.tile_m = tm;
+        gp.tile_n = tn;
+        gp.nmt = (M + tm - 1) / tm;
+        gp.nnt = (N + tn - 1) / tn;
         gp.nz = Z;
         gp.ksplit = 1;
         gp.part = f32(L.part);
         gp.part_n = static_cast<long long>(Z) * M * N;
         long long items;
         if (pr == kP || pr == kDS) {
-            items = static_cast<long long>(Z) * (static_cast<long long>(gp.nmt) * (gp.nmt + 1) / 2 + (pair ? 0 : gp.nmt / 2));
+            const long long n = gp.nmt, h2 = n / 2;
+            const long long tri = kind == 1 ? (n % 2 == 0 ? h2 * (h2 + 1) : (h2 + 1) * (h2 + 1))
+                                            : n * (n + 1) / 2 + (kind == 0 ? h2 : 0);
+            items = static_cast<long long>(Z) * tri;
         } else {
             if (pr == kDc || pr == kDWuk || pr == kDWuv)
                 gp.ksplit = split_for(static_cast<long long>(gp.nmt) * gp.nnt * Z, slots);
@@ -908,8 +968,10 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.items = static_cast<int>(items);
         const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
         note_launch();
-        if (pair) bwd_gemm2_kernel<<<2 * grid, kThreads2, kSmem2, s>>>(ta, tb, ta2, tb2, gp);
-        else bwd_gemm_kernel<<<grid, kThreads, kSmem, s>>>(ta, tb, ta2, tb2, gp);
+        if (kind == 2) bwd_gemm2_kernel<<<2 * grid, kThreads2, kSmem2, s>>>(ta, tb, ta2, tb2, gp);
+        else if (kind == 1)
+            bwd_gemm_kernel<256><<<grid, Shape<256>::kThreadsW, Shape<256>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+        else bwd_gemm_kernel<128><<<grid, Shape<128>::kThreadsW, Shape<128>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess || gp.ksplit == 1) return err;
         const long long n4 = gp.part_n / 4;   // N = r: a multiple of 4
@@ -921,16 +983,16 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     const int Z = static_cast<int>(rowsz);
     // 3. q_abs and do_lat; 4. P (and its row sums), o_lat (and do_lat . o_lat), then dS (reads P and both sums);
     // 5. dq_abs; 6. dc and dq; 7. the weight gradients
-    if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa), false)) != cudaSuccess) return e;
-    if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl), false)) != cudaSuccess) return e;
-    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), false)) != cudaSuccess) return e;
-    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), false)) != cudaSuccess) return e;
-    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS), false)) != cudaSuccess) return e;
-    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), false)) != cudaSuccess) return e;
-    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc, true)) != cudaSuccess) return e;
-    if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq, false)) != cudaSuccess) return e;
-    if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk, false)) != cudaSuccess) return e;
-    return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv, false);
+    if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc, 2)) != cudaSuccess) return e;
+    if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq, 0)) != cudaSuccess) return e;
+    if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk, 1)) != cudaSuccess) return e;
+    return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv, 1);
 }
 
 }  // namespace mla
