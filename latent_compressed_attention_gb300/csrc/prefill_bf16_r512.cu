@@ -281,7 +281,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (warp == 0 && lane == 0) {
                 // ---- ring producer.  Per tile: W_UK[h] into four ring positions, then c tiles [256 keys x 64] for
                 // every score block, streaming on into the next tile as slots free up.  A tile takes 4 + 8 nblk
-                // ring positions, a multiple of the 4 stages, so W_UK always fills slots 0-3 in order.
+                // ring positions, a multiple of the 4 stages, so W_UK always fills slots 0-3 in order.  (One
+                // [256 x 64] load per position: one thread issues them fast enough.)
                 tma_prefetch_desc(&tm_c256);
                 tma_prefetch_desc(&tm_wuk);
                 int it = 0, k = 0;
@@ -395,10 +396,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
         } else {
             // =========================================================== value CTA: control
-            if (warp == 0 && lane == 0) {
-                // ---- TMA producer: per tile, c tiles as the MN-major value operand for every unit, then W_UV[h]
-                tma_prefetch_desc(&tm_c);
-                tma_prefetch_desc(&tm_wuv);
+            if ((warp == 0 || warp == 3) && lane == 0) {
+                // ---- TMA producers (warps 0 and 3, on alternate ring positions: a position is four [128 x 64] loads,
+                // more than one thread issues in the products' time): per tile, c tiles as the MN-major value
+                // operand for every unit, then W_UV[h]
+                const int pi = warp == 3 ? 1 : 0;
+                if (pi == 0) {
+                    tma_prefetch_desc(&tm_c);
+                    tma_prefetch_desc(&tm_wuv);
+                }
                 int it = 0;
                 bool ok = true;
                 for (int k = 0; ok; ++k) {
@@ -407,6 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const TileInfo ti = tile_info(tile, p);
                     for (int j = 0; ok && j < ti.nkv + 1; ++j) {   // j == nkv: the W_UV tile
                         for (int nh = 0; nh < 2; ++nh, ++it) {
+                            if ((it & 1) != pi) continue;
                             const int st = it % kOStages;
                             TR(const long long _a = clock64();)
                             if (it >= kOStages &&
@@ -427,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) *abort_flag = 1;
                 for (int q = (it > kOStages ? it - kOStages : 0); q < it; ++q)
-                    mbar_wait(B_(bars->oc_full[q % kOStages]), (q / kOStages) & 1, p.err);
+                    if ((q & 1) == pi) mbar_wait(B_(bars->oc_full[q % kOStages]), (q / kOStages) & 1, p.err);
             } else if (warp == 1) {
                 // ---- MMA warp: per tile o_lat += P . c, then o = o_lat . W_UV^T; lane 0 issues
                 const bool leader = lane == 0;
