@@ -263,6 +263,19 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
     }
 }
 
+// 32-byte global accesses (sm_100 family): half the requests of 16-byte ones for the epilogue's row-wise reads
+// and writes, whose rows are 256 bytes or more apart.  The address must be 32-byte aligned.
+__device__ __forceinline__ void ld_global_32B(const void *ptr, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(ptr));
+}
+__device__ __forceinline__ void st_global_32B(void *ptr, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
 // The epilogue's per-row inputs of an item, read before its sums are ready: the softmax statistics (P) or
 // delta (dS).
 struct RowIn {
@@ -289,8 +302,8 @@ __device__ __forceinline__ void read_chunk_input(const GemmP &p, int z, int m, i
     if (m >= p.M || (pr != kDS && pr != kOLat)) return;
     const size_t ri = static_cast<size_t>(z) * p.T + m;
     const uint4 *src = reinterpret_cast<const uint4 *>(pr == kDS ? p.p_in + ri * p.Tp + nb : p.dl_in + ri * kR + nb);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) in[q] = __ldg(src + q);
+    ld_global_32B(src, in[0], in[1]);
+    ld_global_32B(src + 2, in[2], in[3]);
 }
 
 // One 32-column chunk of an item's epilogue: row m of batch item z, columns nb .. nb + 31, the fp32 sums v.
@@ -327,6 +340,7 @@ __device__ __forceinline__ void epilogue_chunk(const GemmP &p, int z, int m, int
                 v[i] = vis ? p.scale * pv[i] * (v[i] - drow) : 0.f;
         }
         uint4 *o4 = reinterpret_cast<uint4 *>(o);
+        uint4 w4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             uint32_t wq[4];
@@ -336,12 +350,15 @@ __device__ __forceinline__ void epilogue_chunk(const GemmP &p, int z, int m, int
                 if (pr == kP)   // the row sum of P as rounded
                     rsum += __uint_as_float(wq[e] << 16) + __uint_as_float(wq[e] & 0xFFFF0000u);
             }
-            o4[q] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+            w4[q] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
         }
+        st_global_32B(o4, w4[0], w4[1]);
+        st_global_32B(o4 + 2, w4[2], w4[3]);
     } else if (pr <= kDqAbs) {   // bf16 [z, T, r]
         if (pr == kQAbs) {   // the lo part: bf16(x - bf16(x))
             uint4 *l4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out2) +
                                                   (static_cast<size_t>(z) * p.T + m) * kR + nb);
+            uint4 lo4[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t lw[4];
@@ -351,8 +368,10 @@ __device__ __forceinline__ void epilogue_chunk(const GemmP &p, int z, int m, int
                     const uint32_t hw = pack_bf16x2(x0, x1);
                     lw[e] = pack_bf16x2(x0 - __uint_as_float(hw << 16), x1 - __uint_as_float(hw & 0xFFFF0000u));
                 }
-                l4[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                lo4[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
+            st_global_32B(l4, lo4[0], lo4[1]);
+            st_global_32B(l4 + 2, lo4[2], lo4[3]);
         }
         if (pr == kOLat) {   // do_lat . o_lat over these 32 columns
 #pragma unroll
@@ -367,19 +386,27 @@ __device__ __forceinline__ void epilogue_chunk(const GemmP &p, int z, int m, int
         }
         uint4 *o4 = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.out) +
                                               (static_cast<size_t>(z) * p.T + m) * kR + nb);
+        uint4 b4[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            o4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+            b4[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
                                pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+        st_global_32B(o4, b4[0], b4[1]);
+        st_global_32B(o4 + 2, b4[2], b4[3]);
     } else {   // fp32 gradients
         size_t off;
         if (pr == kDc) off = (static_cast<size_t>(z) * p.T + m) * kR + nb;
         else if (pr == kDq) off = ((static_cast<size_t>(z / p.H) * p.T + m) * p.H + z % p.H) * kD + nb;
         else off = (static_cast<size_t>(z) * p.M + m) * kR + nb;   // dW_UK, dW_UV [H, 128, r]
         float *dst = p.ksplit > 1 ? p.part + static_cast<size_t>(ks) * p.part_n : static_cast<float *>(p.out);
-        float4 *o4 = reinterpret_cast<float4 *>(dst + off);
+        float *o = dst + off;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) o4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 4; ++q)
+            st_global_32B(o + 8 * q,
+                          make_uint4(__float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]), __float_as_uint(v[8 * q + 2]),
+                                     __float_as_uint(v[8 * q + 3])),
+                          make_uint4(__float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
+                                     __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7])));
     }
 }
 
