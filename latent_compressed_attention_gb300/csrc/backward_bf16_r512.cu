@@ -263,19 +263,6 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
     }
 }
 
-// 32-byte global accesses (sm_100 family): half the requests of 16-byte ones for the epilogue's row-wise reads
-// and writes, whose rows are 256 bytes or more apart.  The address must be 32-byte aligned.
-__device__ __forceinline__ void ld_global_32B(const void *ptr, uint4 &a, uint4 &b) {
-    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-                 : "l"(ptr));
-}
-__device__ __forceinline__ void st_global_32B(void *ptr, uint4 a, uint4 b) {
-    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z),
-                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-                 : "memory");
-}
-
 // The epilogue's per-row inputs of an item, read before its sums are ready: the softmax statistics (P) or
 // delta (dS).
 struct RowIn {

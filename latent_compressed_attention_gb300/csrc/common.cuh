@@ -462,6 +462,19 @@ __device__ __forceinline__ void tma2_load_4d(uint32_t dst, const void *tmap, uin
         : "memory");
 }
 
+// 32-byte global accesses (sm_100 family): half the requests of 16-byte ones for row-wise reads and writes
+// whose rows lie far apart (one request per 32 bytes of a row instead of per 16).  The address must be 32-byte aligned.
+__device__ __forceinline__ void ld_global_32B(const void *ptr, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(ptr));
+}
+__device__ __forceinline__ void st_global_32B(void *ptr, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)

@@ -801,10 +801,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     // the packing and the W_UV product
                     const size_t off = ((static_cast<size_t>(ti.b) * p.T + t) * p.H + ti.h) * kD + wg * 64;
                     uint4 gv[8];
+                    if (p.gate && t < p.T) {
     #pragma unroll
-                    for (int v8 = 0; v8 < 8; ++v8)
-                        gv[v8] = (p.gate && t < p.T) ? __ldg(reinterpret_cast<const uint4 *>(p.gate + off) + v8)
-                                                     : make_uint4(0, 0, 0, 0);
+                        for (int v2 = 0; v2 < 4; ++v2)
+                            ld_global_32B(reinterpret_cast<const uint4 *>(p.gate + off) + 2 * v2, gv[2 * v2], gv[2 * v2 + 1]);
+                    } else {
+    #pragma unroll
+                        for (int v8 = 0; v8 < 8; ++v8) gv[v8] = make_uint4(0, 0, 0, 0);
+                    }
                     const float inv_l = 1.f / (l_even + l_odd);
                     if (p.st_l && wg == 0 && t < p.T)
                         p.st_l[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = l_even + l_odd;
@@ -840,6 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     mbar_arrive(B_(bars->ep_read));   // the next tile may overwrite these TMEM columns
                     if (t < p.T) {
                         uint4 *o4 = reinterpret_cast<uint4 *>(p.out + off);
+                        uint4 ov[8];
     #pragma unroll
                         for (int v8 = 0; v8 < 8; ++v8) {
                             float y[8];
@@ -855,9 +860,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     y[2 * i + 1] *= __fdividef(1.f, 1.f + fast_exp2(-g_hi * kLog2e));
                                 }
                             }
-                            o4[v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                            ov[v8] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
                                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                         }
+    #pragma unroll
+                        for (int v2 = 0; v2 < 4; ++v2) st_global_32B(o4 + 2 * v2, ov[2 * v2], ov[2 * v2 + 1]);
                     }
                     TR(if (threadIdx.x == 128) { TR_ADD(TR_O_EPILOGUE, clock64() - t_ep); TR_ADD(TR_O_EP_OUT, clock64() - t_md); })
                 }
