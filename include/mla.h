@@ -103,6 +103,22 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
                                   int dtype, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * mla_absorbed_attn_fwd_lse - mla_absorbed_attn_fwd that also writes each row's
+ * log-sum-exp of the scaled, causally masked scores, for mla_absorbed_attn_bwd_lse:
+ *   lse[b,h,t] = ln sum_{u<=t} exp(scale * q_abs[b,t,h,:] . c[b,u,:])   [B,H,T] fp32
+ * so that attn[b,h,t,u] = exp(scale * q_abs . c_u - lse[b,h,t]) (page "Gated MLA
+ * （矩阵吸收版）", section "完整计算流（四步）", step 2: the softmax's normaliser).
+ * Arguments, workspace (mla_absorbed_attn_fwd_workspace_size) and precision as
+ * for mla_absorbed_attn_fwd; lse is caller-owned device memory, 16-byte aligned,
+ * overwritten.  Supported: BF16 with (r, d_q, d_v) = (512, 128, 128); others
+ * return MLA_ERR_UNSUPPORTED.  lse NULL returns MLA_ERR_NULL.
+ */
+MLA_API int mla_absorbed_attn_fwd_lse(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                      const void *gate, float scale, void *out, float *lse, int B, int T, int H,
+                                      int d_q, int d_v, int r, int dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
  * mla_absorbed_attn_bwd - gradients of the attention (steps 2-4 of section
  * "完整计算流（四步）" of the page "Gated MLA（矩阵吸收版）", which gives the forward
  * only; this takes the chain rule back through it).  For
@@ -138,6 +154,22 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
                                   float scale, const void *dout, void *dq, void *dc, void *dw_uk, void *dw_uv,
                                   void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * mla_absorbed_attn_bwd_lse - mla_absorbed_attn_bwd given what a forward call
+ * mla_absorbed_attn_fwd_lse(q, c, w_uk, w_uv, gate, scale) on the same inputs
+ * returned: its output `out` [B,T,H*d_v] (after the gate) and `lse` [B,H,T].  The
+ * forward is not run again: the attention matrix is rebuilt from lse, and with a
+ * gate dgate = dout * out * (1 - sigmoid(gate)).  Outputs, workspace
+ * (mla_absorbed_attn_bwd_workspace_size) and determinism as for mla_absorbed_attn_bwd.
+ * Supported: BF16 with (r, d_q, d_v) = (512, 128, 128); others return
+ * MLA_ERR_UNSUPPORTED.  out or lse NULL returns MLA_ERR_NULL; both 16-byte aligned.
+ */
+MLA_API int mla_absorbed_attn_bwd_lse(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                      const void *gate, float scale, const void *dout, const void *out,
+                                      const float *lse, void *dq, void *dc, void *dw_uk, void *dw_uv, void *dgate,
+                                      int B, int T, int H, int d_q, int d_v, int r, int dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream);
 
 /*
  * mla_latent_decode_workspace_size - bytes of device workspace mla_latent_decode

@@ -60,6 +60,8 @@ def library():
             vp, i, f, ll, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_size_t
             lib.mla_absorbed_attn_fwd.argtypes = [vp, vp, vp, vp, vp, f, vp, i, i, i, i, i, i, i, vp, sz, vp]
             lib.mla_absorbed_attn_fwd.restype = i
+            lib.mla_absorbed_attn_fwd_lse.argtypes = [vp, vp, vp, vp, vp, f, vp, vp, i, i, i, i, i, i, i, vp, sz, vp]
+            lib.mla_absorbed_attn_fwd_lse.restype = i
             lib.mla_absorbed_attn_fwd_workspace_size.argtypes = [i] * 7
             lib.mla_absorbed_attn_fwd_workspace_size.restype = sz
             lib.mla_latent_decode_workspace_size.argtypes = [i, i, i, i]
@@ -86,6 +88,8 @@ def library():
             lib.mla_absorbed_attn_bwd_workspace_size.restype = sz
             lib.mla_absorbed_attn_bwd.argtypes = [vp] * 5 + [f] + [vp] * 6 + [i] * 7 + [vp, sz, vp]
             lib.mla_absorbed_attn_bwd.restype = i
+            lib.mla_absorbed_attn_bwd_lse.argtypes = [vp] * 5 + [f] + [vp] * 8 + [i] * 7 + [vp, sz, vp]
+            lib.mla_absorbed_attn_bwd_lse.restype = i
             lib.mla_debug_wait_timeout.argtypes = [ctypes.c_uint, vp]
             lib.mla_debug_wait_timeout.restype = i
             lib.mla_get_device_error.argtypes = [vp]
@@ -160,8 +164,11 @@ def mla_absorbed_attn_fwd_workspace_size(B: int, T: int, H: int, d_q: int, d_v: 
     return int(library().mla_absorbed_attn_fwd_workspace_size(B, T, H, d_q, d_v, r, code))
 
 
-def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=None, workspace=None, stream=None):
-    """Causal absorbed Gated-MLA prefill; returns out [B,T,H*d_v] (allocated if not given).
+def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=None, workspace=None, stream=None,
+                          return_lse: bool = False):
+    """Causal absorbed Gated-MLA prefill; returns out [B,T,H*d_v] (allocated if not given), or (out, lse) with
+    return_lse (lse [B,H,T] fp32: each row's log-sum-exp of the scaled scores, for mla_absorbed_attn_bwd; bf16
+    with r = 512, d_q = d_v = 128 only).
 
     q [B,T,H,d_q], c [B,T,r], w_uk [H,d_q,r], w_uv [H,d_v,r], gate [B,T,H*d_v]
     (pre-sigmoid logits) or None; all CUDA, contiguous, one dtype (bf16/fp32).
@@ -187,6 +194,15 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if return_lse:
+        lse = torch.empty((B, H, T), dtype=torch.float32, device=dev)
+        rc = lib.mla_absorbed_attn_fwd_lse(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(),
+                                           None if gate is None else gate.data_ptr(), float(scale), out.data_ptr(),
+                                           lse.data_ptr(), B, T, H, d_q, d_v, r, _dtype_code(q), ws_ptr, ws_bytes,
+                                           _stream_ptr(stream, dev))
+        if rc != 0:
+            raise MLAError(rc, "mla_absorbed_attn_fwd_lse")
+        return out, lse
     rc = lib.mla_absorbed_attn_fwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(),
                                    None if gate is None else gate.data_ptr(), float(scale), out.data_ptr(),
                                    B, T, H, d_q, d_v, r, _dtype_code(q), ws_ptr, ws_bytes, _stream_ptr(stream, dev))
@@ -195,10 +211,13 @@ def mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate=None, scale: float = 1.0, out=N
     return out
 
 
-def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=None, stream=None) -> dict:
+def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=None, stream=None, out=None,
+                          lse=None) -> dict:
     """Gradients of sum(dout * mla_absorbed_attn_fwd(q, c, w_uk, w_uv, gate, scale)): a dict with dq, dc, dw_uk,
     dw_uv and dgate (None without a gate), allocated here as fp32.  Inputs fp32 or bf16 with r, d_q, d_v <= 64,
-    or bf16 with r = 512, d_q = d_v = 128 (tensor cores; the workspace is O(B H T^2))."""
+    or bf16 with r = 512, d_q = d_v = 128 (tensor cores; the workspace is O(B H T^2)).  Given the forward's
+    (out, lse) from mla_absorbed_attn_fwd(..., return_lse=True) (r = 512 only), the forward is not run again."""
+    saved_out = out
     torch = _torch()
     B, T, H, d_q = q.shape
     r = c.shape[-1]
@@ -214,20 +233,35 @@ def mla_absorbed_attn_bwd(q, c, w_uk, w_uv, gate, scale: float, dout, workspace=
     lib = library()
     code = _dtype_code(q)
     f32 = lambda t: torch.empty(t.shape, dtype=torch.float32, device=dev)  # noqa: E731
-    out = dict(dq=f32(q), dc=f32(c), dw_uk=f32(w_uk), dw_uv=f32(w_uv), dgate=None if gate is None else f32(gate))
+    out_grads = dict(dq=f32(q), dc=f32(c), dw_uk=f32(w_uk), dw_uv=f32(w_uv), dgate=None if gate is None else f32(gate))
     need = int(lib.mla_absorbed_attn_bwd_workspace_size(B, T, H, d_q, d_v, r, code))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     ws_ptr = None if workspace is None else workspace.data_ptr()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    grads = out_grads
+    if saved_out is not None or lse is not None:
+        if saved_out is None or lse is None:
+            raise ValueError("out and lse come together (both from mla_absorbed_attn_fwd(..., return_lse=True))")
+        _check(saved_out, "out", dt, dev, (B, T, H * d_v))
+        if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, T) or lse.device != dev or not lse.is_contiguous():
+            raise ValueError("lse: float32 [B, H, T], contiguous, on the inputs' device")
+        rc = lib.mla_absorbed_attn_bwd_lse(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(), ptr(gate),
+                                           float(scale), dout.data_ptr(), saved_out.data_ptr(), lse.data_ptr(),
+                                           grads["dq"].data_ptr(), grads["dc"].data_ptr(), grads["dw_uk"].data_ptr(),
+                                           grads["dw_uv"].data_ptr(), ptr(grads["dgate"]), B, T, H, d_q, d_v, r, code,
+                                           ws_ptr, ws_bytes, _stream_ptr(stream, dev))
+        if rc != 0:
+            raise MLAError(rc, "mla_absorbed_attn_bwd_lse")
+        return grads
     rc = lib.mla_absorbed_attn_bwd(q.data_ptr(), c.data_ptr(), w_uk.data_ptr(), w_uv.data_ptr(), ptr(gate),
-                                   float(scale), dout.data_ptr(), out["dq"].data_ptr(), out["dc"].data_ptr(),
-                                   out["dw_uk"].data_ptr(), out["dw_uv"].data_ptr(), ptr(out["dgate"]),
+                                   float(scale), dout.data_ptr(), grads["dq"].data_ptr(), grads["dc"].data_ptr(),
+                                   grads["dw_uk"].data_ptr(), grads["dw_uv"].data_ptr(), ptr(grads["dgate"]),
                                    B, T, H, d_q, d_v, r, code, ws_ptr, ws_bytes, _stream_ptr(stream, dev))
     if rc != 0:
         raise MLAError(rc, "mla_absorbed_attn_bwd")
-    return out
+    return grads
 
 
 def mla_gated_layer_workspace_size(B: int, T: int, D: int, H: int, d_q: int, d_v: int, r: int, r_q: int,

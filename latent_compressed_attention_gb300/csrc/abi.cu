@@ -117,10 +117,10 @@ MLA_API size_t mla_absorbed_attn_fwd_workspace_size(int B, int T, int H, int d_q
     return prefill_workspace_bytes(B, T, r, d_q, d_v, dtype == MLA_DTYPE_F32);
 }
 
-MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
-                                  const void *gate, float scale, void *out, int B, int T, int H, int d_q,
-                                  int d_v, int r, int dtype, void *workspace, size_t workspace_bytes,
-                                  void *stream) {
+namespace {
+int fwd_impl(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate, float scale, void *out,
+             float *lse, int B, int T, int H, int d_q, int d_v, int r, int dtype, void *workspace,
+             size_t workspace_bytes, void *stream) {
     if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
     if (B < 0 || T < 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0) return MLA_ERR_SHAPE;
     const long long rows = static_cast<long long>(B) * T;
@@ -135,6 +135,8 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
     const bool ok_shape = f32 ? prefill_f32_simt_supports(r, d_q, d_v)
                               : (prefill_bf16_r512_supports(r, d_q, d_v) || prefill_bf16_small_supports(r, d_q, d_v));
     if (!ok_shape || (f32 && T > kPrefillF32MaxT)) return MLA_ERR_UNSUPPORTED;
+    if (lse && (f32 || !prefill_bf16_r512_supports(r, d_q, d_v))) return MLA_ERR_UNSUPPORTED;
+    if (lse && !aligned16(lse)) return MLA_ERR_ALIGN;
     if (rows == 0) return MLA_OK;
     const size_t need = prefill_workspace_bytes(B, T, r, d_q, d_v, f32);
     if (need > 0 && (!workspace || workspace_bytes < need)) return MLA_ERR_WORKSPACE;
@@ -144,6 +146,7 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
     if (device_info(dev) != cudaSuccess) return MLA_ERR_CUDA;
     PrefillArgs a{q, c, w_uk, w_uv, gate, out, scale, B, T, H, d_q, d_v, r, dev->err_word, dev->num_sms,
                   workspace, workspace_bytes};
+    a.lse = lse;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (f32)
@@ -153,6 +156,24 @@ MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk
     else
         e = launch_prefill_bf16_small(a, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+}  // namespace
+
+MLA_API int mla_absorbed_attn_fwd(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                  const void *gate, float scale, void *out, int B, int T, int H, int d_q,
+                                  int d_v, int r, int dtype, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+    return fwd_impl(q, c, w_uk, w_uv, gate, scale, out, nullptr, B, T, H, d_q, d_v, r, dtype, workspace,
+                    workspace_bytes, stream);
+}
+
+MLA_API int mla_absorbed_attn_fwd_lse(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                      const void *gate, float scale, void *out, float *lse, int B, int T, int H,
+                                      int d_q, int d_v, int r, int dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+    if (!lse) return MLA_ERR_NULL;
+    return fwd_impl(q, c, w_uk, w_uv, gate, scale, out, lse, B, T, H, d_q, d_v, r, dtype, workspace,
+                    workspace_bytes, stream);
 }
 
 MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q, int d_v, int r, int dtype) {
@@ -167,10 +188,11 @@ MLA_API size_t mla_absorbed_attn_bwd_workspace_size(int B, int T, int H, int d_q
     return backward_f32_workspace_bytes(B, T, H, r);
 }
 
-MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate,
-                                  float scale, const void *dout, void *dq, void *dc, void *dw_uk, void *dw_uv,
-                                  void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype,
-                                  void *workspace, size_t workspace_bytes, void *stream) {
+namespace {
+int bwd_impl(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate, float scale,
+             const void *dout, const void *out_fwd, const float *lse, void *dq, void *dc, void *dw_uk, void *dw_uv,
+             void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype, void *workspace,
+             size_t workspace_bytes, void *stream) {
     if (dtype != MLA_DTYPE_BF16 && dtype != MLA_DTYPE_F32) return MLA_ERR_DTYPE;
     if (B < 0 || T < 0 || H <= 0 || d_q <= 0 || d_v <= 0 || r <= 0) return MLA_ERR_SHAPE;
     const long long rows = static_cast<long long>(B) * T;
@@ -184,6 +206,8 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
         (dgate && !aligned16(dgate)))
         return MLA_ERR_ALIGN;
     const bool r512 = dtype == MLA_DTYPE_BF16 && backward_bf16_r512_supports(r, d_q, d_v);
+    if (lse && !r512) return MLA_ERR_UNSUPPORTED;
+    if (lse && (!aligned16(lse) || !aligned16(out_fwd))) return MLA_ERR_ALIGN;
     if (r512) {
         if (!mul_fits(rows * H, T + 128LL, LLONG_MAX / 8)) return MLA_ERR_SHAPE;
         if (rows == 0) return MLA_OK;
@@ -195,6 +219,8 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
         BackwardR512Args a{q, c, w_uk, w_uv, gate, dout, static_cast<float *>(dq), static_cast<float *>(dc),
                            static_cast<float *>(dw_uk), static_cast<float *>(dw_uv), static_cast<float *>(dgate),
                            scale, B, T, H, d_q, d_v, r, workspace, workspace_bytes, dev->err_word, dev->num_sms};
+        a.out_fwd = out_fwd;
+        a.lse = lse;
         const cudaError_t e = launch_backward_bf16_r512(a, static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
     }
@@ -207,6 +233,25 @@ MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk
                    dtype == MLA_DTYPE_BF16};
     const cudaError_t e = launch_backward_f32(a, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+}  // namespace
+
+MLA_API int mla_absorbed_attn_bwd(const void *q, const void *c, const void *w_uk, const void *w_uv, const void *gate,
+                                  float scale, const void *dout, void *dq, void *dc, void *dw_uk, void *dw_uv,
+                                  void *dgate, int B, int T, int H, int d_q, int d_v, int r, int dtype,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
+    return bwd_impl(q, c, w_uk, w_uv, gate, scale, dout, nullptr, nullptr, dq, dc, dw_uk, dw_uv, dgate, B, T, H, d_q,
+                    d_v, r, dtype, workspace, workspace_bytes, stream);
+}
+
+MLA_API int mla_absorbed_attn_bwd_lse(const void *q, const void *c, const void *w_uk, const void *w_uv,
+                                      const void *gate, float scale, const void *dout, const void *out,
+                                      const float *lse, void *dq, void *dc, void *dw_uk, void *dw_uv, void *dgate,
+                                      int B, int T, int H, int d_q, int d_v, int r, int dtype, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+    if (!out || !lse) return MLA_ERR_NULL;
+    return bwd_impl(q, c, w_uk, w_uv, gate, scale, dout, out, lse, dq, dc, dw_uk, dw_uv, dgate, B, T, H, d_q, d_v, r,
+                    dtype, workspace, workspace_bytes, stream);
 }
 
 MLA_API size_t mla_latent_decode_workspace_size(int B, int H, int r, int max_len) {

@@ -65,7 +65,7 @@ struct GemmP {
     int M, N;             // output extent of one batch item
     float scale_log2;     // kP: softmax scale * log2(e)
     float scale;          // kDS: softmax scale
-    const float *st_m, *st_l;           // [z, T]: the forward's row statistics
+    const float *lse;                   // [z, T]: each row's log-sum-exp of the scaled scores (natural log)
     float *psum;                        // [z, T]: row sums of P (o_lat's N tile 0 adds up psum_part)
     float *psum_part;                   // [Tp / 128][z, T]: P's row sums, one slot per key tile
     float *dnum_part;                   // [4][z, T]: do_lat . o_lat, one slot per o_lat N tile
@@ -274,8 +274,8 @@ __device__ __forceinline__ void read_row_stats(const GemmP &p, int z, int m, Row
     if (m >= p.M) return;
     const size_t ri = static_cast<size_t>(z) * p.T + m;
     if (pr == kP) {
-        r.mrow = __ldg(p.st_m + ri);
-        r.inv_l = 1.f / __ldg(p.st_l + ri);
+        r.mrow = __ldg(p.lse + ri) * kLog2e;   // P = exp2(s scale log2 e - lse log2 e)
+        r.inv_l = 1.f;
     } else if (pr == kDS) {   // written by earlier launches, added in a fixed order
         float num = 0.f;
 #pragma unroll
@@ -755,10 +755,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
 }
 
 // do = dout * sigmoid(g) (head-major [z, T, d_v] bf16) and dgate = dout * o * sigmoid(g) (1 - sigmoid(g)) (fp32,
-// [B, T, H d_v]).  One warp per (b, t, h), lane j holds columns 4j .. 4j + 3.
+// [B, T, H d_v]), o the output before the gate; given the output after the gate instead (gated: out = o sigmoid(g)),
+// dgate = dout * out * (1 - sigmoid(g)).  One warp per (b, t, h), lane j holds columns 4j .. 4j + 3.
 __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__restrict__ dout, const __nv_bfloat16 *__restrict__ g,
                                                        const __nv_bfloat16 *__restrict__ o, __nv_bfloat16 *__restrict__ do_hm,
-                                                       float *__restrict__ dgate, int B, int T, int H) {
+                                                       float *__restrict__ dgate, int B, int T, int H, bool gated) {
     const long long w = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (w >= static_cast<long long>(B) * T * H) return;
@@ -778,7 +779,7 @@ __global__ void __launch_bounds__(256) bwd_gate_kernel(const __nv_bfloat16 *__re
         const float ov_ = __uint_as_float((ow[i >> 1] << sh) & 0xFFFF0000u);
         const float sg = g ? 1.f / (1.f + expf(-__uint_as_float((gw[i >> 1] << sh) & 0xFFFF0000u))) : 1.f;
         dov[i] = d * sg;
-        dg[i] = d * ov_ * sg * (1.f - sg);
+        dg[i] = gated ? d * ov_ * (1.f - sg) : d * ov_ * sg * (1.f - sg);
     }
     const size_t hm = ((static_cast<size_t>(b) * H + h) * T + t) * kD + lane * 4;
     *reinterpret_cast<uint2 *>(do_hm + hm) = make_uint2(pack_bf16x2(dov[0], dov[1]), pack_bf16x2(dov[2], dov[3]));
@@ -815,7 +816,7 @@ CUresult enc(CUtensorMap *m, const void *ptr, int rank, const cuuint64_t *dims, 
 size_t al(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
-    size_t o, pre, st_m, st_l, psum, psum_part, dnum_part, do_hm, qa, qlo, dl, ol, dqa, P, dS, part, end;
+    size_t o, pre, lse, psum, psum_part, dnum_part, do_hm, qa, qlo, dl, ol, dqa, P, dS, part, end;
 };
 // dc and the weight gradients cut each tile's K steps into up to this many parts (fp32 partial sums in the
 // workspace, added in a fixed order afterwards), so that their few long tiles spread over the SMs
@@ -826,9 +827,8 @@ BwdLayout bwd_layout(long long B, long long T, long long H) {
     BwdLayout L;
     L.o = 0;
     L.pre = L.o + al(static_cast<size_t>(B) * T * H * kD * 2);
-    L.st_m = L.pre + al(prefill_bf16_r512_workspace_bytes(B, T));
-    L.st_l = L.st_m + al(rows * 4);
-    L.psum = L.st_l + al(rows * 4);
+    L.lse = L.pre + al(prefill_bf16_r512_workspace_bytes(B, T));
+    L.psum = L.lse + al(rows * 4);
     L.psum_part = L.psum + al(rows * 4);
     L.dnum_part = L.psum_part + al(rows * 4 * static_cast<size_t>(Tp / 128));
     L.do_hm = L.dnum_part + al(rows * 4 * (kR / kBN));
@@ -861,20 +861,24 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     auto f32 = [&](size_t off) { return reinterpret_cast<float *>(ws + off); };
     const size_t rowsz = static_cast<size_t>(B) * H;   // head-major batch items
 
-    // 1. the forward without the gate: o, and each row's softmax statistics
-    PrefillArgs pa{a.q, a.c, a.w_uk, a.w_uv, nullptr, bf(L.o), a.scale, B, T, H, kD, kD, kR, a.dev_err, a.num_sms,
-                   ws + L.pre, L.st_m - L.pre};
-    pa.stats_m = f32(L.st_m);
-    pa.stats_l = f32(L.st_l);
-    cudaError_t e = launch_prefill_bf16_r512(pa, s);
-    if (e != cudaSuccess) return e;
+    // 1. the forward without the gate: o, and each row's log-sum-exp; or both given by the caller's forward
+    const bool saved = a.lse != nullptr && a.out_fwd != nullptr;
+    const float *lse = saved ? a.lse : f32(L.lse);
+    cudaError_t e = cudaSuccess;
+    if (!saved) {
+        PrefillArgs pa{a.q, a.c, a.w_uk, a.w_uv, nullptr, bf(L.o), a.scale, B, T, H, kD, kD, kR, a.dev_err, a.num_sms,
+                       ws + L.pre, L.lse - L.pre};
+        pa.lse = f32(L.lse);
+        if ((e = launch_prefill_bf16_r512(pa, s)) != cudaSuccess) return e;
+    }
     // 2. the gate's backward, do and delta
     {
         const long long warps = static_cast<long long>(B) * T * H;
         note_launch();
         bwd_gate_kernel<<<static_cast<unsigned>((warps + 7) / 8), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.gate), bf(L.o),
-            bf(L.do_hm), static_cast<float *>(a.dgate), B, T, H);
+            static_cast<const __nv_bfloat16 *>(a.dout), static_cast<const __nv_bfloat16 *>(a.gate),
+            saved ? static_cast<const __nv_bfloat16 *>(a.out_fwd) : bf(L.o), bf(L.do_hm), static_cast<float *>(a.dgate),
+            B, T, H, saved);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // tensor maps (dims innermost first, strides in bytes)
@@ -948,8 +952,7 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.N = N;
         gp.scale_log2 = a.scale * kLog2e;
         gp.scale = a.scale;
-        gp.st_m = f32(L.st_m);
-        gp.st_l = f32(L.st_l);
+        gp.lse = lse;
         gp.psum = f32(L.psum);
         gp.psum_part = f32(L.psum_part);
         gp.dnum_part = f32(L.dnum_part);

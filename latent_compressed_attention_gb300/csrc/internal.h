@@ -17,10 +17,9 @@ struct PrefillArgs {
     int num_sms;
     void *workspace = nullptr;   // prefill_workspace_bytes() bytes (none for the fp32 and small-rank kernels)
     size_t workspace_bytes = 0;
-    // optional (r = 512 kernel): each row's softmax statistics, [B, H, T] fp32: the log2-domain maximum the
-    // kernel used (m) and the sum of exp2(s - m) over the row (l), so attn = exp2(s - m) / l with s the scaled
-    // score in log2 units
-    float *stats_m = nullptr, *stats_l = nullptr;
+    // optional (r = 512 kernel): each row's log-sum-exp of the scaled scores, [B, H, T] fp32, natural log:
+    // lse = ln sum_u exp(scale q_abs . c_u), so attn = exp(scale q_abs . c_u - lse)
+    float *lse = nullptr;
 };
 
 struct DecodeArgs {
@@ -77,6 +76,10 @@ struct BackwardR512Args {
     size_t workspace_bytes;
     int *dev_err;
     int num_sms;
+    // optional: the forward's output (after the gate) and each row's log-sum-exp from a forward call with
+    // lse; given both, the forward is not run again
+    const void *out_fwd = nullptr;
+    const float *lse = nullptr;
 };
 bool backward_bf16_r512_supports(int r, int d_q, int d_v);
 size_t backward_bf16_r512_workspace_bytes(long long B, long long T, long long H);

@@ -63,6 +63,7 @@ constexpr uint32_t kRegsCtl = 88, kRegsMath = 200, kRegsLaunch = 168;
 #endif
 static_assert(128 * kRegsCtl + 256 * kRegsMath <= kThreads * kRegsLaunch, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 // Keep a stale row maximum until the new one exceeds it by this (log2 units):
 // p <= 2^16, far inside the fp32 range of the row sums and the accumulator.
 constexpr float kRescaleLog2 = 16.0f;
@@ -90,7 +91,8 @@ constexpr uint32_t O_ROWINFO = O_P + 2 * kPBytes;    // 2 row-info blocks
 constexpr uint32_t BARS = S_PST + 2 * kPUnit;
 constexpr uint32_t PMAX = BARS + 512;                // [2 parities][2 warpgroups][128 rows] partial maxima
 constexpr uint32_t QMAX = PMAX + 2 * 2 * kBM * 4;    // [2 warpgroups][128 rows] half-row maxima of |x|
-constexpr uint32_t kSmemUsed = QMAX + 2 * kBM * 4;
+constexpr uint32_t LSUM = QMAX + 2 * kBM * 4;        // [128 rows] the second warpgroup's row sums at a tile's end
+constexpr uint32_t kSmemUsed = LSUM + kBM * 4;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 // TMEM columns of the score CTA
 constexpr uint32_t S_QCOL = 0;     // packed f16 q_abs: K step ks (16 latent columns) at columns 8 ks .. 8 ks + 7
@@ -150,7 +152,7 @@ struct Params {
     __nv_bfloat16 *out;
     const float *sscale;   // [B]: 2^-e_b, the scale of sequence b's f16 latent copy
     const __nv_bfloat16 *w_uk;   // [H, d_q, r], read only by the rare recompute of a row beyond f16's range
-    float *st_m, *st_l;          // optional [B, H, T] row statistics (the backward's input)
+    float *lse;                  // optional [B, H, T]: each row's log-sum-exp of the scaled scores (natural log)
     int *err;
     int T, H, n_qtiles, bh_count;
     int n_tiles;   // n_qtiles * bh_count work tiles, numbered heaviest first
@@ -729,8 +731,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         ++nu;
                     }
                     if (!ok) break;
-                    if (p.st_m && wg == 0 && t < p.T)
-                        p.st_m[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = m_run;
+                    if (p.lse) {   // ln sum_u exp(scale s_u) = ln 2 (m + log2 l), l = both warpgroups' sums
+                        if (wg == 1) st_shared_f32(base + LSUM + row * 4, l_part);
+                        named_bar_sync(1, 256);
+                        if (wg == 0 && t < p.T)
+                            p.lse[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] =
+                                kLn2 * (m_run + log2f(l_part + ld_shared_f32(base + LSUM + row * 4)));
+                    }
                     // the first staging buffer takes the next tile's q tile once this tile's last copy has read it
                     if (issuer) bulk_wait_read_all();
                     if (issuer && wg == 0) mbar_arrive(B_(bars->q_free));
@@ -810,8 +817,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         for (int v8 = 0; v8 < 8; ++v8) gv[v8] = make_uint4(0, 0, 0, 0);
                     }
                     const float inv_l = 1.f / (l_even + l_odd);
-                    if (p.st_l && wg == 0 && t < p.T)
-                        p.st_l[(static_cast<size_t>(ti.b) * p.H + ti.h) * p.T + t] = l_even + l_odd;
                     // o_lat/l packed as bf16 pairs in place, the A operand of the W_UV product: warpgroup 0 takes
                     // latent columns 0-255 into TMEM columns 0-127 (chunks in increasing order), warpgroup 1
                     // latent columns 256-511 into columns 384-511 (decreasing order), so no column is written
@@ -1030,8 +1035,7 @@ cudaError_t launch_prefill_bf16_r512(const PrefillArgs &a, cudaStream_t s) {
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.sscale = sscale;
     p.w_uk = static_cast<const __nv_bfloat16 *>(a.w_uk);
-    p.st_m = a.stats_m;
-    p.st_l = a.stats_l;
+    p.lse = a.lse;
     p.err = a.dev_err;
     p.T = a.T;
     p.H = a.H;

@@ -11,7 +11,8 @@ library.
   projection of step 4, in numpy fp64, used to build full-layer inputs;
   ``layer_forward`` composes them with ``prefill`` into the whole layer.
 * ``prefill_backward`` (module ``backward``) takes the chain rule back through
-  steps 2-4 in numpy fp64: the gradients of the prefill's inputs.
+  steps 2-4 in numpy fp64: the gradients of the prefill's inputs; ``prefill_lse``
+  gives each row's softmax normaliser (log-sum-exp of the scaled scores).
 
 Parity status of each function is stated in its docstring; the pins live in
 ``tests/test_oracle.py``.
@@ -154,6 +155,14 @@ def prefill_backward(q, c, w_uk, w_uv, gate, scale: float, dout) -> dict:
     """
     from .backward import prefill_backward as _bwd
     return _bwd(q, c, w_uk, w_uv, gate, scale, dout)
+
+
+def prefill_lse(q, c, w_uk, scale: float = 1.0) -> np.ndarray:
+    """Each row's log-sum-exp of the scaled causal scores, [B,H,T] fp64; see ``oracle.backward.prefill_lse``.
+    Parity: pinned by closed forms and by rebuilding ``prefill``'s output (tests/test_oracle_backward.py).
+    """
+    from .backward import prefill_lse as _lse
+    return _lse(q, c, w_uk, scale)
 
 
 def decode(q_abs, c_cache, lens, w_uv, gate=None, scale: float = 1.0) -> np.ndarray:

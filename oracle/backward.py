@@ -76,3 +76,26 @@ def prefill_backward(q, c, w_uk, w_uv, gate, scale: float, dout) -> dict:
             dw_uk[h] += q[b, :, h, :].T @ d_qabs
     return dict(dq=dq, dc=dc, dw_uk=dw_uk, dw_uv=dw_uv,
                 dgate=None if dgate is None else dgate.reshape(B, T, H * dv))
+
+
+def prefill_lse(q, c, w_uk, scale: float) -> np.ndarray:
+    """Each row's log-sum-exp of the scaled, causally masked scores, in fp64: the normaliser of the softmax of
+    step 2 (page "Gated MLA（矩阵吸收版）", section "完整计算流（四步）"),
+
+        lse[b, h, t] = ln sum_{u <= t} exp(scale * q_abs[b, t, h, :] . c[b, u, :]),   q_abs = q . W_UK[h]
+
+    so that the weights are a[t, u] = exp(s[t, u] - lse[t]).  Returns [B, H, T].
+    Parity: pinned by closed forms (T = 1; zero queries) and by rebuilding ``oracle.prefill``'s output from it
+    (tests/test_oracle_backward.py).
+    """
+    q, c, w_uk = _f64(q), _f64(c), _f64(w_uk)
+    B, T, H, _ = q.shape
+    visible = np.tril(np.ones((T, T), dtype=bool))
+    out = np.empty((B, H, T))
+    for b in range(B):
+        for h in range(H):
+            s = np.where(visible, scale * ((q[b, :, h, :] @ w_uk[h]) @ c[b].T), -np.inf)
+            m = s.max(axis=1)
+            out[b, h] = m + np.log(np.exp(s - m[:, None]).sum(axis=1))
+    return out
+

@@ -337,3 +337,41 @@ def test_backward_workspace_size(lib):
     assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, BF16) == 2 * 128 * 8 * (2 * 32 + 4) * 4
     assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 32, 7) == 0
     assert lib.mla_absorbed_attn_bwd_workspace_size(2, 128, 8, 16, 16, 65, F32) == 0
+
+
+# ----------------------------------------------------------------------------- forward with lse, backward given it
+def fwd_lse_call(lib, lse=FAKE, **kw):
+    a = dict(q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=None, out=FAKE, B=1, T=256, H=2, dq=128, dv=128, r=512,
+             dtype=BF16, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.mla_absorbed_attn_fwd_lse(a["q"], a["c"], a["wuk"], a["wuv"], a["gate"], 1.0, a["out"], lse, a["B"],
+                                         a["T"], a["H"], a["dq"], a["dv"], a["r"], a["dtype"], a["ws"], a["ws_bytes"],
+                                         None)
+
+
+def bwd_lse_call(lib, out=FAKE, lse=FAKE, **kw):
+    a = dict(q=FAKE, c=FAKE, wuk=FAKE, wuv=FAKE, gate=FAKE, dout=FAKE, dq=FAKE, dc=FAKE, dwuk=FAKE, dwuv=FAKE,
+             dgate=FAKE, B=1, T=256, H=2, dq_dim=128, dv=128, r=512, dtype=BF16, ws=FAKE, ws_bytes=1 << 40)
+    a.update(kw)
+    return lib.mla_absorbed_attn_bwd_lse(a["q"], a["c"], a["wuk"], a["wuv"], a["gate"], 1.0, a["dout"], out, lse,
+                                         a["dq"], a["dc"], a["dwuk"], a["dwuv"], a["dgate"], a["B"], a["T"], a["H"],
+                                         a["dq_dim"], a["dv"], a["r"], a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+def test_fwd_lse_refusals(lib):
+    assert fwd_lse_call(lib, lse=None) == ERR_NULL
+    assert fwd_lse_call(lib, lse=FAKE + 4) == ERR_ALIGN
+    # only the r = 512 bf16 kernel writes the statistics
+    assert fwd_lse_call(lib, r=32, dq=16, dv=16) == ERR_UNSUPPORTED
+    assert fwd_lse_call(lib, dtype=F32, r=32, dq=16, dv=16, ws=None, ws_bytes=0) == ERR_UNSUPPORTED
+    assert fwd_lse_call(lib, B=0) == OK
+
+
+def test_bwd_lse_refusals(lib):
+    assert bwd_lse_call(lib, out=None) == ERR_NULL
+    assert bwd_lse_call(lib, lse=None) == ERR_NULL
+    assert bwd_lse_call(lib, lse=FAKE + 4) == ERR_ALIGN
+    assert bwd_lse_call(lib, out=FAKE + 2) == ERR_ALIGN
+    assert bwd_lse_call(lib, r=32, dq_dim=16, dv=16, dtype=F32) == ERR_UNSUPPORTED
+    assert bwd_lse_call(lib, ws=None) == ERR_WORKSPACE
+    assert bwd_lse_call(lib, B=0) == OK

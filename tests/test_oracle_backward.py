@@ -66,3 +66,41 @@ def test_future_tokens_do_not_receive_gradient_from_the_past(oracle):
     dout[:, 1] = 1.0
     got = oracle.prefill_backward(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0, dout)
     assert np.all(got["dq"][:, 2:] == 0.0) and np.all(got["dc"][:, 2:] == 0.0)
+
+
+# ---- prefill_lse: each row's log-sum-exp of the scaled causal scores
+
+def test_lse_single_token_is_the_score(oracle):
+    """T = 1: one visible key, so the log-sum-exp is that key's scaled score."""
+    d, _ = tiny(seed=41, T=1)
+    lse = oracle.prefill_lse(d["q"], d["c"], d["w_uk"], 0.8)
+    for b in range(2):
+        for h in range(2):
+            s = 0.8 * float((d["q"][b, 0, h] @ d["w_uk"][h]) @ d["c"][b, 0])
+            assert abs(lse[b, h, 0] - s) < 1e-12
+
+
+def test_lse_of_zero_queries_counts_the_visible_keys(oracle):
+    """q = 0: every score is 0, so row t sums t + 1 ones."""
+    d, _ = tiny(seed=42, T=6)
+    lse = oracle.prefill_lse(np.zeros_like(d["q"]), d["c"], d["w_uk"], 1.3)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, 7)), lse.shape), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("scale", [0.5, 4.0])
+def test_lse_rebuilds_the_forward_output(oracle, scale):
+    """The weights exp(s - lse) applied to c, then W_UV^T and the gate, give the C forward oracle's output: lse is
+    the normaliser of the same softmax (a dropped term or a wrong mask changes every row after the first)."""
+    d, _ = tiny(seed=43, T=7)
+    lse = oracle.prefill_lse(d["q"], d["c"], d["w_uk"], scale)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], scale)
+    B, T, H, _ = d["q"].shape
+    dv = d["w_uv"].shape[1]
+    out = np.zeros((B, T, H, dv))
+    for b in range(B):
+        for h in range(H):
+            s = scale * (d["q"][b, :, h] @ d["w_uk"][h]) @ d["c"][b].T
+            a = np.where(np.tril(np.ones((T, T), dtype=bool)), np.exp(s - lse[b, h][:, None]), 0.0)
+            out[b, :, h] = (a @ d["c"][b]) @ d["w_uv"][h].T
+    out = out.reshape(B, T, H * dv) / (1.0 + np.exp(-d["gate"]))
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-12)

@@ -127,3 +127,61 @@ def test_bwd_r512_many_items_per_cta(env):
     for k in KEYS:
         if got[k] is not None:
             assert np.array_equal(got[k], again[k].double().cpu().numpy()), k
+
+
+# ---- the forward's log-sum-exp, and the backward given the forward's output and log-sum-exp
+
+TOL_LSE = 2e-2   # natural-log units: the relative error it puts on the softmax weights, the bf16 bar
+
+
+def tensors(env, d):
+    torch = env[0]
+    t = lambda a: None if a is None else torch.tensor(np.asarray(a, np.float32), device="cuda").to(torch.bfloat16)  # noqa: E731
+    return {k: t(d[k]) for k in ("q", "c", "w_uk", "w_uv", "gate", "dout")}
+
+
+@pytest.mark.parametrize("B,T,H,scale", [(1, 300, 2, 1.0), (2, 200, 3, 1.0 / np.sqrt(128.0)), (1, 1, 2, 1.0)])
+def test_fwd_lse_matches_the_oracle(env, B, T, H, scale):
+    """Each row's log-sum-exp from the forward (bf16 inputs, f16 score operands) against the fp64 one; the output
+    of the call is the plain forward's, bit for bit."""
+    torch, lca, oracle = env
+    d = case(B, T, H, seed=51 + T)
+    x = tensors(env, d)
+    plain = lca.mla_absorbed_attn_fwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], scale)
+    out, lse = lca.mla_absorbed_attn_fwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], scale, return_lse=True)
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    assert torch.equal(out, plain)
+    ref = oracle.prefill_lse(d["q"], d["c"], d["w_uk"], scale)
+    got = lse.double().cpu().numpy()
+    assert got.shape == ref.shape and np.all(np.isfinite(got))
+    assert float(np.max(np.abs(got - ref))) <= TOL_LSE
+
+
+@pytest.mark.parametrize("gate", [True, False])
+def test_bwd_lse_matches_the_oracle(env, gate):
+    """The backward given the forward's (out, lse): the forward is not run again, the attention matrix comes
+    from lse and dgate from the gated output; every gradient against the oracle's."""
+    torch, lca, oracle = env
+    d = case(2, 300, 2, seed=61, gate=gate)
+    x = tensors(env, d)
+    out, lse = lca.mla_absorbed_attn_fwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], 1.0, return_lse=True)
+    got = lca.mla_absorbed_attn_bwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], 1.0, x["dout"], out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    ref = oracle.prefill_backward(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0, d["dout"])
+    check({k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref)
+
+
+def test_bwd_lse_peaky(env):
+    """The peaky case (scores spread over several natural-log units) through the saved statistics."""
+    torch, lca, oracle = env
+    d = case(1, 400, 2, seed=9, wuk_std=0.04)
+    d["q"] = W.round_bf16(d["q"] / W.MID_PREFILL_BF16.q_std * 1.5)
+    x = tensors(env, d)
+    out, lse = lca.mla_absorbed_attn_fwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], 1.0, return_lse=True)
+    got = lca.mla_absorbed_attn_bwd(x["q"], x["c"], x["w_uk"], x["w_uv"], x["gate"], 1.0, x["dout"], out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert lca.mla_get_device_error() == 0
+    ref = oracle.prefill_backward(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 1.0, d["dout"])
+    check({k: None if got[k] is None else got[k].double().cpu().numpy() for k in KEYS}, ref)
