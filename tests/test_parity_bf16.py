@@ -252,3 +252,13 @@ def test_small_rank_causality_bitwise(env):
     d2["c"][:, t0 + 1:] = W.round_bf16(d["c"][:, t0 + 1:] + 1)
     out = run_prefill(env, d2, 1.0).reshape(300, -1)
     assert np.array_equal(out[: t0 + 1], base[: t0 + 1])
+
+
+def test_small_rank_many_tiles_per_cta(env):
+    """r = 64, d_q = 32, d_v = 48, a ragged T and 416 tiles: more tiles than resident CTAs (two per SM), so the
+    later tiles run on CTAs launched as earlier ones finish."""
+    _, _, oracle = env
+    d = small_case(2, 1600, 16, 64, 32, 48, seed=77, gate=True)
+    got = run_prefill(env, d, 0.8).reshape(2, 1600, -1)
+    ref = oracle.prefill(d["q"], d["c"], d["w_uk"], d["w_uv"], d["gate"], 0.8)
+    assert rel_err(got, ref) <= TOL_BF16
