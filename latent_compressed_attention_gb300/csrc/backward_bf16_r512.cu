@@ -97,7 +97,7 @@ struct KWalk {
 __device__ __forceinline__ KWalk k_walk(const GemmP &p, int m0) {
     switch (p.problem) {
         case kQAbs: case kDoLat: return {1, 0, kD, 1};
-        case kP: return {1, 0, kR, 2};                                             // hi and lo
+        case kP: return {1, 0, kR, 1};                                             // hi and lo in one step
         case kDS: case kDq: return {1, 0, kR, 1};
         case kOLat: case kDqAbs: return {1, 0, min(p.T, m0 + p.tile_m), 1};      // u <= t
         case kDc: return {p.H, m0, p.T, 2};                                        // t >= u, every head
@@ -230,8 +230,13 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
             for (int j = 0; j < nbp; ++j)
                 for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, h);
             break;
-        case kP: case kDS:   // A = q_abs (hi, then lo) or do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
-            tl3<kPair>(sa, pair ? ta2 : ta, bar, k, m0, zz);
+        case kP:   // A = q_abs [z,T,r] (K-major): hi at sa, lo at sa + 16 KB; B = c [B,T,r] (K-major, rows u)
+            tl3<kPair>(sa, ta, bar, k, m0, zz);
+            tl3<kPair>(sa + kOpBytes, ta2, bar, k, m0, zz);
+            for (int j = 0; j < nbp; ++j) tl3<kPair>(sb + j * 16384, tb, bar, k, n0 + 128 * j, b);
+            break;
+        case kDS:   // A = do_lat [z,T,r] (K-major), B = c [B,T,r] (K-major, rows u)
+            tl3<kPair>(sa, ta, bar, k, m0, zz);
             for (int j = 0; j < nbp; ++j) tl3<kPair>(sb + j * 16384, tb, bar, k, n0 + 128 * j, b);
             break;
         case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
@@ -419,20 +424,24 @@ __device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int s
 // the accumulator alternates between two kW-column halves of the CTA's TMEM, so one item's epilogue overlaps
 // the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256 tiles (B staged as
 // two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue column groups.
-template <int kW>
+// kNA: A operands of a K step (2 for P: the hi and lo parts of q_abs against one c tile, so c is staged once
+// for both products)
+template <int kW, int kNA = 1>
 struct Shape {
-    static constexpr int kStagesW = kW == 256 ? 4 : 3;
-    static constexpr uint32_t kStageW = kOpBytes + kW * 128;   // A [128 x 64] + B [kW x 64]
+    static constexpr int kStagesW = kW == 256 && kNA == 1 ? 4 : 3;
+    static constexpr uint32_t kBOff = kNA * kOpBytes;          // B's offset in a stage
+    static constexpr uint32_t kStageW = kBOff + kW * 128;      // A [128 x 64] (kNA of them) + B [kW x 64]
     static constexpr uint32_t kBarOffW = kStagesW * kStageW;
     static constexpr uint32_t kSmemW = kBarOffW + 256 + 1024;
     static constexpr int kGroups = kW / 128;                   // epilogue column groups of four warps
     static constexpr int kThreadsW = 96 + 128 * kGroups;       // warps 0 and 2 TMA, warp 1 MMA, then the epilogue
     static constexpr int kMinBlocks = kW == 256 ? 1 : 2;
 };
-static_assert(Shape<256>::kSmemW <= 232448 && 2 * Shape<128>::kSmemW <= 233472, "shared memory");
+static_assert(Shape<256>::kSmemW <= 232448 && Shape<256, 2>::kSmemW <= 232448 && 2 * Shape<128>::kSmemW <= 233472,
+              "shared memory");
 
-template <int kW>
-__global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
+template <int kW, int kNA>
+__global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMinBlocks)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
                     const GemmP p) {
@@ -440,7 +449,7 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    using S = Shape<kW>;
+    using S = Shape<kW, kNA>;
     constexpr int kStages = S::kStagesW;
     constexpr uint32_t kStageBytes = S::kStageW;
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + S::kBarOffW);
@@ -493,7 +502,7 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
                 const int pr = s % w.pairs, s2 = s / w.pairs;
                 const uint32_t bar = smem_u32(full + st);
                 mbar_arrive_expect_tx(bar, kStageBytes);
-                load_step<false>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + kOpBytes,
+                load_step<false>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes, base + st * kStageBytes + S::kBOff,
                                  bar, t.z, s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * kBM, t.nt * kW,
                                  S::kGroups);
             }
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
         // two 64-wide slabs 8 KB apart, 2 KB per K step; K-major: 32 bytes per K step), so the issue loop is
         // one add per operand per MMA
         const uint64_t a0 = make_smem_desc(base, amn ? 8192 : 16, 1024);
-        const uint64_t b0 = make_smem_desc(base + kOpBytes, bmn ? 8192 : 16, 1024);
+        const uint64_t b0 = make_smem_desc(base + S::kBOff, bmn ? 8192 : 16, 1024);
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         int it = 0, lt = 0;
@@ -525,8 +534,11 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
                 tc_fence_after();
                 const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
+                for (int kk = 0; kk < kBK / 16; ++kk) {
                     umma_bf16(d, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (j | kk) != 0);
+                    if constexpr (kNA == 2)   // the lo part against the same B slice
+                        umma_bf16(d, desc_add(as, kOpBytes + kk * a_step), desc_add(bs, kk * b_step), idesc, true);
+                }
                 umma_commit(smem_u32(empty + st));
             }
             if (!ok) break;
@@ -549,8 +561,9 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
             const int m = t.mt * kBM + row, n0 = t.nt * kW + 128 * g;
             const uint32_t trow = tmem + acc * kW + 128 * g + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             RowIn rin;
-            uint4 cur[4];
+            uint4 cur[4], nxt[4];
             read_row_stats(p, z, m, rin);   // in flight while the products finish
+            read_chunk_input(p, z, m, n0, cur);
             const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
             if (!ok) *abort_flag = 1;   // every later wait of every role then returns at once
             tc_fence_after();
@@ -562,7 +575,7 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
             }
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                read_chunk_input(p, z, m, n0 + c4 * 32, cur);
+                if (c4 < 3) read_chunk_input(p, z, m, n0 + (c4 + 1) * 32, nxt);   // one chunk ahead
                 float v[32];
                 if (any) {
                     tmem_ld32(trow + c4 * 32, v);
@@ -576,6 +589,8 @@ __global__ void __launch_bounds__(Shape<kW>::kThreadsW, Shape<kW>::kMinBlocks)
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
                 epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
             }
             epilogue_row(p, z, m, t.nt * S::kGroups + g, rsum);
         }
@@ -714,8 +729,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
             const int m = t.mt * 256 + 128 * static_cast<int>(rank) + row, n0 = t.nt * 256 + 128 * g;
             const uint32_t trow = tmem + acc * 256 + 128 * g + (static_cast<uint32_t>((warp & 3) * 32) << 16);
             RowIn rin;
-            uint4 cur[4];
+            uint4 cur[4], nxt[4];
             read_row_stats(p, z, m, rin);   // in flight while the products finish
+            read_chunk_input(p, z, m, n0, cur);
             const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
             if (!ok) *abort_flag = 1;
             tc_fence_after();
@@ -732,7 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
             if (!any) release();
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                read_chunk_input(p, z, m, n0 + c4 * 32, cur);
+                if (c4 < 3) read_chunk_input(p, z, m, n0 + (c4 + 1) * 32, nxt);   // one chunk ahead
                 float v[32];
                 if (any) {
                     tmem_ld32(trow + c4 * 32, v);
@@ -743,6 +759,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
                 epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
             }
             epilogue_row(p, z, m, 2 * t.nt + g, rsum);
         }
@@ -924,10 +942,12 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     ETT(&mP_k, &mP_mn, L.P);
     ETT(&mdS_k, &mdS_mn, L.dS);
     if (!okm) return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<128>::kSmemW))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<256>::kSmemW))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape<256, 2>::kSmemW))) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kSmem2))) != cudaSuccess)
         return e;
@@ -940,6 +960,7 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     // pairs (one CTA per SM)
     auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                     const CUtensorMap &tb2, int M, int N, int Z, void *out, int kind) {
+        if (pr == kP && kind != 1) return cudaErrorInvalidValue;   // P's staging (hi and lo together): 128 x 256 only
         const int tm = kind == 2 ? 256 : 128, tn = kind == 0 ? 128 : 256;
         const int slots = kind == 0 ? 2 * sms : (kind == 1 ? sms : sms / 2);   // CTAs, or pairs, resident at once
         GemmP gp{};
@@ -986,9 +1007,11 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
         note_launch();
         if (kind == 2) bwd_gemm2_kernel<<<2 * grid, kThreads2, kSmem2, s>>>(ta, tb, ta2, tb2, gp);
+        else if (pr == kP)
+            bwd_gemm_kernel<256, 2><<<grid, Shape<256, 2>::kThreadsW, Shape<256, 2>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
         else if (kind == 1)
-            bwd_gemm_kernel<256><<<grid, Shape<256>::kThreadsW, Shape<256>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
-        else bwd_gemm_kernel<128><<<grid, Shape<128>::kThreadsW, Shape<128>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+            bwd_gemm_kernel<256, 1><<<grid, Shape<256>::kThreadsW, Shape<256>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+        else bwd_gemm_kernel<128, 1><<<grid, Shape<128>::kThreadsW, Shape<128>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess || gp.ksplit == 1) return err;
         const long long n4 = gp.part_n / 4;   // N = r: a multiple of 4
