@@ -39,7 +39,6 @@ namespace {
 constexpr int kR = 512, kD = 128;
 constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr uint32_t kOpBytes = 128 * 128;            // an operand's stage: [128 x 64] K-major or 2 x [64 x 64] MN-major
-constexpr uint32_t kStageBytes = 2 * kOpBytes;      // A and B of a 128 x 128 tile
 // warp 0 TMA, warp 1 MMA, then the epilogue warps (thread = row)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -114,7 +113,7 @@ struct Item {
 __device__ __forceinline__ Item item_of(const GemmP &p, int idx) {
     Item t{0, 0, 0, 0};
     if (causal_tiles(p.problem)) {
-        if (p.tile_n == 256) {
+        if (p.tile_m == 128 && p.tile_n == 256) {
             // 128-row tiles by 256-column blocks, the lower triangle (block nt starts at or left of the diagonal:
             // nt <= mt / 2) of one batch item after another; row tile mt starts at item C(mt) of its batch item,
             // C(2a) = a (a + 1), C(2a + 1) = (a + 1)^2.  At even mt the diagonal block's right half is zeros.
@@ -425,23 +424,27 @@ __device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int s
 // the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256 tiles (B staged as
 // two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue column groups.
 // kNA: A operands of a K step (2 for P: the hi and lo parts of q_abs against one c tile, so c is staged once
-// for both products)
-template <int kW, int kNA = 1>
+// for both products).  kPIn (dS): the item's tile of P [128 x kW] is staged in shared memory by TMA for the
+// epilogue, which would otherwise wait on its rows' global loads.
+template <int kW, int kNA = 1, bool kPIn = false>
 struct Shape {
-    static constexpr int kStagesW = kW == 256 && kNA == 1 ? 4 : 3;
+    static constexpr int kStagesW = kW == 256 && kNA == 1 && !kPIn ? 4 : 3;
     static constexpr uint32_t kBOff = kNA * kOpBytes;          // B's offset in a stage
     static constexpr uint32_t kStageW = kBOff + kW * 128;      // A [128 x 64] (kNA of them) + B [kW x 64]
-    static constexpr uint32_t kBarOffW = kStagesW * kStageW;
+    static constexpr uint32_t kPOff = kStagesW * kStageW;      // the P tile: kW / 64 boxes [128 x 64]
+    static constexpr uint32_t kPBytes = kPIn ? 128 * kW * 2 : 0;
+    static constexpr uint32_t kBarOffW = kPOff + kPBytes;
     static constexpr uint32_t kSmemW = kBarOffW + 256 + 1024;
     static constexpr int kGroups = kW / 128;                   // epilogue column groups of four warps
     static constexpr int kThreadsW = 96 + 128 * kGroups;       // warps 0 and 2 TMA, warp 1 MMA, then the epilogue
     static constexpr int kMinBlocks = kW == 256 ? 1 : 2;
 };
-static_assert(Shape<256>::kSmemW <= 232448 && Shape<256, 2>::kSmemW <= 232448 && 2 * Shape<128>::kSmemW <= 233472,
+static_assert(Shape<256>::kSmemW <= 232448 && Shape<256, 2>::kSmemW <= 232448 &&
+                  Shape<256, 1, true>::kSmemW <= 232448 && 2 * Shape<128>::kSmemW <= 233472,
               "shared memory");
 
-template <int kW, int kNA>
-__global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMinBlocks)
+template <int kW, int kNA, bool kPIn>
+__global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA, kPIn>::kMinBlocks)
     bwd_gemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                     const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
                     const GemmP p) {
@@ -449,14 +452,16 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
-    using S = Shape<kW, kNA>;
+    using S = Shape<kW, kNA, kPIn>;
     constexpr int kStages = S::kStagesW;
     constexpr uint32_t kStageBytes = S::kStageW;
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + S::kBarOffW);
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;     // [2] the accumulator holds an item's finished sums
     uint64_t *acc_empty = acc_full + 2;       // [2] the epilogue has read them out
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *p_full = acc_empty + 2;         // kPIn: the P tile has landed
+    uint64_t *p_empty = p_full + 1;           // kPIn: every epilogue warp has read it
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(p_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
@@ -470,6 +475,8 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
             mbar_init(smem_u32(acc_full + i), 1);
             mbar_init(smem_u32(acc_empty + i), 128 * S::kGroups);
         }
+        mbar_init(smem_u32(p_full), 1);
+        mbar_init(smem_u32(p_empty), 4 * S::kGroups);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -551,6 +558,21 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
         // 128 g .. 128 g + 127 of the accumulator, g = (w - 3) / 4
         const int g = (warp - 3) >> 2;
         const int row = (warp & 3) * 32 + lane;
+        // kPIn: thread (warp 3, lane 0) loads each item's P tile, the first before the loop and the next one once
+        // every epilogue warp has read the current one
+        const bool p_loader = kPIn && warp == 3 && lane == 0;
+        const uint32_t p_base = base + S::kPOff;
+        int p_loads = 0, p_landed = 0;
+        auto load_p = [&](int pidx) {
+            const Item u = item_of(p, pidx);
+            const uint32_t bar = smem_u32(p_full);
+            mbar_arrive_expect_tx(bar, S::kPBytes);
+#pragma unroll
+            for (int j = 0; j < kW / 64; ++j)
+                tma_load_3d(p_base + j * 16384, &tm_a2, bar, u.nt * kW + 64 * j, u.mt * kBM, u.z);
+            ++p_loads;
+        };
+        if (p_loader && static_cast<int>(blockIdx.x) < p.items) load_p(static_cast<int>(blockIdx.x));
         int lt = 0;
         for (int idx = static_cast<int>(blockIdx.x); idx < p.items; idx += G, ++lt) {
             const Item t = item_of(p, idx);
@@ -563,8 +585,12 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
             RowIn rin;
             uint4 cur[4], nxt[4];
             read_row_stats(p, z, m, rin);   // in flight while the products finish
-            read_chunk_input(p, z, m, n0, cur);
-            const bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
+            if constexpr (!kPIn) read_chunk_input(p, z, m, n0, cur);
+            bool ok = mbar_wait(smem_u32(acc_full + acc), (lt >> 1) & 1, p.err, abort_flag);
+            if constexpr (kPIn) {
+                ok = ok && mbar_wait(smem_u32(p_full), lt & 1, p.err, abort_flag);
+                if (ok && p_loader) ++p_landed;
+            }
             if (!ok) *abort_flag = 1;   // every later wait of every role then returns at once
             tc_fence_after();
             if (!__all_sync(0xffffffffu, ok)) break;
@@ -575,7 +601,20 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
             }
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                if (c4 < 3) read_chunk_input(p, z, m, n0 + (c4 + 1) * 32, nxt);   // one chunk ahead
+                if constexpr (kPIn) {   // this chunk's 64 bytes of the row, from the 128-byte-swizzled boxes
+                    const int cb = 128 * g + 32 * c4;
+                    const uint32_t rb = p_base + (cb >> 6) * 16384 + row * 128;
+                    const int j0 = (cb & 63) >> 3;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cur[q] = ld_shared_v4(rb + (((j0 + q) ^ (row & 7)) << 4));
+                    if (c4 == 3) {   // this warp is done with the P tile
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(p_empty));
+                        __syncwarp();   // converged again for the TMEM load
+                    }
+                } else if (c4 < 3) {
+                    read_chunk_input(p, z, m, n0 + (c4 + 1) * 32, nxt);   // one chunk ahead
+                }
                 float v[32];
                 if (any) {
                     tmem_ld32(trow + c4 * 32, v);
@@ -589,11 +628,23 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
                     for (int i = 0; i < 32; ++i) v[i] = 0.f;
                 }
                 epilogue_chunk(p, z, m, n0 + c4 * 32, t.ks, v, rin.mrow, rin.inv_l, rin.drow, rsum, cur);
+                if constexpr (!kPIn) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+                    for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+                }
             }
             epilogue_row(p, z, m, t.nt * S::kGroups + g, rsum);
+            if (p_loader && idx + G < p.items) {
+                if (!mbar_wait(smem_u32(p_empty), lt & 1, p.err, abort_flag)) {
+                    *abort_flag = 1;
+                } else {
+                    fence_proxy_async_smem();   // the warps' reads of the tile come before the TMA overwrites it
+                    load_p(idx + G);
+                }
+            }
         }
+        if (p_loader)   // no load of the P tile may still be landing at exit
+            for (int q = p_landed; q < p_loads; ++q) mbar_wait(smem_u32(p_full), q & 1, p.err);
     }
     __syncwarp();
     tc_fence_before();
@@ -601,17 +652,25 @@ __global__ void __launch_bounds__(Shape<kW, kNA>::kThreadsW, Shape<kW, kNA>::kMi
     if (warp == 1) tmem_dealloc(tmem, 2 * kW);
 }
 
-// The pair form, for dc (few tiles, each with a long K): a cluster of two CTAs, one
-// per SM, computes 256 x 256 tiles with cta_group::2 MMAs.  CTA r of the pair stages rows 128 r .. 128 r + 127
-// of the tile's A and columns 128 r .. 128 r + 127 of its B, so each SM loads 32 KB per K step of 64 for
-// twice the products of a 128 x 128 tile, and holds rows 128 r .. 128 r + 127 of the 256 x 256 sums in TMEM
-// (two 256-column accumulators).  The even CTA issues the MMAs; both CTAs' loads complete on its barriers, its
-// commits arrive on both CTAs' barriers, and both CTAs' epilogue warps report to it when an accumulator is read.
-constexpr int kStages2 = 6;
-constexpr uint32_t kSmem2 = kStages2 * kStageBytes + 256 + 1024;   // one CTA per SM
+// The pair form: a cluster of two CTAs, one per SM, computes 256 x 256 tiles with cta_group::2 MMAs.  CTA r of
+// the pair stages rows 128 r .. 128 r + 127 of the tile's A and columns 128 r .. 128 r + 127 of its B, so each SM
+// loads 32 KB per K step of 64 for twice the products of a 128 x 128 tile, and holds rows 128 r .. 128 r + 127 of
+// the 256 x 256 sums in TMEM (two 256-column accumulators).  Per SM the tensor core reads 8 KB of shared memory
+// per 16-deep product instead of the 12 KB of a 128 x 256 tile, which with the TMA writes keeps the SM's
+// shared-memory traffic under its bandwidth at the full product rate.  The even CTA issues the MMAs; both CTAs'
+// loads complete on its barriers, its commits arrive on both CTAs' barriers, and both CTAs' epilogue warps report
+// to it when an accumulator is read.  kNA = 2 (P): each CTA stages both q_abs parts with its half of the c tile.
+template <int kNA>
+struct Shape2 {
+    static constexpr int kStages = kNA == 2 ? 4 : 6;
+    static constexpr uint32_t kBOff = kNA * kOpBytes;
+    static constexpr uint32_t kStage = kBOff + kOpBytes;
+    static constexpr uint32_t kSmem = kStages * kStage + 256 + 1024;   // one CTA per SM
+};
 constexpr int kThreads2 = 352;   // warps 0 and 2 TMA, warp 1 MMA (even CTA), warps 3-10 epilogue (two column halves)
-static_assert(kSmem2 <= 232448, "exceeds the 227 KB shared-memory limit");
+static_assert(Shape2<1>::kSmem <= 232448 && Shape2<2>::kSmem <= 232448, "exceeds the 227 KB shared-memory limit");
 
+template <int kNA>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     bwd_gemm2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                      const __grid_constant__ CUtensorMap tm_a2, const __grid_constant__ CUtensorMap tm_b2,
@@ -620,6 +679,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
+    using S2 = Shape2<kNA>;
+    constexpr int kStages2 = S2::kStages;
+    constexpr uint32_t kStageBytes = S2::kStage;
     uint64_t *full = reinterpret_cast<uint64_t *>(gbase + kStages2 * kStageBytes);   // even CTA: both CTAs' loads
     uint64_t *empty = full + kStages2;         // each CTA's own: the stage's products completed
     uint64_t *acc_full = empty + kStages2;     // [2] each CTA's own: the accumulator holds an item's sums
@@ -671,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
                 const int pr = s % w.pairs, s2 = s / w.pairs;
                 if (rank == 0) mbar_arrive_expect_tx(smem_u32(full + st), 2 * kStageBytes);
                 load_step<true>(p, &tm_a, &tm_b, &tm_a2, &tm_b2, base + st * kStageBytes,
-                                base + st * kStageBytes + kOpBytes, mapa_shared(smem_u32(full + st), 0), t.z,
+                                base + st * kStageBytes + S2::kBOff, mapa_shared(smem_u32(full + st), 0), t.z,
                                 s2 / w.inner, w.lo + (s2 % w.inner) * kBK, pr, t.mt * 256 + 128 * rank,
                                 t.nt * 256 + 128 * rank);
             }
@@ -684,7 +746,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const bool amn = a_mn(p.problem), bmn = b_mn(p.problem);
         const uint32_t idesc = make_idesc_bf16(256, 256, amn ? 1 : 0, bmn ? 1 : 0);
         const uint64_t a0 = make_smem_desc(base, amn ? 8192 : 16, 1024);
-        const uint64_t b0 = make_smem_desc(base + kOpBytes, bmn ? 8192 : 16, 1024);
+        const uint64_t b0 = make_smem_desc(base + S2::kBOff, bmn ? 8192 : 16, 1024);
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         int it = 0, lt = 0;
@@ -701,8 +763,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
                 tc_fence_after();
                 const uint64_t as = desc_add(a0, st * kStageBytes), bs = desc_add(b0, st * kStageBytes);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
+                for (int kk = 0; kk < kBK / 16; ++kk) {
                     umma2(d, desc_add(as, kk * a_step), desc_add(bs, kk * b_step), idesc, (j | kk) != 0);
+                    if constexpr (kNA == 2)   // the lo part against the same B slice
+                        umma2(d, desc_add(as, kOpBytes + kk * a_step), desc_add(bs, kk * b_step), idesc, true);
+                }
                 umma2_commit(smem_u32(empty + st), 0x3);
             }
             if (!ok) break;
@@ -942,14 +1007,18 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     ETT(&mP_k, &mP_mn, L.P);
     ETT(&mdS_k, &mdS_mn, L.dS);
     if (!okm) return cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<128>::kSmemW))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<256>::kSmemW))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<256, 2>::kSmemW))) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kSmem2))) != cudaSuccess)
+        (e = cudaFuncSetAttribute(bwd_gemm_kernel<256, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape<256, 1, true>::kSmemW))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_gemm2_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape2<1>::kSmem))) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_gemm2_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(Shape2<2>::kSmem))) != cudaSuccess)
         return e;
     const int sms = a.num_sms > 1 ? a.num_sms : 2;
     auto split_for = [&](long long base_items, int slots) {   // parts per tile: about four items per slot
@@ -960,7 +1029,7 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     // pairs (one CTA per SM)
     auto gemm = [&](int pr, const CUtensorMap &ta, const CUtensorMap &tb, const CUtensorMap &ta2,
                     const CUtensorMap &tb2, int M, int N, int Z, void *out, int kind) {
-        if (pr == kP && kind != 1) return cudaErrorInvalidValue;   // P's staging (hi and lo together): 128 x 256 only
+        if (pr == kP && kind == 0) return cudaErrorInvalidValue;   // P's staging (hi and lo together): 128 x 256 or pairs
         const int tm = kind == 2 ? 256 : 128, tn = kind == 0 ? 128 : 256;
         const int slots = kind == 0 ? 2 * sms : (kind == 1 ? sms : sms / 2);   // CTAs, or pairs, resident at once
         GemmP gp{};
@@ -1006,12 +1075,16 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
         gp.items = static_cast<int>(items);
         const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
         note_launch();
-        if (kind == 2) bwd_gemm2_kernel<<<2 * grid, kThreads2, kSmem2, s>>>(ta, tb, ta2, tb2, gp);
+        if (kind == 2 && pr == kP) bwd_gemm2_kernel<2><<<2 * grid, kThreads2, Shape2<2>::kSmem, s>>>(ta, tb, ta2, tb2, gp);
+        else if (kind == 2) bwd_gemm2_kernel<1><<<2 * grid, kThreads2, Shape2<1>::kSmem, s>>>(ta, tb, ta2, tb2, gp);
         else if (pr == kP)
-            bwd_gemm_kernel<256, 2><<<grid, Shape<256, 2>::kThreadsW, Shape<256, 2>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+            bwd_gemm_kernel<256, 2, false><<<grid, Shape<256, 2>::kThreadsW, Shape<256, 2>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+        else if (pr == kDS && kind == 1)   // ta2: P [z, T, Tp] in [128 x 64] boxes
+            bwd_gemm_kernel<256, 1, true><<<grid, Shape<256, 1, true>::kThreadsW, Shape<256, 1, true>::kSmemW, s>>>(
+                ta, tb, ta2, tb2, gp);
         else if (kind == 1)
-            bwd_gemm_kernel<256, 1><<<grid, Shape<256>::kThreadsW, Shape<256>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
-        else bwd_gemm_kernel<128, 1><<<grid, Shape<128>::kThreadsW, Shape<128>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+            bwd_gemm_kernel<256, 1, false><<<grid, Shape<256>::kThreadsW, Shape<256>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
+        else bwd_gemm_kernel<128, 1, false><<<grid, Shape<128>::kThreadsW, Shape<128>::kSmemW, s>>>(ta, tb, ta2, tb2, gp);
         cudaError_t err = cudaGetLastError();
         if (err != cudaSuccess || gp.ksplit == 1) return err;
         const long long n4 = gp.part_n / 4;   // N = r: a multiple of 4
@@ -1025,10 +1098,10 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     // 5. dq_abs; 6. dc and dq; 7. the weight gradients
     if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa), 1)) != cudaSuccess) return e;
     if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl), 1)) != cudaSuccess) return e;
-    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), 1)) != cudaSuccess) return e;
-    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), 1)) != cudaSuccess) return e;
-    if ((e = gemm(kDS, mdl_k, mc_k, mdl_k, mc_k, T, T, Z, bf(L.dS), 1)) != cudaSuccess) return e;
-    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), 2)) != cudaSuccess) return e;
+    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), 2)) != cudaSuccess) return e;
+    if ((e = gemm(kDS, mdl_k, mc_k, mP_k, mc_k, T, T, Z, bf(L.dS), 1)) != cudaSuccess) return e;
+    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), 2)) != cudaSuccess) return e;
     if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc, 2)) != cudaSuccess) return e;
     if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq, 0)) != cudaSuccess) return e;
     if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk, 1)) != cudaSuccess) return e;
