@@ -196,6 +196,14 @@ __device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
     return w;
 }
 
+// The item of turn n of a persistent loop for slot `slot` of `slots` (a CTA, or a CTA pair): turn 0 deals items
+// 0 .. slots - 1 in slot order, turn 1 the next slots items in reverse order, and so on, so that a heavy-first
+// order of items of unequal K gives every slot about the same total (a plain stride gives slot 0 the heaviest
+// item of every turn).
+__device__ __forceinline__ int turn_item(int n, int slot, int slots) {
+    return n * slots + ((n & 1) ? slots - 1 - slot : slot);
+}
+
 // TMA loads of one K step into stage memory: A at sa, B at sb (each 16 KB).  z: batch item of the output tile,
 // o: the outer K index, k: the inner K offset, pair: which operand pair (dc).
 template <bool kPair>
@@ -419,10 +427,11 @@ __device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int s
     }
 }
 
-// Persistent: CTA i takes items i, i + G, i + 2G, ... (G = the grid).  The TMA ring runs on across items, and
-// the accumulator alternates between two kW-column halves of the CTA's TMEM, so one item's epilogue overlaps
-// the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256 tiles (B staged as
-// two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue column groups.
+// Persistent: CTA i takes items i, 2G - 1 - i, 2G + i, ... (G = the grid; turn_item).  The TMA ring runs on
+// across items, and the accumulator alternates between two kW-column halves of the CTA's TMEM, so one item's
+// epilogue overlaps the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256
+// tiles (B staged as two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue
+// column groups.
 // kNA: A operands of a K step (2 for P: the hi and lo parts of q_abs against one c tile, so c is staged once
 // for both products).  kPIn (dS): the item's tile of P [128 x kW] is staged in shared memory by TMA for the
 // epilogue, which would otherwise wait on its rows' global loads.
@@ -498,7 +507,8 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         }
         bool ok = true;
         int it = 0;
-        for (int idx = static_cast<int>(blockIdx.x); ok && idx < p.items; idx += G) {
+        const int slot = static_cast<int>(blockIdx.x);
+        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(++turn, slot, G)) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
@@ -528,7 +538,8 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         int it = 0, lt = 0;
-        for (int idx = static_cast<int>(blockIdx.x); ok && idx < p.items; idx += G, ++lt) {
+        const int slot = static_cast<int>(blockIdx.x);
+        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(++turn, slot, G), ++lt) {
             const Walk w = walk_of(p, item_of(p, idx));
             const int acc = lt & 1;
             if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
@@ -574,7 +585,8 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         };
         if (p_loader && static_cast<int>(blockIdx.x) < p.items) load_p(static_cast<int>(blockIdx.x));
         int lt = 0;
-        for (int idx = static_cast<int>(blockIdx.x); idx < p.items; idx += G, ++lt) {
+        const int slot = static_cast<int>(blockIdx.x);
+        for (int turn = 0, idx = slot; idx < p.items; idx = turn_item(++turn, slot, G), ++lt) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             const bool any = w.s_hi > w.s_lo;
@@ -634,12 +646,12 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
                 }
             }
             epilogue_row(p, z, m, t.nt * S::kGroups + g, rsum);
-            if (p_loader && idx + G < p.items) {
+            if (p_loader && turn_item(turn + 1, slot, G) < p.items) {
                 if (!mbar_wait(smem_u32(p_empty), lt & 1, p.err, abort_flag)) {
                     *abort_flag = 1;
                 } else {
                     fence_proxy_async_smem();   // the warps' reads of the tile come before the TMA overwrites it
-                    load_p(idx + G);
+                    load_p(turn_item(turn + 1, slot, G));
                 }
             }
         }
@@ -721,7 +733,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         }
         bool ok = true;
         int it = 0;
-        for (int idx = pair_id; ok && idx < p.items; idx += n_pairs) {
+        for (int turn = 0, idx = pair_id; ok && idx < p.items; idx = turn_item(++turn, pair_id, n_pairs)) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
@@ -750,7 +762,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         int it = 0, lt = 0;
-        for (int idx = pair_id; ok && idx < p.items; idx += n_pairs, ++lt) {
+        for (int turn = 0, idx = pair_id; ok && idx < p.items; idx = turn_item(++turn, pair_id, n_pairs), ++lt) {
             const Walk w = walk_of(p, item_of(p, idx));
             const int acc = lt & 1;
             if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
@@ -785,7 +797,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const int g = (warp - 3) >> 2;
         const int row = (warp & 3) * 32 + lane;
         int lt = 0;
-        for (int idx = pair_id; idx < p.items; idx += n_pairs, ++lt) {
+        for (int turn = 0, idx = pair_id; idx < p.items; idx = turn_item(++turn, pair_id, n_pairs), ++lt) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             const bool any = w.s_hi > w.s_lo;
