@@ -196,12 +196,13 @@ __device__ __forceinline__ Walk walk_of(const GemmP &p, const Item &t) {
     return w;
 }
 
-// The item of turn n of a persistent loop for slot `slot` of `slots` (a CTA, or a CTA pair): turn 0 deals items
-// 0 .. slots - 1 in slot order, turn 1 the next slots items in reverse order, and so on, so that a heavy-first
-// order of items of unequal K gives every slot about the same total (a plain stride gives slot 0 the heaviest
-// item of every turn).
-__device__ __forceinline__ int turn_item(int n, int slot, int slots) {
-    return n * slots + ((n & 1) ? slots - 1 - slot : slot);
+// The item of turn n of a persistent loop for slot `slot` of `slots` (a CTA, or a CTA pair).  Where K depends
+// on the row tile (o_lat, dq_abs, dc: heavy-first orders), turn 0 deals items 0 .. slots - 1 in slot order,
+// turn 1 the next slots items in reverse order, and so on, so every slot's total comes out about the same (a
+// plain stride gives slot 0 the heaviest item of every turn); items of equal K keep the plain stride.
+__device__ __forceinline__ int turn_item(const GemmP &p, int n, int slot, int slots) {
+    const bool back = (n & 1) && (p.problem == kOLat || p.problem == kDqAbs || p.problem == kDc);
+    return n * slots + (back ? slots - 1 - slot : slot);
 }
 
 // TMA loads of one K step into stage memory: A at sa, B at sb (each 16 KB).  z: batch item of the output tile,
@@ -427,7 +428,7 @@ __device__ __forceinline__ void epilogue_row(const GemmP &p, int z, int m, int s
     }
 }
 
-// Persistent: CTA i takes items i, 2G - 1 - i, 2G + i, ... (G = the grid; turn_item).  The TMA ring runs on
+// Persistent: CTA i takes item i, then 2G - 1 - i or i + G, ... (G = the grid; turn_item).  The TMA ring runs on
 // across items, and the accumulator alternates between two kW-column halves of the CTA's TMEM, so one item's
 // epilogue overlaps the next item's products.  kW = 128: 128 x 128 tiles, two CTAs per SM; kW = 256: 128 x 256
 // tiles (B staged as two 128-column parts, 87 instead of 64 FLOPs per staged byte), one CTA per SM, two epilogue
@@ -508,7 +509,7 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         bool ok = true;
         int it = 0;
         const int slot = static_cast<int>(blockIdx.x);
-        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(++turn, slot, G)) {
+        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(p, ++turn, slot, G)) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
@@ -539,7 +540,7 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         bool ok = true;
         int it = 0, lt = 0;
         const int slot = static_cast<int>(blockIdx.x);
-        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(++turn, slot, G), ++lt) {
+        for (int turn = 0, idx = slot; ok && idx < p.items; idx = turn_item(p, ++turn, slot, G), ++lt) {
             const Walk w = walk_of(p, item_of(p, idx));
             const int acc = lt & 1;
             if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
         if (p_loader && static_cast<int>(blockIdx.x) < p.items) load_p(static_cast<int>(blockIdx.x));
         int lt = 0;
         const int slot = static_cast<int>(blockIdx.x);
-        for (int turn = 0, idx = slot; idx < p.items; idx = turn_item(++turn, slot, G), ++lt) {
+        for (int turn = 0, idx = slot; idx < p.items; idx = turn_item(p, ++turn, slot, G), ++lt) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             const bool any = w.s_hi > w.s_lo;
@@ -646,12 +647,12 @@ __global__ void __launch_bounds__(Shape<kW, kNA, kPIn>::kThreadsW, Shape<kW, kNA
                 }
             }
             epilogue_row(p, z, m, t.nt * S::kGroups + g, rsum);
-            if (p_loader && turn_item(turn + 1, slot, G) < p.items) {
+            if (p_loader && turn_item(p, turn + 1, slot, G) < p.items) {
                 if (!mbar_wait(smem_u32(p_empty), lt & 1, p.err, abort_flag)) {
                     *abort_flag = 1;
                 } else {
                     fence_proxy_async_smem();   // the warps' reads of the tile come before the TMA overwrites it
-                    load_p(turn_item(turn + 1, slot, G));
+                    load_p(turn_item(p, turn + 1, slot, G));
                 }
             }
         }
@@ -733,7 +734,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         }
         bool ok = true;
         int it = 0;
-        for (int turn = 0, idx = pair_id; ok && idx < p.items; idx = turn_item(++turn, pair_id, n_pairs)) {
+        for (int turn = 0, idx = pair_id;
+             ok && idx < p.items; idx = turn_item(p, ++turn, pair_id, n_pairs)) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             for (int s = w.s_lo; s < w.s_hi; ++s, ++it) {
@@ -762,7 +764,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const uint32_t a_step = amn ? 2048u : 32u, b_step = bmn ? 2048u : 32u;
         bool ok = true;
         int it = 0, lt = 0;
-        for (int turn = 0, idx = pair_id; ok && idx < p.items; idx = turn_item(++turn, pair_id, n_pairs), ++lt) {
+        for (int turn = 0, idx = pair_id;
+             ok && idx < p.items; idx = turn_item(p, ++turn, pair_id, n_pairs), ++lt) {
             const Walk w = walk_of(p, item_of(p, idx));
             const int acc = lt & 1;
             if (!(ok = mbar_wait(smem_u32(acc_empty + acc), ((lt >> 1) & 1) ^ 1, p.err, abort_flag))) break;
@@ -797,7 +800,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads2, 1)
         const int g = (warp - 3) >> 2;
         const int row = (warp & 3) * 32 + lane;
         int lt = 0;
-        for (int turn = 0, idx = pair_id; idx < p.items; idx = turn_item(++turn, pair_id, n_pairs), ++lt) {
+        for (int turn = 0, idx = pair_id;
+             idx < p.items; idx = turn_item(p, ++turn, pair_id, n_pairs), ++lt) {
             const Item t = item_of(p, idx);
             const Walk w = walk_of(p, t);
             const bool any = w.s_hi > w.s_lo;
