@@ -9,14 +9,16 @@
 //   dq_abs = dS . c, dc += dS^T . q_abs + A^T . do_lat (summed over heads)            (step 2, both uses of c)
 //   dq = dq_abs . W_UK[h]^T, dW_UK[h] = sum q^T dq_abs                                (step 2, the absorb)
 //
-// Design: the forward kernel recomputes the output o (no gate) and each row's softmax statistics (m, l);
-// every product above is then one launch of a batched tcgen05 GEMM over materialised per-head matrices:
-// the attention matrix P and the score gradient dS ([T, T] per head, bf16, only the causal tiles written
-// or read), q_abs, do_lat, o_lat and dq_abs ([T, r] per head, bf16).  The GEMM takes each operand K-major
-// or MN-major through its own TMA tensor map, skips tiles above the diagonal, limits K to the causal range
-// of each tile, runs K over a second index (heads for dc, sequences for the weight gradients), and fuses
-// the softmax (P = exp2(S - m) / l) and the dS epilogues.  fp32 accumulation in TMEM; the gradients are
-// written in fp32, the intermediate matrices in bf16.
+// Design: the forward's output and each row's log-sum-exp lse of the scaled scores are given by the caller
+// (saved from its forward) or recomputed by the forward kernel; every product above is then one launch of a
+// batched tcgen05 GEMM over materialised per-head matrices: the attention matrix P and the score gradient dS
+// ([T, T] per head, bf16, only the causal tiles written or read), q_abs, do_lat, o_lat and dq_abs ([T, r] per
+// head, bf16).  The GEMM takes each operand K-major or MN-major through its own TMA tensor map, skips tiles
+// above the diagonal, limits K to the causal range of each tile, runs K over a second index (heads for dc,
+// sequences for the weight gradients), and fuses the softmax (P = exp2(S scale log2 e - lse log2 e)) and the
+// dS epilogues.  fp32 accumulation in TMEM; the gradients are written in fp32, the intermediate matrices in
+// bf16.  Two persistent kernels run the products: bwd_gemm_kernel (128-row tiles, one CTA) and
+// bwd_gemm2_kernel (256 x 256 tiles on a CTA pair, which halves each SM's shared-memory traffic per product).
 //
 // delta is the mean of dA under the rounded attention matrix the products use, delta_t = sum_u P dA / sum_u P
 // (the numerator is do_lat_t . o_lat_t with o_lat = P . c; both sums come from the P and o_lat epilogues),
@@ -39,14 +41,14 @@ namespace {
 constexpr int kR = 512, kD = 128;
 constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr uint32_t kOpBytes = 128 * 128;            // an operand's stage: [128 x 64] K-major or 2 x [64 x 64] MN-major
-// warp 0 TMA, warp 1 MMA, then the epilogue warps (thread = row)
+// warps 0 and 2 TMA (alternate ring positions), warp 1 MMA, then the epilogue warps (thread = row)
 constexpr float kLog2e = 1.4426950408889634f;
 
 // The products of the backward.  Operand layouts: "K" = K-major (K contiguous), "MN" = M or N contiguous.
 enum Problem : int {
     kQAbs = 0,   // q_abs[z]   = q[b,:,h,:] . W_UK[h]          M=T  N=r   K=d        A K   B MN   bf16 hi, lo [z,T,r]
     kDoLat,      // do_lat[z]  = do[z] . W_UV[h]                M=T  N=r   K=d_v      A K   B MN   bf16
-    kP,          // P[z]       = exp2(S - m) / l, S = q_abs.c^T  M=T  N=T   K=(hi,lo)r A K   B K    bf16 [z,T,Tp]
+    kP,          // P[z]       = exp2(S - lse), S = q_abs.c^T    M=T  N=T   K=(hi,lo)r A K   B K    bf16 [z,T,Tp]
                  //              (+ this tile's row sums of the rounded P)
     kDS,         // dS[z]      = scale P (do_lat . c^T - delta)  M=T  N=T   K=r        A K   B K    bf16
     kOLat,       // o_lat[z]   = P . c                          M=T  N=r   K=u<=t     A K   B MN   bf16
