@@ -249,16 +249,16 @@ __device__ __forceinline__ void load_step(const GemmP &p, const CUtensorMap *ta,
             tl3<kPair>(sa, ta, bar, k, m0, zz);
             for (int j = 0; j < nbp; ++j) tl3<kPair>(sb + j * 16384, tb, bar, k, n0 + 128 * j, b);
             break;
-        case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u)
+        case kOLat: case kDqAbs:   // A = P or dS [z,T,Tp] (K-major over u), B = c [B,T,r] (MN-major: rows u;
+                                   // slab map: both 64-column slabs of a part in one box)
             tl3<kPair>(sa, ta, bar, k, m0, zz);
-            for (int j = 0; j < nbp; ++j)
-                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, tb, bar, n0 + 128 * j + 64 * s, k, b);
+            for (int j = 0; j < nbp; ++j) tl4<kPair>(sb + j * 16384, tb, bar, 0, k, (n0 + 128 * j) / 64, b);
             break;
-        case kDc: {   // A = P^T or dS^T (MN-major: rows t, u contiguous), B = do_lat or q_abs (MN-major: rows t)
+        case kDc: {   // A = P^T or dS^T (MN-major: rows t, u contiguous), B = do_lat or q_abs (MN-major: rows t);
+                      // slab maps: both 64-column slabs of an operand part in one box
             const CUtensorMap *a = pair ? ta2 : ta, *bm = pair ? tb2 : tb;
-            for (int s = 0; s < 2; ++s) tl3<kPair>(sa + s * 8192, a, bar, m0 + 64 * s, k, zz);
-            for (int j = 0; j < nbp; ++j)
-                for (int s = 0; s < 2; ++s) tl3<kPair>(sb + j * 16384 + s * 8192, bm, bar, n0 + 128 * j + 64 * s, k, zz);
+            tl4<kPair>(sa, a, bar, 0, k, m0 / 64, zz);
+            for (int j = 0; j < nbp; ++j) tl4<kPair>(sb + j * 16384, bm, bar, 0, k, (n0 + 128 * j) / 64, zz);
             break;
         }
         case kDq:   // A = dq_abs [z,T,r] (K-major), B = W_UK [H,d,r] (K-major: rows d)
@@ -985,7 +985,7 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     // tensor maps (dims innermost first, strides in bytes)
     const cuuint64_t uT = T, uH = H, uB = B, uZ = rowsz, uTp = Tp;
     CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqa_mn, mqlo_k, mqlo_mn, mdl_k, mdl_mn, mol_mn, mdqa_k,
-        mdqa_mn, mc_k, mc_mn, mP_k, mP_mn, mdS_k, mdS_mn;
+        mdqa_mn, mc_k, mP_k, mdS_k, mc_sl, mP_sl, mdS_sl, mdl_sl, mqa_sl;
     bool okm = true;
     auto E = [&](CUtensorMap *m, const void *ptr, int rank, std::initializer_list<cuuint64_t> d,
                  std::initializer_list<cuuint64_t> st, std::initializer_list<cuuint32_t> bx) {
@@ -1017,13 +1017,19 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     EKM(&mdqa_k, &mdqa_mn, L.dqa);
     E(&mol_mn, bf(L.ol), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
     E(&mc_k, a.c, 3, {kR, uT, uB}, {kR * 2, kR * 2 * uT}, {64, 128, 1});
-    E(&mc_mn, a.c, 3, {kR, uT, uB}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
-    auto ETT = [&](CUtensorMap *mk, CUtensorMap *mm, size_t off) {   // a [z, T, Tp] matrix
-        E(mk, bf(off), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 128, 1});
-        E(mm, bf(off), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 64, 1});
+    // slab maps of MN-major operands: [64 columns] x [rows] x [column slab of 64] x [batch], so one box
+    // {64, 64, 2, 1} brings two 64-column slabs, 8 KB apart in shared memory (the MN-major operand layout),
+    // in one TMA instruction instead of two
+    auto ESL = [&](CUtensorMap *m, const void *ptr, cuuint64_t cols, cuuint64_t nz) {
+        E(m, ptr, 4, {64, uT, cols / 64, nz}, {cols * 2, 128, cols * 2 * uT}, {64, 64, 2, 1});
     };
-    ETT(&mP_k, &mP_mn, L.P);
-    ETT(&mdS_k, &mdS_mn, L.dS);
+    ESL(&mc_sl, a.c, kR, uB);
+    ESL(&mdl_sl, bf(L.dl), kR, uZ);
+    ESL(&mqa_sl, bf(L.qa), kR, uZ);
+    E(&mP_k, bf(L.P), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 128, 1});
+    E(&mdS_k, bf(L.dS), 3, {uTp, uT, uZ}, {uTp * 2, uTp * 2 * uT}, {64, 128, 1});
+    ESL(&mP_sl, bf(L.P), uTp, uZ);
+    ESL(&mdS_sl, bf(L.dS), uTp, uZ);
     if (!okm) return cudaErrorInvalidValue;
     if ((e = cudaFuncSetAttribute(bwd_gemm_kernel<128, 1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(Shape<128>::kSmemW))) != cudaSuccess ||
@@ -1117,10 +1123,10 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     if ((e = gemm(kQAbs, mq_k, mwuk_mn, mq_k, mwuk_mn, T, kR, Z, bf(L.qa), 1)) != cudaSuccess) return e;
     if ((e = gemm(kDoLat, mdo_k, mwuv_mn, mdo_k, mwuv_mn, T, kR, Z, bf(L.dl), 1)) != cudaSuccess) return e;
     if ((e = gemm(kP, mqa_k, mc_k, mqlo_k, mc_k, T, T, Z, bf(L.P), 2)) != cudaSuccess) return e;
-    if ((e = gemm(kOLat, mP_k, mc_mn, mP_k, mc_mn, T, kR, Z, bf(L.ol), 2)) != cudaSuccess) return e;
+    if ((e = gemm(kOLat, mP_k, mc_sl, mP_k, mc_sl, T, kR, Z, bf(L.ol), 2)) != cudaSuccess) return e;
     if ((e = gemm(kDS, mdl_k, mc_k, mP_k, mc_k, T, T, Z, bf(L.dS), 1)) != cudaSuccess) return e;
-    if ((e = gemm(kDqAbs, mdS_k, mc_mn, mdS_k, mc_mn, T, kR, Z, bf(L.dqa), 2)) != cudaSuccess) return e;
-    if ((e = gemm(kDc, mP_mn, mdl_mn, mdS_mn, mqa_mn, T, kR, B, a.dc, 2)) != cudaSuccess) return e;
+    if ((e = gemm(kDqAbs, mdS_k, mc_sl, mdS_k, mc_sl, T, kR, Z, bf(L.dqa), 2)) != cudaSuccess) return e;
+    if ((e = gemm(kDc, mP_sl, mdl_sl, mdS_sl, mqa_sl, T, kR, B, a.dc, 2)) != cudaSuccess) return e;
     if ((e = gemm(kDq, mdqa_k, mwuk_k, mdqa_k, mwuk_k, T, kD, Z, a.dq, 0)) != cudaSuccess) return e;
     if ((e = gemm(kDWuk, mq_mn, mdqa_mn, mq_mn, mdqa_mn, kD, kR, H, a.dw_uk, 1)) != cudaSuccess) return e;
     return gemm(kDWuv, mdo_mn, mol_mn, mdo_mn, mol_mn, kD, kR, H, a.dw_uv, 1);
