@@ -984,8 +984,8 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     }
     // tensor maps (dims innermost first, strides in bytes)
     const cuuint64_t uT = T, uH = H, uB = B, uZ = rowsz, uTp = Tp;
-    CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqa_mn, mqlo_k, mqlo_mn, mdl_k, mdl_mn, mol_mn, mdqa_k,
-        mdqa_mn, mc_k, mP_k, mdS_k, mc_sl, mP_sl, mdS_sl, mdl_sl, mqa_sl;
+    CUtensorMap mq_k, mq_mn, mwuk_mn, mwuk_k, mwuv_mn, mdo_k, mdo_mn, mqa_k, mqlo_k, mdl_k, mol_mn, mdqa_k, mdqa_mn,
+        mc_k, mP_k, mdS_k, mc_sl, mP_sl, mdS_sl, mdl_sl, mqa_sl;
     bool okm = true;
     auto E = [&](CUtensorMap *m, const void *ptr, int rank, std::initializer_list<cuuint64_t> d,
                  std::initializer_list<cuuint64_t> st, std::initializer_list<cuuint32_t> bx) {
@@ -1007,14 +1007,14 @@ cudaError_t launch_backward_bf16_r512(const BackwardR512Args &a, cudaStream_t s)
     E(&mwuv_mn, a.w_uv, 3, {kR, kD, uH}, {kR * 2, kR * kD * 2}, {64, 64, 1});
     E(&mdo_k, bf(L.do_hm), 3, {kD, uT, uZ}, {kD * 2, kD * 2 * uT}, {64, 128, 1});
     E(&mdo_mn, bf(L.do_hm), 3, {kD, uT, uZ}, {kD * 2, kD * 2 * uT}, {64, 64, 1});
-    auto EKM = [&](CUtensorMap *mk, CUtensorMap *mm, size_t off) {   // a [z, T, r] matrix, K-major and MN-major boxes
+    auto EK = [&](CUtensorMap *mk, size_t off) {   // a [z, T, r] matrix, K-major boxes [128 rows x 64]
         E(mk, bf(off), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 128, 1});
-        E(mm, bf(off), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
     };
-    EKM(&mqa_k, &mqa_mn, L.qa);
-    EKM(&mqlo_k, &mqlo_mn, L.qlo);
-    EKM(&mdl_k, &mdl_mn, L.dl);
-    EKM(&mdqa_k, &mdqa_mn, L.dqa);
+    EK(&mqa_k, L.qa);
+    EK(&mqlo_k, L.qlo);
+    EK(&mdl_k, L.dl);
+    EK(&mdqa_k, L.dqa);
+    E(&mdqa_mn, bf(L.dqa), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});   // dW_UK's B: MN-major
     E(&mol_mn, bf(L.ol), 3, {kR, uT, uZ}, {kR * 2, kR * 2 * uT}, {64, 64, 1});
     E(&mc_k, a.c, 3, {kR, uT, uB}, {kR * 2, kR * 2 * uT}, {64, 128, 1});
     // slab maps of MN-major operands: [64 columns] x [rows] x [column slab of 64] x [batch], so one box
